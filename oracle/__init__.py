@@ -1,0 +1,213 @@
+"""CPU oracle for the split-K W4A16-g128 projection matmul (test infrastructure).
+
+Only the tests, the smoke check and the bench's CPU-baseline leg use this
+package; the library under ``split_w4a16_quantized_gb300`` never imports it and
+shares no code with it.  The arithmetic lives in ``qmm_oracle.c`` (plain C,
+fp64); this module compiles it with gcc and wraps it with ctypes.
+
+Sources the oracle follows (cited per function in the C file):
+  * tiny-llm book, "Week 2 Day 7: Split-K Prefill" (Tasks 2-4)
+  * gpu-kernels-explained, "Split-K, streams and overlap" (Maths; A100 table)
+  * "Optimize Prefill vs Decode Kernels" (Required reasoning process, step 5)
+
+Parity pins: every function here is checked by ``tests/test_oracle.py``
+against values the pages print, closed forms, exact rational brute force on
+tiny shapes and library routines; none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "qmm_oracle.c")
+_LIB = os.path.join(_HERE, "_build", "libqmm_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+# -ffp-contract=off keeps every a*b+c a separately rounded multiply and add on
+# both x86-64 and aarch64, so the oracle gives the same bits on both hosts.
+_CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math"]
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle (gcc, OpenMP when available).  Returns the .so path."""
+    os.makedirs(os.path.dirname(_LIB), exist_ok=True)
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    tmp = _LIB + ".tmp%d" % os.getpid()
+    base = ["gcc", *_CFLAGS, "-o", tmp, _SRC, "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True, capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        I64 = ctypes.c_int64
+        I = ctypes.c_int
+        sig = {
+            "oracle_bf16_round": [P, I64, P],
+            "oracle_bf16_value": [P, I64, P],
+            "oracle_unpack": [P, I64, I64, P],
+            "oracle_dequant": [P, P, P, I64, I64, P],
+            "oracle_qmm": [P, P, P, P, I64, I64, I64, P, I],
+            "oracle_qmm_sampled": [P, P, P, P, I64, I64, I64, P, I64, P, I64, P, I],
+            "oracle_qmm_partitioned": [P, P, P, P, I64, I64, I64, I, I, P, P, I],
+            "oracle_splitk_plan": [I64, I64, I64, I64, I64, I64, I64, I64, P],
+            "oracle_waves": [I64, I64, I64],
+            "oracle_gemm": [P, P, I64, I64, I64, P, I],
+            "oracle_gemm_partitioned": [P, P, I64, I64, I64, I64, I, P, I],
+        }
+        for name, args in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = I64 if name == "oracle_waves" else I
+        _lib = lib
+        return lib
+
+
+def default_threads() -> int:
+    return max(1, os.cpu_count() or 1)
+
+
+def _ptr(a: np.ndarray):
+    assert a.flags["C_CONTIGUOUS"]
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def _check(rc, what):
+    if rc != 0:
+        raise ValueError("%s failed (%d)" % (what, rc))
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+# ---- number formats ------------------------------------------------------
+
+def bf16_round(x) -> np.ndarray:
+    """Round float64 values to BF16 (nearest, ties to even); returns bits."""
+    x = _c(x, np.float64)
+    out = np.empty(x.shape, np.uint16)
+    _check(_load().oracle_bf16_round(_ptr(x), x.size, _ptr(out)), "bf16_round")
+    return out
+
+
+def bf16_value(b) -> np.ndarray:
+    """BF16 bits -> float64 (exact)."""
+    b = _c(b, np.uint16)
+    out = np.empty(b.shape, np.float64)
+    _load().oracle_bf16_value(_ptr(b), b.size, _ptr(out))
+    return out
+
+
+# ---- W4A16-g128 ----------------------------------------------------------
+
+def unpack(Wq, Kred: int) -> np.ndarray:
+    Wq = _c(Wq, np.uint32)
+    nout = Wq.shape[0]
+    q = np.empty((nout, Kred), np.uint8)
+    _check(_load().oracle_unpack(_ptr(Wq), nout, Kred, _ptr(q)), "unpack")
+    return q
+
+
+def dequant(Wq, scales, biases, Kred: int) -> np.ndarray:
+    """BF16 bits of w[n,k] = BF16(scale*q + bias) [Nout, Kred]."""
+    Wq, scales, biases = _c(Wq, np.uint32), _c(scales, np.uint16), _c(biases, np.uint16)
+    nout = Wq.shape[0]
+    w = np.empty((nout, Kred), np.uint16)
+    _check(_load().oracle_dequant(_ptr(Wq), _ptr(scales), _ptr(biases), nout, Kred, _ptr(w)),
+           "dequant")
+    return w
+
+
+def qmm(A, Wq, scales, biases, threads: int | None = None) -> np.ndarray:
+    """fp64 C = A @ W^T [M, Nout]."""
+    A, Wq = _c(A, np.uint16), _c(Wq, np.uint32)
+    scales, biases = _c(scales, np.uint16), _c(biases, np.uint16)
+    M, Kred = A.shape
+    nout = Wq.shape[0]
+    C = np.empty((M, nout), np.float64)
+    _check(_load().oracle_qmm(_ptr(A), _ptr(Wq), _ptr(scales), _ptr(biases), M, Kred, nout,
+                              _ptr(C), threads or default_threads()), "qmm")
+    return C
+
+
+def qmm_sampled(A, Wq, scales, biases, rows, cols, threads: int | None = None) -> np.ndarray:
+    """fp64 C[rows][:, cols] computed element by element."""
+    A, Wq = _c(A, np.uint16), _c(Wq, np.uint32)
+    scales, biases = _c(scales, np.uint16), _c(biases, np.uint16)
+    rows, cols = _c(rows, np.int64), _c(cols, np.int64)
+    M, Kred = A.shape
+    nout = Wq.shape[0]
+    out = np.empty((rows.size, cols.size), np.float64)
+    _check(_load().oracle_qmm_sampled(_ptr(A), _ptr(Wq), _ptr(scales), _ptr(biases), M, Kred,
+                                      nout, _ptr(rows), rows.size, _ptr(cols), cols.size,
+                                      _ptr(out), threads or default_threads()), "qmm_sampled")
+    return out
+
+
+def qmm_partitioned(A, Wq, scales, biases, split: int, partial_mode: int = 0,
+                    with_partials: bool = False, threads: int | None = None):
+    """Partition emulation: returns (C bf16 bits [M,Nout], partial planes or None)."""
+    A, Wq = _c(A, np.uint16), _c(Wq, np.uint32)
+    scales, biases = _c(scales, np.uint16), _c(biases, np.uint16)
+    M, Kred = A.shape
+    nout = Wq.shape[0]
+    C = np.empty((M, nout), np.uint16)
+    P = np.empty((split, M, nout), np.float64) if with_partials else None
+    _check(_load().oracle_qmm_partitioned(
+        _ptr(A), _ptr(Wq), _ptr(scales), _ptr(biases), M, Kred, nout, split, partial_mode,
+        _ptr(C), _ptr(P) if P is not None else None, threads or default_threads()),
+        "qmm_partitioned")
+    return C, P
+
+
+def splitk_plan(M, Kred, Nout, bm, bn, target, cap, min_k=128) -> int:
+    s = ctypes.c_int(0)
+    _check(_load().oracle_splitk_plan(M, Kred, Nout, bm, bn, target, cap, min_k,
+                                      ctypes.byref(s)), "splitk_plan")
+    return s.value
+
+
+def waves(tiles, split, sms) -> int:
+    r = _load().oracle_waves(tiles, split, sms)
+    if r < 0:
+        raise ValueError("waves: bad arguments")
+    return int(r)
+
+
+# ---- dense BF16 GEMM -----------------------------------------------------
+
+def gemm(A, W, threads: int | None = None) -> np.ndarray:
+    A, W = _c(A, np.uint16), _c(W, np.uint16)
+    M, K = A.shape
+    N = W.shape[0]
+    C = np.empty((M, N), np.float64)
+    _check(_load().oracle_gemm(_ptr(A), _ptr(W), M, N, K, _ptr(C),
+                               threads or default_threads()), "gemm")
+    return C
+
+
+def gemm_partitioned(A, W, split: int, ktile: int = 64, threads: int | None = None):
+    A, W = _c(A, np.uint16), _c(W, np.uint16)
+    M, K = A.shape
+    N = W.shape[0]
+    C = np.empty((M, N), np.uint16)
+    _check(_load().oracle_gemm_partitioned(_ptr(A), _ptr(W), M, N, K, ktile, split, _ptr(C),
+                                           threads or default_threads()), "gemm_partitioned")
+    return C

@@ -1,0 +1,332 @@
+/*
+ * CPU oracle for the split-K W4A16-g128 projection matmul and the dense BF16
+ * split-K GEMM.  TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the
+ * bench's CPU baseline call it; the library never does.  It shares no code,
+ * header, table or helper with the CUDA path.
+ *
+ * Plain, slow and meant to be read against the sources:
+ *   [TL] tiny-llm book, "Week 2 Day 7: Split-K Prefill"
+ *        (Why Split the Reduction Dimension?; Task 2: Reuse the Day 6 Kernel
+ *        for Each Partition; Task 3: Choose Partitions From Occupancy;
+ *        Task 4: Reduce and Verify)
+ *   [SK] gpu-kernels-explained, "Split-K, streams and overlap"
+ *        (second Concept section; Maths, "Split-K"; the A100 model table)
+ *   [PD] "Optimize Prefill vs Decode Kernels" (Required reasoning process,
+ *        step 5: at least ~512 reduction elements per split)
+ * The weight format (w = scale*q + bias, q in 0..15, eight nibbles per
+ * uint32 low nibble first, BF16 scale and bias per 128-group along the
+ * reduction axis) is the MLX-style affine "w4a16_g128" format [TL] checks
+ * against.
+ *
+ * Conventions: M activation rows, Kred reduction length, Nout output width
+ * ([TL] writes K for the output width and N for the reduction length).
+ * A is BF16 [M, Kred]; Wq uint32 [Nout, Kred/8]; scales, biases BF16
+ * [Nout, Kred/128]; C = A . W^T is [M, Nout].  BF16 values travel as uint16
+ * bit patterns.  Floating point is fp64 unless a step rounds on purpose.
+ * Every function returns 0 on success and a negative code on bad arguments.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define QO_GROUP 128
+
+/* ---- number formats ---------------------------------------------------- */
+
+/* BF16 bit pattern -> double (exact: BF16 is the top half of an fp32). */
+static double bf16_value(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* Round a finite double to the nearest BF16 value, ties to even.
+ * BF16 keeps 8 significant bits: write |x| = m * 2^e with m in [0.5, 1),
+ * round m * 2^8 to an integer (nearbyint rounds half to even in the default
+ * rounding mode) and scale back.  Values below the BF16 normal range or
+ * above its maximum are refused; the workloads never produce them. */
+static int bf16_round(double x, uint16_t *out) {
+    if (!isfinite(x)) return -1;
+    if (x == 0.0) { *out = signbit(x) ? 0x8000u : 0u; return 0; }
+    int e;
+    double m = frexp(fabs(x), &e);
+    if (e < -125) return -2;                  /* |x| < 2^-126: subnormal */
+    double y = ldexp(nearbyint(ldexp(m, 8)), e - 8);
+    if (y > 3.3895313892515355e38) return -3; /* above BF16 max */
+    float f = (float)y;                       /* exact: 8 significant bits */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    *out = (uint16_t)((u >> 16) | (signbit(x) ? 0x8000u : 0u));
+    return 0;
+}
+
+int oracle_bf16_round(const double *x, int64_t n, uint16_t *out) {
+    for (int64_t i = 0; i < n; ++i)
+        if (bf16_round(x[i], &out[i])) return -1;
+    return 0;
+}
+
+int oracle_bf16_value(const uint16_t *b, int64_t n, double *out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = bf16_value(b[i]);
+    return 0;
+}
+
+/* ---- W4A16-g128: unpack and dequant ------------------------------------ */
+
+/* q[n, k] = (Wq[n, k/8] >> 4*(k%8)) & 0xF : eight nibbles per word, the
+ * lowest nibble holds the smallest k. */
+static int nibble(const uint32_t *Wq, int64_t Kred, int64_t n, int64_t k) {
+    uint32_t word = Wq[n * (Kred / 8) + k / 8];
+    return (int)((word >> (4 * (k % 8))) & 0xFu);
+}
+
+int oracle_unpack(const uint32_t *Wq, int64_t Nout, int64_t Kred, uint8_t *q) {
+    if (Nout < 1 || Kred < 8 || Kred % 8) return -1;
+    for (int64_t n = 0; n < Nout; ++n)
+        for (int64_t k = 0; k < Kred; ++k)
+            q[n * Kred + k] = (uint8_t)nibble(Wq, Kred, n, k);
+    return 0;
+}
+
+/* w[n, k] = BF16(scale[n, g] * q[n, k] + bias[n, g]) with g = k / 128.
+ * The product of a BF16 scale and a 4-bit integer has at most 12 significant
+ * bits, so scale*q + bias is exact in fp64 and the single rounding to BF16
+ * is the correctly rounded dequantized weight.  Rows are dequantized one at
+ * a time into a caller buffer of Kred doubles (the BF16 values, exactly). */
+static int dequant_row(const uint32_t *Wq, const uint16_t *scales, const uint16_t *biases,
+                       int64_t Kred, int64_t n, double *w) {
+    int64_t G = Kred / QO_GROUP;
+    for (int64_t k = 0; k < Kred; ++k) {
+        int64_t g = k / QO_GROUP;
+        double s = bf16_value(scales[n * G + g]);
+        double b = bf16_value(biases[n * G + g]);
+        uint16_t wb;
+        if (bf16_round(s * (double)nibble(Wq, Kred, n, k) + b, &wb)) return -1;
+        w[k] = bf16_value(wb);
+    }
+    return 0;
+}
+
+int oracle_dequant(const uint32_t *Wq, const uint16_t *scales, const uint16_t *biases,
+                   int64_t Nout, int64_t Kred, uint16_t *w_bf16) {
+    if (Nout < 1 || Kred < QO_GROUP || Kred % QO_GROUP) return -1;
+    double *row = (double *)malloc(sizeof(double) * (size_t)Kred);
+    if (!row) return -4;
+    int rc = 0;
+    for (int64_t n = 0; n < Nout && !rc; ++n) {
+        rc = dequant_row(Wq, scales, biases, Kred, n, row);
+        for (int64_t k = 0; k < Kred && !rc; ++k) rc = bf16_round(row[k], &w_bf16[n * Kred + k]);
+    }
+    free(row);
+    return rc ? -1 : 0;
+}
+
+/* Dequantize the whole weight into doubles (row-major [Nout, Kred]). */
+static double *dequant_all(const uint32_t *Wq, const uint16_t *scales, const uint16_t *biases,
+                           int64_t Nout, int64_t Kred, int nthreads) {
+    double *w = (double *)malloc(sizeof(double) * (size_t)(Nout * Kred));
+    if (!w) return NULL;
+    int bad = 0;
+#pragma omp parallel for num_threads(nthreads) schedule(static) reduction(| : bad)
+    for (int64_t n = 0; n < Nout; ++n)
+        bad |= dequant_row(Wq, scales, biases, Kred, n, w + n * Kred) != 0;
+    if (bad) { free(w); return NULL; }
+    return w;
+}
+
+static double *bf16_matrix(const uint16_t *x, int64_t rows, int64_t cols, int nthreads) {
+    double *d = (double *)malloc(sizeof(double) * (size_t)(rows * cols));
+    if (!d) return NULL;
+#pragma omp parallel for num_threads(nthreads) schedule(static)
+    for (int64_t i = 0; i < rows * cols; ++i) d[i] = bf16_value(x[i]);
+    return d;
+}
+
+/* sum over k in [k0, k1) of a[k] * w[k], fp64, ascending k */
+static double dot(const double *a, const double *w, int64_t k0, int64_t k1) {
+    double acc = 0.0;
+    for (int64_t k = k0; k < k1; ++k) acc += a[k] * w[k];
+    return acc;
+}
+
+/* ---- W4A16-g128: the matmul -------------------------------------------- */
+
+/* C64[m, n] = sum_k A[m, k] * w[n, k]: the plain definition of C = A @ W^T
+ * [TL, Why Split the Reduction Dimension?], in fp64. */
+int oracle_qmm(const uint16_t *A, const uint32_t *Wq, const uint16_t *scales,
+               const uint16_t *biases, int64_t M, int64_t Kred, int64_t Nout,
+               double *C64, int nthreads) {
+    if (M < 1 || Nout < 1 || Kred < QO_GROUP || Kred % QO_GROUP || nthreads < 1) return -1;
+    double *w = dequant_all(Wq, scales, biases, Nout, Kred, nthreads);
+    double *a = bf16_matrix(A, M, Kred, nthreads);
+    if (!w || !a) { free(w); free(a); return -4; }
+#pragma omp parallel for num_threads(nthreads) schedule(static) collapse(2)
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < Nout; ++n)
+            C64[m * Nout + n] = dot(a + m * Kred, w + n * Kred, 0, Kred);
+    free(w);
+    free(a);
+    return 0;
+}
+
+/* The same definition on a sample: out[i, j] = C64[rows[i], cols[j]].
+ * Only the sampled weight rows are dequantized. */
+int oracle_qmm_sampled(const uint16_t *A, const uint32_t *Wq, const uint16_t *scales,
+                       const uint16_t *biases, int64_t M, int64_t Kred, int64_t Nout,
+                       const int64_t *rows, int64_t nr, const int64_t *cols, int64_t nc,
+                       double *out, int nthreads) {
+    if (M < 1 || Nout < 1 || Kred < QO_GROUP || Kred % QO_GROUP || nthreads < 1) return -1;
+    for (int64_t i = 0; i < nr; ++i) if (rows[i] < 0 || rows[i] >= M) return -1;
+    for (int64_t j = 0; j < nc; ++j) if (cols[j] < 0 || cols[j] >= Nout) return -1;
+    double *w = (double *)malloc(sizeof(double) * (size_t)(nc * Kred));
+    double *a = (double *)malloc(sizeof(double) * (size_t)(nr * Kred));
+    if (!w || !a) { free(w); free(a); return -4; }
+    int bad = 0;
+    for (int64_t j = 0; j < nc && !bad; ++j)
+        bad = dequant_row(Wq, scales, biases, Kred, cols[j], w + j * Kred);
+    for (int64_t i = 0; i < nr; ++i)
+        for (int64_t k = 0; k < Kred; ++k) a[i * Kred + k] = bf16_value(A[rows[i] * Kred + k]);
+    if (!bad) {
+#pragma omp parallel for num_threads(nthreads) schedule(static) collapse(2)
+        for (int64_t i = 0; i < nr; ++i)
+            for (int64_t j = 0; j < nc; ++j)
+                out[i * nc + j] = dot(a + i * Kred, w + j * Kred, 0, Kred);
+    }
+    free(w);
+    free(a);
+    return bad ? -1 : 0;
+}
+
+/* Partition emulation [TL, Task 2 and Task 4].  With split s dividing
+ * G = Kred/128, partition p covers groups [p*G/s, (p+1)*G/s): equal length,
+ * starting and ending on group boundaries.  Each partition's fp64 sum is
+ * rounded to the partial-plane type (partial_mode 0: BF16, 1: FP32) and
+ * stored in its own plane partial[p, m, n]; the planes are then added in
+ * FP32 in ascending p and the sum is rounded once to BF16.  With s = 1 there
+ * is no partial plane: C = BF16(C64).  Outputs: C_bf16 [M, Nout] and, if
+ * partials is not NULL, the planes as doubles [s, M, Nout]. */
+int oracle_qmm_partitioned(const uint16_t *A, const uint32_t *Wq, const uint16_t *scales,
+                           const uint16_t *biases, int64_t M, int64_t Kred, int64_t Nout,
+                           int split, int partial_mode, uint16_t *C_bf16, double *partials,
+                           int nthreads) {
+    if (M < 1 || Nout < 1 || Kred < QO_GROUP || Kred % QO_GROUP || nthreads < 1) return -1;
+    int64_t G = Kred / QO_GROUP;
+    if (split < 1 || G % split || (partial_mode != 0 && partial_mode != 1)) return -1;
+    int64_t span = (G / split) * QO_GROUP;
+    double *w = dequant_all(Wq, scales, biases, Nout, Kred, nthreads);
+    double *a = bf16_matrix(A, M, Kred, nthreads);
+    if (!w || !a) { free(w); free(a); return -4; }
+    int bad = 0;
+#pragma omp parallel for num_threads(nthreads) schedule(static) collapse(2) reduction(| : bad)
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < Nout; ++n) {
+            const double *am = a + m * Kred, *wn = w + n * Kred;
+            uint16_t c;
+            if (split == 1) {
+                bad |= bf16_round(dot(am, wn, 0, Kred), &c) != 0;
+                if (partials) partials[m * Nout + n] = dot(am, wn, 0, Kred);
+            } else {
+                float acc = 0.0f; /* the reduce adds the planes in FP32 */
+                for (int p = 0; p < split; ++p) {
+                    double exact = dot(am, wn, p * span, (p + 1) * span);
+                    double plane;
+                    if (partial_mode == 0) {
+                        uint16_t pb;
+                        bad |= bf16_round(exact, &pb) != 0;
+                        plane = bf16_value(pb);
+                    } else {
+                        plane = (double)(float)exact;
+                    }
+                    if (partials) partials[((int64_t)p * M + m) * Nout + n] = plane;
+                    acc = acc + (float)plane;
+                }
+                bad |= bf16_round((double)acc, &c) != 0;
+            }
+            C_bf16[m * Nout + n] = c;
+        }
+    free(w);
+    free(a);
+    return bad ? -1 : 0;
+}
+
+/* ---- occupancy policy and wave count ----------------------------------- */
+
+/* [TL, Task 3]: base = ceil(M/BM)*ceil(Nout/BN);
+ * s = min(cap, floor(target/base), Kred/128), then decreased by one until
+ * Kred is divisible by s*128; s <= 1 means the unsplit kernel.  The
+ * Kred/128 bound becomes floor(Kred/min_k) when a minimum number of
+ * reduction elements per split is asked for [PD, step 5]; min_k = 128
+ * is the rule as [TL] states it. */
+int oracle_splitk_plan(int64_t M, int64_t Kred, int64_t Nout, int64_t bm, int64_t bn,
+                       int64_t target, int64_t cap, int64_t min_k, int *split) {
+    if (M < 1 || Nout < 1 || Kred < QO_GROUP || Kred % QO_GROUP) return -1;
+    if (bm < 1 || bn < 1 || target < 0 || cap < 1 || min_k < QO_GROUP || min_k % QO_GROUP) return -1;
+    int64_t base = ((M + bm - 1) / bm) * ((Nout + bn - 1) / bn);
+    int64_t s = cap;
+    if (target / base < s) s = target / base;
+    if (Kred / min_k < s) s = Kred / min_k;
+    while (s > 1 && Kred % (s * QO_GROUP) != 0) s -= 1;
+    if (s <= 1) s = 1;
+    *split = (int)s;
+    return 0;
+}
+
+/* [SK, Maths, Split-K]: tiles*s blocks run in ceil(tiles*s / SMs) waves. */
+int64_t oracle_waves(int64_t tiles, int64_t split, int64_t sms) {
+    if (tiles < 1 || split < 1 || sms < 1) return -1;
+    return (tiles * split + sms - 1) / sms;
+}
+
+/* ---- dense BF16 split-K GEMM ------------------------------------------- */
+
+/* C64[m, n] = sum_k A[m, k] * W[n, k] for BF16 A [M, K] and W [N, K]. */
+int oracle_gemm(const uint16_t *A, const uint16_t *W, int64_t M, int64_t N, int64_t K,
+                double *C64, int nthreads) {
+    if (M < 1 || N < 1 || K < 1 || nthreads < 1) return -1;
+    double *a = bf16_matrix(A, M, K, nthreads);
+    double *w = bf16_matrix(W, N, K, nthreads);
+    if (!a || !w) { free(a); free(w); return -4; }
+#pragma omp parallel for num_threads(nthreads) schedule(static) collapse(2)
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) C64[m * N + n] = dot(a + m * K, w + n * K, 0, K);
+    free(a);
+    free(w);
+    return 0;
+}
+
+/* Split-K with k cut into T = K/ktile tiles [SK, Concept: "cuts the k
+ * dimension into s slices"].  When s does not divide T the slices are as
+ * equal as whole tiles allow: the first T mod s slices get one extra tile.
+ * Partial sums are FP32 planes [s, M, N] [SK, Maths: 4-byte partials];
+ * the second pass adds them in FP32, ascending slice, and rounds to BF16. */
+int oracle_gemm_partitioned(const uint16_t *A, const uint16_t *W, int64_t M, int64_t N,
+                            int64_t K, int64_t ktile, int split, uint16_t *C_bf16,
+                            int nthreads) {
+    if (M < 1 || N < 1 || ktile < 1 || K < ktile || K % ktile || nthreads < 1) return -1;
+    int64_t T = K / ktile;
+    if (split < 1 || split > T) return -1;
+    double *a = bf16_matrix(A, M, K, nthreads);
+    double *w = bf16_matrix(W, N, K, nthreads);
+    if (!a || !w) { free(a); free(w); return -4; }
+    int bad = 0;
+#pragma omp parallel for num_threads(nthreads) schedule(static) collapse(2) reduction(| : bad)
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) {
+            float acc = 0.0f;
+            int64_t t0 = 0;
+            for (int p = 0; p < split; ++p) {
+                int64_t nt = T / split + (p < T % split ? 1 : 0);
+                double exact = dot(a + m * K, w + n * K, t0 * ktile, (t0 + nt) * ktile);
+                acc = acc + (float)exact;
+                t0 += nt;
+            }
+            uint16_t c;
+            bad |= bf16_round((double)acc, &c) != 0;
+            C_bf16[m * N + n] = c;
+        }
+    free(a);
+    free(w);
+    return bad ? -1 : 0;
+}

@@ -1,0 +1,302 @@
+"""Pins for the CPU oracle: every oracle function is checked against something
+other than itself -- values the pages print, closed forms, exact rational
+brute force on tiny shapes, and library routines (torch's BF16 conversion,
+numpy's float32 view).  CPU only."""
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from split_w4a16_quantized_gb300 import inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _torch_bf16_bits(x64):
+    """Library rounding: float64 -> float32 (exact for the values used) -> BF16."""
+    x32 = np.asarray(x64, np.float64).astype(np.float32)
+    assert np.array_equal(x32.astype(np.float64), np.asarray(x64, np.float64))
+    return torch.from_numpy(x32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def _bits_to_f64(b):
+    return inputs.bf16_bits_to_f32(b).astype(np.float64)
+
+
+def _bf16_bits(v):
+    return int(_torch_bf16_bits(np.array([v]))[0])
+
+
+# ---- number formats --------------------------------------------------------
+
+def test_bf16_value_all_finite_patterns():
+    b = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref32 = (b.astype(np.uint32) << 16).view(np.float32)
+    fin = np.isfinite(ref32)
+    ref = np.where(fin, ref32, 0).astype(np.float64)
+    got = oracle.bf16_value(b)
+    assert np.array_equal(got[fin], ref[fin])
+
+
+def test_bf16_round_matches_torch_rne():
+    rng = np.random.default_rng(1)
+    x = rng.standard_normal(200000).astype(np.float32).astype(np.float64)
+    x *= np.exp2(rng.integers(-60, 60, x.size)).astype(np.float64)
+    assert np.array_equal(oracle.bf16_round(x), _torch_bf16_bits(x))
+
+
+def test_bf16_round_ties_to_even():
+    # 1 + 2^-8 is halfway between 1 and 1 + 2^-7: the even neighbour is 1.
+    # 1 + 3*2^-8 is halfway between 1 + 2^-7 (odd) and 1 + 2^-6 (even).
+    x = np.array([1 + 2.0 ** -8, 1 + 3 * 2.0 ** -8, -(1 + 2.0 ** -8), 0.0, -0.0, 3.0])
+    got = oracle.bf16_round(x)
+    assert list(got) == [0x3F80, 0x3F82, 0xBF80, 0x0000, 0x8000, 0x4040]
+
+
+# ---- unpack ----------------------------------------------------------------
+
+def test_unpack_fixed_words():
+    Wq = np.array([[0x76543210, 0xFEDCBA98]], np.uint32)
+    assert list(oracle.unpack(Wq, 16)[0]) == list(range(16))
+
+
+def test_unpack_single_nibbles():
+    for j in range(8):
+        q = oracle.unpack(np.array([[1 << (4 * j)]], np.uint32), 8)[0]
+        assert list(q) == [1 if i == j else 0 for i in range(8)]
+        q = oracle.unpack(np.array([[0xF << (4 * j)]], np.uint32), 8)[0]
+        assert list(q) == [15 if i == j else 0 for i in range(8)]
+
+
+def test_unpack_inverts_generator_packing():
+    p = inputs.make_w4a16(1, 512, 37, seed=3)
+    assert np.array_equal(oracle.unpack(p["Wq"], 512), p["q"])
+
+
+# ---- dequant ---------------------------------------------------------------
+
+def test_dequant_matches_library_rounding():
+    p = inputs.make_w4a16(1, 768, 50, seed=4)
+    G = 768 // 128
+    s = np.repeat(_bits_to_f64(p["scales"]), 128, axis=1)
+    b = np.repeat(_bits_to_f64(p["biases"]), 128, axis=1)
+    exact = s * p["q"].astype(np.float64) + b
+    assert np.array_equal(oracle.dequant(p["Wq"], p["scales"], p["biases"], 768),
+                          _torch_bf16_bits(exact))
+    assert G == 6
+
+
+def test_dequant_group_index():
+    # scale_g = 2^-g, q = 1, bias 0: every element of group g dequantizes to 2^-g
+    Kred, G = 512, 4
+    Wq = np.full((1, Kred // 8), 0x11111111, np.uint32)
+    scales = np.array([[_bf16_bits(2.0 ** -g) for g in range(G)]], np.uint16)
+    biases = np.zeros((1, G), np.uint16)
+    w = _bits_to_f64(oracle.dequant(Wq, scales, biases, Kred))[0]
+    assert np.array_equal(w, np.repeat(2.0 ** -np.arange(G), 128))
+
+
+# ---- the matmul ------------------------------------------------------------
+
+def _exact_qmm(p):
+    """Exact rational C = A @ W^T with W rounded to BF16 by torch."""
+    Kred = p["Kred"]
+    a = _bits_to_f64(p["A"])
+    s = np.repeat(_bits_to_f64(p["scales"]), 128, axis=1)
+    b = np.repeat(_bits_to_f64(p["biases"]), 128, axis=1)
+    w = _bits_to_f64(_torch_bf16_bits(s * p["q"].astype(np.float64) + b))
+    M, N = a.shape[0], w.shape[0]
+    C = [[sum((Fraction(a[m, k]) * Fraction(w[n, k]) for k in range(Kred)), Fraction(0))
+          for n in range(N)] for m in range(M)]
+    mag = np.abs(a) @ np.abs(w).T
+    return C, mag
+
+
+@pytest.mark.parametrize("M,Kred,Nout,seed", [(1, 128, 1, 0), (2, 128, 5, 1), (3, 256, 4, 2),
+                                              (3, 256, 5, 3)])
+def test_qmm_exact_brute_force(M, Kred, Nout, seed):
+    p = inputs.make_w4a16(M, Kred, Nout, seed=seed)
+    C = oracle.qmm(p["A"], p["Wq"], p["scales"], p["biases"], threads=2)
+    exact, mag = _exact_qmm(p)
+    for m in range(M):
+        for n in range(Nout):
+            assert abs(Fraction(C[m, n]) - exact[m][n]) <= Fraction(mag[m, n]) * Fraction(1, 2 ** 45)
+
+
+def test_qmm_closed_form_constant_rows():
+    # q = c_n, scale = s_n, bias = b_n on row n: C[m, n] = BF16(s_n c_n + b_n) * sum_k A[m, k]
+    M, Kred, Nout = 4, 384, 6
+    c = np.array([0, 3, 7, 8, 12, 15])
+    Wq = np.array([[int(ci) * 0x11111111] * (Kred // 8) for ci in c], np.uint32)
+    sv = np.array([0.0078125, 0.01171875, 0.015625, 0.005859375, 0.009765625, 0.0185546875])
+    bv = np.array([-0.0625, -0.09375, -0.125, -0.046875, -0.078125, -0.1484375])
+    scales = np.repeat(_torch_bf16_bits(sv)[:, None], 3, axis=1)
+    biases = np.repeat(_torch_bf16_bits(bv)[:, None], 3, axis=1)
+    a_bits = inputs.f32_to_bf16_bits(np.random.default_rng(5).standard_normal((M, Kred)))
+    C = oracle.qmm(a_bits, Wq, scales, biases, threads=1)
+    wv = _bits_to_f64(_torch_bf16_bits(_bits_to_f64(scales[:, 0]) * c + _bits_to_f64(biases[:, 0])))
+    rowsum = [math.fsum(r) for r in _bits_to_f64(a_bits)]
+    for m in range(M):
+        for n in range(Nout):
+            assert C[m, n] == pytest.approx(wv[n] * rowsum[m], rel=1e-13, abs=1e-13)
+
+
+def test_qmm_identity_weights():
+    # one-hot q rows (q[n, n] = 1), scale 1, bias 0: C = A[:, :Nout] exactly
+    Kred, Nout, M = 128, 100, 7
+    q = np.zeros((Nout, Kred), np.uint8)
+    q[np.arange(Nout), np.arange(Nout)] = 1
+    Wq = inputs.pack_nibbles(q)
+    scales = np.full((Nout, 1), 0x3F80, np.uint16)
+    biases = np.zeros((Nout, 1), np.uint16)
+    a = inputs.make_w4a16(M, Kred, 1, seed=6)["A"]
+    C = oracle.qmm(a, Wq, scales, biases, threads=1)
+    assert np.array_equal(C, _bits_to_f64(a)[:, :Nout])
+
+
+def test_qmm_one_hot_activations_give_transposed_weights():
+    # A = identity [Kred, Kred]: C[m, n] = w[n, m], which pins operand order
+    p = inputs.make_w4a16(1, 256, 9, seed=7)
+    eye = np.where(np.eye(256, dtype=bool), np.uint16(0x3F80), np.uint16(0))
+    C = oracle.qmm(eye, p["Wq"], p["scales"], p["biases"], threads=2)
+    w = _bits_to_f64(oracle.dequant(p["Wq"], p["scales"], p["biases"], 256))
+    assert np.array_equal(C, w.T)
+
+
+def test_qmm_sampled_matches_full():
+    p = inputs.make_w4a16(9, 640, 33, seed=8)
+    C = oracle.qmm(p["A"], p["Wq"], p["scales"], p["biases"], threads=2)
+    rows, cols = np.array([0, 4, 8]), np.array([0, 1, 17, 32])
+    S = oracle.qmm_sampled(p["A"], p["Wq"], p["scales"], p["biases"], rows, cols, threads=2)
+    assert np.array_equal(S, C[np.ix_(rows, cols)])
+
+
+# ---- partition emulation ---------------------------------------------------
+
+def test_partitioned_split1_is_rounded_exact():
+    p = inputs.make_w4a16(5, 1280, 40, seed=9)
+    C64 = oracle.qmm(p["A"], p["Wq"], p["scales"], p["biases"], threads=2)
+    for mode in (0, 1):
+        C, _ = oracle.qmm_partitioned(p["A"], p["Wq"], p["scales"], p["biases"], 1, mode)
+        # bf16_round is itself pinned against torch's rounding above
+        assert np.array_equal(C, oracle.bf16_round(C64))
+
+
+def test_partition_boundaries_follow_groups():
+    # activations nonzero only in group g: only the partition holding g gets a nonzero plane
+    Kred, G, s = 1280, 10, 5
+    p = inputs.make_w4a16(2, Kred, 8, seed=10)
+    for g in range(G):
+        a = np.zeros((2, Kred), np.uint16)
+        a[:, g * 128:(g + 1) * 128] = p["A"][:, g * 128:(g + 1) * 128]
+        _, P = oracle.qmm_partitioned(a, p["Wq"], p["scales"], p["biases"], s, 1,
+                                      with_partials=True)
+        nonzero = [bool(np.any(P[i] != 0)) for i in range(s)]
+        assert nonzero == [i == g // (G // s) for i in range(s)]
+
+
+def test_partitioned_error_bound():
+    p = inputs.make_w4a16(8, 2560, 64, seed=11)
+    C64 = oracle.qmm(p["A"], p["Wq"], p["scales"], p["biases"], threads=2)
+    for s in (2, 4, 5, 10):
+        C, P = oracle.qmm_partitioned(p["A"], p["Wq"], p["scales"], p["biases"], s, 0,
+                                      with_partials=True)
+        got = oracle.bf16_value(C)
+        # BF16 keeps 8 significant bits: each rounding is off by at most 2^-8 relative
+        bound = 2.0 ** -8 * (np.abs(P).sum(axis=0) + np.abs(C64)) + 2.0 ** -20 * np.abs(P).sum(axis=0)
+        assert np.all(np.abs(got - C64) <= bound + 1e-30)
+        assert np.allclose(P.sum(axis=0), C64, rtol=0, atol=2.0 ** -8 * np.abs(P).sum(axis=0).max())
+
+
+def test_partitioned_rejects_nondividing_split():
+    p = inputs.make_w4a16(1, 2560, 4, seed=12)
+    with pytest.raises(ValueError):
+        oracle.qmm_partitioned(p["A"], p["Wq"], p["scales"], p["biases"], 3, 0)
+
+
+# ---- policy and waves ------------------------------------------------------
+
+def test_plan_pages_stated_schedules():
+    gold = _golden("splitk_policy_pages.json")
+    pol = gold["policy"]
+    for c in gold["cases"]:
+        s = oracle.splitk_plan(c["M"], c["Kred"], c["Nout"], pol["bm"], pol["bn"],
+                               pol["target"], pol["cap"], pol["min_k"])
+        assert s == c["split"], c
+
+
+def _plan_property(M, Kred, Nout, bm, bn, target, cap, min_k):
+    """The largest s >= 2 that divides Kred/128 and stays within every bound, else 1."""
+    base = math.ceil(M / bm) * math.ceil(Nout / bn)
+    ok = [s for s in range(2, Kred // 128 + 1)
+          if (Kred // 128) % s == 0 and s <= cap and s * base <= target and s * min_k <= Kred]
+    return max(ok) if ok else 1
+
+
+def test_plan_matches_divisor_formulation():
+    rng = np.random.default_rng(13)
+    for _ in range(3000):
+        M = int(rng.integers(1, 3000))
+        Kred = 128 * int(rng.integers(1, 101))
+        Nout = int(rng.integers(1, 12000))
+        bm, bn = int(rng.choice([8, 16, 32, 64, 128])), int(rng.choice([32, 64, 128, 256]))
+        target = int(rng.integers(0, 2000))
+        cap = int(rng.integers(1, 33))
+        min_k = 128 * int(rng.integers(1, 9))
+        assert oracle.splitk_plan(M, Kred, Nout, bm, bn, target, cap, min_k) == \
+            _plan_property(M, Kred, Nout, bm, bn, target, cap, min_k)
+
+
+def test_waves_model_table():
+    gold = _golden("splitk_waves_model.json")
+    tiles = (gold["output"][0] // gold["tile"][0]) * (gold["output"][1] // gold["tile"][1])
+    assert tiles == gold["tiles"]
+    a = gold["a100"]
+    for r in a["rows"]:
+        assert tiles * r["split"] == r["blocks"]
+        assert oracle.waves(tiles, r["split"], a["sms"]) == r["waves"]
+    best = max(s for s in range(1, 64) if oracle.waves(tiles, s, a["sms"]) == 1)
+    assert best == a["best_split_one_wave"]
+    assert round(1 - tiles / a["sms"], 2) == a["idle_fraction_unsplit"]
+    h = gold["h100"]
+    best = max(s for s in range(1, 64) if oracle.waves(tiles, s, h["sms"]) == 1)
+    assert best == h["best_split_one_wave"] and tiles * best == h["blocks"]
+
+
+# ---- dense GEMM ------------------------------------------------------------
+
+def test_gemm_exact_brute_force():
+    d = inputs.make_dense(3, 4, 96, seed=14)
+    C = oracle.gemm(d["A"], d["W"], threads=1)
+    a, w = _bits_to_f64(d["A"]), _bits_to_f64(d["W"])
+    for m in range(3):
+        for n in range(4):
+            exact = sum((Fraction(a[m, k]) * Fraction(w[n, k]) for k in range(96)), Fraction(0))
+            assert abs(Fraction(C[m, n]) - exact) <= Fraction(float(np.abs(a[m]) @ np.abs(w[n]))) \
+                * Fraction(1, 2 ** 45)
+
+
+@pytest.mark.parametrize("split", [1, 2, 4, 6, 7, 9, 12, 16])
+def test_gemm_partitioned_covers_every_tile(split):
+    # integer-valued operands: every partial and sum is exact, so C = BF16(C64)
+    # for any split; a dropped or doubled k-tile would change the result
+    rng = np.random.default_rng(15)
+    K = 64 * 37
+    a = inputs.f32_to_bf16_bits(rng.integers(-2, 3, (5, K)).astype(np.float32))
+    w = inputs.f32_to_bf16_bits(rng.integers(-2, 3, (6, K)).astype(np.float32))
+    C64 = oracle.gemm(a, w, threads=2)
+    C = oracle.gemm_partitioned(a, w, split, ktile=64, threads=2)
+    assert np.array_equal(C, oracle.bf16_round(C64))
+    ones = np.full((1, K), 0x3F80, np.uint16)
+    assert oracle.bf16_value(oracle.gemm_partitioned(ones, ones, split, 64))[0, 0] == \
+        oracle.bf16_value(oracle.bf16_round(np.array([float(K)])))[0]
