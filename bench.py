@@ -1,0 +1,489 @@
+"""Benchmark of the split-K W4A16-g128 projection matmul on GB300.
+
+One step = the seven Qwen3-4B projections (q, k, v, o, gate, up, down) at
+M = 32 and M = 128 activation rows: 14 calls of qmm_w4a16_g128 with the
+split chosen by the GB300 occupancy policy (each call = partition kernel +
+reduce when it splits, one kernel when it does not).  Every call owns its
+own weights; R rotating copies of the whole input set (more than twice the
+L2 size together) make every step stream its weights from HBM.  Steps are
+replayed as CUDA graphs; timing uses CUDA events on the launching stream.
+
+Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle on
+the same workload instead.  Under torchrun each rank runs its own replica
+(the matmul has no cross-GPU exchange); the job value is the max-over-ranks
+time divided by all calls of all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from split_w4a16_quantized_gb300 import inputs  # noqa: E402
+
+METRIC = "µs/call and % of HBM/tensor roofline, W4A16-g128 split-K proj, M=16..2048"
+UNIT = "us/call"
+M_LIST = (32, 128)
+PROJ = list(inputs.PROJECTIONS)
+WORKLOAD = "Qwen3-4B projections q,k,v,o,gate,up,down (Kred->Nout) x M in {32,128}: " \
+           "14 W4A16-g128 matmuls per step"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def algorithmic(M, Kred, Nout, split, partial_bytes=2):
+    """Algorithmic bytes and flops of one call: packed weights, scales and
+    biases, A, C, and the partial planes written and read back."""
+    G = Kred // 128
+    nbytes = Nout * Kred // 2 + 4 * Nout * G + 2 * M * Kred + 2 * M * Nout
+    if split > 1:
+        nbytes += 2 * partial_bytes * split * M * Nout
+    return nbytes, 2.0 * M * Nout * Kred
+
+
+def roofline_time_s(nbytes, flops, peaks):
+    t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+    t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+    return (t_hbm, "hbm") if t_hbm >= t_tc else (t_tc, "tensor")
+
+
+def calls():
+    return [(name, M) + inputs.PROJECTIONS[name] for M in M_LIST for name in PROJ]
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms."""
+    FIELDS = "index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active," \
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown," \
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap"
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        busy = [s for s in sm if mx and s >= 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(busy) if busy else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(
+                    (num(r[3]) for r in rows if num(r[3]) is not None), default=None)}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+class Workload:
+    """Device buffers for R rotating copies of the 14-call step."""
+
+    def __init__(self, device, Q, l2_bytes):
+        self.Q = Q
+        self.device = device
+        self.calls = calls()
+        self.host = []
+        for name, M, Kred, Nout in self.calls:
+            self.host.append(inputs.make_w4a16(M, Kred, Nout, seed=0))
+        self.set_bytes = sum(p["A"].nbytes + p["Wq"].nbytes + p["scales"].nbytes +
+                             p["biases"].nbytes for p in self.host)
+        self.R = max(2, -(-2 * l2_bytes // self.set_bytes) + 1)
+        first = [Q.to_device(p, device) for p in self.host]
+        self.sets = [first] + [[{k: v.clone() for k, v in d.items()} for d in first]
+                               for _ in range(self.R - 1)]
+        self.C = [[torch.empty((M, Nout), dtype=torch.bfloat16, device=device)
+                   for (_, M, _, Nout) in self.calls] for _ in range(self.R)]
+        self.split = []
+        ws_max = 16
+        for (_, M, Kred, Nout) in self.calls:
+            pol = Q.qmm_policy_preset(Q.QMM_PRESET_GB300, M)
+            s = Q.qmm_splitk_plan(M, Kred, Nout, pol)
+            self.split.append(s)
+            ws_max = max(ws_max, Q.qmm_splitk_workspace_bytes(M, Nout, s, Q.QMM_PARTIAL_BF16))
+        self.ws = torch.empty(ws_max, dtype=torch.uint8, device=device)
+
+    def call(self, i, r, split_req=0):
+        d = self.sets[r][i]
+        return self.Q.qmm_w4a16_g128(d["A"], d["Wq"], d["scales"], d["biases"], self.C[r][i],
+                                     split_req=split_req, workspace=self.ws)
+
+    def step(self, r):
+        for i in range(len(self.calls)):
+            self.call(i, r)
+
+    def launches_per_step(self):
+        return sum(2 if s > 1 else 1 for s in self.split)
+
+
+def timed_launches(fn, n, flush, stream):
+    """Average device time of fn() over n launches, each on a cold L2: a
+    read of a buffer larger than L2 precedes every launch and keeps the
+    stream backed up, so host launch overhead stays outside the events."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n)]
+    torch.sum(flush)  # backlog
+    for i in range(n):
+        torch.sum(flush)
+        evs[i][0].record(stream)
+        fn(i)
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in evs) * 1e3  # µs
+
+
+def run_gpu(args, rank, world, local_rank):
+    from split_w4a16_quantized_gb300 import build as qbuild
+    qbuild.build()
+    from split_w4a16_quantized_gb300 import qmm as Q
+    import torch.distributed as dist
+
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    props = torch.cuda.get_device_properties(device)
+    l2 = int(getattr(props, "L2_cache_size", 128 << 20))
+    sms = props.multi_processor_count
+    peaks, peak_src = load_peaks()
+    wl = Workload(device, Q, l2)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=device).fill_(1)
+
+    # warm-up: eager step per set (first calls set kernel attributes), then graphs
+    for r in range(wl.R):
+        wl.step(r)
+    torch.cuda.synchronize()
+    graphs = []
+    cap = torch.cuda.Stream()
+    cap.wait_stream(stream)
+    with torch.cuda.stream(cap):
+        for r in range(wl.R):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cap):
+                wl.step(r)
+            graphs.append(g)
+    stream.wait_stream(cap)
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local_rank).start()
+    time.sleep(0.3)
+    for k in range(args.warmup):
+        graphs[k % wl.R].replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(args.steps):
+        graphs[k % wl.R].replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ms = t0.elapsed_time(t1)
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    if args.launch_list:
+        return {"ms": ms, "wl": wl, "launch_list": True}
+
+    # per call: policy split vs the unsplit control, cold L2, CUDA events
+    per_call = []
+    reps = 16
+    for i, (name, M, Kred, Nout) in enumerate(wl.calls):
+        s = wl.split[i]
+        us_s = timed_launches(lambda j: wl.call(i, j % wl.R, 0), reps, flush, stream)
+        us_1 = timed_launches(lambda j: wl.call(i, j % wl.R, 1), reps, flush, stream) \
+            if s > 1 else us_s
+        nb, fl = algorithmic(M, Kred, Nout, s)
+        nb1, _ = algorithmic(M, Kred, Nout, 1)
+        t_roof, bound = roofline_time_s(nb, fl, peaks)
+        t_roof1, _ = roofline_time_s(nb1, fl, peaks)
+        per_call.append({"proj": name, "M": M, "Kred": Kred, "Nout": Nout, "split": s,
+                         "us_split": round(us_s, 3), "us_unsplit": round(us_1, 3),
+                         "bytes": nb, "flops": fl, "bound": bound,
+                         "roof_frac_split": round(t_roof * 1e6 / us_s, 4),
+                         "roof_frac_unsplit": round(t_roof1 * 1e6 / us_1, 4),
+                         "tbps_split": round(nb / us_s / 1e6, 3),
+                         "tflops_split": round(fl / us_s / 1e6, 2)})
+    sample = clocks.stop()
+    dense = dense_sweep(Q, device, flush, stream, sms) if rank == 0 else None
+    e2e = run_e2e(wl, Q, device, stream, min(args.steps, 20))
+    return {"ms": ms, "per_call": per_call, "clocks": sample, "wl": wl, "peaks": peaks,
+            "peak_src": peak_src, "l2": l2, "sms": sms, "dense": dense, "e2e": e2e}
+
+
+def dense_sweep(Q, device, flush, stream, sms):
+    """Dense BF16 split-K GEMM 512 x 512 x 16384 (128 x 128 tiles) over the
+    split counts of the one-wave / two-wave model; cold L2, CUDA events."""
+    d = inputs.make_dense(512, 512, 16384, seed=0)
+    f = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(device)
+    A, W = f(d["A"]), f(d["W"])
+    C = torch.empty((512, 512), dtype=torch.bfloat16, device=device)
+    ws = torch.empty(Q.qmm_gemm_workspace_bytes(512, 512, 16), dtype=torch.uint8, device=device)
+    out = []
+    for s in (1, 2, 4, 6, 8, 9, 12, 16):
+        Q.qmm_gemm_bf16_splitk(A, W, C, s, ws)
+        us = timed_launches(lambda j: Q.qmm_gemm_bf16_splitk(A, W, C, s, ws), 8, flush, stream)
+        out.append({"split": s, "blocks": 16 * s, "waves": -(-16 * s // sms), "us": round(us, 3),
+                    "tflops": round(2 * 512 * 512 * 16384 / us / 1e6, 2)})
+    return out
+
+
+def run_e2e(wl, Q, device, stream, steps):
+    """The same step through the public API with host buffers: per step the
+    pinned-host inputs of all 14 calls are copied in, the calls run, and
+    every output is copied back; all of it inside the timed region."""
+    host_in, host_out, h2d, d2h = [], [], 0, 0
+    for p, (_, M, _, Nout) in zip(wl.host, wl.calls):
+        t = {"A": torch.from_numpy(p["A"].view(np.int16)).view(torch.bfloat16).pin_memory(),
+             "Wq": torch.from_numpy(p["Wq"].view(np.int32)).pin_memory(),
+             "scales": torch.from_numpy(p["scales"].view(np.int16)).view(torch.bfloat16).pin_memory(),
+             "biases": torch.from_numpy(p["biases"].view(np.int16)).view(torch.bfloat16).pin_memory()}
+        host_in.append(t)
+        host_out.append(torch.empty((M, Nout), dtype=torch.bfloat16).pin_memory())
+        h2d += sum(v.numel() * v.element_size() for v in t.values())
+        d2h += M * Nout * 2
+    dev = wl.sets[0]
+
+    def one_step():
+        for i in range(len(wl.calls)):
+            for k, v in host_in[i].items():
+                dev[i][k].copy_(v, non_blocking=True)
+            wl.call(i, 0)
+            host_out[i].copy_(wl.C[0][i], non_blocking=True)
+
+    one_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        one_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return {"value": round(ms * 1e3 / len(wl.calls), 3), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline and reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_steps(problems, min_seconds, max_steps=None, threads=None):
+    """Run the oracle over the whole step (all 14 calls) until min_seconds
+    have passed (at least one step); returns (seconds per step, steps)."""
+    import oracle
+    oracle.build()
+    n, t0 = 0, time.perf_counter()
+    while True:
+        for p in problems:
+            oracle.qmm(p["A"], p["Wq"], p["scales"], p["biases"], threads=threads)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds or (max_steps and n >= max_steps):
+            return el / n, n
+
+
+def cpu_baseline(problems):
+    import oracle
+    threads = oracle.default_threads()
+    sec, n = oracle_steps(problems, 10.0, threads=threads)
+    return {"value": round(sec * 1e6 / len(problems), 1), "unit": UNIT, "cores": threads,
+            "kind": "oracle",
+            "sample": "%d full step(s) of the workload (all 14 calls, fp64 C = A.W^T) on %d "
+                      "host threads" % (n, threads)}
+
+
+def run_reference(args, rank, world):
+    """The CPU oracle on the same workload.  Each step is a bounded sample:
+    one call of the 14 (in turn), all M rows and a subset of the output
+    columns sized so that warm-up and timed steps together take about 90 s;
+    the sample's time is scaled to the whole call by Nout / columns (the
+    oracle's cost is linear in the columns it computes)."""
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    problems = [inputs.make_w4a16(M, Kred, Nout, seed=0) for (_, M, Kred, Nout) in calls()]
+    threads = oracle.default_threads()
+    budget = max(0.02, 90.0 / (args.steps + args.warmup))
+    rng = np.random.default_rng(0)
+
+    def run(p, cols):
+        rows = np.arange(p["M"])
+        t0 = time.perf_counter()
+        oracle.qmm_sampled(p["A"], p["Wq"], p["scales"], p["biases"], rows, cols, threads=threads)
+        return time.perf_counter() - t0
+
+    cols_of = []
+    for p in problems:
+        probe = np.arange(min(64, p["Nout"]))
+        t = run(p, probe)
+        nc = int(min(p["Nout"], max(8, len(probe) * budget / max(t, 1e-6))))
+        cols_of.append(np.sort(rng.choice(p["Nout"], nc, replace=False)))
+    for k in range(args.warmup):
+        i = k % len(problems)
+        run(problems[i], cols_of[i])
+    est, wall = [], 0.0
+    for k in range(args.steps):
+        i = k % len(problems)
+        t = run(problems[i], cols_of[i])
+        wall += t
+        est.append(t * problems[i]["Nout"] / len(cols_of[i]))
+    value = round(statistics.mean(est) * 1e6, 1)
+    sample = "each step: one of the 14 calls in turn, all M rows x %d..%d of Nout columns, " \
+             "scaled to the full call by Nout/columns" % (min(len(c) for c in cols_of),
+                                                          max(len(c) for c in cols_of))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(wall * 1e3 / max(1, args.steps), 3), "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "calls_per_step": 1,
+                       "oracle": "plain C, fp64 accumulate, OpenMP"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--launch-list", action="store_true",
+                    help="only the timed graph steps (for a profiler's launch list)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    res = run_gpu(args, rank, world, local_rank)
+    wl = res["wl"]
+    ncalls = len(wl.calls)
+    value_us = res["ms"] * 1e3 / (world * args.steps * ncalls)
+    if res.get("launch_list"):
+        if rank == 0:
+            print(json.dumps({"launch_list": True, "value": value_us, "unit": UNIT,
+                              "steps": args.steps, "splits": wl.split,
+                              "gpu_launches": args.steps * wl.launches_per_step()}), flush=True)
+        return
+
+    dom = max(res["per_call"], key=lambda c: c["us_split"])
+    peaks = res["peaks"]
+    if dom["bound"] == "hbm":
+        achieved = dom["bytes"] / dom["us_split"] / 1e3  # GB/s
+        peak, unit = peaks["hbm_gbs"], "GB/s"
+    else:
+        achieved = dom["flops"] / dom["us_split"] / 1e6  # TFLOP/s
+        peak, unit = peaks["bf16_tflops"], "TFLOP/s"
+    bm, bn = 0, 0
+    from split_w4a16_quantized_gb300 import qmm as Q
+    bm, bn = Q.qmm_kernel_tile(dom["M"])
+    roof = {"bound": dom["bound"], "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+            "frac": round(achieved / peak, 4), "traffic": None,
+            "peak_source": res["peak_src"] + " (burst)",
+            "kernel": "w4a16_kernel BM=%d BN=%d%s" % (bm, bn, " + reduce" if dom["split"] > 1 else ""),
+            "call": "%s M=%d split=%d" % (dom["proj"], dom["M"], dom["split"]),
+            "per_launch": {"bytes": dom["bytes"], "flops": dom["flops"], "us": dom["us_split"]},
+            "timing": "CUDA events on the launching stream around each of 16 launches, "
+                      "L2 flushed (read of a >2xL2 buffer) before each"}
+    out = {"metric": METRIC, "value": round(value_us, 4), "unit": UNIT, "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(res["ms"] / args.steps, 6), "higher_is_better": False,
+           "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+           "config": {"workload": WORKLOAD, "calls_per_step": ncalls,
+                      "policy": "GB300 preset per M (target_blocks = 2 x SMs, cap 16)",
+                      "l2": "inputs larger than L2: %d rotating input sets x %.0f MB (L2 %d MB)"
+                            % (wl.R, wl.set_bytes / 2**20, res["l2"] >> 20),
+                      "graphs": "one CUDA graph per step, replayed", "parallelism":
+                      "replicas x%d" % world, "sms": res["sms"]},
+           "roofline": roof, "gpu_launches": args.steps * wl.launches_per_step(),
+           "clocks": res["clocks"], "e2e": res["e2e"], "per_call": res["per_call"],
+           "dense_splitk_512x512x16384": res["dense"]}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(wl.host)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,164 @@
+/*
+ * qmm.h — C ABI of libqmm: split-K W4A16-g128 projection matmul for GB300
+ * (sm_103a), plus the dense BF16 split-K GEMM the same split/reduce scheme
+ * is modelled on.
+ *
+ * Operation (tiny-llm book, "Week 2 Day 7: Split-K Prefill", Why Split the
+ * Reduction Dimension?):  C = A . W^T, with
+ *   A       BF16 [M, Kred] row-major activations,
+ *   W       [Nout, Kred] stored 4-bit affine-quantized in groups of 128 along
+ *           the reduction axis (the "w4a16_g128" format):
+ *             Wq      uint32 [Nout, Kred/8] row-major; word j of row n holds
+ *                     q[n, 8j+i] in bits 4i..4i+3 (low nibble first), q in 0..15
+ *             scales  BF16 [Nout, Kred/128] row-major
+ *             biases  BF16 [Nout, Kred/128] row-major
+ *             w[n, k] = scale[n, k/128] * q[n, k] + bias[n, k/128]
+ *   C       BF16 [M, Nout] row-major.
+ * The source chapter names the output width K and the reduction length N;
+ * this header uses Kred (reduction) and Nout (output width) throughout.
+ *
+ * Split-K (same chapter, Task 2 and Task 4): the reduction axis is cut into
+ * `split` partitions of equal length that start and end on 128-group
+ * boundaries; partition p writes its own partial plane [M, Nout] of the
+ * workspace (no atomics); a second kernel adds the planes in FP32, in
+ * ascending p, and rounds once to BF16.
+ *
+ * Conventions for every entry point:
+ *   - Device pointers are CUDA device memory owned by the caller; the
+ *     library never allocates, frees or keeps them.  Host pointers are
+ *     marked "host".
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Every launch is asynchronous and stream-ordered; no entry
+ *     point synchronizes.
+ *   - Arguments are checked on the host before any launch; a bad argument
+ *     returns an error code and launches nothing.  A launch failure returns
+ *     QMM_ECUDA.  Nothing aborts, traps or prints.
+ *   - C (and the workspace) must not alias any input.
+ *   - Alignment: A, Wq, C, workspace and partial planes 16-byte aligned;
+ *     scales and biases 2-byte aligned (QMM_EALIGN otherwise).
+ */
+#ifndef QMM_H
+#define QMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* return codes */
+enum {
+    QMM_OK = 0,
+    QMM_EINVAL = -1,     /* null pointer, non-positive size, unknown enum value */
+    QMM_ESHAPE = -2,     /* Kred not a multiple of 128, split not dividing Kred/128, size overflow */
+    QMM_EWORKSPACE = -3, /* workspace missing or smaller than qmm_splitk_workspace_bytes() */
+    QMM_ECUDA = -4,      /* a CUDA call or kernel launch failed */
+    QMM_EALIGN = -5,     /* a pointer breaks the alignment rules above */
+    QMM_ENODEV = -6      /* no CUDA device, or not compute capability 10.3 */
+};
+
+/* partial-plane element type (tiny-llm split-K chapter, Task 2: BF16 planes;
+ * an FP32 temporary is the bring-up mode that doubles the partial traffic) */
+enum { QMM_PARTIAL_BF16 = 0, QMM_PARTIAL_F32 = 1 };
+
+/* policy presets */
+enum { QMM_PRESET_PAGES = 0, QMM_PRESET_GB300 = 1 };
+
+/* Occupancy split policy (tiny-llm split-K chapter, Task 3):
+ *   base  = ceil(M/bm) * ceil(Nout/bn)
+ *   split = min(cap, floor(target_blocks/base), floor(Kred/min_k_per_split))
+ *   then split is lowered until Kred is divisible by split*128;
+ *   split <= 1 selects the unsplit kernel.
+ * min_k_per_split = 128 is the chapter's rule (its third bound is Kred/128);
+ * a larger value keeps at least that many reduction elements per split
+ * ("Optimize Prefill vs Decode Kernels", reasoning step 5).  It must be a
+ * positive multiple of 128.  bm, bn, cap >= 1; target_blocks >= 0. */
+typedef struct {
+    int bm;
+    int bn;
+    int target_blocks;
+    int cap;
+    int min_k_per_split;
+} qmm_policy;
+
+/* Fill *out with a policy preset.
+ *   QMM_PRESET_PAGES: the tiny-llm chapter's values (bm = bn = 32,
+ *     target_blocks = 320, cap = 16, min_k_per_split = 128); M and num_sms
+ *     are ignored.
+ *   QMM_PRESET_GB300: bm/bn = the tile of the kernel family this library
+ *     dispatches for M (qmm_kernel_tile), target_blocks = a multiple of
+ *     num_sms (the chapter calls its 320/16 tuning parameters, not GPU
+ *     properties), min_k_per_split = 512 for M <= 8 (decode) else 128.
+ *     num_sms <= 0 queries the current CUDA device.
+ * Returns QMM_OK, QMM_EINVAL (bad which/M/out) or QMM_ENODEV (query failed).
+ * Host only; launches nothing. */
+int qmm_policy_preset(int which, int M, int num_sms, qmm_policy *out);
+
+/* Tile (rows of A, rows of W per CTA) of the W4A16 kernel family dispatched
+ * for M.  Host only.  Returns QMM_OK or QMM_EINVAL. */
+int qmm_kernel_tile(int M, int *bm, int *bn);
+
+/* The occupancy split rule above for one matmul shape.  Pure host function,
+ * deterministic, no CUDA calls.  *split_out >= 1 (1 = unsplit).
+ * Returns QMM_OK, QMM_EINVAL (null, M/Nout < 1, bad policy fields) or
+ * QMM_ESHAPE (Kred not a positive multiple of 128). */
+int qmm_splitk_plan(int M, int Kred, int Nout, const qmm_policy *pol, int *split_out);
+
+/* Bytes of workspace the split path needs: split*M*Nout*(2 or 4), or 0 when
+ * split <= 1.  Returns 0 for invalid arguments as well. */
+size_t qmm_splitk_workspace_bytes(int M, int Nout, int split, int partial_dtype);
+
+/* C = A . W^T for the W4A16-g128 format (see the top of this header).
+ *   split_req  0: split from the policy; 1: the unsplit kernel (the
+ *              control, writes C directly); s > 1: forced split, must
+ *              divide Kred/128 (QMM_ESHAPE otherwise).
+ *   pol        policy used when split_req == 0; NULL = QMM_PRESET_GB300
+ *              for this M on the current device.
+ *   workspace  device buffer for the partial planes [split, M, Nout] of
+ *              partial_dtype; needed only when the split used is > 1, of
+ *              at least qmm_splitk_workspace_bytes(M, Nout, split, dtype)
+ *              bytes (ws_bytes).  Contents on return are unspecified.
+ *   split_used host, nullable: receives the split that was dispatched
+ *              (1 = unsplit).
+ * Launches one kernel (split 1) or the partition kernel followed by
+ * qmm_splitk_reduce's kernel, both on `stream`. */
+int qmm_w4a16_g128(const void *A, const uint32_t *Wq, const void *scales, const void *biases,
+                   void *C, int M, int Kred, int Nout, int split_req, const qmm_policy *pol,
+                   void *workspace, size_t ws_bytes, int partial_dtype, void *stream,
+                   int *split_used);
+
+/* C[m, n] = BF16(sum_{p=0}^{split-1} partials[p, m, n]), the sum taken in
+ * FP32 in ascending p and rounded once (tiny-llm split-K chapter, Task 4:
+ * one reduction thread per output element).  partials is [split, M, Nout]
+ * of partial_dtype, planes contiguous.  split >= 1. */
+int qmm_splitk_reduce(const void *partials, int partial_dtype, int split, int M, int Nout,
+                      void *C, void *stream);
+
+/* Dense BF16 split-K GEMM C = A . W^T, A [M, K] and W [N, K] BF16
+ * row-major, C BF16 [M, N] (gpu-kernels-explained, "Split-K, streams and
+ * overlap": output tiles of 128 x 128, k cut into `split` slices, partial
+ * sums written as FP32 planes and added by a second pass).  k is cut into
+ * K/64 tiles; when split does not divide that count the first (K/64 mod
+ * split) slices take one extra tile.  K must be a positive multiple of 64,
+ * 1 <= split <= K/64.  split = 1 writes C directly; split > 1 needs a
+ * workspace of qmm_gemm_workspace_bytes(M, N, split) bytes. */
+int qmm_gemm_bf16_splitk(const void *A, const void *W, void *C, int M, int N, int K, int split,
+                         void *workspace, size_t ws_bytes, void *stream);
+size_t qmm_gemm_workspace_bytes(int M, int N, int split);
+
+/* Test probes of the kernels' weight loader: q[n, k] (uint8 [Nout, Kred])
+ * and the dequantized BF16 w[n, k] ([Nout, Kred]) exactly as the matmul
+ * kernels form them in registers.  Device buffers, stream-ordered. */
+int qmm_unpack_probe(const uint32_t *Wq, int Nout, int Kred, uint8_t *q, void *stream);
+int qmm_dequant_probe(const uint32_t *Wq, const void *scales, const void *biases, int Nout,
+                      int Kred, void *w, void *stream);
+
+/* Static description of a return code. */
+const char *qmm_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QMM_H */

@@ -184,8 +184,9 @@ int oracle_qmm_sampled(const uint16_t *A, const uint32_t *Wq, const uint16_t *sc
     double *a = (double *)malloc(sizeof(double) * (size_t)(nr * Kred));
     if (!w || !a) { free(w); free(a); return -4; }
     int bad = 0;
-    for (int64_t j = 0; j < nc && !bad; ++j)
-        bad = dequant_row(Wq, scales, biases, Kred, cols[j], w + j * Kred);
+#pragma omp parallel for num_threads(nthreads) schedule(static) reduction(| : bad)
+    for (int64_t j = 0; j < nc; ++j)
+        bad |= dequant_row(Wq, scales, biases, Kred, cols[j], w + j * Kred) != 0;
     for (int64_t i = 0; i < nr; ++i)
         for (int64_t k = 0; k < Kred; ++k) a[i * Kred + k] = bf16_value(A[rows[i] * Kred + k]);
     if (!bad) {

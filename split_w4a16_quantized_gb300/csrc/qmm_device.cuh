@@ -1,0 +1,88 @@
+// Device helpers shared by the libqmm kernels (inline PTX for sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cstdint>
+
+namespace qmm {
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// 16-byte asynchronous global->shared copy; pred == false fills 16 zero bytes
+// (src-size 0) and reads nothing from src.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool pred) {
+    const int n = pred ? 16 : 0;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(n)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+// d = a * b + c on two BF16 lanes, one rounding to nearest even (fused).
+__device__ __forceinline__ uint32_t fma_bf16x2(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;\n" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// (x & 0x000F000F) | 0x43004300: the nibbles at bits 0..3 and 16..19 of x
+// become the BF16 pair (128 + lo, 128 + hi).  128 = 0x4300 has a unit last
+// mantissa place, so OR-ing a 4-bit integer into the mantissa adds it exactly.
+__device__ __forceinline__ uint32_t nibbles_to_bf16x2_biased(uint32_t x) {
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;\n" : "=r"(r) : "r"(x), "n"(0x000F000F), "n"(0x43004300));
+    return r;
+}
+
+constexpr uint32_t kBf16x2One = 0x3F803F80u;     // (1.0, 1.0)
+constexpr uint32_t kBf16x2Neg128 = 0xC300C300u;  // (-128, -128)
+
+// Dequantize one packed word (eight 4-bit q, low nibble first) with the
+// group's scale and bias, each replicated in both halves of ss / bb.
+// out[i] holds the BF16 pair (w(nibble i), w(nibble i + 4)), i = 0..3.
+// Each w is BF16(scale * q + bias) with a single rounding: q is formed
+// exactly as (128 + q) - 128, and the fused multiply-add rounds once.
+__device__ __forceinline__ void dequant_word(uint32_t word, uint32_t ss, uint32_t bb,
+                                             uint32_t out[4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t biased = nibbles_to_bf16x2_biased(word >> (4 * i));
+        const uint32_t q = fma_bf16x2(biased, kBf16x2One, kBf16x2Neg128);
+        out[i] = fma_bf16x2(q, ss, bb);
+    }
+}
+
+// scale and bias BF16 bit patterns replicated into both halves of a pair
+__device__ __forceinline__ uint32_t bf16_pair(uint16_t v) {
+    return static_cast<uint32_t>(v) * 0x00010001u;
+}
+
+// m16n8k16 BF16 MMA with FP32 accumulate: d += a (16x16, row) * b (16x8, col)
+__device__ __forceinline__ void mma_bf16_16816(float d[4], const uint32_t a[4], uint32_t b0,
+                                               uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t r[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+}  // namespace qmm

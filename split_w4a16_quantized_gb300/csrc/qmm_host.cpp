@@ -1,0 +1,217 @@
+// Host side of libqmm: argument checks, the occupancy split plan and the
+// dispatch of the W4A16 matmul, the reduce and the dense split-K GEMM.
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstdint>
+
+#include "../../include/qmm.h"
+#include "qmm_internal.h"
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+bool policy_ok(const qmm_policy* p) {
+    return p && p->bm >= 1 && p->bn >= 1 && p->cap >= 1 && p->target_blocks >= 0 &&
+           p->min_k_per_split >= qmm::kGroup && p->min_k_per_split % qmm::kGroup == 0;
+}
+
+int device_sms(int* sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return QMM_ENODEV;
+    if (cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return QMM_ENODEV;
+    return QMM_OK;
+}
+
+int check_device() {
+    int dev = 0, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return QMM_ENODEV;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return QMM_ENODEV;
+    return (major == 10 && minor == 3) ? QMM_OK : QMM_ENODEV;
+}
+
+// Launches go through cudaLaunchKernelEx, which reports its own error; the
+// caller's pending CUDA error state is left alone.
+int launched(int err) { return err == cudaSuccess ? QMM_OK : QMM_ECUDA; }
+
+size_t partial_elem_bytes(int dtype) { return dtype == QMM_PARTIAL_F32 ? 4 : 2; }
+
+}  // namespace
+
+extern "C" {
+
+const char* qmm_strerror(int code) {
+    switch (code) {
+        case QMM_OK: return "ok";
+        case QMM_EINVAL: return "invalid argument";
+        case QMM_ESHAPE: return "unsupported shape or split";
+        case QMM_EWORKSPACE: return "workspace missing or too small";
+        case QMM_ECUDA: return "CUDA launch or runtime error";
+        case QMM_EALIGN: return "misaligned pointer";
+        case QMM_ENODEV: return "no usable CUDA device (compute capability 10.3 required)";
+        default: return "unknown error";
+    }
+}
+
+int qmm_kernel_tile(int M, int* bm, int* bn) {
+    if (M < 1 || !bm || !bn) return QMM_EINVAL;
+    const qmm::Family& f = qmm::kFamilies[qmm::family_index(M)];
+    *bm = f.bm;
+    *bn = f.bn;
+    return QMM_OK;
+}
+
+int qmm_policy_preset(int which, int M, int num_sms, qmm_policy* out) {
+    if (!out) return QMM_EINVAL;
+    if (which == QMM_PRESET_PAGES) {
+        // tiny-llm split-K chapter, Task 3: 32x32 tiles, ~320 threadgroups, cap 16
+        *out = qmm_policy{32, 32, 320, 16, qmm::kGroup};
+        return QMM_OK;
+    }
+    if (which != QMM_PRESET_GB300 || M < 1) return QMM_EINVAL;
+    if (num_sms <= 0) {
+        int rc = device_sms(&num_sms);
+        if (rc != QMM_OK) return rc;
+    }
+    int bm = 0, bn = 0;
+    qmm_kernel_tile(M, &bm, &bn);
+    *out = qmm_policy{bm, bn, qmm::kTargetPerSm * num_sms, qmm::kCap,
+                      M <= qmm::kDecodeMaxM ? qmm::kDecodeMinK : qmm::kGroup};
+    return QMM_OK;
+}
+
+// The split is the largest divisor of G = Kred/128 that stays within the
+// three bounds (cap, target/base, Kred/min_k).  Stepping a candidate down by
+// one until it divides G, as the chapter words it, ends on that divisor.
+int qmm_splitk_plan(int M, int Kred, int Nout, const qmm_policy* pol, int* split_out) {
+    if (!split_out || !policy_ok(pol) || M < 1 || Nout < 1) return QMM_EINVAL;
+    if (Kred < qmm::kGroup || Kred % qmm::kGroup) return QMM_ESHAPE;
+    const int64_t G = Kred / qmm::kGroup;
+    const int64_t base = ceil_div(M, pol->bm) * ceil_div(Nout, pol->bn);
+    int64_t bound = pol->cap;
+    if (pol->target_blocks / base < bound) bound = pol->target_blocks / base;
+    if (Kred / pol->min_k_per_split < bound) bound = Kred / pol->min_k_per_split;
+    int best = 1;
+    for (int64_t d = 2; d <= bound && d <= G; ++d)
+        if (G % d == 0) best = static_cast<int>(d);
+    *split_out = best;
+    return QMM_OK;
+}
+
+size_t qmm_splitk_workspace_bytes(int M, int Nout, int split, int partial_dtype) {
+    if (M < 1 || Nout < 1 || split < 1) return 0;
+    if (partial_dtype != QMM_PARTIAL_BF16 && partial_dtype != QMM_PARTIAL_F32) return 0;
+    if (split == 1) return 0;
+    return static_cast<size_t>(split) * static_cast<size_t>(M) * static_cast<size_t>(Nout) *
+           partial_elem_bytes(partial_dtype);
+}
+
+size_t qmm_gemm_workspace_bytes(int M, int N, int split) {
+    if (M < 1 || N < 1 || split <= 1) return 0;
+    return static_cast<size_t>(split) * static_cast<size_t>(M) * static_cast<size_t>(N) * 4;
+}
+
+int qmm_splitk_reduce(const void* partials, int partial_dtype, int split, int M, int Nout,
+                      void* C, void* stream) {
+    if (!partials || !C || split < 1 || M < 1 || Nout < 1) return QMM_EINVAL;
+    if (partial_dtype != QMM_PARTIAL_BF16 && partial_dtype != QMM_PARTIAL_F32) return QMM_EINVAL;
+    if (!aligned(partials, 16) || !aligned(C, 16)) return QMM_EALIGN;
+    int rc = check_device();
+    if (rc != QMM_OK) return rc;
+    return launched(qmm::launch_reduce(partials, partial_dtype, split, M, Nout, C, stream));
+}
+
+int qmm_w4a16_g128(const void* A, const uint32_t* Wq, const void* scales, const void* biases,
+                   void* C, int M, int Kred, int Nout, int split_req, const qmm_policy* pol,
+                   void* workspace, size_t ws_bytes, int partial_dtype, void* stream,
+                   int* split_used) {
+    if (!A || !Wq || !scales || !biases || !C || M < 1 || Nout < 1 || split_req < 0)
+        return QMM_EINVAL;
+    if (partial_dtype != QMM_PARTIAL_BF16 && partial_dtype != QMM_PARTIAL_F32) return QMM_EINVAL;
+    if (pol && !policy_ok(pol)) return QMM_EINVAL;
+    if (Kred < qmm::kGroup || Kred % qmm::kGroup) return QMM_ESHAPE;
+    if (!aligned(A, 16) || !aligned(Wq, 16) || !aligned(C, 16) || !aligned(scales, 2) ||
+        !aligned(biases, 2))
+        return QMM_EALIGN;
+    const int fam = qmm::family_index(M);
+    if (ceil_div(M, qmm::kFamilies[fam].bm) > 65535) return QMM_ESHAPE;
+    int rc = check_device();
+    if (rc != QMM_OK) return rc;
+
+    const int G = Kred / qmm::kGroup;
+    int split = split_req;
+    if (split_req == 0) {
+        qmm_policy local;
+        if (!pol) {
+            rc = qmm_policy_preset(QMM_PRESET_GB300, M, 0, &local);
+            if (rc != QMM_OK) return rc;
+            pol = &local;
+        }
+        rc = qmm_splitk_plan(M, Kred, Nout, pol, &split);
+        if (rc != QMM_OK) return rc;
+    } else if (split > G || G % split != 0 || split > 65535) {
+        return QMM_ESHAPE;
+    }
+
+    if (split == 1) {
+        rc = launched(qmm::launch_w4a16(fam, A, Wq, scales, biases, C, qmm::kOutBf16, M, Kred,
+                                        Nout, 1, stream));
+    } else {
+        const size_t need = qmm_splitk_workspace_bytes(M, Nout, split, partial_dtype);
+        if (!workspace || ws_bytes < need) return QMM_EWORKSPACE;
+        if (!aligned(workspace, 16)) return QMM_EALIGN;
+        const int mode = partial_dtype == QMM_PARTIAL_F32 ? qmm::kOutF32 : qmm::kOutBf16;
+        rc = launched(qmm::launch_w4a16(fam, A, Wq, scales, biases, workspace, mode, M, Kred,
+                                        Nout, split, stream));
+        if (rc == QMM_OK)
+            rc = launched(qmm::launch_reduce(workspace, partial_dtype, split, M, Nout, C, stream));
+    }
+    if (rc == QMM_OK && split_used) *split_used = split;
+    return rc;
+}
+
+int qmm_gemm_bf16_splitk(const void* A, const void* W, void* C, int M, int N, int K, int split,
+                         void* workspace, size_t ws_bytes, void* stream) {
+    if (!A || !W || !C || M < 1 || N < 1 || K < 1 || split < 1) return QMM_EINVAL;
+    if (K % 64 || split > K / 64 || split > 65535) return QMM_ESHAPE;
+    if (ceil_div(M, 128) > 65535) return QMM_ESHAPE;
+    if (!aligned(A, 16) || !aligned(W, 16) || !aligned(C, 16)) return QMM_EALIGN;
+    int rc = check_device();
+    if (rc != QMM_OK) return rc;
+    if (split == 1)
+        return launched(qmm::launch_gemm(A, W, C, qmm::kOutBf16, M, N, K, 1, stream));
+    if (!workspace || ws_bytes < qmm_gemm_workspace_bytes(M, N, split)) return QMM_EWORKSPACE;
+    if (!aligned(workspace, 16)) return QMM_EALIGN;
+    rc = launched(qmm::launch_gemm(A, W, workspace, qmm::kOutF32, M, N, K, split, stream));
+    if (rc == QMM_OK)
+        rc = launched(qmm::launch_reduce(workspace, QMM_PARTIAL_F32, split, M, N, C, stream));
+    return rc;
+}
+
+int qmm_unpack_probe(const uint32_t* Wq, int Nout, int Kred, uint8_t* q, void* stream) {
+    if (!Wq || !q || Nout < 1) return QMM_EINVAL;
+    if (Kred < qmm::kGroup || Kred % qmm::kGroup) return QMM_ESHAPE;
+    if (!aligned(Wq, 16) || !aligned(q, 16)) return QMM_EALIGN;
+    int rc = check_device();
+    if (rc != QMM_OK) return rc;
+    return launched(qmm::launch_unpack_probe(Wq, Nout, Kred, q, stream));
+}
+
+int qmm_dequant_probe(const uint32_t* Wq, const void* scales, const void* biases, int Nout,
+                      int Kred, void* w, void* stream) {
+    if (!Wq || !scales || !biases || !w || Nout < 1) return QMM_EINVAL;
+    if (Kred < qmm::kGroup || Kred % qmm::kGroup) return QMM_ESHAPE;
+    if (!aligned(Wq, 16) || !aligned(w, 16) || !aligned(scales, 2) || !aligned(biases, 2))
+        return QMM_EALIGN;
+    int rc = check_device();
+    if (rc != QMM_OK) return rc;
+    return launched(qmm::launch_dequant_probe(Wq, scales, biases, Nout, Kred, w, stream));
+}
+
+}  // extern "C"

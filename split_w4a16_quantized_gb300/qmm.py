@@ -1,0 +1,252 @@
+"""Python binding of libqmm (ctypes): argument marshalling only.
+
+Every function here has the name of the C entry point it calls (include/qmm.h)
+and hands device pointers, sizes and the current CUDA stream to it; all
+arithmetic runs in the library's CUDA kernels.  torch is used for device
+memory and streams only.  If libqmm.so has not been built the first call
+raises -- there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libqmm.so")
+
+QMM_OK, QMM_EINVAL, QMM_ESHAPE, QMM_EWORKSPACE, QMM_ECUDA, QMM_EALIGN, QMM_ENODEV = \
+    0, -1, -2, -3, -4, -5, -6
+QMM_PARTIAL_BF16, QMM_PARTIAL_F32 = 0, 1
+QMM_PRESET_PAGES, QMM_PRESET_GB300 = 0, 1
+
+
+class qmm_policy(ctypes.Structure):
+    _fields_ = [("bm", ctypes.c_int), ("bn", ctypes.c_int), ("target_blocks", ctypes.c_int),
+                ("cap", ctypes.c_int), ("min_k_per_split", ctypes.c_int)]
+
+    def as_tuple(self):
+        return (self.bm, self.bn, self.target_blocks, self.cap, self.min_k_per_split)
+
+    def __repr__(self):
+        return "qmm_policy(bm=%d, bn=%d, target_blocks=%d, cap=%d, min_k_per_split=%d)" % \
+            self.as_tuple()
+
+
+class QmmError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__("%s: %s (%d)" % (what, qmm_strerror(code), code))
+
+
+_lock = threading.Lock()
+_lib = None
+
+_P, _I, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+_SIGS = {
+    "qmm_policy_preset": (_I, [_I, _I, _I, ctypes.POINTER(qmm_policy)]),
+    "qmm_kernel_tile": (_I, [_I, ctypes.POINTER(_I), ctypes.POINTER(_I)]),
+    "qmm_splitk_plan": (_I, [_I, _I, _I, ctypes.POINTER(qmm_policy), ctypes.POINTER(_I)]),
+    "qmm_splitk_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
+    "qmm_w4a16_g128": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, ctypes.POINTER(qmm_policy),
+                            _P, _SZ, _I, _P, ctypes.POINTER(_I)]),
+    "qmm_splitk_reduce": (_I, [_P, _I, _I, _I, _I, _P, _P]),
+    "qmm_gemm_bf16_splitk": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _SZ, _P]),
+    "qmm_gemm_workspace_bytes": (_SZ, [_I, _I, _I]),
+    "qmm_unpack_probe": (_I, [_P, _I, _I, _P, _P]),
+    "qmm_dequant_probe": (_I, [_P, _P, _P, _I, _I, _P, _P]),
+    "qmm_strerror": (ctypes.c_char_p, [_I]),
+}
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libqmm.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError("libqmm.so is not built; run "
+                                   "`python -m split_w4a16_quantized_gb300.build`")
+            h = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in _SIGS.items():
+                fn = getattr(h, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = h
+        return _lib
+
+
+def _check(rc: int, what: str):
+    if rc != QMM_OK:
+        raise QmmError(rc, what)
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        stream = stream.cuda_stream
+    return ctypes.c_void_p(int(stream))
+
+
+def _dev(t: torch.Tensor, dtypes, name: str) -> ctypes.c_void_p:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError("%s must be a CUDA tensor" % name)
+    if t.dtype not in dtypes:
+        raise TypeError("%s has dtype %s, expected one of %s" % (name, t.dtype, dtypes))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return ctypes.c_void_p(t.data_ptr())
+
+
+_BF16 = (torch.bfloat16,)
+_WORDS = (torch.int32, torch.uint32) if hasattr(torch, "uint32") else (torch.int32,)
+
+
+# ---- host-only entry points ---------------------------------------------
+
+def qmm_strerror(code: int) -> str:
+    return lib().qmm_strerror(code).decode()
+
+
+def qmm_policy_preset(which: int, M: int = 1, num_sms: int = 0) -> qmm_policy:
+    out = qmm_policy()
+    _check(lib().qmm_policy_preset(which, M, num_sms, ctypes.byref(out)), "qmm_policy_preset")
+    return out
+
+
+def qmm_kernel_tile(M: int):
+    bm, bn = _I(0), _I(0)
+    _check(lib().qmm_kernel_tile(M, ctypes.byref(bm), ctypes.byref(bn)), "qmm_kernel_tile")
+    return bm.value, bn.value
+
+
+def qmm_splitk_plan(M: int, Kred: int, Nout: int, pol: qmm_policy) -> int:
+    s = _I(0)
+    _check(lib().qmm_splitk_plan(M, Kred, Nout, ctypes.byref(pol), ctypes.byref(s)),
+           "qmm_splitk_plan")
+    return s.value
+
+
+def qmm_splitk_workspace_bytes(M: int, Nout: int, split: int,
+                               partial_dtype: int = QMM_PARTIAL_BF16) -> int:
+    return int(lib().qmm_splitk_workspace_bytes(M, Nout, split, partial_dtype))
+
+
+def qmm_gemm_workspace_bytes(M: int, N: int, split: int) -> int:
+    return int(lib().qmm_gemm_workspace_bytes(M, N, split))
+
+
+# ---- device entry points -------------------------------------------------
+
+def qmm_w4a16_g128(A: torch.Tensor, Wq: torch.Tensor, scales: torch.Tensor,
+                   biases: torch.Tensor, C: torch.Tensor, split_req: int = 0,
+                   pol: qmm_policy | None = None, workspace: torch.Tensor | None = None,
+                   partial_dtype: int = QMM_PARTIAL_BF16, stream=None) -> int:
+    """C = A @ W^T (W in the W4A16-g128 format); returns the split dispatched.
+    Shapes: A [M, Kred] bf16, Wq [Nout, Kred/8] int32, scales/biases
+    [Nout, Kred/128] bf16, C [M, Nout] bf16; workspace any contiguous CUDA
+    tensor of at least qmm_splitk_workspace_bytes(...) bytes."""
+    M, Kred = A.shape
+    Nout = Wq.shape[0]
+    if tuple(Wq.shape) != (Nout, Kred // 8) or tuple(C.shape) != (M, Nout) or \
+            tuple(scales.shape) != (Nout, Kred // 128) or tuple(biases.shape) != (Nout, Kred // 128):
+        raise ValueError("qmm_w4a16_g128: inconsistent shapes")
+    ws, ws_bytes = None, 0
+    if workspace is not None:
+        if not workspace.is_cuda or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous CUDA tensor")
+        ws, ws_bytes = ctypes.c_void_p(workspace.data_ptr()), \
+            workspace.numel() * workspace.element_size()
+    used = _I(0)
+    rc = lib().qmm_w4a16_g128(
+        _dev(A, _BF16, "A"), _dev(Wq, _WORDS, "Wq"), _dev(scales, _BF16, "scales"),
+        _dev(biases, _BF16, "biases"), _dev(C, _BF16, "C"), M, Kred, Nout, split_req,
+        ctypes.byref(pol) if pol is not None else None, ws, ws_bytes, partial_dtype,
+        _stream(stream), ctypes.byref(used))
+    _check(rc, "qmm_w4a16_g128")
+    return used.value
+
+
+def qmm_splitk_reduce(partials: torch.Tensor, partial_dtype: int, split: int, M: int, Nout: int,
+                      C: torch.Tensor, stream=None) -> None:
+    want = (torch.float32,) if partial_dtype == QMM_PARTIAL_F32 else _BF16
+    if partials.numel() < split * M * Nout or C.numel() < M * Nout:
+        raise ValueError("qmm_splitk_reduce: buffers too small")
+    _check(lib().qmm_splitk_reduce(_dev(partials, want, "partials"), partial_dtype, split, M, Nout,
+                                   _dev(C, _BF16, "C"), _stream(stream)), "qmm_splitk_reduce")
+
+
+def qmm_gemm_bf16_splitk(A: torch.Tensor, W: torch.Tensor, C: torch.Tensor, split: int,
+                         workspace: torch.Tensor | None = None, stream=None) -> None:
+    M, K = A.shape
+    N = W.shape[0]
+    if W.shape[1] != K or tuple(C.shape) != (M, N):
+        raise ValueError("qmm_gemm_bf16_splitk: inconsistent shapes")
+    ws, ws_bytes = None, 0
+    if workspace is not None:
+        ws, ws_bytes = ctypes.c_void_p(workspace.data_ptr()), \
+            workspace.numel() * workspace.element_size()
+    _check(lib().qmm_gemm_bf16_splitk(_dev(A, _BF16, "A"), _dev(W, _BF16, "W"),
+                                      _dev(C, _BF16, "C"), M, N, K, split, ws, ws_bytes,
+                                      _stream(stream)), "qmm_gemm_bf16_splitk")
+
+
+def qmm_unpack_probe(Wq: torch.Tensor, Kred: int, q: torch.Tensor, stream=None) -> None:
+    Nout = Wq.shape[0]
+    if q.numel() < Nout * Kred:
+        raise ValueError("qmm_unpack_probe: q too small")
+    _check(lib().qmm_unpack_probe(_dev(Wq, _WORDS, "Wq"), Nout, Kred,
+                                  _dev(q, (torch.uint8,), "q"), _stream(stream)),
+           "qmm_unpack_probe")
+
+
+def qmm_dequant_probe(Wq: torch.Tensor, scales: torch.Tensor, biases: torch.Tensor, Kred: int,
+                      w: torch.Tensor, stream=None) -> None:
+    Nout = Wq.shape[0]
+    if w.numel() < Nout * Kred:
+        raise ValueError("qmm_dequant_probe: w too small")
+    _check(lib().qmm_dequant_probe(_dev(Wq, _WORDS, "Wq"), _dev(scales, _BF16, "scales"),
+                                   _dev(biases, _BF16, "biases"), Nout, Kred,
+                                   _dev(w, _BF16, "w"), _stream(stream)), "qmm_dequant_probe")
+
+
+# ---- convenience ---------------------------------------------------------
+
+def w4a16_matmul(A, Wq, scales, biases, split_req: int = 0, pol=None,
+                 partial_dtype: int = QMM_PARTIAL_BF16, stream=None):
+    """Allocate C (and the workspace the plan needs) with torch and call
+    qmm_w4a16_g128.  Returns (C, split_used)."""
+    M, Kred = A.shape
+    Nout = Wq.shape[0]
+    if split_req == 0:
+        if pol is None:
+            pol = qmm_policy_preset(QMM_PRESET_GB300, M)
+        split = qmm_splitk_plan(M, Kred, Nout, pol)
+    else:
+        split = split_req
+    C = torch.empty((M, Nout), dtype=torch.bfloat16, device=A.device)
+    nbytes = qmm_splitk_workspace_bytes(M, Nout, split, partial_dtype)
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=A.device) if nbytes else None
+    used = qmm_w4a16_g128(A, Wq, scales, biases, C, split_req=split_req, pol=pol, workspace=ws,
+                          partial_dtype=partial_dtype, stream=stream)
+    return C, used
+
+
+def to_device(problem: dict, device="cuda") -> dict:
+    """Move a problem from split_w4a16_quantized_gb300.inputs to the GPU as the
+    tensors qmm_w4a16_g128 takes."""
+    import numpy as np
+
+    def bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16) \
+            .to(device)
+
+    return {
+        "A": bf16(problem["A"]),
+        "Wq": torch.from_numpy(np.ascontiguousarray(problem["Wq"]).view(np.int32)).to(device),
+        "scales": bf16(problem["scales"]),
+        "biases": bf16(problem["biases"]),
+    }

@@ -1,0 +1,125 @@
+"""Host-side checks of the C-ABI library (CPU only): it builds, loads and
+exports every entry point include/qmm.h declares; the split plan is
+bit-exact against the oracle's; argument errors come back as codes before any
+CUDA work."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from split_w4a16_quantized_gb300 import build, inputs
+from split_w4a16_quantized_gb300 import qmm as Q
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+M_LIST = [1, 2, 4, 8, 9, 16, 17, 32, 33, 64, 100, 128, 129, 256, 2048, 4096]
+SHAPES = list(inputs.PROJECTIONS.values()) + [inputs.RAGGED]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    build.build()
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "qmm.h")).read()
+    return sorted(set(re.findall(r"^[A-Za-z_][\w \*]*?\b(qmm_\w+)\s*\(", text, re.M)))
+
+
+def test_exports_every_declared_symbol():
+    names = _declared()
+    assert "qmm_w4a16_g128" in names and "qmm_splitk_plan" in names and "qmm_splitk_reduce" in names
+    lib = ctypes.CDLL(Q.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(Q._SIGS), "binding and header disagree"
+
+
+def test_strerror_codes():
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        assert Q.qmm_strerror(code) != "unknown error"
+    assert Q.qmm_strerror(7) == "unknown error"
+
+
+def test_pages_preset_values():
+    p = Q.qmm_policy_preset(Q.QMM_PRESET_PAGES)
+    assert p.as_tuple() == (32, 32, 320, 16, 128)
+
+
+@pytest.mark.parametrize("sms", [148, 152])
+def test_gb300_preset(sms):
+    for M in M_LIST:
+        p = Q.qmm_policy_preset(Q.QMM_PRESET_GB300, M, sms)
+        assert (p.bm, p.bn) == Q.qmm_kernel_tile(M)
+        assert p.target_blocks % sms == 0 and p.target_blocks >= sms
+        assert p.min_k_per_split == (512 if M <= 8 else 128)
+
+
+def _policies():
+    out = [Q.qmm_policy_preset(Q.QMM_PRESET_PAGES)]
+    for sms in (108, 132, 148, 152):
+        out += [Q.qmm_policy_preset(Q.QMM_PRESET_GB300, M, sms) for M in (1, 16, 32, 128)]
+    return out
+
+
+def test_plan_bit_exact_against_oracle_on_workload_shapes():
+    for pol in _policies():
+        for M in M_LIST:
+            for Kred, Nout in SHAPES:
+                got = Q.qmm_splitk_plan(M, Kred, Nout, pol)
+                assert got == oracle.splitk_plan(M, Kred, Nout, *pol.as_tuple()), (pol, M, Kred, Nout)
+
+
+def test_plan_bit_exact_against_oracle_fuzz():
+    rng = np.random.default_rng(21)
+    for _ in range(20000):
+        M = int(rng.integers(1, 5000))
+        Kred = 128 * int(rng.integers(1, 129))
+        Nout = int(rng.integers(1, 20000))
+        pol = Q.qmm_policy(int(rng.integers(1, 257)), int(rng.integers(1, 257)),
+                           int(rng.integers(0, 5000)), int(rng.integers(1, 65)),
+                           128 * int(rng.integers(1, 17)))
+        assert Q.qmm_splitk_plan(M, Kred, Nout, pol) == \
+            oracle.splitk_plan(M, Kred, Nout, *pol.as_tuple())
+
+
+def test_plan_errors():
+    pol = Q.qmm_policy_preset(Q.QMM_PRESET_PAGES)
+    s = ctypes.c_int(0)
+    lib = Q.lib()
+    assert lib.qmm_splitk_plan(16, 2500, 1024, ctypes.byref(pol), ctypes.byref(s)) == Q.QMM_ESHAPE
+    assert lib.qmm_splitk_plan(0, 2560, 1024, ctypes.byref(pol), ctypes.byref(s)) == Q.QMM_EINVAL
+    assert lib.qmm_splitk_plan(16, 2560, 1024, None, ctypes.byref(s)) == Q.QMM_EINVAL
+    bad = Q.qmm_policy(32, 32, 320, 16, 100)
+    assert lib.qmm_splitk_plan(16, 2560, 1024, ctypes.byref(bad), ctypes.byref(s)) == Q.QMM_EINVAL
+
+
+def test_workspace_bytes():
+    assert Q.qmm_splitk_workspace_bytes(16, 1024, 1) == 0
+    assert Q.qmm_splitk_workspace_bytes(16, 1024, 10) == 10 * 16 * 1024 * 2
+    assert Q.qmm_splitk_workspace_bytes(16, 1024, 10, Q.QMM_PARTIAL_F32) == 10 * 16 * 1024 * 4
+    assert Q.qmm_splitk_workspace_bytes(16, 1024, 10, 7) == 0
+    assert Q.qmm_gemm_workspace_bytes(512, 512, 6) == 6 * 512 * 512 * 4
+    assert Q.qmm_gemm_workspace_bytes(512, 512, 1) == 0
+
+
+def test_argument_errors_before_any_cuda_work():
+    # fake, never-dereferenced addresses: every call must fail validation first
+    lib = Q.lib()
+    P = ctypes.c_void_p
+    a, w, s, b, c = P(0x10000), P(0x20000), P(0x30000), P(0x40000), P(0x50000)
+    call = lambda *x: lib.qmm_w4a16_g128(*x)
+    assert call(None, w, s, b, c, 16, 2560, 1024, 0, None, None, 0, 0, None, None) == Q.QMM_EINVAL
+    assert call(a, w, s, b, c, 0, 2560, 1024, 0, None, None, 0, 0, None, None) == Q.QMM_EINVAL
+    assert call(a, w, s, b, c, 16, 2500, 1024, 0, None, None, 0, 0, None, None) == Q.QMM_ESHAPE
+    assert call(a, w, s, b, c, 16, 2560, 1024, 0, None, None, 0, 5, None, None) == Q.QMM_EINVAL
+    assert call(P(0x10002), w, s, b, c, 16, 2560, 1024, 0, None, None, 0, 0, None, None) == \
+        Q.QMM_EALIGN
+    assert call(a, w, P(0x30001), b, c, 16, 2560, 1024, 0, None, None, 0, 0, None, None) == \
+        Q.QMM_EALIGN
+    assert lib.qmm_splitk_reduce(None, 0, 2, 16, 16, c, None) == Q.QMM_EINVAL
+    assert lib.qmm_splitk_reduce(a, 0, 2, 16, 16, P(0x50008), None) == Q.QMM_EALIGN
+    assert lib.qmm_gemm_bf16_splitk(a, w, c, 512, 512, 1000, 2, None, 0, None) == Q.QMM_ESHAPE
+    assert lib.qmm_gemm_bf16_splitk(a, w, c, 512, 512, 1024, 17, None, 0, None) == Q.QMM_ESHAPE

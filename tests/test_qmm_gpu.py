@@ -1,0 +1,297 @@
+"""GPU parity tests: the CUDA path through the C ABI against the CPU oracle.
+
+Tolerances (per element, against the oracle's fp64 C64):
+  |C_gpu - C64| <= 0.02  * max(1, |C64|)  with BF16 partial planes,
+  |C_gpu - C64| <= 0.008 * max(1, |C64|)  with FP32 partial planes or split 1.
+Unpacking, dequantized weights, split plans and the reduce are bit-exact.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from split_w4a16_quantized_gb300 import build, inputs
+from split_w4a16_quantized_gb300 import qmm as Q
+
+pytestmark = pytest.mark.gpu
+
+TOL_BF16, TOL_F32 = 0.02, 0.008
+NAN_BF16 = 0x7FC0
+CANARY = 64
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+
+
+def _bits(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def _val(bits: np.ndarray) -> np.ndarray:
+    return inputs.bf16_bits_to_f32(bits).astype(np.float64)
+
+
+def _tol(split: int, partial_dtype: int) -> float:
+    return TOL_BF16 if split > 1 and partial_dtype == Q.QMM_PARTIAL_BF16 else TOL_F32
+
+
+def _assert_close(got_bits, ref64, tol, what=""):
+    got = _val(got_bits)
+    assert np.all(np.isfinite(got)), "non-finite output " + what
+    err = np.abs(got - ref64)
+    lim = tol * np.maximum(1.0, np.abs(ref64))
+    bad = np.argwhere(err > lim)
+    assert bad.size == 0, "%s: %d elements out of tolerance, first %s err %g lim %g" % (
+        what, len(bad), bad[0], err[tuple(bad[0])], lim[tuple(bad[0])])
+
+
+def _run(d, M, Nout, split_req=0, pol=None, partial_dtype=Q.QMM_PARTIAL_BF16):
+    """Call qmm_w4a16_g128 into a NaN-filled C with a canary tail; returns (C bits, split)."""
+    Kred = d["A"].shape[1]
+    if split_req == 0:
+        p = pol or Q.qmm_policy_preset(Q.QMM_PRESET_GB300, M)
+        split = Q.qmm_splitk_plan(M, Kred, Nout, p)
+    else:
+        split = split_req
+    nbytes = Q.qmm_splitk_workspace_bytes(M, Nout, split, partial_dtype)
+    ws = torch.full((max(nbytes, 16) // 2,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    buf = torch.full((M * Nout + CANARY,), 0, dtype=torch.int16, device="cuda")
+    buf.fill_(NAN_BF16)
+    C = buf[:M * Nout].view(torch.bfloat16).view(M, Nout)
+    used = Q.qmm_w4a16_g128(d["A"], d["Wq"], d["scales"], d["biases"], C, split_req=split_req,
+                            pol=pol, workspace=ws if nbytes else None, partial_dtype=partial_dtype)
+    torch.cuda.synchronize()
+    assert np.all(buf[M * Nout:].cpu().numpy() == np.int16(NAN_BF16)), "canary overwritten"
+    assert used == split
+    return _bits(C), used
+
+
+# ---- probes: bit-exact -----------------------------------------------------
+
+@pytest.mark.parametrize("Nout,Kred", [(1000, 2560), (37, 256), (16, 128)])
+def test_unpack_probe_bit_exact(Nout, Kred):
+    p = inputs.make_w4a16(1, Kred, Nout, seed=31)
+    d = Q.to_device(p)
+    q = torch.empty((Nout, Kred), dtype=torch.uint8, device="cuda")
+    Q.qmm_unpack_probe(d["Wq"], Kred, q)
+    torch.cuda.synchronize()
+    assert np.array_equal(q.cpu().numpy(), oracle.unpack(p["Wq"], Kred))
+
+
+@pytest.mark.parametrize("Nout,Kred", [(1000, 2560), (37, 256)])
+def test_dequant_probe_bit_exact(Nout, Kred):
+    p = inputs.make_w4a16(1, Kred, Nout, seed=32)
+    d = Q.to_device(p)
+    w = torch.empty((Nout, Kred), dtype=torch.bfloat16, device="cuda")
+    Q.qmm_dequant_probe(d["Wq"], d["scales"], d["biases"], Kred, w)
+    torch.cuda.synchronize()
+    assert np.array_equal(_bits(w), oracle.dequant(p["Wq"], p["scales"], p["biases"], Kred))
+
+
+# ---- the K-projection at M = 16 (policy vs unsplit) ------------------------
+
+@pytest.mark.parametrize("partial_dtype", [Q.QMM_PARTIAL_BF16, Q.QMM_PARTIAL_F32])
+def test_k_projection_m16_policy_and_unsplit(partial_dtype):
+    Kred, Nout = inputs.PROJECTIONS["k"]
+    p = inputs.make_w4a16(16, Kred, Nout, seed=0)
+    d = Q.to_device(p)
+    C64 = oracle.qmm(p["A"], p["Wq"], p["scales"], p["biases"])
+    got, s = _run(d, 16, Nout, 0, partial_dtype=partial_dtype)
+    assert s > 1, "an under-filled grid must split"
+    _assert_close(got, C64, _tol(s, partial_dtype), "policy")
+    got1, s1 = _run(d, 16, Nout, 1)
+    assert s1 == 1
+    _assert_close(got1, C64, TOL_F32, "unsplit")
+
+
+@pytest.mark.parametrize("name,splits", [("k", [2, 4, 5, 10, 20]), ("o", [2, 4, 8, 16, 32]),
+                                         ("down", [2, 4, 19, 38, 76])])
+def test_forced_splits(name, splits):
+    Kred, Nout = inputs.PROJECTIONS[name]
+    p = inputs.make_w4a16(16, Kred, Nout, seed=1)
+    d = Q.to_device(p)
+    C64 = oracle.qmm(p["A"], p["Wq"], p["scales"], p["biases"])
+    for s in splits:
+        for dt in (Q.QMM_PARTIAL_BF16, Q.QMM_PARTIAL_F32):
+            got, used = _run(d, 16, Nout, s, partial_dtype=dt)
+            _assert_close(got, C64, _tol(s, dt), "%s s=%d dt=%d" % (name, s, dt))
+
+
+# ---- every kernel family, ragged tiles -------------------------------------
+
+@pytest.mark.parametrize("M", [1, 3, 8, 9, 16, 17, 31, 32, 33, 64, 65, 100, 128])
+def test_families_ragged(M):
+    Kred, Nout = 1280, 1000  # Nout = 1000: partial last column tile
+    p = inputs.make_w4a16(M, Kred, Nout, seed=100 + M)
+    d = Q.to_device(p)
+    C64 = oracle.qmm(p["A"], p["Wq"], p["scales"], p["biases"])
+    for split_req in (0, 1, 2, 5, 10):
+        for dt in (Q.QMM_PARTIAL_BF16, Q.QMM_PARTIAL_F32):
+            got, s = _run(d, M, Nout, split_req, partial_dtype=dt)
+            _assert_close(got, C64, _tol(s, dt), "M=%d req=%d dt=%d" % (M, split_req, dt))
+
+
+def test_odd_output_width_scalar_stores():
+    M, Kred, Nout = 5, 512, 77
+    p = inputs.make_w4a16(M, Kred, Nout, seed=7)
+    d = Q.to_device(p)
+    C64 = oracle.qmm(p["A"], p["Wq"], p["scales"], p["biases"])
+    for split_req in (1, 2, 4):
+        got, s = _run(d, M, Nout, split_req)
+        _assert_close(got, C64, _tol(s, 0), "req=%d" % split_req)
+
+
+def test_minimum_shape():
+    p = inputs.make_w4a16(1, 128, 1, seed=8)
+    d = Q.to_device(p)
+    got, s = _run(d, 1, 1, 0)
+    _assert_close(got, oracle.qmm(p["A"], p["Wq"], p["scales"], p["biases"]), TOL_F32)
+
+
+# ---- the projection workloads at full size, sampled ------------------------
+
+def _sample(M, Nout, rng):
+    rows = np.unique(np.concatenate([[0, M - 1], rng.integers(0, M, 6)]))
+    cols = np.unique(np.concatenate([[0, Nout - 1], rng.integers(0, Nout, 126)]))
+    return rows, cols
+
+
+@pytest.mark.parametrize("M", [16, 32, 64, 128, 2048])
+@pytest.mark.parametrize("name", list(inputs.PROJECTIONS) + ["ragged"])
+def test_projection_full_size_sampled(name, M):
+    Kred, Nout = inputs.RAGGED if name == "ragged" else inputs.PROJECTIONS[name]
+    p = inputs.make_w4a16(M, Kred, Nout, seed=0)
+    d = Q.to_device(p)
+    rng = np.random.default_rng(M * 7 + Nout)
+    rows, cols = _sample(M, Nout, rng)
+    ref = oracle.qmm_sampled(p["A"], p["Wq"], p["scales"], p["biases"], rows, cols)
+    got, s = _run(d, M, Nout, 0)
+    _assert_close(got[np.ix_(rows, cols)], ref, _tol(s, 0), "policy s=%d" % s)
+    got1, _ = _run(d, M, Nout, 1)
+    _assert_close(got1[np.ix_(rows, cols)], ref, TOL_F32, "unsplit")
+    # property at every element: split and unsplit agree within both tolerances
+    _assert_close(got, _val(got1), _tol(s, 0) + TOL_F32, "split vs unsplit")
+
+
+def test_fallback_shape_runs_the_unsplit_kernel_exactly():
+    # base grid already fills the target: the policy must pick split 1 and the
+    # result must be bit-identical to the unsplit control
+    Kred, Nout = inputs.PROJECTIONS["gate"]
+    M = 2048
+    p = inputs.make_w4a16(M, Kred, Nout, seed=2)
+    d = Q.to_device(p)
+    for pol in (Q.qmm_policy_preset(Q.QMM_PRESET_PAGES), None):
+        got, s = _run(d, M, Nout, 0, pol=pol)
+        assert s == 1
+        got1, _ = _run(d, M, Nout, 1)
+        assert np.array_equal(got, got1)
+
+
+@pytest.mark.parametrize("M", [1, 4, 8])
+@pytest.mark.parametrize("name", ["k", "o", "down"])
+def test_decode_regime(name, M):
+    Kred, Nout = inputs.PROJECTIONS[name]
+    p = inputs.make_w4a16(M, Kred, Nout, seed=3)
+    d = Q.to_device(p)
+    C64 = oracle.qmm(p["A"], p["Wq"], p["scales"], p["biases"])
+    got, s = _run(d, M, Nout, 0)
+    assert Kred // s >= 512, "decode splits keep >= 512 reduction elements"
+    _assert_close(got, C64, _tol(s, 0), "s=%d" % s)
+
+
+def test_deterministic():
+    Kred, Nout = inputs.PROJECTIONS["k"]
+    p = inputs.make_w4a16(32, Kred, Nout, seed=4)
+    d = Q.to_device(p)
+    a, _ = _run(d, 32, Nout, 0)
+    b, _ = _run(d, 32, Nout, 0)
+    assert np.array_equal(a, b)
+
+
+# ---- the reduce on its own: bit-exact --------------------------------------
+
+@pytest.mark.parametrize("split", [1, 2, 3, 7, 16])
+@pytest.mark.parametrize("M,Nout", [(16, 1024), (5, 77), (3, 8)])
+@pytest.mark.parametrize("dt", [Q.QMM_PARTIAL_BF16, Q.QMM_PARTIAL_F32])
+def test_reduce_bit_exact(split, M, Nout, dt):
+    rng = np.random.default_rng(split * 1000 + M + Nout)
+    planes = rng.standard_normal((split, M, Nout)).astype(np.float32) * 4
+    if dt == Q.QMM_PARTIAL_BF16:
+        bits = inputs.f32_to_bf16_bits(planes)
+        planes = inputs.bf16_bits_to_f32(bits)
+        dev = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()
+    else:
+        dev = torch.from_numpy(planes).cuda()
+    acc = np.zeros((M, Nout), np.float32)
+    for p in range(split):  # FP32, ascending partition
+        acc = (acc + planes[p]).astype(np.float32)
+    want = inputs.f32_to_bf16_bits(acc)
+    C = torch.empty((M, Nout), dtype=torch.bfloat16, device="cuda")
+    Q.qmm_splitk_reduce(dev, dt, split, M, Nout, C)
+    torch.cuda.synchronize()
+    assert np.array_equal(_bits(C), want)
+
+
+# ---- dense BF16 split-K GEMM -----------------------------------------------
+
+@pytest.fixture(scope="module")
+def dense512():
+    d = inputs.make_dense(512, 512, 16384, seed=0)
+    return d, oracle.gemm(d["A"], d["W"])
+
+
+def _dense_dev(d):
+    f = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda()
+    return f(d["A"]), f(d["W"])
+
+
+@pytest.mark.parametrize("split", [1, 2, 4, 6, 8, 9, 12, 16])
+def test_dense_gemm_splits(dense512, split):
+    d, C64 = dense512
+    A, W = _dense_dev(d)
+    C = torch.empty((512, 512), dtype=torch.bfloat16, device="cuda")
+    nb = Q.qmm_gemm_workspace_bytes(512, 512, split)
+    ws = torch.empty(max(nb, 16), dtype=torch.uint8, device="cuda") if nb else None
+    Q.qmm_gemm_bf16_splitk(A, W, C, split, ws)
+    torch.cuda.synchronize()
+    _assert_close(_bits(C), C64, TOL_F32, "s=%d" % split)
+
+
+@pytest.mark.parametrize("split", [1, 3, 10])
+def test_dense_gemm_ragged(split):
+    d = inputs.make_dense(200, 130, 640, seed=5)
+    C64 = oracle.gemm(d["A"], d["W"])
+    A, W = _dense_dev(d)
+    C = torch.empty((200, 130), dtype=torch.bfloat16, device="cuda")
+    nb = Q.qmm_gemm_workspace_bytes(200, 130, split)
+    ws = torch.empty(max(nb, 16), dtype=torch.uint8, device="cuda") if nb else None
+    Q.qmm_gemm_bf16_splitk(A, W, C, split, ws)
+    torch.cuda.synchronize()
+    _assert_close(_bits(C), C64, TOL_F32, "s=%d" % split)
+
+
+# ---- error codes with real device buffers ----------------------------------
+
+def test_error_codes_on_device():
+    Kred, Nout, M = 2560, 1024, 16
+    p = inputs.make_w4a16(M, Kred, Nout, seed=9)
+    d = Q.to_device(p)
+    C = torch.empty((M, Nout), dtype=torch.bfloat16, device="cuda")
+    small = torch.empty(64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(Q.QmmError) as e:
+        Q.qmm_w4a16_g128(d["A"], d["Wq"], d["scales"], d["biases"], C, split_req=4, workspace=small)
+    assert e.value.code == Q.QMM_EWORKSPACE
+    with pytest.raises(Q.QmmError) as e:
+        Q.qmm_w4a16_g128(d["A"], d["Wq"], d["scales"], d["biases"], C, split_req=3)
+    assert e.value.code == Q.QMM_ESHAPE
+    lib = Q.lib()
+    rc = lib.qmm_w4a16_g128(ctypes.c_void_p(d["A"].data_ptr() + 2), ctypes.c_void_p(d["Wq"].data_ptr()),
+                            ctypes.c_void_p(d["scales"].data_ptr()), ctypes.c_void_p(d["biases"].data_ptr()),
+                            ctypes.c_void_p(C.data_ptr()), M, Kred, Nout, 1, None, None, 0, 0, None, None)
+    assert rc == Q.QMM_EALIGN
