@@ -67,6 +67,21 @@ def roofline_time_s(nbytes, flops, peaks):
     return (t_hbm, "hbm") if t_hbm >= t_tc else (t_tc, "tensor")
 
 
+def max_over_ranks(ms: float, device=None) -> float:
+    """The largest per-rank time (the job ends when the slowest rank ends)."""
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value_us(ms_max: float, world: int, steps: int, ncalls: int) -> float:
+    """Whole-job µs per call: the max-over-ranks time over every call of every rank."""
+    return ms_max * 1e3 / (world * steps * ncalls)
+
+
 def calls():
     return [(name, M) + inputs.PROJECTIONS[name] for M in M_LIST for name in PROJ]
 
@@ -238,11 +253,7 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    ms = t0.elapsed_time(t1)
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(t0.elapsed_time(t1), device)
 
     if args.launch_list:
         return {"ms": ms, "wl": wl, "launch_list": True}
@@ -436,7 +447,7 @@ def main():
     res = run_gpu(args, rank, world, local_rank)
     wl = res["wl"]
     ncalls = len(wl.calls)
-    value_us = res["ms"] * 1e3 / (world * args.steps * ncalls)
+    value_us = job_value_us(res["ms"], world, args.steps, ncalls)
     if res.get("launch_list"):
         if rank == 0:
             print(json.dumps({"launch_list": True, "value": value_us, "unit": UNIT,

@@ -154,6 +154,23 @@ int qmm_unpack_probe(const uint32_t *Wq, int Nout, int Kred, uint8_t *q, void *s
 int qmm_dequant_probe(const uint32_t *Wq, const void *scales, const void *biases, int Nout,
                       int Kred, void *w, void *stream);
 
+/* Kernel families used by qmm_w4a16_g128 (process-wide, thread-safe):
+ *   QMM_KERNELS_DEFAULT   the tuned table: per M, the family measured fastest
+ *   QMM_KERNELS_MMA_SYNC  register-dequant mma.sync kernels for every M
+ *   QMM_KERNELS_TCGEN05   tcgen05 kernels (dequantized weights in tensor
+ *                         memory) for every M
+ * qmm_kernel_tile and the GB300 policy preset follow the choice.  Returns
+ * the previous setting, or QMM_EINVAL for an unknown value.  Meant for A/B
+ * measurements and tests; the default needs no call. */
+enum { QMM_KERNELS_DEFAULT = 0, QMM_KERNELS_MMA_SYNC = 1, QMM_KERNELS_TCGEN05 = 2 };
+int qmm_set_kernels(int which);
+
+/* Status word of the tcgen05 kernels: 0 = ok, 1 = a bounded wait inside a
+ * kernel ran out (the kernel stopped early; its output is not valid).
+ * Synchronizes with the device (cudaMemcpyFromSymbol); clear != 0 resets the
+ * word.  Returns QMM_OK, QMM_EINVAL, QMM_ENODEV or QMM_ECUDA. */
+int qmm_kernel_status(int *status, int clear);
+
 /* Static description of a return code. */
 const char *qmm_strerror(int code);
 

@@ -2,8 +2,10 @@
 // dispatch of the W4A16 matmul, the reduce and the dense split-K GEMM.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <climits>
 #include <cstdint>
+#include <mutex>
 
 #include "../../include/qmm.h"
 #include "qmm_internal.h"
@@ -42,9 +44,56 @@ int launched(int err) { return err == cudaSuccess ? QMM_OK : QMM_ECUDA; }
 
 size_t partial_elem_bytes(int dtype) { return dtype == QMM_PARTIAL_F32 ? 4 : 2; }
 
+std::atomic<int> g_kernels{QMM_KERNELS_DEFAULT};
+
+template <size_t N>
+const qmm::Family& pick(const qmm::Family (&table)[N], int M) {
+    for (size_t i = 0; i + 1 < N; ++i)
+        if (M <= table[i].max_m) return table[i];
+    return table[N - 1];
+}
+
 }  // namespace
 
+namespace qmm {
+
+const Family& family_for(int M) {
+    switch (g_kernels.load(std::memory_order_relaxed)) {
+        case QMM_KERNELS_MMA_SYNC: return pick(kMmaFamilies, M);
+        case QMM_KERNELS_TCGEN05: return pick(kTcFamilies, M);
+        default: return pick(kDefaultFamilies, M);
+    }
+}
+
+int smem_optin_bytes() {
+    static int limit = -1;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        int dev = 0, v = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) == cudaSuccess)
+            limit = v;
+    });
+    return limit;
+}
+
+}  // namespace qmm
+
 extern "C" {
+
+int qmm_set_kernels(int which) {
+    if (which != QMM_KERNELS_DEFAULT && which != QMM_KERNELS_MMA_SYNC &&
+        which != QMM_KERNELS_TCGEN05)
+        return QMM_EINVAL;
+    return g_kernels.exchange(which);
+}
+
+int qmm_kernel_status(int* status, int clear) {
+    if (!status) return QMM_EINVAL;
+    int rc = check_device();
+    if (rc != QMM_OK) return rc;
+    return qmm::read_tc_status(status, clear != 0) == cudaSuccess ? QMM_OK : QMM_ECUDA;
+}
 
 const char* qmm_strerror(int code) {
     switch (code) {
@@ -61,7 +110,7 @@ const char* qmm_strerror(int code) {
 
 int qmm_kernel_tile(int M, int* bm, int* bn) {
     if (M < 1 || !bm || !bn) return QMM_EINVAL;
-    const qmm::Family& f = qmm::kFamilies[qmm::family_index(M)];
+    const qmm::Family& f = qmm::family_for(M);
     *bm = f.bm;
     *bn = f.bn;
     return QMM_OK;
@@ -139,8 +188,8 @@ int qmm_w4a16_g128(const void* A, const uint32_t* Wq, const void* scales, const 
     if (!aligned(A, 16) || !aligned(Wq, 16) || !aligned(C, 16) || !aligned(scales, 2) ||
         !aligned(biases, 2))
         return QMM_EALIGN;
-    const int fam = qmm::family_index(M);
-    if (ceil_div(M, qmm::kFamilies[fam].bm) > 65535) return QMM_ESHAPE;
+    const qmm::Family fam = qmm::family_for(M);
+    if (ceil_div(M, fam.bm) > 65535) return QMM_ESHAPE;
     int rc = check_device();
     if (rc != QMM_OK) return rc;
 

@@ -11,26 +11,43 @@ constexpr int kGroup = 128;  // quantization group length along the reduction ax
 
 // W4A16 kernel families, picked by the number of activation rows M.
 // BM = activation rows per CTA, BN = weight rows (output columns) per CTA.
+enum KernelKind { kKindMma = 0, kKindTc = 1 };
 struct Family {
     int max_m;  // family serves M <= max_m (the last one serves every larger M)
     int bm;
     int bn;
+    int kind;
 };
 
-// Keep in step with the template instantiations in qmm_w4a16.cu.
-constexpr Family kFamilies[] = {
-    {8, 8, 64},
-    {16, 16, 64},
-    {32, 32, 128},
-    {1 << 30, 64, 128},
+// mma.sync kernels with register dequant (qmm_w4a16.cu); keep in step with
+// the template instantiations there.
+constexpr Family kMmaFamilies[] = {
+    {8, 8, 64, kKindMma},
+    {16, 16, 64, kKindMma},
+    {32, 32, 128, kKindMma},
+    {1 << 30, 64, 128, kKindMma},
 };
-constexpr int kNumFamilies = sizeof(kFamilies) / sizeof(kFamilies[0]);
+// tcgen05 kernels, dequantized weights in tensor memory (qmm_w4a16_tc.cu);
+// bm is the MMA N (activation rows), bn the MMA M (weight rows).
+constexpr Family kTcFamilies[] = {
+    {16, 16, 128, kKindTc},
+    {32, 32, 128, kKindTc},
+    {64, 64, 128, kKindTc},
+    {128, 128, 128, kKindTc},
+    {1 << 30, 256, 128, kKindTc},
+};
+// The default table: per M, the family that measured fastest on GB300.
+constexpr Family kDefaultFamilies[] = {
+    {8, 8, 64, kKindMma},
+    {16, 16, 64, kKindMma},
+    {32, 32, 128, kKindMma},
+    {1 << 30, 64, 128, kKindMma},
+};
 
-inline int family_index(int M) {
-    for (int i = 0; i < kNumFamilies - 1; ++i)
-        if (M <= kFamilies[i].max_m) return i;
-    return kNumFamilies - 1;
-}
+// Process-wide choice of table (qmm_set_kernels); returns the family for M.
+const Family& family_for(int M);
+
+int smem_optin_bytes();
 
 // GB300 preset tuning constants: target = kTargetPerSm * SMs CTAs, cap.
 constexpr int kTargetPerSm = 2;
@@ -42,9 +59,12 @@ enum OutMode { kOutBf16 = 0, kOutF32 = 1 };
 
 // Kernel launchers (qmm_w4a16.cu, qmm_reduce.cu, qmm_gemm.cu).  They assume
 // validated arguments and return the cudaError_t of the launch as int.
-int launch_w4a16(int family, const void* A, const uint32_t* Wq, const void* scales,
+int launch_w4a16(const Family& fam, const void* A, const uint32_t* Wq, const void* scales,
                  const void* biases, void* out, int out_mode, int M, int Kred, int Nout,
                  int split, void* stream);
+int launch_w4a16_tc(int bm, const void* A, const uint32_t* Wq, const void* scales, const void* biases,
+                    void* out, int out_mode, int M, int Kred, int Nout, int split, void* stream);
+int read_tc_status(int* out, bool clear);
 int launch_reduce(const void* partials, int partial_dtype, int split, int M, int Nout, void* C,
                   void* stream);
 int launch_gemm(const void* A, const void* W, void* out, int out_mode, int M, int N, int K,

@@ -89,18 +89,6 @@ __global__ void __launch_bounds__(C::THREADS) w4a16_kernel(const W4Params p) {
     const int ngrp = p.gpp, gbeg = part * p.gpp;
     const size_t wrow = static_cast<size_t>(p.Kred) / 8;  // words per weight row
 
-    // scale and bias of this CTA's rows for every group of the partition
-    for (int i = tid; i < ngrp * BN; i += C::THREADS) {
-        const int r = i / ngrp, gi = i - r * ngrp, n = n0 + r;
-        uint32_t v = 0;
-        if (n < p.Nout) {
-            const size_t o = static_cast<size_t>(n) * p.G + gbeg + gi;
-            v = static_cast<uint32_t>(__ldg(p.scales + o)) |
-                (static_cast<uint32_t>(__ldg(p.biases + o)) << 16);
-        }
-        sb[gi * BN + r] = v;
-    }
-
     auto load_stage = [&](int i, int slot) {
         const int grp = gbeg + i;
         uint8_t* ws = pipe + slot * C::STAGE;
@@ -193,6 +181,18 @@ __global__ void __launch_bounds__(C::THREADS) w4a16_kernel(const W4Params p) {
     for (int s = 0; s < STAGES - 1; ++s) {
         if (s < ngrp) load_stage(s, s);
         cp_async_commit();
+    }
+    // scale and bias of this CTA's rows for every group of the partition,
+    // loaded while the first copies are in flight
+    for (int i = tid; i < ngrp * BN; i += C::THREADS) {
+        const int r = i / ngrp, gi = i - r * ngrp, n = n0 + r;
+        uint32_t v = 0;
+        if (n < p.Nout) {
+            const size_t o = static_cast<size_t>(n) * p.G + gbeg + gi;
+            v = static_cast<uint32_t>(__ldg(p.scales + o)) |
+                (static_cast<uint32_t>(__ldg(p.biases + o)) << 16);
+        }
+        sb[gi * BN + r] = v;
     }
     cp_async_wait<STAGES - 2>();
     __syncthreads();
@@ -303,22 +303,10 @@ __global__ void probe_kernel(const uint32_t* __restrict__ Wq, const uint16_t* __
     }
 }
 
-int smem_optin_limit() {
-    static int limit = -1;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        int dev = 0, v = 0;
-        if (cudaGetDevice(&dev) == cudaSuccess &&
-            cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) == cudaSuccess)
-            limit = v;
-    });
-    return limit;
-}
-
 template <class C>
 int launch_cfg(const W4Params& p, int split, cudaStream_t stream) {
     auto kern = w4a16_kernel<C>;
-    const int limit = smem_optin_limit();
+    const int limit = smem_optin_bytes();
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
@@ -340,16 +328,18 @@ using Fam0 = W4Cfg<8, 1, 4, 4>;    // M <= 8:  BM 8,  BN 64
 using Fam1 = W4Cfg<16, 1, 4, 4>;   // M <= 16: BM 16, BN 64
 using Fam2 = W4Cfg<32, 2, 4, 4>;   // M <= 32: BM 32, BN 128
 using Fam3 = W4Cfg<64, 1, 8, 4>;   // larger:  BM 64, BN 128
-static_assert(Fam0::BM == kFamilies[0].bm && Fam0::BN == kFamilies[0].bn, "family 0");
-static_assert(Fam1::BM == kFamilies[1].bm && Fam1::BN == kFamilies[1].bn, "family 1");
-static_assert(Fam2::BM == kFamilies[2].bm && Fam2::BN == kFamilies[2].bn, "family 2");
-static_assert(Fam3::BM == kFamilies[3].bm && Fam3::BN == kFamilies[3].bn, "family 3");
+static_assert(Fam0::BM == kMmaFamilies[0].bm && Fam0::BN == kMmaFamilies[0].bn, "family 0");
+static_assert(Fam1::BM == kMmaFamilies[1].bm && Fam1::BN == kMmaFamilies[1].bn, "family 1");
+static_assert(Fam2::BM == kMmaFamilies[2].bm && Fam2::BN == kMmaFamilies[2].bn, "family 2");
+static_assert(Fam3::BM == kMmaFamilies[3].bm && Fam3::BN == kMmaFamilies[3].bn, "family 3");
 
 }  // namespace
 
-int launch_w4a16(int family, const void* A, const uint32_t* Wq, const void* scales,
+int launch_w4a16(const Family& fam, const void* A, const uint32_t* Wq, const void* scales,
                  const void* biases, void* out, int out_mode, int M, int Kred, int Nout,
                  int split, void* stream) {
+    if (fam.kind == kKindTc)
+        return launch_w4a16_tc(fam.bm, A, Wq, scales, biases, out, out_mode, M, Kred, Nout, split, stream);
     W4Params p;
     p.A = static_cast<const uint16_t*>(A);
     p.Wq = Wq;
@@ -363,10 +353,10 @@ int launch_w4a16(int family, const void* A, const uint32_t* Wq, const void* scal
     p.gpp = p.G / split;
     p.out_mode = out_mode;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    switch (family) {
-        case 0: return launch_cfg<Fam0>(p, split, st);
-        case 1: return launch_cfg<Fam1>(p, split, st);
-        case 2: return launch_cfg<Fam2>(p, split, st);
+    switch (fam.bm) {
+        case Fam0::BM: return launch_cfg<Fam0>(p, split, st);
+        case Fam1::BM: return launch_cfg<Fam1>(p, split, st);
+        case Fam2::BM: return launch_cfg<Fam2>(p, split, st);
         default: return launch_cfg<Fam3>(p, split, st);
     }
 }

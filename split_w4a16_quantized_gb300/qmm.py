@@ -21,6 +21,7 @@ QMM_OK, QMM_EINVAL, QMM_ESHAPE, QMM_EWORKSPACE, QMM_ECUDA, QMM_EALIGN, QMM_ENODE
     0, -1, -2, -3, -4, -5, -6
 QMM_PARTIAL_BF16, QMM_PARTIAL_F32 = 0, 1
 QMM_PRESET_PAGES, QMM_PRESET_GB300 = 0, 1
+QMM_KERNELS_DEFAULT, QMM_KERNELS_MMA_SYNC, QMM_KERNELS_TCGEN05 = 0, 1, 2
 
 
 class qmm_policy(ctypes.Structure):
@@ -58,6 +59,8 @@ _SIGS = {
     "qmm_unpack_probe": (_I, [_P, _I, _I, _P, _P]),
     "qmm_dequant_probe": (_I, [_P, _P, _P, _I, _I, _P, _P]),
     "qmm_strerror": (ctypes.c_char_p, [_I]),
+    "qmm_set_kernels": (_I, [_I]),
+    "qmm_kernel_status": (_I, [ctypes.POINTER(_I), _I]),
 }
 
 
@@ -115,6 +118,21 @@ def qmm_policy_preset(which: int, M: int = 1, num_sms: int = 0) -> qmm_policy:
     out = qmm_policy()
     _check(lib().qmm_policy_preset(which, M, num_sms, ctypes.byref(out)), "qmm_policy_preset")
     return out
+
+
+def qmm_set_kernels(which: int) -> int:
+    """Select the kernel table (QMM_KERNELS_*); returns the previous one."""
+    prev = lib().qmm_set_kernels(which)
+    if prev < 0:
+        raise QmmError(prev, "qmm_set_kernels")
+    return prev
+
+
+def qmm_kernel_status(clear: bool = True) -> int:
+    """0, or 1 if a bounded wait inside a tcgen05 kernel ran out (synchronizes)."""
+    st = _I(0)
+    _check(lib().qmm_kernel_status(ctypes.byref(st), int(clear)), "qmm_kernel_status")
+    return st.value
 
 
 def qmm_kernel_tile(M: int):

@@ -29,6 +29,22 @@ def built():
     build.build()
 
 
+KERNELS = {"default": Q.QMM_KERNELS_DEFAULT, "mma": Q.QMM_KERNELS_MMA_SYNC,
+           "tc": Q.QMM_KERNELS_TCGEN05}
+
+
+@pytest.fixture(params=["mma", "tc"])
+def family(request):
+    """Run the test once per kernel family table; check the status word after."""
+    prev = Q.qmm_set_kernels(KERNELS[request.param])
+    Q.qmm_kernel_status(clear=True)
+    yield request.param
+    try:
+        assert Q.qmm_kernel_status(clear=True) == 0, "a bounded wait ran out in a kernel"
+    finally:
+        Q.qmm_set_kernels(prev)
+
+
 def _bits(t: torch.Tensor) -> np.ndarray:
     return t.detach().cpu().view(torch.int16).numpy().view(np.uint16)
 
@@ -96,6 +112,23 @@ def test_dequant_probe_bit_exact(Nout, Kred):
 
 # ---- the K-projection at M = 16 (policy vs unsplit) ------------------------
 
+@pytest.mark.parametrize("M", [1, 16, 40, 128, 300])
+def test_one_hot_weights_copy_activations(family, M):
+    # q[n, k] = 1 at k = n, scale 1, bias 0: C = A[:, :Nout] exactly, which
+    # pins the k order and the row/column mapping of every kernel family
+    Kred, Nout = 256, 200
+    q = np.zeros((Nout, Kred), np.uint8)
+    q[np.arange(Nout), np.arange(Nout)] = 1
+    prob = inputs.make_w4a16(M, Kred, Nout, seed=40)
+    prob["Wq"] = inputs.pack_nibbles(q)
+    prob["scales"] = np.full((Nout, 2), 0x3F80, np.uint16)
+    prob["biases"] = np.zeros((Nout, 2), np.uint16)
+    d = Q.to_device(prob)
+    for split_req in (1, 2):
+        got, _ = _run(d, M, Nout, split_req, partial_dtype=Q.QMM_PARTIAL_F32)
+        assert np.array_equal(got, prob["A"][:, :Nout]), "split %d" % split_req
+
+
 @pytest.mark.parametrize("partial_dtype", [Q.QMM_PARTIAL_BF16, Q.QMM_PARTIAL_F32])
 def test_k_projection_m16_policy_and_unsplit(partial_dtype):
     Kred, Nout = inputs.PROJECTIONS["k"]
@@ -112,7 +145,7 @@ def test_k_projection_m16_policy_and_unsplit(partial_dtype):
 
 @pytest.mark.parametrize("name,splits", [("k", [2, 4, 5, 10, 20]), ("o", [2, 4, 8, 16, 32]),
                                          ("down", [2, 4, 19, 38, 76])])
-def test_forced_splits(name, splits):
+def test_forced_splits(family, name, splits):
     Kred, Nout = inputs.PROJECTIONS[name]
     p = inputs.make_w4a16(16, Kred, Nout, seed=1)
     d = Q.to_device(p)
@@ -125,8 +158,8 @@ def test_forced_splits(name, splits):
 
 # ---- every kernel family, ragged tiles -------------------------------------
 
-@pytest.mark.parametrize("M", [1, 3, 8, 9, 16, 17, 31, 32, 33, 64, 65, 100, 128])
-def test_families_ragged(M):
+@pytest.mark.parametrize("M", [1, 3, 8, 9, 16, 17, 31, 32, 33, 64, 65, 100, 128, 129, 300])
+def test_families_ragged(family, M):
     Kred, Nout = 1280, 1000  # Nout = 1000: partial last column tile
     p = inputs.make_w4a16(M, Kred, Nout, seed=100 + M)
     d = Q.to_device(p)
@@ -195,7 +228,7 @@ def test_fallback_shape_runs_the_unsplit_kernel_exactly():
 
 @pytest.mark.parametrize("M", [1, 4, 8])
 @pytest.mark.parametrize("name", ["k", "o", "down"])
-def test_decode_regime(name, M):
+def test_decode_regime(family, name, M):
     Kred, Nout = inputs.PROJECTIONS[name]
     p = inputs.make_w4a16(M, Kred, Nout, seed=3)
     d = Q.to_device(p)
@@ -205,7 +238,7 @@ def test_decode_regime(name, M):
     _assert_close(got, C64, _tol(s, 0), "s=%d" % s)
 
 
-def test_deterministic():
+def test_deterministic(family):
     Kred, Nout = inputs.PROJECTIONS["k"]
     p = inputs.make_w4a16(32, Kred, Nout, seed=4)
     d = Q.to_device(p)
