@@ -65,6 +65,8 @@ const Family& family_for(int M) {
     }
 }
 
+bool gemm_uses_tc() { return g_kernels.load(std::memory_order_relaxed) != QMM_KERNELS_MMA_SYNC; }
+
 int smem_optin_bytes() {
     static int limit = -1;
     static std::once_flag once;
@@ -234,10 +236,14 @@ int qmm_gemm_bf16_splitk(const void* A, const void* W, void* C, int M, int N, in
     int rc = check_device();
     if (rc != QMM_OK) return rc;
     if (split == 1)
-        return launched(qmm::launch_gemm(A, W, C, qmm::kOutBf16, M, N, K, 1, stream));
+        return launched(qmm::gemm_uses_tc()
+                            ? qmm::launch_gemm_tc(A, W, C, qmm::kOutBf16, M, N, K, 1, stream)
+                            : qmm::launch_gemm(A, W, C, qmm::kOutBf16, M, N, K, 1, stream));
     if (!workspace || ws_bytes < qmm_gemm_workspace_bytes(M, N, split)) return QMM_EWORKSPACE;
     if (!aligned(workspace, 16)) return QMM_EALIGN;
-    rc = launched(qmm::launch_gemm(A, W, workspace, qmm::kOutF32, M, N, K, split, stream));
+    rc = launched(qmm::gemm_uses_tc()
+                      ? qmm::launch_gemm_tc(A, W, workspace, qmm::kOutF32, M, N, K, split, stream)
+                      : qmm::launch_gemm(A, W, workspace, qmm::kOutF32, M, N, K, split, stream));
     if (rc == QMM_OK)
         rc = launched(qmm::launch_reduce(workspace, QMM_PARTIAL_F32, split, M, N, C, stream));
     return rc;

@@ -67,6 +67,9 @@ int launch_w4a16_tc(int bm, const void* A, const uint32_t* Wq, const void* scale
 int read_tc_status(int* out, bool clear);
 int launch_reduce(const void* partials, int partial_dtype, int split, int M, int Nout, void* C,
                   void* stream);
+int launch_gemm_tc(const void* A, const void* W, void* out, int out_mode, int M, int N, int K,
+                   int split, void* stream);
+bool gemm_uses_tc();
 int launch_gemm(const void* A, const void* W, void* out, int out_mode, int M, int N, int K,
                 int split, void* stream);
 int launch_unpack_probe(const uint32_t* Wq, int Nout, int Kred, uint8_t* q, void* stream);

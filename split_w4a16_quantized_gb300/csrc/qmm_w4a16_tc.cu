@@ -39,6 +39,46 @@ namespace qmm {
 
 __device__ int g_tc_status = 0;
 
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// 2-D row-major tensor [rows, cols] of `elem` bytes, box [box_rows, box_cols]
+bool encode_2d(CUtensorMap* map, CUtensorMapDataType type, const void* ptr, uint64_t rows,
+               uint64_t cols, int elem, uint32_t box_rows, uint32_t box_cols,
+               CUtensorMapSwizzle swizzle) {
+    auto fn = tensor_map_encoder();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * elem};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, type, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int* tc_status_ptr() {
+    static int* ptr = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_tc_status) == cudaSuccess) ptr = static_cast<int*>(p);
+    });
+    return ptr;
+}
+
+
 namespace {
 
 constexpr int kWRows = 128;              // weight rows per CTA (MMA M)
@@ -256,45 +296,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    });
-    return fn;
-}
-
-// 2-D row-major tensor [rows, cols] of `elem` bytes, box [box_rows, box_cols]
-bool encode_2d(CUtensorMap* map, CUtensorMapDataType type, const void* ptr, uint64_t rows,
-               uint64_t cols, int elem, uint32_t box_rows, uint32_t box_cols,
-               CUtensorMapSwizzle swizzle) {
-    auto fn = tensor_map_encoder();
-    if (!fn) return false;
-    const cuuint64_t dims[2] = {cols, rows};
-    const cuuint64_t strides[1] = {cols * elem};
-    const cuuint32_t box[2] = {box_cols, box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    return fn(map, type, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-int* status_ptr() {
-    static int* ptr = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_tc_status) == cudaSuccess) ptr = static_cast<int*>(p);
-    });
-    return ptr;
-}
-
 template <int BNA>
 int launch_tc(const void* A, const uint32_t* Wq, const void* scales, const void* biases,
               void* out, int out_mode, int M, int Kred, int Nout, int split, cudaStream_t st) {
@@ -307,7 +308,7 @@ int launch_tc(const void* A, const uint32_t* Wq, const void* scales, const void*
         attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, limit);
     });
     if (attr_err != cudaSuccess) return attr_err;
-    int* status = status_ptr();
+    int* status = tc_status_ptr();
     if (!status) return cudaErrorInvalidSymbol;
 
     TcParams p;

@@ -285,7 +285,7 @@ def _dense_dev(d):
 
 
 @pytest.mark.parametrize("split", [1, 2, 4, 6, 8, 9, 12, 16])
-def test_dense_gemm_splits(dense512, split):
+def test_dense_gemm_splits(family, dense512, split):
     d, C64 = dense512
     A, W = _dense_dev(d)
     C = torch.empty((512, 512), dtype=torch.bfloat16, device="cuda")
@@ -297,7 +297,7 @@ def test_dense_gemm_splits(dense512, split):
 
 
 @pytest.mark.parametrize("split", [1, 3, 10])
-def test_dense_gemm_ragged(split):
+def test_dense_gemm_ragged(family, split):
     d = inputs.make_dense(200, 130, 640, seed=5)
     C64 = oracle.gemm(d["A"], d["W"])
     A, W = _dense_dev(d)
