@@ -219,7 +219,7 @@ def run_gpu(args, rank, world, local_rank):
     peaks, peak_src = load_peaks()
     wl = Workload(device, Q, l2)
     stream = torch.cuda.current_stream()
-    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=device).fill_(1)
+    flush = torch.empty(max(4 * l2, 512 << 20) // 4, dtype=torch.float32, device=device).fill_(1)
 
     # warm-up: eager step per set (first calls set kernel attributes), then graphs
     for r in range(wl.R):
@@ -258,6 +258,27 @@ def run_gpu(args, rank, world, local_rank):
     if args.launch_list:
         return {"ms": ms, "wl": wl, "launch_list": True}
 
+    # the same step with programmatic dependent launch off, for comparison
+    prev = Q.qmm_set_pdl(False)
+    graphs_nopdl = []
+    with torch.cuda.stream(cap):
+        for r in range(wl.R):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cap):
+                wl.step(r)
+            graphs_nopdl.append(g)
+    Q.qmm_set_pdl(prev)
+    torch.cuda.synchronize()
+    for k in range(args.warmup):
+        graphs_nopdl[k % wl.R].replay()
+    t0.record(stream)
+    for k in range(args.steps):
+        graphs_nopdl[k % wl.R].replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms_nopdl = t0.elapsed_time(t1)
+    del graphs_nopdl
+
     # per call: policy split vs the unsplit control, cold L2, CUDA events
     per_call = []
     reps = 16
@@ -280,7 +301,8 @@ def run_gpu(args, rank, world, local_rank):
     sample = clocks.stop()
     dense = dense_sweep(Q, device, flush, stream, sms) if rank == 0 else None
     e2e = run_e2e(wl, Q, device, stream, min(args.steps, 20))
-    return {"ms": ms, "per_call": per_call, "clocks": sample, "wl": wl, "peaks": peaks,
+    return {"ms": ms, "ms_nopdl": ms_nopdl, "per_call": per_call, "clocks": sample, "wl": wl,
+            "peaks": peaks,
             "peak_src": peak_src, "l2": l2, "sms": sms, "dense": dense, "e2e": e2e}
 
 
@@ -484,6 +506,7 @@ def main():
                             % (wl.R, wl.set_bytes / 2**20, res["l2"] >> 20),
                       "graphs": "one CUDA graph per step, replayed", "parallelism":
                       "replicas x%d" % world, "sms": res["sms"]},
+           "value_without_pdl": round(job_value_us(res["ms_nopdl"], 1, args.steps, ncalls), 4),
            "roofline": roof, "gpu_launches": args.steps * wl.launches_per_step(),
            "clocks": res["clocks"], "e2e": res["e2e"], "per_call": res["per_call"],
            "dense_splitk_512x512x16384": res["dense"]}

@@ -165,6 +165,15 @@ int qmm_dequant_probe(const uint32_t *Wq, const void *scales, const void *biases
 enum { QMM_KERNELS_DEFAULT = 0, QMM_KERNELS_MMA_SYNC = 1, QMM_KERNELS_TCGEN05 = 2 };
 int qmm_set_kernels(int which);
 
+/* Programmatic dependent launch (on by default): each kernel of the library
+ * is launched with programmatic stream serialization, lets the next kernel on
+ * the stream start launching early, and reads or writes global memory only
+ * after the kernels before it on the stream have completed (griddepcontrol),
+ * so stream order is kept while launch latency overlaps.  enable = 0 turns
+ * it off (plain stream-ordered launches).  Process-wide; returns the
+ * previous setting. */
+int qmm_set_pdl(int enable);
+
 /* Status word of the tcgen05 kernels: 0 = ok, 1 = a bounded wait inside a
  * kernel ran out (the kernel stopped early; its output is not valid).
  * Synchronizes with the device (cudaMemcpyFromSymbol); clear != 0 resets the

@@ -6,6 +6,16 @@
 
 namespace qmm {
 
+// Programmatic dependent launch.  pdl_trigger lets the next kernel on the
+// stream begin launching (its blocks run up to their own pdl_wait);
+// pdl_wait blocks until the kernels before this one on the stream have
+// completed and their memory writes are visible.  Without the launch
+// attribute both are no-ops.
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -40,6 +40,8 @@ __global__ void __launch_bounds__(GB_THREADS) gemm_kernel(const GemmParams p) {
     const int nt = T / p.split + (part < T % p.split ? 1 : 0);
     const int t0 = part * (T / p.split) + (part < T % p.split ? part : T % p.split);
     const int kbeg = t0 * 64, nk = nt * 2;
+    pdl_trigger();
+    pdl_wait();
 
     auto load = [&](int i, int slot) {
         uint8_t* as = smem + slot * 2 * GB_TILE;
@@ -152,6 +154,8 @@ int launch_gemm(const void* A, const void* W, void* out, int out_mode, int M, in
     p.split = split;
     p.out_mode = out_mode;
     cudaLaunchConfig_t cfg = {};
+    LaunchAttrs la;
+    apply_pdl(cfg, la);
     cfg.gridDim = dim3((N + GB_N - 1) / GB_N, (M + GB_M - 1) / GB_M, split);
     cfg.blockDim = dim3(GB_THREADS, 1, 1);
     cfg.dynamicSmemBytes = GB_SMEM;

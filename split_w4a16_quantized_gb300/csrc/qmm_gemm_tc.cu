@@ -67,6 +67,7 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     const int nt = T / p.split + (part < T % p.split ? 1 : 0);
     const int t0 = part * (T / p.split) + (part < T % p.split ? part : T % p.split);
 
+    pdl_trigger();
     if (tid == 0) {
         abort_flag = 0;
         for (int s = 0; s < stages; ++s) {
@@ -82,6 +83,7 @@ __global__ void __launch_bounds__(kThreadsG, 1)
         tmem_alloc(tmem_slot, kTile);
         tmem_relinquish();
     }
+    pdl_wait();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -215,6 +217,8 @@ int launch_gemm_tc(const void* A, const void* W, void* out, int out_mode, int M,
                    CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
+    LaunchAttrs la;
+    apply_pdl(cfg, la);
     cfg.gridDim = dim3((N + kTile - 1) / kTile, (M + kTile - 1) / kTile, split);
     cfg.blockDim = dim3(kThreadsG, 1, 1);
     cfg.dynamicSmemBytes = fixed + stages * 2 * kOpBytes;

@@ -45,6 +45,7 @@ int launched(int err) { return err == cudaSuccess ? QMM_OK : QMM_ECUDA; }
 size_t partial_elem_bytes(int dtype) { return dtype == QMM_PARTIAL_F32 ? 4 : 2; }
 
 std::atomic<int> g_kernels{QMM_KERNELS_DEFAULT};
+std::atomic<int> g_pdl{1};
 
 template <size_t N>
 const qmm::Family& pick(const qmm::Family (&table)[N], int M) {
@@ -64,6 +65,8 @@ const Family& family_for(int M) {
         default: return pick(kDefaultFamilies, M);
     }
 }
+
+bool pdl_enabled() { return g_pdl.load(std::memory_order_relaxed) != 0; }
 
 bool gemm_uses_tc() { return g_kernels.load(std::memory_order_relaxed) != QMM_KERNELS_MMA_SYNC; }
 
@@ -89,6 +92,8 @@ int qmm_set_kernels(int which) {
         return QMM_EINVAL;
     return g_kernels.exchange(which);
 }
+
+int qmm_set_pdl(int enable) { return g_pdl.exchange(enable ? 1 : 0); }
 
 int qmm_kernel_status(int* status, int clear) {
     if (!status) return QMM_EINVAL;

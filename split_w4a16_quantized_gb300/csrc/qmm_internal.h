@@ -2,6 +2,8 @@
 // libqmm (not part of the C ABI).
 #pragma once
 
+#include <cuda_runtime.h>
+
 #include <cstddef>
 #include <cstdint>
 
@@ -48,6 +50,19 @@ constexpr Family kDefaultFamilies[] = {
 const Family& family_for(int M);
 
 int smem_optin_bytes();
+
+// Programmatic dependent launch of the library's kernels (qmm_set_pdl).
+bool pdl_enabled();
+struct LaunchAttrs {
+    cudaLaunchAttribute attr[1];
+};
+inline void apply_pdl(cudaLaunchConfig_t& cfg, LaunchAttrs& la) {
+    if (!pdl_enabled()) return;
+    la.attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    la.attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = la.attr;
+    cfg.numAttrs = 1;
+}
 
 // GB300 preset tuning constants: target = kTargetPerSm * SMs CTAs, cap.
 constexpr int kTargetPerSm = 2;

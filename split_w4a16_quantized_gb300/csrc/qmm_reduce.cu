@@ -41,6 +41,8 @@ template <typename T>
 __global__ void __launch_bounds__(256) reduce_vec8(const T* __restrict__ partials, int split,
                                                    int64_t plane, __nv_bfloat16* __restrict__ C) {
     const int64_t nvec = plane / 8;
+    pdl_trigger();
+    pdl_wait();
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < nvec;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         float acc[8];
@@ -65,6 +67,8 @@ __global__ void __launch_bounds__(256) reduce_vec8(const T* __restrict__ partial
 template <typename T>
 __global__ void __launch_bounds__(256) reduce_scalar(const T* __restrict__ partials, int split,
                                                      int64_t plane, __nv_bfloat16* __restrict__ C) {
+    pdl_trigger();
+    pdl_wait();
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < plane;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         float acc = 0.f;
@@ -94,6 +98,8 @@ int launch_typed(const T* partials, int split, int64_t plane, __nv_bfloat16* C,
     const int64_t max_blocks = static_cast<int64_t>(num_sms()) * 8;
     if (blocks > max_blocks) blocks = max_blocks;
     cudaLaunchConfig_t cfg = {};
+    LaunchAttrs la;
+    apply_pdl(cfg, la);
     cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
     cfg.blockDim = dim3(256, 1, 1);
     cfg.stream = stream;

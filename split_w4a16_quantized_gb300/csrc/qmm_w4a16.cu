@@ -88,6 +88,8 @@ __global__ void __launch_bounds__(C::THREADS) w4a16_kernel(const W4Params p) {
     const int n0 = blockIdx.x * BN, m0 = blockIdx.y * BM, part = blockIdx.z;
     const int ngrp = p.gpp, gbeg = part * p.gpp;
     const size_t wrow = static_cast<size_t>(p.Kred) / 8;  // words per weight row
+    pdl_trigger();
+    pdl_wait();
 
     auto load_stage = [&](int i, int slot) {
         const int grp = gbeg + i;
@@ -316,6 +318,8 @@ int launch_cfg(const W4Params& p, int split, cudaStream_t stream) {
     const size_t smem = static_cast<size_t>(C::FIXED) + static_cast<size_t>(C::BN) * p.gpp * 4;
     if (limit < 0 || smem > static_cast<size_t>(limit)) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
+    LaunchAttrs la;
+    apply_pdl(cfg, la);
     cfg.gridDim = dim3((p.Nout + C::BN - 1) / C::BN, (p.M + C::BM - 1) / C::BM, split);
     cfg.blockDim = dim3(C::THREADS, 1, 1);
     cfg.dynamicSmemBytes = smem;

@@ -154,6 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ngrp = p.gpp, gbeg = part * p.gpp;
     volatile int* abort = &abort_flag;
 
+    pdl_trigger();
     if (tid == 0) {
         abort_flag = 0;
         for (int s = 0; s < stages; ++s) {
@@ -173,6 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(tmem_slot, C::TMEM_COLS);
         tmem_relinquish();
     }
+    pdl_wait();  // global memory is read only after the previous kernel is done
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -340,6 +342,8 @@ int launch_tc(const void* A, const uint32_t* Wq, const void* scales, const void*
         return cudaErrorInvalidValue;
 
     cudaLaunchConfig_t cfg = {};
+    LaunchAttrs la;
+    apply_pdl(cfg, la);
     cfg.gridDim = dim3((Nout + kWRows - 1) / kWRows, (M + BNA - 1) / BNA, split);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = fixed + stages * per_stage;

@@ -60,6 +60,7 @@ _SIGS = {
     "qmm_dequant_probe": (_I, [_P, _P, _P, _I, _I, _P, _P]),
     "qmm_strerror": (ctypes.c_char_p, [_I]),
     "qmm_set_kernels": (_I, [_I]),
+    "qmm_set_pdl": (_I, [_I]),
     "qmm_kernel_status": (_I, [ctypes.POINTER(_I), _I]),
 }
 
@@ -126,6 +127,11 @@ def qmm_set_kernels(which: int) -> int:
     if prev < 0:
         raise QmmError(prev, "qmm_set_kernels")
     return prev
+
+
+def qmm_set_pdl(enable: bool) -> int:
+    """Programmatic dependent launch on/off; returns the previous setting."""
+    return lib().qmm_set_pdl(int(bool(enable)))
 
 
 def qmm_kernel_status(clear: bool = True) -> int:
