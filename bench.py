@@ -82,7 +82,12 @@ def job_value_us(ms_max: float, world: int, steps: int, ncalls: int) -> float:
     return ms_max * 1e3 / (world * steps * ncalls)
 
 
+ONLY = None  # (projection, M) when --only restricts the step to one call
+
+
 def calls():
+    if ONLY is not None:
+        return [(ONLY[0], ONLY[1]) + inputs.PROJECTIONS[ONLY[0]]]
     return [(name, M) + inputs.PROJECTIONS[name] for M in M_LIST for name in PROJ]
 
 
@@ -452,7 +457,13 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--launch-list", action="store_true",
                     help="only the timed graph steps (for a profiler's launch list)")
+    ap.add_argument("--only", default=None, metavar="PROJ:M",
+                    help="restrict the step to one call, e.g. gate:128 (profiling aid)")
     args = ap.parse_args()
+    if args.only:
+        global ONLY
+        name, m = args.only.split(":")
+        ONLY = (name, int(m))
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
 
