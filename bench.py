@@ -103,6 +103,8 @@ class ClockSampler:
         self.path = None
 
     def start(self):
+        import atexit
+        atexit.register(self._kill)
         try:
             fd, self.path = tempfile.mkstemp(suffix=".csv")
             os.close(fd)
@@ -114,6 +116,10 @@ class ClockSampler:
         except OSError:
             self.proc = None
         return self
+
+    def _kill(self):
+        if self.proc is not None and self.proc.poll() is None:
+            self.proc.kill()
 
     def stop(self):
         if self.proc is None:
@@ -218,6 +224,8 @@ def run_gpu(args, rank, world, local_rank):
 
     device = torch.device("cuda", local_rank)
     torch.cuda.set_device(device)
+    Q.qmm_set_kernels({"default": Q.QMM_KERNELS_DEFAULT, "mma": Q.QMM_KERNELS_MMA_SYNC,
+                       "tc": Q.QMM_KERNELS_TCGEN05}[args.kernels])
     props = torch.cuda.get_device_properties(device)
     l2 = int(getattr(props, "L2_cache_size", 128 << 20))
     sms = props.multi_processor_count
@@ -242,8 +250,9 @@ def run_gpu(args, rank, world, local_rank):
     stream.wait_stream(cap)
     torch.cuda.synchronize()
 
-    clocks = ClockSampler(local_rank).start()
-    time.sleep(0.3)
+    clocks = ClockSampler(local_rank).start() if not args.launch_list else None
+    if clocks:
+        time.sleep(0.3)
     for k in range(args.warmup):
         graphs[k % wl.R].replay()
     torch.cuda.synchronize()
@@ -457,6 +466,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--launch-list", action="store_true",
                     help="only the timed graph steps (for a profiler's launch list)")
+    ap.add_argument("--kernels", choices=["default", "mma", "tc"], default="default",
+                    help="kernel table for the W4A16 calls (A/B comparisons)")
     ap.add_argument("--only", default=None, metavar="PROJ:M",
                     help="restrict the step to one call, e.g. gate:128 (profiling aid)")
     args = ap.parse_args()
@@ -515,6 +526,7 @@ def main():
                       "policy": "GB300 preset per M (target_blocks = 2 x SMs, cap 16)",
                       "l2": "inputs larger than L2: %d rotating input sets x %.0f MB (L2 %d MB)"
                             % (wl.R, wl.set_bytes / 2**20, res["l2"] >> 20),
+                      "kernels": args.kernels,
                       "graphs": "one CUDA graph per step, replayed", "parallelism":
                       "replicas x%d" % world, "sms": res["sms"]},
            "value_without_pdl": round(job_value_us(res["ms_nopdl"], 1, args.steps, ncalls), 4),

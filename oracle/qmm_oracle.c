@@ -200,6 +200,35 @@ int oracle_qmm_sampled(const uint16_t *A, const uint32_t *Wq, const uint16_t *sc
     return bad ? -1 : 0;
 }
 
+/* One output element of the partition emulation below: the fp64 sum of each
+ * partition rounded to the plane type, the planes added in FP32 in
+ * ascending p, the sum rounded once to BF16.  planes (nullable) receives
+ * the split plane values. */
+static int emulate_element(const double *am, const double *wn, int64_t Kred, int split,
+                           int partial_mode, uint16_t *c, double *planes) {
+    if (split == 1) {
+        double exact = dot(am, wn, 0, Kred);
+        if (planes) planes[0] = exact;
+        return bf16_round(exact, c);
+    }
+    int64_t span = (Kred / QO_GROUP / split) * QO_GROUP;
+    float acc = 0.0f; /* the reduce adds the planes in FP32 */
+    for (int p = 0; p < split; ++p) {
+        double exact = dot(am, wn, p * span, (p + 1) * span);
+        double plane;
+        if (partial_mode == 0) {
+            uint16_t pb;
+            if (bf16_round(exact, &pb)) return -1;
+            plane = bf16_value(pb);
+        } else {
+            plane = (double)(float)exact;
+        }
+        if (planes) planes[p] = plane;
+        acc = acc + (float)plane;
+    }
+    return bf16_round((double)acc, c);
+}
+
 /* Partition emulation [TL, Task 2 and Task 4].  With split s dividing
  * G = Kred/128, partition p covers groups [p*G/s, (p+1)*G/s): equal length,
  * starting and ending on group boundaries.  Each partition's fp64 sum is
@@ -214,8 +243,8 @@ int oracle_qmm_partitioned(const uint16_t *A, const uint32_t *Wq, const uint16_t
                            int nthreads) {
     if (M < 1 || Nout < 1 || Kred < QO_GROUP || Kred % QO_GROUP || nthreads < 1) return -1;
     int64_t G = Kred / QO_GROUP;
-    if (split < 1 || G % split || (partial_mode != 0 && partial_mode != 1)) return -1;
-    int64_t span = (G / split) * QO_GROUP;
+    if (split < 1 || split > 4096 || G % split || (partial_mode != 0 && partial_mode != 1))
+        return -1;
     double *w = dequant_all(Wq, scales, biases, Nout, Kred, nthreads);
     double *a = bf16_matrix(A, M, Kred, nthreads);
     if (!w || !a) { free(w); free(a); return -4; }
@@ -223,30 +252,47 @@ int oracle_qmm_partitioned(const uint16_t *A, const uint32_t *Wq, const uint16_t
 #pragma omp parallel for num_threads(nthreads) schedule(static) collapse(2) reduction(| : bad)
     for (int64_t m = 0; m < M; ++m)
         for (int64_t n = 0; n < Nout; ++n) {
-            const double *am = a + m * Kred, *wn = w + n * Kred;
+            double planes_mn[4096];
             uint16_t c;
-            if (split == 1) {
-                bad |= bf16_round(dot(am, wn, 0, Kred), &c) != 0;
-                if (partials) partials[m * Nout + n] = dot(am, wn, 0, Kred);
-            } else {
-                float acc = 0.0f; /* the reduce adds the planes in FP32 */
-                for (int p = 0; p < split; ++p) {
-                    double exact = dot(am, wn, p * span, (p + 1) * span);
-                    double plane;
-                    if (partial_mode == 0) {
-                        uint16_t pb;
-                        bad |= bf16_round(exact, &pb) != 0;
-                        plane = bf16_value(pb);
-                    } else {
-                        plane = (double)(float)exact;
-                    }
-                    if (partials) partials[((int64_t)p * M + m) * Nout + n] = plane;
-                    acc = acc + (float)plane;
-                }
-                bad |= bf16_round((double)acc, &c) != 0;
-            }
+            bad |= emulate_element(a + m * Kred, w + n * Kred, Kred, split, partial_mode, &c,
+                                   partials ? planes_mn : NULL) != 0;
             C_bf16[m * Nout + n] = c;
+            if (partials)
+                for (int p = 0; p < split; ++p) partials[((int64_t)p * M + m) * Nout + n] = planes_mn[p];
         }
+    free(w);
+    free(a);
+    return bad ? -1 : 0;
+}
+
+/* The partition emulation on a sample: out[i, j] = C_bf16[rows[i], cols[j]]
+ * of oracle_qmm_partitioned, computed element by element. */
+int oracle_qmm_partitioned_sampled(const uint16_t *A, const uint32_t *Wq, const uint16_t *scales,
+                                   const uint16_t *biases, int64_t M, int64_t Kred, int64_t Nout,
+                                   const int64_t *rows, int64_t nr, const int64_t *cols,
+                                   int64_t nc, int split, int partial_mode, uint16_t *out,
+                                   int nthreads) {
+    if (M < 1 || Nout < 1 || Kred < QO_GROUP || Kred % QO_GROUP || nthreads < 1) return -1;
+    int64_t G = Kred / QO_GROUP;
+    if (split < 1 || G % split || (partial_mode != 0 && partial_mode != 1)) return -1;
+    for (int64_t i = 0; i < nr; ++i) if (rows[i] < 0 || rows[i] >= M) return -1;
+    for (int64_t j = 0; j < nc; ++j) if (cols[j] < 0 || cols[j] >= Nout) return -1;
+    double *w = (double *)malloc(sizeof(double) * (size_t)(nc * Kred));
+    double *a = (double *)malloc(sizeof(double) * (size_t)(nr * Kred));
+    if (!w || !a) { free(w); free(a); return -4; }
+    int bad = 0;
+#pragma omp parallel for num_threads(nthreads) schedule(static) reduction(| : bad)
+    for (int64_t j = 0; j < nc; ++j)
+        bad |= dequant_row(Wq, scales, biases, Kred, cols[j], w + j * Kred) != 0;
+    for (int64_t i = 0; i < nr; ++i)
+        for (int64_t k = 0; k < Kred; ++k) a[i * Kred + k] = bf16_value(A[rows[i] * Kred + k]);
+    if (!bad) {
+#pragma omp parallel for num_threads(nthreads) schedule(static) collapse(2) reduction(| : bad)
+        for (int64_t i = 0; i < nr; ++i)
+            for (int64_t j = 0; j < nc; ++j)
+                bad |= emulate_element(a + i * Kred, w + j * Kred, Kred, split, partial_mode,
+                                       &out[i * nc + j], NULL) != 0;
+    }
     free(w);
     free(a);
     return bad ? -1 : 0;

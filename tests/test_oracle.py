@@ -218,6 +218,17 @@ def test_partitioned_error_bound():
         assert np.allclose(P.sum(axis=0), C64, rtol=0, atol=2.0 ** -8 * np.abs(P).sum(axis=0).max())
 
 
+def test_partitioned_sampled_matches_full():
+    p = inputs.make_w4a16(7, 1280, 45, seed=16)
+    rows, cols = np.array([0, 3, 6]), np.array([1, 2, 30, 44])
+    for s in (1, 2, 5, 10):
+        for mode in (0, 1):
+            C, _ = oracle.qmm_partitioned(p["A"], p["Wq"], p["scales"], p["biases"], s, mode)
+            S = oracle.qmm_partitioned_sampled(p["A"], p["Wq"], p["scales"], p["biases"], rows,
+                                               cols, s, mode)
+            assert np.array_equal(S, C[np.ix_(rows, cols)])
+
+
 def test_partitioned_rejects_nondividing_split():
     p = inputs.make_w4a16(1, 2560, 4, seed=12)
     with pytest.raises(ValueError):

@@ -1,8 +1,13 @@
 """GPU parity tests: the CUDA path through the C ABI against the CPU oracle.
 
-Tolerances (per element, against the oracle's fp64 C64):
-  |C_gpu - C64| <= 0.02  * max(1, |C64|)  with BF16 partial planes,
-  |C_gpu - C64| <= 0.008 * max(1, |C64|)  with FP32 partial planes or split 1.
+Tolerances, per element:
+  BF16 partial planes (split > 1): |C_gpu - C_emu| <= 0.02 * max(1, |C_emu|),
+      C_emu = the oracle's partition emulation (same split, each partition's
+      fp64 sum rounded to BF16, planes added in FP32, one BF16 cast) -- the
+      arithmetic the chapter specifies for the split path; and, against the
+      fp64 C64, the bound that arithmetic implies: 2^-8 per BF16 rounding of
+      every plane and of C.
+  FP32 partial planes or split 1: |C_gpu - C64| <= 0.008 * max(1, |C64|).
 Unpacking, dequantized weights, split plans and the reduce are bit-exact.
 """
 import ctypes
@@ -65,6 +70,32 @@ def _assert_close(got_bits, ref64, tol, what=""):
     bad = np.argwhere(err > lim)
     assert bad.size == 0, "%s: %d elements out of tolerance, first %s err %g lim %g" % (
         what, len(bad), bad[0], err[tuple(bad[0])], lim[tuple(bad[0])])
+
+
+def _check_full(p, got_bits, split, dt, C64, what=""):
+    """Whole-output parity of one call (see the module docstring)."""
+    if split > 1 and dt == Q.QMM_PARTIAL_BF16:
+        emu, planes = oracle.qmm_partitioned(p["A"], p["Wq"], p["scales"], p["biases"], split, 0,
+                                             with_partials=True)
+        _assert_close(got_bits, _val(emu), TOL_BF16, what + " vs BF16-partial emulation")
+        bound = 2.0 ** -8 * (1 + 2.0 ** -7) * (np.abs(planes).sum(axis=0) + np.abs(C64)) \
+            + 1e-4 * np.maximum(1.0, np.abs(C64))
+        err = np.abs(_val(got_bits) - C64)
+        assert np.all(err <= bound), what + ": error above the BF16-partial bound, max excess %g" \
+            % (err - bound).max()
+    else:
+        _assert_close(got_bits, C64, TOL_F32, what)
+
+
+def _check_sampled(p, got_bits, split, dt, rows, cols, what=""):
+    got = got_bits[np.ix_(rows, cols)]
+    if split > 1 and dt == Q.QMM_PARTIAL_BF16:
+        emu = oracle.qmm_partitioned_sampled(p["A"], p["Wq"], p["scales"], p["biases"], rows,
+                                             cols, split, 0)
+        _assert_close(got, _val(emu), TOL_BF16, what + " vs BF16-partial emulation")
+    else:
+        ref = oracle.qmm_sampled(p["A"], p["Wq"], p["scales"], p["biases"], rows, cols)
+        _assert_close(got, ref, TOL_F32, what)
 
 
 def _run(d, M, Nout, split_req=0, pol=None, partial_dtype=Q.QMM_PARTIAL_BF16):
@@ -137,7 +168,7 @@ def test_k_projection_m16_policy_and_unsplit(partial_dtype):
     C64 = oracle.qmm(p["A"], p["Wq"], p["scales"], p["biases"])
     got, s = _run(d, 16, Nout, 0, partial_dtype=partial_dtype)
     assert s > 1, "an under-filled grid must split"
-    _assert_close(got, C64, _tol(s, partial_dtype), "policy")
+    _check_full(p, got, s, partial_dtype, C64, "policy")
     got1, s1 = _run(d, 16, Nout, 1)
     assert s1 == 1
     _assert_close(got1, C64, TOL_F32, "unsplit")
@@ -153,7 +184,7 @@ def test_forced_splits(family, name, splits):
     for s in splits:
         for dt in (Q.QMM_PARTIAL_BF16, Q.QMM_PARTIAL_F32):
             got, used = _run(d, 16, Nout, s, partial_dtype=dt)
-            _assert_close(got, C64, _tol(s, dt), "%s s=%d dt=%d" % (name, s, dt))
+            _check_full(p, got, s, dt, C64, "%s s=%d dt=%d" % (name, s, dt))
 
 
 # ---- every kernel family, ragged tiles -------------------------------------
@@ -167,7 +198,7 @@ def test_families_ragged(family, M):
     for split_req in (0, 1, 2, 5, 10):
         for dt in (Q.QMM_PARTIAL_BF16, Q.QMM_PARTIAL_F32):
             got, s = _run(d, M, Nout, split_req, partial_dtype=dt)
-            _assert_close(got, C64, _tol(s, dt), "M=%d req=%d dt=%d" % (M, split_req, dt))
+            _check_full(p, got, s, dt, C64, "M=%d req=%d dt=%d" % (M, split_req, dt))
 
 
 def test_odd_output_width_scalar_stores():
@@ -177,7 +208,7 @@ def test_odd_output_width_scalar_stores():
     C64 = oracle.qmm(p["A"], p["Wq"], p["scales"], p["biases"])
     for split_req in (1, 2, 4):
         got, s = _run(d, M, Nout, split_req)
-        _assert_close(got, C64, _tol(s, 0), "req=%d" % split_req)
+        _check_full(p, got, s, Q.QMM_PARTIAL_BF16, C64, "req=%d" % split_req)
 
 
 def test_minimum_shape():
@@ -203,13 +234,14 @@ def test_projection_full_size_sampled(name, M):
     d = Q.to_device(p)
     rng = np.random.default_rng(M * 7 + Nout)
     rows, cols = _sample(M, Nout, rng)
-    ref = oracle.qmm_sampled(p["A"], p["Wq"], p["scales"], p["biases"], rows, cols)
     got, s = _run(d, M, Nout, 0)
-    _assert_close(got[np.ix_(rows, cols)], ref, _tol(s, 0), "policy s=%d" % s)
+    _check_sampled(p, got, s, Q.QMM_PARTIAL_BF16, rows, cols, "policy s=%d" % s)
     got1, _ = _run(d, M, Nout, 1)
-    _assert_close(got1[np.ix_(rows, cols)], ref, TOL_F32, "unsplit")
-    # property at every element: split and unsplit agree within both tolerances
-    _assert_close(got, _val(got1), _tol(s, 0) + TOL_F32, "split vs unsplit")
+    _check_sampled(p, got1, 1, Q.QMM_PARTIAL_BF16, rows, cols, "unsplit")
+    # property at every element: split and unsplit agree within the BF16-partial
+    # error the split adds (2^-8 per plane, planes of about |C|/sqrt(s) each)
+    lim = 0.02 * np.maximum(1.0, np.abs(_val(got1))) * max(1.0, np.sqrt(s) / 2)
+    assert np.all(np.abs(_val(got) - _val(got1)) <= lim), "split vs unsplit"
 
 
 def test_fallback_shape_runs_the_unsplit_kernel_exactly():
@@ -235,7 +267,7 @@ def test_decode_regime(family, name, M):
     C64 = oracle.qmm(p["A"], p["Wq"], p["scales"], p["biases"])
     got, s = _run(d, M, Nout, 0)
     assert Kred // s >= 512, "decode splits keep >= 512 reduction elements"
-    _assert_close(got, C64, _tol(s, 0), "s=%d" % s)
+    _check_full(p, got, s, Q.QMM_PARTIAL_BF16, C64, "s=%d" % s)
 
 
 def test_deterministic(family):
