@@ -67,7 +67,7 @@ def _load():
             "oracle_qmm_sampled": [P, P, P, P, I64, I64, I64, P, I64, P, I64, P, I],
             "oracle_qmm_partitioned": [P, P, P, P, I64, I64, I64, I, I, P, P, I],
             "oracle_qmm_partitioned_sampled": [P, P, P, P, I64, I64, I64, P, I64, P, I64, I, I,
-                                               P, I],
+                                               P, P, I],
             "oracle_splitk_plan": [I64, I64, I64, I64, I64, I64, I64, I64, P],
             "oracle_waves": [I64, I64, I64],
             "oracle_gemm": [P, P, I64, I64, I64, P, I],
@@ -180,19 +180,23 @@ def qmm_partitioned(A, Wq, scales, biases, split: int, partial_mode: int = 0,
 
 
 def qmm_partitioned_sampled(A, Wq, scales, biases, rows, cols, split: int,
-                            partial_mode: int = 0, threads: int | None = None) -> np.ndarray:
-    """Partition emulation at sampled elements: BF16 bits [len(rows), len(cols)]."""
+                            partial_mode: int = 0, with_partials: bool = False,
+                            threads: int | None = None):
+    """Partition emulation at sampled elements: BF16 bits [len(rows), len(cols)],
+    and with_partials the plane values [len(rows), len(cols), split]."""
     A, Wq = _c(A, np.uint16), _c(Wq, np.uint32)
     scales, biases = _c(scales, np.uint16), _c(biases, np.uint16)
     rows, cols = _c(rows, np.int64), _c(cols, np.int64)
     M, Kred = A.shape
     nout = Wq.shape[0]
     out = np.empty((rows.size, cols.size), np.uint16)
+    planes = np.empty((rows.size, cols.size, split), np.float64) if with_partials else None
     _check(_load().oracle_qmm_partitioned_sampled(
         _ptr(A), _ptr(Wq), _ptr(scales), _ptr(biases), M, Kred, nout, _ptr(rows), rows.size,
-        _ptr(cols), cols.size, split, partial_mode, _ptr(out), threads or default_threads()),
+        _ptr(cols), cols.size, split, partial_mode, _ptr(out),
+        _ptr(planes) if planes is not None else None, threads or default_threads()),
         "qmm_partitioned_sampled")
-    return out
+    return (out, planes) if with_partials else out
 
 
 def splitk_plan(M, Kred, Nout, bm, bn, target, cap, min_k=128) -> int:

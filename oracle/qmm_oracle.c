@@ -266,12 +266,13 @@ int oracle_qmm_partitioned(const uint16_t *A, const uint32_t *Wq, const uint16_t
 }
 
 /* The partition emulation on a sample: out[i, j] = C_bf16[rows[i], cols[j]]
- * of oracle_qmm_partitioned, computed element by element. */
+ * of oracle_qmm_partitioned, computed element by element; planes (nullable)
+ * receives the split plane values, [nr, nc, split]. */
 int oracle_qmm_partitioned_sampled(const uint16_t *A, const uint32_t *Wq, const uint16_t *scales,
                                    const uint16_t *biases, int64_t M, int64_t Kred, int64_t Nout,
                                    const int64_t *rows, int64_t nr, const int64_t *cols,
                                    int64_t nc, int split, int partial_mode, uint16_t *out,
-                                   int nthreads) {
+                                   double *planes, int nthreads) {
     if (M < 1 || Nout < 1 || Kred < QO_GROUP || Kred % QO_GROUP || nthreads < 1) return -1;
     int64_t G = Kred / QO_GROUP;
     if (split < 1 || G % split || (partial_mode != 0 && partial_mode != 1)) return -1;
@@ -291,7 +292,8 @@ int oracle_qmm_partitioned_sampled(const uint16_t *A, const uint32_t *Wq, const 
         for (int64_t i = 0; i < nr; ++i)
             for (int64_t j = 0; j < nc; ++j)
                 bad |= emulate_element(a + i * Kred, w + j * Kred, Kred, split, partial_mode,
-                                       &out[i * nc + j], NULL) != 0;
+                                       &out[i * nc + j],
+                                       planes ? planes + (i * nc + j) * split : NULL) != 0;
     }
     free(w);
     free(a);

@@ -189,14 +189,12 @@ int* tc_status_ptr();
 
 int launch_gemm_tc(const void* A, const void* W, void* out, int out_mode, int M, int N, int K,
                    int split, void* stream) {
-    const int limit = smem_optin_bytes();
+    static int limit = -1;
     static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [&] {
-        attr_err = cudaFuncSetAttribute(gemm_tc_kernel,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, limit);
+    std::call_once(once, [] {
+        limit = set_max_dynamic_smem(reinterpret_cast<const void*>(gemm_tc_kernel));
     });
-    if (attr_err != cudaSuccess) return attr_err;
+    if (limit < 0) return cudaErrorInvalidValue;
     GemmTcParams p;
     p.out = out;
     p.status = tc_status_ptr();

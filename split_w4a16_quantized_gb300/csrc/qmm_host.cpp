@@ -82,6 +82,17 @@ int smem_optin_bytes() {
     return limit;
 }
 
+int set_max_dynamic_smem(const void* kernel) {
+    const int limit = smem_optin_bytes();
+    cudaFuncAttributes fa;
+    if (limit < 0 || cudaFuncGetAttributes(&fa, kernel) != cudaSuccess) return -1;
+    const int dyn = limit - static_cast<int>(fa.sharedSizeBytes);
+    if (dyn <= 0 ||
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn) != cudaSuccess)
+        return -1;
+    return dyn;
+}
+
 }  // namespace qmm
 
 extern "C" {

@@ -51,6 +51,11 @@ const Family& family_for(int M);
 
 int smem_optin_bytes();
 
+// Raise a kernel's dynamic shared-memory limit to what the device allows next
+// to the kernel's own static shared memory; returns that dynamic limit in
+// bytes, or -1 on failure.
+int set_max_dynamic_smem(const void* kernel);
+
 // Programmatic dependent launch of the library's kernels (qmm_set_pdl).
 bool pdl_enabled();
 struct LaunchAttrs {

@@ -308,13 +308,10 @@ __global__ void probe_kernel(const uint32_t* __restrict__ Wq, const uint16_t* __
 template <class C>
 int launch_cfg(const W4Params& p, int split, cudaStream_t stream) {
     auto kern = w4a16_kernel<C>;
-    const int limit = smem_optin_bytes();
+    static int limit = -1;
     static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [&] {
-        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, limit);
-    });
-    if (attr_err != cudaSuccess) return attr_err;
+    std::call_once(once, [&] { limit = set_max_dynamic_smem(reinterpret_cast<const void*>(kern)); });
+    if (limit < 0) return cudaErrorInvalidValue;
     const size_t smem = static_cast<size_t>(C::FIXED) + static_cast<size_t>(C::BN) * p.gpp * 4;
     if (limit < 0 || smem > static_cast<size_t>(limit)) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};

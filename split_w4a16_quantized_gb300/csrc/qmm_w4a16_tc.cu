@@ -303,13 +303,10 @@ int launch_tc(const void* A, const uint32_t* Wq, const void* scales, const void*
               void* out, int out_mode, int M, int Kred, int Nout, int split, cudaStream_t st) {
     using C = TcCfg<BNA>;
     auto kern = w4a16_tc_kernel<BNA>;
-    const int limit = smem_optin_bytes();
+    static int limit = -1;
     static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [&] {
-        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, limit);
-    });
-    if (attr_err != cudaSuccess) return attr_err;
+    std::call_once(once, [&] { limit = set_max_dynamic_smem(reinterpret_cast<const void*>(kern)); });
+    if (limit < 0) return cudaErrorInvalidValue;
     int* status = tc_status_ptr();
     if (!status) return cudaErrorInvalidSymbol;
 

@@ -227,6 +227,11 @@ def test_partitioned_sampled_matches_full():
             S = oracle.qmm_partitioned_sampled(p["A"], p["Wq"], p["scales"], p["biases"], rows,
                                                cols, s, mode)
             assert np.array_equal(S, C[np.ix_(rows, cols)])
+        _, P = oracle.qmm_partitioned(p["A"], p["Wq"], p["scales"], p["biases"], s, 0,
+                                      with_partials=True)
+        _, Ps = oracle.qmm_partitioned_sampled(p["A"], p["Wq"], p["scales"], p["biases"], rows,
+                                               cols, s, 0, with_partials=True)
+        assert np.array_equal(Ps, np.moveaxis(P, 0, 2)[np.ix_(rows, cols)])
 
 
 def test_partitioned_rejects_nondividing_split():

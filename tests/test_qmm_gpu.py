@@ -72,12 +72,37 @@ def _assert_close(got_bits, ref64, tol, what=""):
         what, len(bad), bad[0], err[tuple(bad[0])], lim[tuple(bad[0])])
 
 
+def _ulp_bf16(x):
+    """One BF16 unit in the last place at |x| (8 significant bits); 0 at 0."""
+    ax = np.abs(x)
+    e = np.floor(np.log2(np.where(ax > 0, ax, 1.0)))
+    return np.where(ax > 0, 2.0 ** (e - 7), 0.0)
+
+
+def _assert_emulated(got_bits, emu_bits, planes, what):
+    """Within 0.02 * max(1, |C_emu|) of the partition emulation, widened per
+    element by one BF16 ulp of each partial plane (planes: [..., split]): the
+    GPU forms each partition sum in FP32 in its own order, so when the exact
+    sum sits within FP32 error of a BF16 rounding boundary the plane may round
+    to the other neighbour -- a one-ulp step that, for planes much larger than
+    their sum, exceeds 0.02 * max(1, |C|) on its own."""
+    emu = _val(emu_bits)
+    got = _val(got_bits)
+    assert np.all(np.isfinite(got)), "non-finite output " + what
+    lim = TOL_BF16 * np.maximum(1.0, np.abs(emu)) + _ulp_bf16(planes).sum(axis=-1)
+    err = np.abs(got - emu)
+    bad = np.argwhere(err > lim)
+    assert bad.size == 0, "%s: %d elements out of tolerance, first %s err %g lim %g" % (
+        what, len(bad), bad[0], err[tuple(bad[0])], lim[tuple(bad[0])])
+
+
 def _check_full(p, got_bits, split, dt, C64, what=""):
     """Whole-output parity of one call (see the module docstring)."""
     if split > 1 and dt == Q.QMM_PARTIAL_BF16:
         emu, planes = oracle.qmm_partitioned(p["A"], p["Wq"], p["scales"], p["biases"], split, 0,
                                              with_partials=True)
-        _assert_close(got_bits, _val(emu), TOL_BF16, what + " vs BF16-partial emulation")
+        _assert_emulated(got_bits, emu, np.moveaxis(planes, 0, -1),
+                         what + " vs BF16-partial emulation")
         bound = 2.0 ** -8 * (1 + 2.0 ** -7) * (np.abs(planes).sum(axis=0) + np.abs(C64)) \
             + 1e-4 * np.maximum(1.0, np.abs(C64))
         err = np.abs(_val(got_bits) - C64)
@@ -90,9 +115,9 @@ def _check_full(p, got_bits, split, dt, C64, what=""):
 def _check_sampled(p, got_bits, split, dt, rows, cols, what=""):
     got = got_bits[np.ix_(rows, cols)]
     if split > 1 and dt == Q.QMM_PARTIAL_BF16:
-        emu = oracle.qmm_partitioned_sampled(p["A"], p["Wq"], p["scales"], p["biases"], rows,
-                                             cols, split, 0)
-        _assert_close(got, _val(emu), TOL_BF16, what + " vs BF16-partial emulation")
+        emu, planes = oracle.qmm_partitioned_sampled(p["A"], p["Wq"], p["scales"], p["biases"],
+                                                     rows, cols, split, 0, with_partials=True)
+        _assert_emulated(got, emu, planes, what + " vs BF16-partial emulation")
     else:
         ref = oracle.qmm_sampled(p["A"], p["Wq"], p["scales"], p["biases"], rows, cols)
         _assert_close(got, ref, TOL_F32, what)
@@ -238,10 +263,12 @@ def test_projection_full_size_sampled(name, M):
     _check_sampled(p, got, s, Q.QMM_PARTIAL_BF16, rows, cols, "policy s=%d" % s)
     got1, _ = _run(d, M, Nout, 1)
     _check_sampled(p, got1, 1, Q.QMM_PARTIAL_BF16, rows, cols, "unsplit")
-    # property at every element: split and unsplit agree within the BF16-partial
-    # error the split adds (2^-8 per plane, planes of about |C|/sqrt(s) each)
-    lim = 0.02 * np.maximum(1.0, np.abs(_val(got1))) * max(1.0, np.sqrt(s) / 2)
-    assert np.all(np.abs(_val(got) - _val(got1)) <= lim), "split vs unsplit"
+    # properties at every element: the split and the unsplit control agree up to
+    # the BF16-partial rounding noise (aggregate) and never differ grossly
+    a, b = _val(got), _val(got1)
+    assert np.all(np.isfinite(a)) and np.all(np.isfinite(b))
+    assert np.linalg.norm(a - b) <= 0.01 * np.linalg.norm(b), "split vs unsplit (L2)"
+    assert np.all(np.abs(a - b) <= 0.25 * np.maximum(1.0, np.abs(b))), "split vs unsplit (max)"
 
 
 def test_fallback_shape_runs_the_unsplit_kernel_exactly():
