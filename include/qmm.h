@@ -34,8 +34,9 @@
  *     returns an error code and launches nothing.  A launch failure returns
  *     QMM_ECUDA.  Nothing aborts, traps or prints.
  *   - C (and the workspace) must not alias any input.
- *   - Alignment: A, Wq, C, workspace and partial planes 16-byte aligned;
- *     scales and biases 2-byte aligned (QMM_EALIGN otherwise).
+ *   - Alignment: A, Wq, scales, biases, C, workspace and partial planes
+ *     16-byte aligned (QMM_EALIGN otherwise; every allocator hands out at
+ *     least that).
  */
 #ifndef QMM_H
 #define QMM_H

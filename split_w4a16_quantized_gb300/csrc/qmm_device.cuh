@@ -74,6 +74,54 @@ __device__ __forceinline__ uint32_t bf16_pair(uint16_t v) {
     return static_cast<uint32_t>(v) * 0x00010001u;
 }
 
+// Copy one row of a per-group parameter array (scales or biases, BF16
+// [Nout, G], 16-byte-aligned base) for groups [gbeg, gbeg + gpp) into
+// dst[gi * stride].  The row's values are contiguous, so they are fetched as
+// whole 16-byte chunks (up to eight loads in flight per thread, one memory
+// round trip per 64 groups) and unpacked in registers; a chunk that would
+// cross the end of the array is read element by element.  Rows at or past
+// Nout get zeros.
+__device__ __forceinline__ void load_group_row(const uint16_t* __restrict__ src, int Nout, int G,
+                                               int n, int gbeg, int gpp, uint16_t* dst,
+                                               int stride) {
+    if (n >= Nout) {
+        for (int gi = 0; gi < gpp; ++gi) dst[gi * stride] = 0;
+        return;
+    }
+    const size_t total = static_cast<size_t>(Nout) * G;
+    const size_t e0 = static_cast<size_t>(n) * G + gbeg;
+    const size_t a0 = e0 & ~static_cast<size_t>(7);
+    const int off = static_cast<int>(e0 - a0);
+    const int nch = (off + gpp + 7) >> 3;
+    for (int c0 = 0; c0 < nch; c0 += 8) {
+        uint4 v[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const size_t e = a0 + static_cast<size_t>(c0 + c) * 8;
+            if (c0 + c < nch && e + 8 <= total) {
+                v[c] = __ldg(reinterpret_cast<const uint4*>(src + e));
+            } else if (c0 + c < nch) {
+                uint16_t t[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) t[j] = e + j < total ? __ldg(src + e + j) : 0;
+                v[c] = make_uint4(t[0] | (t[1] << 16), t[2] | (t[3] << 16), t[4] | (t[5] << 16),
+                                  t[6] | (t[7] << 16));
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            if (c0 + c >= nch) break;
+            const uint32_t w[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int gi = (c0 + c) * 8 + j - off;
+                if (gi >= 0 && gi < gpp)
+                    dst[gi * stride] = static_cast<uint16_t>(w[j >> 1] >> (16 * (j & 1)));
+            }
+        }
+    }
+}
+
 // m16n8k16 BF16 MMA with FP32 accumulate: d += a (16x16, row) * b (16x8, col)
 __device__ __forceinline__ void mma_bf16_16816(float d[4], const uint32_t a[4], uint32_t b0,
                                                uint32_t b1) {

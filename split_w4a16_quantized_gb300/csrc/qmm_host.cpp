@@ -146,9 +146,8 @@ int qmm_policy_preset(int which, int M, int num_sms, qmm_policy* out) {
         int rc = device_sms(&num_sms);
         if (rc != QMM_OK) return rc;
     }
-    int bm = 0, bn = 0;
-    qmm_kernel_tile(M, &bm, &bn);
-    *out = qmm_policy{bm, bn, qmm::kTargetPerSm * num_sms, qmm::kCap,
+    const qmm::Family& f = qmm::family_for(M);
+    *out = qmm_policy{f.bm, f.bn, f.ctas_per_sm * num_sms, qmm::kCap,
                       M <= qmm::kDecodeMaxM ? qmm::kDecodeMinK : qmm::kGroup};
     return QMM_OK;
 }
@@ -203,8 +202,8 @@ int qmm_w4a16_g128(const void* A, const uint32_t* Wq, const void* scales, const 
     if (partial_dtype != QMM_PARTIAL_BF16 && partial_dtype != QMM_PARTIAL_F32) return QMM_EINVAL;
     if (pol && !policy_ok(pol)) return QMM_EINVAL;
     if (Kred < qmm::kGroup || Kred % qmm::kGroup) return QMM_ESHAPE;
-    if (!aligned(A, 16) || !aligned(Wq, 16) || !aligned(C, 16) || !aligned(scales, 2) ||
-        !aligned(biases, 2))
+    if (!aligned(A, 16) || !aligned(Wq, 16) || !aligned(C, 16) || !aligned(scales, 16) ||
+        !aligned(biases, 16))
         return QMM_EALIGN;
     const qmm::Family fam = qmm::family_for(M);
     if (ceil_div(M, fam.bm) > 65535) return QMM_ESHAPE;

@@ -19,31 +19,34 @@ struct Family {
     int bm;
     int bn;
     int kind;
+    int ctas_per_sm;  // CTAs resident per SM (sets the policy's target of one wave)
 };
 
 // mma.sync kernels with register dequant (qmm_w4a16.cu); keep in step with
 // the template instantiations there.
 constexpr Family kMmaFamilies[] = {
-    {8, 8, 64, kKindMma},
-    {16, 16, 64, kKindMma},
-    {32, 32, 128, kKindMma},
-    {1 << 30, 64, 128, kKindMma},
+    {8, 8, 64, kKindMma, 2},
+    {16, 16, 64, kKindMma, 2},
+    {32, 32, 128, kKindMma, 2},
+    {1 << 30, 64, 128, kKindMma, 2},
 };
 // tcgen05 kernels, dequantized weights in tensor memory (qmm_w4a16_tc.cu);
 // bm is the MMA N (activation rows), bn the MMA M (weight rows).
 constexpr Family kTcFamilies[] = {
-    {16, 16, 128, kKindTc},
-    {32, 32, 128, kKindTc},
-    {64, 64, 128, kKindTc},
-    {128, 128, 128, kKindTc},
-    {1 << 30, 256, 128, kKindTc},
+    {16, 16, 128, kKindTc, 1},
+    {32, 32, 128, kKindTc, 1},
+    {64, 64, 128, kKindTc, 1},
+    {128, 128, 128, kKindTc, 1},
+    {1 << 30, 256, 128, kKindTc, 1},
 };
-// The default table: per M, the family that measured fastest on GB300.
+// The default table: per M, the family that measured fastest on GB300 (the
+// tcgen05 kernels beat the mma.sync ones at every M of the workloads).
 constexpr Family kDefaultFamilies[] = {
-    {8, 8, 64, kKindMma},
-    {16, 16, 64, kKindMma},
-    {32, 32, 128, kKindMma},
-    {1 << 30, 64, 128, kKindMma},
+    {16, 16, 128, kKindTc, 1},
+    {32, 32, 128, kKindTc, 1},
+    {64, 64, 128, kKindTc, 1},
+    {128, 128, 128, kKindTc, 1},
+    {1 << 30, 256, 128, kKindTc, 1},
 };
 
 // Process-wide choice of table (qmm_set_kernels); returns the family for M.
@@ -69,8 +72,8 @@ inline void apply_pdl(cudaLaunchConfig_t& cfg, LaunchAttrs& la) {
     cfg.numAttrs = 1;
 }
 
-// GB300 preset tuning constants: target = kTargetPerSm * SMs CTAs, cap.
-constexpr int kTargetPerSm = 2;
+// GB300 preset tuning constants: target = one wave of the family's CTAs
+// (ctas_per_sm * SMs), cap.
 constexpr int kCap = 16;
 constexpr int kDecodeMaxM = 8;      // M <= this keeps >= kDecodeMinK reduction elements per split
 constexpr int kDecodeMinK = 512;

@@ -81,7 +81,9 @@ __global__ void __launch_bounds__(C::THREADS) w4a16_kernel(const W4Params p) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t* pipe = smem;
     uint8_t* perm = smem + STAGES * C::STAGE;
-    uint32_t* sb = reinterpret_cast<uint32_t*>(smem + C::FIXED);  // [gpp][BN] scale | bias<<16
+    // per-group scales and biases of this CTA's rows: sc[gi * BN + r], bi[...]
+    uint16_t* sc = reinterpret_cast<uint16_t*>(smem + C::FIXED);
+    uint16_t* bi = sc + p.gpp * BN;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g8 = lane >> 2, t4 = lane & 3;
@@ -144,9 +146,8 @@ __global__ void __launch_bounds__(C::THREADS) w4a16_kernel(const W4Params p) {
             for (int h = 0; h < 2; ++h) {
                 const int R = warp * 16 * WT + wt * 16 + g8 + 8 * h;
                 wv[wt][h] = *reinterpret_cast<const uint4*>(ws + R * 64 + t4 * 16);
-                const uint32_t v = sb[i * BN + R];
-                ss[wt][h] = bf16_pair(static_cast<uint16_t>(v & 0xFFFFu));
-                bb[wt][h] = bf16_pair(static_cast<uint16_t>(v >> 16));
+                ss[wt][h] = bf16_pair(sc[i * BN + R]);
+                bb[wt][h] = bf16_pair(bi[i * BN + R]);
             }
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
@@ -184,17 +185,12 @@ __global__ void __launch_bounds__(C::THREADS) w4a16_kernel(const W4Params p) {
         if (s < ngrp) load_stage(s, s);
         cp_async_commit();
     }
-    // scale and bias of this CTA's rows for every group of the partition,
+    // scales and biases of this CTA's rows for every group of the partition,
     // loaded while the first copies are in flight
-    for (int i = tid; i < ngrp * BN; i += C::THREADS) {
-        const int r = i / ngrp, gi = i - r * ngrp, n = n0 + r;
-        uint32_t v = 0;
-        if (n < p.Nout) {
-            const size_t o = static_cast<size_t>(n) * p.G + gbeg + gi;
-            v = static_cast<uint32_t>(__ldg(p.scales + o)) |
-                (static_cast<uint32_t>(__ldg(p.biases + o)) << 16);
-        }
-        sb[gi * BN + r] = v;
+    for (int t = tid; t < 2 * BN; t += C::THREADS) {
+        const int r = t % BN;
+        load_group_row(t < BN ? p.scales : p.biases, p.Nout, p.G, n0 + r, gbeg, ngrp,
+                       (t < BN ? sc : bi) + r, BN);
     }
     cp_async_wait<STAGES - 2>();
     __syncthreads();

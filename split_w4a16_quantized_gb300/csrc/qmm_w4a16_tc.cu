@@ -139,8 +139,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int stages = p.stages;
     uint8_t* aring = base;                                  // stages x ACT_STAGE
     uint8_t* wring = aring + stages * C::ACT_STAGE;         // stages x kWStage
-    uint32_t* sb = reinterpret_cast<uint32_t*>(wring + stages * kWStage);  // gpp x 128
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sb + p.gpp * kWRows);
+    // per-group scales and biases of this CTA's rows: sc[gi * 128 + r], bi[...]
+    uint16_t* sc = reinterpret_cast<uint16_t*>(wring + stages * kWStage);
+    uint16_t* bi = sc + p.gpp * kWRows;
+    uint32_t* sb = reinterpret_cast<uint32_t*>(bi + p.gpp * kWRows);  // end of the tables
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sb);
     uint64_t* full = bars;
     uint64_t* empty = bars + kMaxStages;
     uint64_t* a_full = bars + 2 * kMaxStages;
@@ -219,17 +222,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit(acc_full);
     } else if (warp >= 4) {
         // ---- dequantizers ----
-        // scale | bias << 16 of this CTA's rows for every group, loaded while
-        // the first TMA copies are in flight
-        for (int i = tid - 128; i < ngrp * kWRows; i += kThreads - 128) {
-            const int r = i / ngrp, gi = i - r * ngrp, n = n0 + r;
-            uint32_t v = 0;
-            if (n < p.Nout) {
-                const size_t o = static_cast<size_t>(n) * p.G + gbeg + gi;
-                v = static_cast<uint32_t>(__ldg(p.scales + o)) |
-                    (static_cast<uint32_t>(__ldg(p.biases + o)) << 16);
-            }
-            sb[gi * kWRows + r] = v;
+        // scales (threads 128..255) and biases (256..383) of this CTA's rows for
+        // every group, loaded while the first TMA copies are in flight
+        {
+            const int t = tid - 128, r = t & (kWRows - 1);
+            load_group_row(t < kWRows ? p.scales : p.biases, p.Nout, p.G, n0 + r, gbeg, ngrp,
+                           (t < kWRows ? sc : bi) + r, kWRows);
         }
         asm volatile("bar.sync 1, %0;\n" ::"n"(kThreads - 128) : "memory");
         const int quarter = warp & 3, par = (warp - 4) >> 2;
@@ -245,10 +243,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 wv[c] = *reinterpret_cast<const uint4*>(wr + ((c ^ ((row >> 1) & 3)) << 4));
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
-            const uint32_t v = sb[i * kWRows + row];
             uint32_t w[64];
-            dequant_row_group(wv, bf16_pair(static_cast<uint16_t>(v & 0xFFFFu)),
-                              bf16_pair(static_cast<uint16_t>(v >> 16)), w);
+            dequant_row_group(wv, bf16_pair(sc[i * kWRows + row]), bf16_pair(bi[i * kWRows + row]),
+                              w);
             if (!mbar_wait_warp(&a_empty[ab], ((i >> 1) & 1) ^ 1, abort, p.status)) break;
             const uint32_t ta = tmem + lane_base + C::ACOL + ab * 64;
             tmem_st16(ta + 0, w);
