@@ -7,7 +7,7 @@
 #include <cstdint>
 #include <mutex>
 
-#include "../../include/qmm.h"
+#include "qmm.h"
 #include "qmm_internal.h"
 
 namespace {

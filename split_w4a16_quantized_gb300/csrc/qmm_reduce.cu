@@ -10,7 +10,7 @@
 #include <cstdint>
 #include <mutex>
 
-#include "../../include/qmm.h"
+#include "qmm.h"
 #include "qmm_device.cuh"
 #include "qmm_internal.h"
 

@@ -13,14 +13,20 @@
 //     dequantized operand would otherwise exhaust at HBM rate.
 //   - MMA B operand = activations, BNA rows x 16 k, loaded by TMA into
 //     128-byte-swizzled shared memory (K-major).
-//   - D = FP32 accumulator in tensor memory, 128 lanes x BNA columns.
-// Warp roles (12 warps):
-//   warp 0      TMA producer (one thread): per 128-group one 8 KB weight box
-//               and two activation boxes into a STAGES-deep ring;
-//   warp 1      tensor-memory allocator; one thread issues tcgen05.mma;
-//   warps 4-11  dequantizers, then the epilogue: warp w serves lanes
-//               32*(w%4).. of tensor memory and the groups of parity
-//               (w-4)/4, writing into one of two tensor-memory A buffers.
+//   - D = FP32 accumulators in tensor memory, 128 lanes x BNA columns each.
+// Warp roles (16 warps):
+//   warp 0      TMA producer (one thread): packed weights into a deep ring
+//               the dequantizers release on read, activation tiles into a
+//               ring the MMAs release;
+//   warps 1..N  MMA issuers (N = 3, 2 or 1 by tile width), each owning every
+//               N-th group and its own accumulator; warp 1 also allocates
+//               tensor memory.  An issuing thread spends tens of nanoseconds
+//               per tcgen05.mma, so narrow tiles need several issuers; the
+//               accumulators are added in a fixed order in the epilogue, so
+//               results stay deterministic;
+//   warps 4-15  three dequantizer sets of four warps (warp w serves tensor
+//               memory lanes 32*(w%4).. and every third group), then the
+//               epilogue.
 // Every mbarrier wait is bounded (qmm_sm100.cuh): a wait that runs out sets
 // the status word, the CTA stops issuing work, waits (bounded) for what is in
 // flight, frees its tensor memory and exits.
@@ -68,6 +74,18 @@ bool encode_2d(CUtensorMap* map, CUtensorMapDataType type, const void* ptr, uint
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// rank-dimensional tiled map (dims[0] innermost; strides in bytes of dims 1..)
+bool encode_tiled(CUtensorMap* map, CUtensorMapDataType type, int rank, const void* ptr,
+                  const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
+                  CUtensorMapSwizzle swizzle) {
+    auto fn = tensor_map_encoder();
+    if (!fn) return false;
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    return fn(map, type, static_cast<cuuint32_t>(rank), const_cast<void*>(ptr), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int* tc_status_ptr() {
     static int* ptr = nullptr;
     static std::once_flag once;
@@ -81,28 +99,73 @@ int* tc_status_ptr() {
 
 namespace {
 
-constexpr int kWRows = 128;              // weight rows per CTA (MMA M)
-constexpr int kWStage = kWRows * 64;     // packed weight bytes per group
-constexpr int kMaxStages = 8;
-constexpr int kThreads = 384;
+constexpr int kWRows = 128;            // weight rows per CTA (MMA M)
+constexpr int kWGroup = kWRows * 64;   // packed weight bytes of one group
+constexpr int kMaxWStages = 16;
+constexpr int kMaxActStages = 16;
+constexpr int kMaxAStages = 8;
+constexpr int kDeqSets = 3;            // dequantizer warp sets (4 warps: one per lane quarter)
+constexpr int kCtlWarps = 4;           // producer, MMA issuers, allocator
+constexpr int kThreads = 32 * (kCtlWarps + 4 * kDeqSets);  // 512
+
+// Ring position of group i: stage j = i / gps, slot j % n, phase (j / n) & 1.
+// The divisions use multiply-high by a host-computed reciprocal (exact for
+// the small j of one partition), so the control warps -- which share their
+// schedulers with busy dequantizer warps -- spend few instructions per group.
+struct Ring {
+    int n;          // stages
+    uint32_t magic; // ceil(2^32 / n)
+    int gps_log2;   // groups per stage = 1 << gps_log2
+};
+__device__ __forceinline__ void ring_pos(const Ring& r, int i, int& slot, uint32_t& phase,
+                                         int& within) {
+    const uint32_t j = static_cast<uint32_t>(i) >> r.gps_log2;
+    const uint32_t q = __umulhi(j, r.magic);
+    slot = static_cast<int>(j - q * r.n);
+    phase = q & 1u;
+    within = i & ((1 << r.gps_log2) - 1);
+}
 
 struct TcParams {
     const uint16_t* scales;
     const uint16_t* biases;
     void* out;
     int* status;
-    int M, Kred, Nout, G, gpp, out_mode, stages;
+    int M, Kred, Nout, G, gpp, out_mode;
+    Ring wr, ar;    // weight ring, activation ring (same groups per stage)
 };
 
 template <int BNA>
 struct TcCfg {
     static_assert(BNA % 16 == 0 && BNA >= 16 && BNA <= 256, "MMA N");
-    static constexpr int ACT_BOX = BNA * 128;       // one 64-k activation box
-    static constexpr int ACT_STAGE = 2 * ACT_BOX;   // one 128-group
-    static constexpr int ACOL = BNA < 64 ? 64 : BNA;  // first A-buffer column
-    static constexpr int NEED = ACOL + 2 * 64;
-    static constexpr int TMEM_COLS = NEED <= 128 ? 128 : NEED <= 256 ? 256 : 512;
+    static constexpr int ACT_BOX = BNA * 128;       // one 64-k activation chunk
+    static constexpr int ACT_GROUP = 2 * ACT_BOX;   // one 128-group
+    // MMA issuers, each with its own accumulator: an issuing thread spends
+    // tens of nanoseconds per tcgen05.mma, about the tensor time of an N = 128
+    // MMA, so narrower tiles spread the issue over threads
+    static constexpr int NACC = BNA <= 32 ? 3 : BNA <= 64 ? 2 : 1;
+    static constexpr int DCOLS = NACC * BNA;
+    // tensor memory: accumulators in [0, DCOLS), then A buffers of 64 columns
+    // (one 128-group of weights: 128 lanes x 128 k BF16)
+    static constexpr int ACOL = DCOLS <= 64 ? 64 : (DCOLS + 63) / 64 * 64;
+    // Group i goes to A buffer i % A_STAGES, dequantizer set i % 3 and issuer
+    // i % NACC.  A_STAGES is a multiple of lcm(3, NACC), so every buffer has
+    // one writing set and one issuer, each of which passes every lap of its
+    // barriers: a parity wait is then never satisfied by a completion two laps
+    // old, which a buffer shared round-robin between sets would allow.
+    static constexpr int A_LCM = NACC == 2 ? 6 : 3;
+    static constexpr int A_AVAIL = (512 - ACOL) / 64 < 6 ? (512 - ACOL) / 64 : 6;
+    static constexpr int A_STAGES = A_AVAIL / A_LCM * A_LCM;
+    static constexpr int TMEM_COLS = 512;
     static constexpr uint32_t IDESC = idesc_bf16_f32(kWRows, BNA);
+    // groups per TMA stage: one copy of several groups amortizes the
+    // producer's barrier work over more bytes
+    static constexpr int GPS_LOG2 = BNA <= 32 ? 2 : BNA <= 128 ? 1 : 0;
+    static constexpr int GPS = 1 << GPS_LOG2;
+    static constexpr int W_STAGE = GPS * kWGroup;
+    static constexpr int ACT_STAGE = GPS * ACT_GROUP;
+    static_assert(A_STAGES >= 3 && A_STAGES <= kMaxAStages && A_STAGES % A_LCM == 0, "A ring");
+    static_assert(NACC <= kCtlWarps - 1, "issuer warps");
 };
 
 // pair (q[2c], q[2c+1]) of a packed word as BF16 (128 + q): byte c of x holds
@@ -128,6 +191,224 @@ __device__ __forceinline__ void dequant_row_group(const uint4 wv[4], uint32_t ss
     }
 }
 
+// A ring of n stages of gps groups each, its groups dealt round-robin to
+// `users` consumers (dequantizer sets or MMA issuers), waits by parity: a
+// consumer's wait on lap L of a slot is sound only if it also waited on lap
+// L - 1 of that slot.  That holds when every stage holds a group of every
+// consumer, or when n * gps is a multiple of the consumer count (the stage
+// one lap back then holds the same consumers' groups).
+__host__ __device__ constexpr bool ring_laps_ok(int n, int gps, int users) {
+    return gps >= users || (n * gps) % users == 0;
+}
+
+// Shared-memory carve-up of one CTA (base 1024-aligned).
+struct TcSmem {
+    uint8_t* act;       // ar.n x ACT_STAGE
+    uint8_t* w;         // wr.n x W_STAGE
+    uint64_t* w_full;   // [kMaxWStages]
+    uint64_t* w_empty;
+    uint64_t* act_full; // [kMaxActStages]
+    uint64_t* act_empty;
+    uint64_t* a_full;   // [kMaxAStages]
+    uint64_t* a_empty;
+    uint64_t* acc_full;
+    uint32_t* tmem_slot;
+};
+
+__host__ __device__ constexpr size_t tc_bar_bytes() {
+    return (2 * kMaxWStages + 2 * kMaxActStages + 2 * kMaxAStages + 1) * 8 + 16;
+}
+
+template <int BNA>
+__device__ __forceinline__ TcSmem carve(uint8_t* base, const TcParams& p) {
+    using C = TcCfg<BNA>;
+    TcSmem s;
+    s.act = base;
+    s.w = s.act + p.ar.n * C::ACT_STAGE;
+    uint64_t* b = reinterpret_cast<uint64_t*>(s.w + p.wr.n * C::W_STAGE);
+    s.w_full = b;
+    s.w_empty = b + kMaxWStages;
+    s.act_full = b + 2 * kMaxWStages;
+    s.act_empty = s.act_full + kMaxActStages;
+    s.a_full = s.act_empty + kMaxActStages;
+    s.a_empty = s.a_full + kMaxAStages;
+    s.acc_full = s.a_empty + kMaxAStages;
+    s.tmem_slot = reinterpret_cast<uint32_t*>(s.acc_full + 1);
+    return s;
+}
+
+// Producer (one thread): per stage, one 3-D TMA copy of GPS groups of packed
+// weights into the weight ring (released by the dequantizers as soon as they
+// have read it) and one of the matching activation chunks into the
+// activation ring (released by the MMA commits).  Both rings are polled
+// without blocking, so neither waits behind the other.
+template <int BNA>
+__device__ __forceinline__ void tc_producer(const TcSmem& sm, const TcParams& p,
+                                            const CUtensorMap* wmap, const CUtensorMap* amap,
+                                            int n0, int m0, int gbeg, volatile int* abort) {
+    using C = TcCfg<BNA>;
+    const int nst = (p.gpp + C::GPS - 1) >> C::GPS_LOG2;
+    int jw = 0, ja = 0, sw = 0, sa = 0;
+    uint32_t pw = 0, pa = 0;
+    const unsigned long long t0 = globaltimer_ns();
+    for (uint32_t spin = 0; jw < nst || ja < nst; ++spin) {
+        bool progress = false;
+        if (jw < nst && mbar_probe(&sm.w_empty[sw], pw ^ 1)) {
+            mbar_arrive_expect_tx(&sm.w_full[sw], C::W_STAGE);
+            tma_load_3d(sm.w + sw * C::W_STAGE, wmap, &sm.w_full[sw], 0, n0, gbeg + jw * C::GPS);
+            ++jw;
+            if (++sw == p.wr.n) { sw = 0; pw ^= 1; }
+            progress = true;
+        }
+        if (ja < nst && mbar_probe(&sm.act_empty[sa], pa ^ 1)) {
+            mbar_arrive_expect_tx(&sm.act_full[sa], C::ACT_STAGE);
+            tma_load_3d(sm.act + sa * C::ACT_STAGE, amap, &sm.act_full[sa], 0, m0,
+                        (gbeg + ja * C::GPS) * 2);
+            ++ja;
+            if (++sa == p.ar.n) { sa = 0; pa ^= 1; }
+            progress = true;
+        }
+        if (!progress && (spin & 255u) == 0) {
+            if (*abort) break;
+            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                *abort = 1;
+                atomicExch(p.status, kStatusTimeout);
+                break;
+            }
+        }
+    }
+    if (*abort) {  // let copies in flight land before the CTA exits
+        for (int j = jw > p.wr.n ? jw - p.wr.n : 0; j < jw; ++j)
+            mbar_wait(&sm.w_full[j % p.wr.n], (j / p.wr.n) & 1, nullptr, p.status);
+        for (int j = ja > p.ar.n ? ja - p.ar.n : 0; j < ja; ++j)
+            mbar_wait(&sm.act_full[j % p.ar.n], (j / p.ar.n) & 1, nullptr, p.status);
+    }
+}
+
+// MMA issuer c (one warp, lane 0 issues): groups c, c + NACC, ... into
+// accumulator c.
+template <int BNA>
+__device__ __forceinline__ void tc_issuer(const TcSmem& sm, const TcParams& p, uint32_t tmem,
+                                          int c, int lane, volatile int* abort) {
+    using C = TcCfg<BNA>;
+    const uint32_t d_tm = tmem + c * BNA;
+    for (int i = c; i < p.gpp; i += C::NACC) {
+        int sa, within;
+        uint32_t ph;
+        ring_pos(p.ar, i, sa, ph, within);
+        const int ab = i % C::A_STAGES;
+        if (!mbar_wait_warp(&sm.act_full[sa], ph, abort, p.status)) break;
+        if (!mbar_wait_warp(&sm.a_full[ab], (i / C::A_STAGES) & 1, abort, p.status)) break;
+        tc_fence_after();
+        if (lane == 0) {
+            const uint32_t a_tm = tmem + C::ACOL + ab * 64;
+            const uint32_t b_sm = smem_addr(sm.act + sa * C::ACT_STAGE + within * C::ACT_GROUP);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint64_t bdesc =
+                    sdesc_kmajor_sw128(b_sm + (kk >> 2) * C::ACT_BOX + (kk & 3) * 32);
+                umma_bf16_tmem_a(d_tm, a_tm + kk * 8, bdesc, C::IDESC, (i != c) || kk != 0);
+            }
+            umma_commit(&sm.act_empty[sa]);
+            umma_commit(&sm.a_empty[ab]);
+        }
+        __syncwarp();
+    }
+    if (lane == 0) umma_commit(sm.acc_full);
+}
+
+// Dequantizer warp of lane quarter `quarter` in set `set`: groups set,
+// set + kDeqSets, ...; weight row = 32 * quarter + lane.
+template <int BNA>
+__device__ __forceinline__ void tc_dequant(const TcSmem& sm, const TcParams& p, uint32_t tmem,
+                                           int quarter, int set, int lane, int n0, int gbeg,
+                                           volatile int* abort) {
+    using C = TcCfg<BNA>;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    // this row's scale and bias, fetched one of the set's groups ahead so the
+    // load overlaps the previous group (rows past Nout dequantize to zero)
+    const bool live = n0 + row < p.Nout;
+    const size_t gp = static_cast<size_t>(live ? n0 + row : 0) * p.G + gbeg;
+    uint16_t s_next = 0, b_next = 0;
+    if (live && set < p.gpp) {
+        s_next = __ldg(p.scales + gp + set);
+        b_next = __ldg(p.biases + gp + set);
+    }
+    for (int i = set; i < p.gpp; i += kDeqSets) {
+        const uint16_t s_cur = s_next, b_cur = b_next;
+        if (live && i + kDeqSets < p.gpp) {
+            s_next = __ldg(p.scales + gp + i + kDeqSets);
+            b_next = __ldg(p.biases + gp + i + kDeqSets);
+        }
+        int sw, within;
+        uint32_t ph;
+        ring_pos(p.wr, i, sw, ph, within);
+        const int ab = i % C::A_STAGES;
+        if (!mbar_wait_warp(&sm.w_full[sw], ph, abort, p.status)) break;
+        const uint8_t* wr = sm.w + sw * C::W_STAGE + within * kWGroup + row * 64;
+        uint4 wv[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c)  // 64-byte swizzle of the TMA box
+            wv[c] = *reinterpret_cast<const uint4*>(wr + ((c ^ ((row >> 1) & 3)) << 4));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.w_empty[sw]);
+        uint32_t w[64];
+        dequant_row_group(wv, bf16_pair(s_cur), bf16_pair(b_cur), w);
+        if (!mbar_wait_warp(&sm.a_empty[ab], ((i / C::A_STAGES) & 1) ^ 1, abort, p.status)) break;
+        const uint32_t ta = tmem + lane_base + C::ACOL + ab * 64;
+        tmem_st16(ta + 0, w);
+        tmem_st16(ta + 16, w + 16);
+        tmem_st16(ta + 32, w + 32);
+        tmem_st16(ta + 48, w + 48);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.a_full[ab]);
+    }
+}
+
+// Epilogue of one warp: columns (activation rows) in 16-column chunks c with
+// c % kDeqSets == set; the used accumulators are added in a fixed order.
+template <int BNA>
+__device__ __forceinline__ void tc_epilogue(const TcSmem& sm, const TcParams& p, uint32_t tmem,
+                                            int quarter, int set, int lane, int n0, int m0,
+                                            int part, volatile int* abort) {
+    using C = TcCfg<BNA>;
+    if (!mbar_wait_warp(sm.acc_full, 0, abort, p.status)) return;
+    tc_fence_after();
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    const int n = n0 + quarter * 32 + lane;
+    const int nacc = p.gpp < C::NACC ? p.gpp : C::NACC;  // accumulators that received groups
+    const size_t plane = static_cast<size_t>(part) * p.M * p.Nout;
+    for (int c = set; c < BNA / 16; c += kDeqSets) {
+        uint32_t d[16];
+        tmem_ld16(tmem + lane_base + c * 16, d);
+        tmem_ld_wait();
+        float v[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(d[j]);
+        for (int a = 1; a < nacc; ++a) {
+            tmem_ld16(tmem + lane_base + a * BNA + c * 16, d);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] += __uint_as_float(d[j]);
+        }
+        if (n >= p.Nout) continue;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const int m = m0 + c * 16 + j;
+            if (m < p.M) {
+                const size_t o = plane + static_cast<size_t>(m) * p.Nout + n;
+                if (p.out_mode == kOutBf16)
+                    static_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(v[j]);
+                else
+                    static_cast<float*>(p.out)[o] = v[j];
+            }
+        }
+    }
+}
+
 template <int BNA>
 __global__ void __launch_bounds__(kThreads, 1)
     w4a16_tc_kernel(const __grid_constant__ CUtensorMap wmap,
@@ -136,159 +417,68 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    const int stages = p.stages;
-    uint8_t* aring = base;                                  // stages x ACT_STAGE
-    uint8_t* wring = aring + stages * C::ACT_STAGE;         // stages x kWStage
-    // per-group scales and biases of this CTA's rows: sc[gi * 128 + r], bi[...]
-    uint16_t* sc = reinterpret_cast<uint16_t*>(wring + stages * kWStage);
-    uint16_t* bi = sc + p.gpp * kWRows;
-    uint32_t* sb = reinterpret_cast<uint32_t*>(bi + p.gpp * kWRows);  // end of the tables
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sb);
-    uint64_t* full = bars;
-    uint64_t* empty = bars + kMaxStages;
-    uint64_t* a_full = bars + 2 * kMaxStages;
-    uint64_t* a_empty = a_full + 2;
-    uint64_t* acc_full = a_empty + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+    const TcSmem sm = carve<BNA>(base, p);
     __shared__ int abort_flag;
+    volatile int* abort = &abort_flag;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n0 = blockIdx.x * kWRows, m0 = blockIdx.y * BNA, part = blockIdx.z;
-    const int ngrp = p.gpp, gbeg = part * p.gpp;
-    volatile int* abort = &abort_flag;
+    const int gbeg = part * p.gpp;
 
     pdl_trigger();
     if (tid == 0) {
         abort_flag = 0;
-        for (int s = 0; s < stages; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1 + 4);  // MMA commit + the four dequant warps
+        for (int s = 0; s < p.wr.n; ++s) {
+            mbar_init(&sm.w_full[s], 1);
+            mbar_init(&sm.w_empty[s], 4 * C::GPS);  // four dequant warps per group
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&a_full[b], 4);
-            mbar_init(&a_empty[b], 1);
+        for (int s = 0; s < p.ar.n; ++s) {
+            mbar_init(&sm.act_full[s], 1);
+            mbar_init(&sm.act_empty[s], C::GPS);  // one issuer commit per group
         }
-        mbar_init(acc_full, 1);
+        for (int b = 0; b < C::A_STAGES; ++b) {
+            mbar_init(&sm.a_full[b], 4);
+            mbar_init(&sm.a_empty[b], 1);
+        }
+        mbar_init(sm.acc_full, C::NACC);
         mbar_fence_init();
         tma_prefetch_map(&wmap);
         tma_prefetch_map(&amap);
     }
-    if (warp == 1) {
-        tmem_alloc(tmem_slot, C::TMEM_COLS);
-        tmem_relinquish();
-    }
-    pdl_wait();  // global memory is read only after the previous kernel is done
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
+    pdl_wait();       // global memory is read only after the previous kernel is done
+    __syncthreads();  // barriers initialized; the producer starts at once
+    uint32_t tmem = 0;
+    // warp 1 allocates tensor memory while the first copies are in flight and
+    // hands the address to the issuers and dequantizers through named barrier 2
+    constexpr int kTmemBarThreads = 32 * C::NACC + 32 * 4 * kDeqSets;
 
-    if (warp == 0 && lane == 0) {
-        // ---- TMA producer ----
-        int issued = 0;
-        for (int i = 0; i < ngrp; ++i) {
-            const int s = i % stages;
-            if (!mbar_wait(&empty[s], ((i / stages) & 1) ^ 1, abort, p.status)) break;
-            mbar_arrive_expect_tx(&full[s], kWStage + C::ACT_STAGE);
-            const int g = gbeg + i;
-            tma_load_2d(wring + s * kWStage, &wmap, &full[s], g * 16, n0);
-            tma_load_2d(aring + s * C::ACT_STAGE, &amap, &full[s], g * kGroup, m0);
-            tma_load_2d(aring + s * C::ACT_STAGE + C::ACT_BOX, &amap, &full[s], g * kGroup + 64,
-                        m0);
-            issued = i + 1;
+    if (warp == 0) {
+        if (lane == 0) tc_producer<BNA>(sm, p, &wmap, &amap, n0, m0, gbeg, abort);
+    } else if (warp <= C::NACC) {
+        if (warp == 1) {
+            tmem_alloc(sm.tmem_slot, C::TMEM_COLS);
+            tmem_relinquish();
         }
-        if (*abort) {  // let copies in flight land before the CTA exits
-            const int first = issued > stages ? issued - stages : 0;
-            for (int i = first; i < issued; ++i)
-                mbar_wait(&full[i % stages], (i / stages) & 1, nullptr, p.status);
-        }
-    } else if (warp == 1 && lane == 0) {
-        // ---- MMA issuer ----
-        for (int i = 0; i < ngrp; ++i) {
-            const int s = i % stages, ab = i & 1;
-            if (!mbar_wait(&full[s], (i / stages) & 1, abort, p.status)) break;
-            if (!mbar_wait(&a_full[ab], (i >> 1) & 1, abort, p.status)) break;
-            tc_fence_after();
-            const uint32_t a_tm = tmem + C::ACOL + ab * 64;
-            const uint32_t b_sm = smem_addr(aring + s * C::ACT_STAGE);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint64_t bdesc = sdesc_kmajor_sw128(b_sm + (kk >> 2) * C::ACT_BOX + (kk & 3) * 32);
-                umma_bf16_tmem_a(tmem, a_tm + kk * 8, bdesc, C::IDESC, (i | kk) != 0);
-            }
-            umma_commit(&empty[s]);
-            umma_commit(&a_empty[ab]);
-        }
-        umma_commit(acc_full);
-    } else if (warp >= 4) {
-        // ---- dequantizers ----
-        // scales (threads 128..255) and biases (256..383) of this CTA's rows for
-        // every group, loaded while the first TMA copies are in flight
-        {
-            const int t = tid - 128, r = t & (kWRows - 1);
-            load_group_row(t < kWRows ? p.scales : p.biases, p.Nout, p.G, n0 + r, gbeg, ngrp,
-                           (t < kWRows ? sc : bi) + r, kWRows);
-        }
-        asm volatile("bar.sync 1, %0;\n" ::"n"(kThreads - 128) : "memory");
-        const int quarter = warp & 3, par = (warp - 4) >> 2;
-        const int row = quarter * 32 + lane;
-        const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-        for (int i = par; i < ngrp; i += 2) {
-            const int s = i % stages, ab = i & 1;
-            if (!mbar_wait_warp(&full[s], (i / stages) & 1, abort, p.status)) break;
-            const uint8_t* wr = wring + s * kWStage + row * 64;
-            uint4 wv[4];
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-                wv[c] = *reinterpret_cast<const uint4*>(wr + ((c ^ ((row >> 1) & 3)) << 4));
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
-            uint32_t w[64];
-            dequant_row_group(wv, bf16_pair(sc[i * kWRows + row]), bf16_pair(bi[i * kWRows + row]),
-                              w);
-            if (!mbar_wait_warp(&a_empty[ab], ((i >> 1) & 1) ^ 1, abort, p.status)) break;
-            const uint32_t ta = tmem + lane_base + C::ACOL + ab * 64;
-            tmem_st16(ta + 0, w);
-            tmem_st16(ta + 16, w + 16);
-            tmem_st16(ta + 32, w + 32);
-            tmem_st16(ta + 48, w + 48);
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&a_full[ab]);
-        }
-        // ---- epilogue: D lane = weight row, column = activation row ----
-        if (mbar_wait_warp(acc_full, 0, abort, p.status)) {
-            tc_fence_after();
-            const int n = n0 + row;
-            const size_t plane = static_cast<size_t>(part) * p.M * p.Nout;
-            for (int c = par; c < BNA / 16; c += 2) {
-                uint32_t d[16];
-                tmem_ld16(tmem + lane_base + c * 16, d);
-                tmem_ld_wait();
-                if (n < p.Nout) {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int m = m0 + c * 16 + j;
-                        if (m < p.M) {
-                            const size_t o = plane + static_cast<size_t>(m) * p.Nout + n;
-                            const float f = __uint_as_float(d[j]);
-                            if (p.out_mode == kOutBf16)
-                                static_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(f);
-                            else
-                                static_cast<float*>(p.out)[o] = f;
-                        }
-                    }
-                }
-            }
-        }
+        tc_fence_before();
+        asm volatile("bar.sync 2, %0;\n" ::"n"(kTmemBarThreads) : "memory");
+        tc_fence_after();
+        tmem = *sm.tmem_slot;
+        tc_issuer<BNA>(sm, p, tmem, warp - 1, lane, abort);
+    } else if (warp >= kCtlWarps) {
+        tc_fence_before();
+        asm volatile("bar.sync 2, %0;\n" ::"n"(kTmemBarThreads) : "memory");
+        tc_fence_after();
+        tmem = *sm.tmem_slot;
+        const int quarter = warp & 3, set = (warp - kCtlWarps) >> 2;
+        tc_dequant<BNA>(sm, p, tmem, quarter, set, lane, n0, gbeg, abort);
+        tc_epilogue<BNA>(sm, p, tmem, quarter, set, lane, n0, m0, part, abort);
     }
 
     // ---- teardown: every MMA has finished before tensor memory is freed ----
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
-        if (lane == 0 && *abort) mbar_wait(acc_full, 0, nullptr, p.status);
+        if (lane == 0 && *abort) mbar_wait(sm.acc_full, 0, nullptr, p.status);
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
@@ -318,29 +508,63 @@ int launch_tc(const void* A, const uint32_t* Wq, const void* scales, const void*
     p.G = Kred / kGroup;
     p.gpp = p.G / split;
     p.out_mode = out_mode;
-    // alignment slack + scale/bias table + barriers and tensor-memory slot,
-    // with room for the kernel's few bytes of static shared memory
-    const size_t fixed = 1024 + static_cast<size_t>(p.gpp) * kWRows * 4 +
-                         (2 * kMaxStages + 5) * 8 + 16 + 128;
-    const size_t per_stage = C::ACT_STAGE + kWStage;
-    int stages = kMaxStages;
-    while (stages > 2 && fixed + stages * per_stage > static_cast<size_t>(limit)) --stages;
-    if (fixed + stages * per_stage > static_cast<size_t>(limit)) return cudaErrorInvalidValue;
-    p.stages = stages;
+    // ring depths (stages of GPS groups): the activation ring is shallow,
+    // its stages come from L2; the weight ring carries the HBM stream and
+    // takes the rest of shared memory.  Both depths keep every slot's
+    // consumers passing every lap (ring_laps_ok).
+    const size_t fixed = 1024 + tc_bar_bytes() + 128;
+    const int nst = (p.gpp + C::GPS - 1) / C::GPS;
+    int ast = BNA <= 64 ? 4 : BNA <= 128 ? 3 : 2;
+    if (ast > nst + 1) ast = nst + 1 < 2 ? 2 : nst + 1;
+    int wst = 0;
+    for (; ast >= 2; --ast) {
+        if (!ring_laps_ok(ast, C::GPS, C::NACC)) continue;
+        const long room = static_cast<long>(limit) - static_cast<long>(fixed) -
+                          static_cast<long>(ast) * C::ACT_STAGE;
+        wst = room > 0 ? static_cast<int>(room / C::W_STAGE) : 0;
+        if (wst > kMaxWStages) wst = kMaxWStages;
+        while (wst > 0 && !ring_laps_ok(wst, C::GPS, kDeqSets)) --wst;
+        if (wst >= 3) break;
+    }
+    if (ast < 2 || wst < 3) return cudaErrorInvalidValue;
+    auto ring = [](int n) {
+        Ring r;
+        r.n = n;
+        r.magic = static_cast<uint32_t>((0x100000000ull + n - 1) / n);
+        r.gps_log2 = C::GPS_LOG2;
+        return r;
+    };
+    p.wr = ring(wst);
+    p.ar = ring(ast);
 
     CUtensorMap wmap, amap;
-    if (!encode_2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, Wq, Nout, Kred / 8, 4, kWRows, 16,
-                   CU_TENSOR_MAP_SWIZZLE_64B) ||
-        !encode_2d(&amap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, M, Kred, 2, BNA, 64,
-                   CU_TENSOR_MAP_SWIZZLE_128B))
-        return cudaErrorInvalidValue;
+    // weights as [group][row][16 words] boxes of GPS groups x 128 rows (64-byte
+    // rows, 64-byte swizzle); activations as [64-k chunk][row][64] boxes of
+    // 2*GPS chunks x BNA rows (128-byte swizzle, the MMA's K-major layout)
+    {
+        const cuuint64_t wdims[3] = {16, static_cast<cuuint64_t>(Nout),
+                                     static_cast<cuuint64_t>(Kred / kGroup)};
+        const cuuint64_t wstr[2] = {static_cast<cuuint64_t>(Kred) / 2, 64};
+        const cuuint32_t wbox[3] = {16, kWRows, static_cast<cuuint32_t>(C::GPS)};
+        const cuuint64_t adims[3] = {64, static_cast<cuuint64_t>(M),
+                                     static_cast<cuuint64_t>(Kred / 64)};
+        const cuuint64_t astr[2] = {static_cast<cuuint64_t>(Kred) * 2, 128};
+        const cuuint32_t abox[3] = {64, static_cast<cuuint32_t>(BNA),
+                                    static_cast<cuuint32_t>(2 * C::GPS)};
+        if (!encode_tiled(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, Wq, wdims, wstr, wbox,
+                          CU_TENSOR_MAP_SWIZZLE_64B) ||
+            !encode_tiled(&amap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, A, adims, astr, abox,
+                          CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+    }
 
     cudaLaunchConfig_t cfg = {};
     LaunchAttrs la;
     apply_pdl(cfg, la);
     cfg.gridDim = dim3((Nout + kWRows - 1) / kWRows, (M + BNA - 1) / BNA, split);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = fixed + stages * per_stage;
+    cfg.dynamicSmemBytes = fixed + static_cast<size_t>(ast) * C::ACT_STAGE +
+                           static_cast<size_t>(wst) * C::W_STAGE;
     cfg.stream = st;
     return cudaLaunchKernelEx(&cfg, kern, wmap, amap, p);
 }
