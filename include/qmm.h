@@ -184,6 +184,41 @@ int qmm_kernel_status(int *status, int clear);
 /* Static description of a return code. */
 const char *qmm_strerror(int code);
 
+/* Allocation-free qmm_w4a16_g128.  The tiny-llm split-K chapter has no
+ * counterpart to this call: it exists for callers that cannot allocate
+ * device memory where they run the matmul.
+ *
+ * It computes the same C as qmm_w4a16_g128, with the same arguments
+ * (workspace excepted), split rules, alignment rules, kernels and rounding.
+ * For equal inputs, split and partial_dtype, the result is bitwise equal.
+ * The partial planes live in a fixed buffer of qmm_static_scratch_bytes()
+ * (8 MiB), 256-byte aligned, that is a file-scope __device__ array of the
+ * library.  The call allocates nothing, neither with cudaMalloc nor any
+ * other allocator.
+ *   - Set-up: the first call on a device looks the buffer's address up with
+ *     cudaGetSymbolAddress, with that device current, and caches it. Make
+ *     that first call before any stream capture on the device.
+ *   - Limit: a call whose planes (split * M * Nout * 2 bytes for BF16
+ *     partials, * 4 for FP32) exceed qmm_static_scratch_bytes() returns
+ *     QMM_EWORKSPACE and launches nothing.  The split is the policy's
+ *     (split_req = 0) or the forced one.  Unsplit calls (split 1) use none
+ *     of the buffer.
+ *   - Races: every call on a device shares the one buffer.  Two calls whose
+ *     kernels can overlap on the GPU (different streams without ordering
+ *     between them) race on it and give undefined results.  Calls ordered
+ *     on one stream are safe.
+ *   - Nothing has to start at zero: each call's partition kernel writes
+ *     every element of the planes it uses before its reduce reads them.
+ * Returns the codes of qmm_w4a16_g128.  QMM_ECUDA also covers a failed
+ * address lookup. */
+int qmm_w4a16_g128_noalloc(const void *A, const uint32_t *Wq, const void *scales,
+                           const void *biases, void *C, int M, int Kred, int Nout, int split_req,
+                           const qmm_policy *pol, int partial_dtype, void *stream,
+                           int *split_used);
+
+/* Size in bytes of the fixed partial-plane buffer of qmm_w4a16_g128_noalloc. */
+size_t qmm_static_scratch_bytes(void);
+
 #ifdef __cplusplus
 }
 #endif

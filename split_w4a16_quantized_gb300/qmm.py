@@ -62,6 +62,9 @@ _SIGS = {
     "qmm_set_kernels": (_I, [_I]),
     "qmm_set_pdl": (_I, [_I]),
     "qmm_kernel_status": (_I, [ctypes.POINTER(_I), _I]),
+    "qmm_w4a16_g128_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I,
+                                    ctypes.POINTER(qmm_policy), _I, _P, ctypes.POINTER(_I)]),
+    "qmm_static_scratch_bytes": (_SZ, []),
 }
 
 
@@ -191,6 +194,31 @@ def qmm_w4a16_g128(A: torch.Tensor, Wq: torch.Tensor, scales: torch.Tensor,
         ctypes.byref(pol) if pol is not None else None, ws, ws_bytes, partial_dtype,
         _stream(stream), ctypes.byref(used))
     _check(rc, "qmm_w4a16_g128")
+    return used.value
+
+
+def qmm_static_scratch_bytes() -> int:
+    return int(lib().qmm_static_scratch_bytes())
+
+
+def qmm_w4a16_g128_noalloc(A: torch.Tensor, Wq: torch.Tensor, scales: torch.Tensor,
+                           biases: torch.Tensor, C: torch.Tensor, split_req: int = 0,
+                           pol: qmm_policy | None = None, partial_dtype: int = QMM_PARTIAL_BF16,
+                           stream=None) -> int:
+    """qmm_w4a16_g128 with the partial planes in the library's fixed device
+    buffer (no workspace argument, no allocation); returns the split."""
+    M, Kred = A.shape
+    Nout = Wq.shape[0]
+    if tuple(Wq.shape) != (Nout, Kred // 8) or tuple(C.shape) != (M, Nout) or \
+            tuple(scales.shape) != (Nout, Kred // 128) or tuple(biases.shape) != (Nout, Kred // 128):
+        raise ValueError("qmm_w4a16_g128_noalloc: inconsistent shapes")
+    used = _I(0)
+    rc = lib().qmm_w4a16_g128_noalloc(
+        _dev(A, _BF16, "A"), _dev(Wq, _WORDS, "Wq"), _dev(scales, _BF16, "scales"),
+        _dev(biases, _BF16, "biases"), _dev(C, _BF16, "C"), M, Kred, Nout, split_req,
+        ctypes.byref(pol) if pol is not None else None, partial_dtype, _stream(stream),
+        ctypes.byref(used))
+    _check(rc, "qmm_w4a16_g128_noalloc")
     return used.value
 
 
