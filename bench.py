@@ -61,6 +61,45 @@ def algorithmic(M, Kred, Nout, split, partial_bytes=2):
     return nbytes, 2.0 * M * Nout * Kred
 
 
+def partition_algorithmic(M, Kred, Nout, split, partial_bytes=2):
+    """Algorithmic bytes and flops of the partition kernel alone: packed
+    weights, scales and biases, A, and the partial planes it writes."""
+    G = Kred // 128
+    nbytes = Nout * Kred // 2 + 4 * Nout * G + 2 * M * Kred + partial_bytes * split * M * Nout
+    return nbytes, 2.0 * M * Nout * Kred
+
+
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
+# the partition kernel, from one ncu capture per entry, keyed by the call and
+# a hash of the kernel's sources at capture time: once the sources change the
+# figure no longer describes the kernel and is reported as null.
+NCU_TRAFFIC = {
+    # python bench.py --only down:128 --launch-list --steps 1 --warmup 3 under
+    # ncu --set full -k regex:w4a16_tc -s 2 -c 1: 15.760384 MB read, 0 written
+    ("down", 128, 4): (15760384, "99898f93af84c1c9"),
+}
+TC_SOURCES = ("qmm_w4a16_tc.cu", "qmm_sm100.cuh", "qmm_device.cuh", "qmm_internal.h")
+
+
+def tc_source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for name in TC_SOURCES:
+        with open(os.path.join(ROOT, "split_w4a16_quantized_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def policy_desc():
+    from split_w4a16_quantized_gb300 import qmm as Q
+    parts = []
+    for M in M_LIST:
+        p = Q.qmm_policy_preset(Q.QMM_PRESET_GB300, M)
+        parts.append("M=%d: tile %dx%d, target_blocks %d, cap %d, min_k %d"
+                     % (M, p.bm, p.bn, p.target_blocks, p.cap, p.min_k_per_split))
+    return "GB300 preset (" + "; ".join(parts) + ")"
+
+
 def roofline_time_s(nbytes, flops, peaks):
     t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
     t_tc = flops / (peaks["bf16_tflops"] * 1e12)
@@ -312,10 +351,27 @@ def run_gpu(args, rank, world, local_rank):
                          "roof_frac_unsplit": round(t_roof1 * 1e6 / us_1, 4),
                          "tbps_split": round(nb / us_s / 1e6, 3),
                          "tflops_split": round(fl / us_s / 1e6, 2)})
+    # the dominant call's partition kernel on its own (the roofline's kernel),
+    # and its reduce, on the same planes, cold L2, CUDA events
+    dom_i = max(range(len(per_call)), key=lambda i: per_call[i]["us_split"])
+    name, M, Kred, Nout = wl.calls[dom_i]
+    s = wl.split[dom_i]
+    dom = {"index": dom_i, "split": s}
+    if s > 1:
+        planes = wl.ws[:s * M * Nout * 2].view(torch.bfloat16).view(s, M, Nout)
+
+        def part(j):
+            d = wl.sets[j % wl.R][dom_i]
+            Q.qmm_w4a16_g128_partition(d["A"], d["Wq"], d["scales"], d["biases"], planes, s)
+        dom["us_partition"] = timed_launches(part, reps, flush, stream)
+        dom["us_reduce"] = timed_launches(
+            lambda j: Q.qmm_splitk_reduce(planes, Q.QMM_PARTIAL_BF16, s, M, Nout,
+                                          wl.C[j % wl.R][dom_i]), reps, flush, stream)
     sample = clocks.stop()
     dense = dense_sweep(Q, device, flush, stream, sms) if rank == 0 else None
     e2e = run_e2e(wl, Q, device, stream, min(args.steps, 20))
-    return {"ms": ms, "ms_nopdl": ms_nopdl, "per_call": per_call, "clocks": sample, "wl": wl,
+    return {"ms": ms, "ms_nopdl": ms_nopdl, "per_call": per_call, "dom": dom,
+            "clocks": sample, "wl": wl,
             "peaks": peaks,
             "peak_src": peak_src, "l2": l2, "sms": sms, "dense": dense, "e2e": e2e}
 
@@ -499,31 +555,45 @@ def main():
                               "gpu_launches": args.steps * wl.launches_per_step()}), flush=True)
         return
 
-    dom = max(res["per_call"], key=lambda c: c["us_split"])
+    dc = res["per_call"][res["dom"]["index"]]
     peaks = res["peaks"]
-    if dom["bound"] == "hbm":
-        achieved = dom["bytes"] / dom["us_split"] / 1e3  # GB/s
-        peak, unit = peaks["hbm_gbs"], "GB/s"
-    else:
-        achieved = dom["flops"] / dom["us_split"] / 1e6  # TFLOP/s
-        peak, unit = peaks["bf16_tflops"], "TFLOP/s"
-    bm, bn = 0, 0
     from split_w4a16_quantized_gb300 import qmm as Q
-    bm, bn = Q.qmm_kernel_tile(dom["M"])
-    roof = {"bound": dom["bound"], "achieved": round(achieved, 2), "peak": peak, "unit": unit,
-            "frac": round(achieved / peak, 4), "traffic": None,
-            "peak_source": res["peak_src"] + " (burst)",
-            "kernel": "w4a16_kernel BM=%d BN=%d%s" % (bm, bn, " + reduce" if dom["split"] > 1 else ""),
-            "call": "%s M=%d split=%d" % (dom["proj"], dom["M"], dom["split"]),
-            "per_launch": {"bytes": dom["bytes"], "flops": dom["flops"], "us": dom["us_split"]},
-            "timing": "CUDA events on the launching stream around each of 16 launches, "
-                      "L2 flushed (read of a >2xL2 buffer) before each"}
+    bm, bn = Q.qmm_kernel_tile(dc["M"])
+    split = dc["split"]
+    if split > 1:  # the partition kernel alone
+        nb, fl = partition_algorithmic(dc["M"], dc["Kred"], dc["Nout"], split)
+        us = res["dom"]["us_partition"]
+        kernel = "partition kernel (%s), BM=%d BN=%d, grid %d x %d x %d" % (
+            "tcgen05" if args.kernels != "mma" else "mma.sync", bm, bn,
+            -(-dc["Nout"] // bn), -(-dc["M"] // bm), split)
+    else:
+        nb, fl = algorithmic(dc["M"], dc["Kred"], dc["Nout"], 1)
+        us = dc["us_split"]
+        kernel = "unsplit kernel, BM=%d BN=%d" % (bm, bn)
+    _, bound = roofline_time_s(nb, fl, peaks)
+    if bound == "hbm":
+        achieved, peak, unit = nb / us / 1e3, peaks["hbm_gbs"], "GB/s"
+    else:
+        achieved, peak, unit = fl / us / 1e6, peaks["bf16_tflops"], "TFLOP/s"
+    traffic = None
+    key = (dc["proj"], dc["M"], split)
+    if args.kernels != "mma" and key in NCU_TRAFFIC and NCU_TRAFFIC[key][1] == tc_source_hash():
+        traffic = NCU_TRAFFIC[key][0]
+    roof = {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+            "frac": round(achieved / peak, 4), "traffic": traffic,
+            "peak_source": res["peak_src"] + " (burst)", "kernel": kernel,
+            "call": "%s M=%d Kred=%d Nout=%d split=%d" % (dc["proj"], dc["M"], dc["Kred"],
+                                                        dc["Nout"], split),
+            "per_launch": {"algorithmic_bytes": nb, "flops": fl, "us": round(us, 3)},
+            "reduce_us": round(res["dom"].get("us_reduce", 0.0), 3),
+            "timing": "CUDA events on the launching stream around each of 16 launches of the "
+                      "kernel alone, L2 flushed (read of a >2xL2 buffer) before each"}
     out = {"metric": METRIC, "value": round(value_us, 4), "unit": UNIT, "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": round(res["ms"] / args.steps, 6), "higher_is_better": False,
            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
            "config": {"workload": WORKLOAD, "calls_per_step": ncalls,
-                      "policy": "GB300 preset per M (target_blocks = 2 x SMs, cap 16)",
+                      "policy": policy_desc(),
                       "l2": "inputs larger than L2: %d rotating input sets x %.0f MB (L2 %d MB)"
                             % (wl.R, wl.set_bytes / 2**20, res["l2"] >> 20),
                       "kernels": args.kernels,

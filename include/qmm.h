@@ -129,6 +129,22 @@ int qmm_w4a16_g128(const void *A, const uint32_t *Wq, const void *scales, const 
                    void *workspace, size_t ws_bytes, int partial_dtype, void *stream,
                    int *split_used);
 
+/* The partition kernel of qmm_w4a16_g128 alone (tiny-llm split-K chapter,
+ * Task 2: grid z = partition, each partition writes its own plane, no
+ * atomics): partials[p, m, n] = round(sum over the groups of partition p of
+ * A[m, k] * w[n, k]), FP32 accumulation rounded once to partial_dtype (RNE).
+ * Partition p covers groups [p*G/split, (p+1)*G/split), G = Kred/128.
+ *   split      1 <= split <= G, must divide G (QMM_ESHAPE otherwise); no
+ *              policy is applied (take it from qmm_splitk_plan).
+ *   partials   device buffer [split, M, Nout] of partial_dtype, planes
+ *              contiguous, of at least split*M*Nout*(2 or 4) bytes
+ *              (partials_bytes; QMM_EWORKSPACE when smaller).
+ * qmm_w4a16_g128 with a split > 1 is exactly this call followed by
+ * qmm_splitk_reduce on the same planes.  One kernel launch on `stream`. */
+int qmm_w4a16_g128_partition(const void *A, const uint32_t *Wq, const void *scales,
+                             const void *biases, void *partials, size_t partials_bytes, int M,
+                             int Kred, int Nout, int split, int partial_dtype, void *stream);
+
 /* C[m, n] = BF16(sum_{p=0}^{split-1} partials[p, m, n]), the sum taken in
  * FP32 in ascending p and rounded once (tiny-llm split-K chapter, Task 4:
  * one reduction thread per output element).  partials is [split, M, Nout]

@@ -242,6 +242,30 @@ int qmm_w4a16_g128(const void* A, const uint32_t* Wq, const void* scales, const 
     return rc;
 }
 
+int qmm_w4a16_g128_partition(const void* A, const uint32_t* Wq, const void* scales,
+                             const void* biases, void* partials, size_t partials_bytes, int M,
+                             int Kred, int Nout, int split, int partial_dtype, void* stream) {
+    if (!A || !Wq || !scales || !biases || !partials || M < 1 || Nout < 1 || split < 1)
+        return QMM_EINVAL;
+    if (partial_dtype != QMM_PARTIAL_BF16 && partial_dtype != QMM_PARTIAL_F32) return QMM_EINVAL;
+    if (Kred < qmm::kGroup || Kred % qmm::kGroup) return QMM_ESHAPE;
+    const int G = Kred / qmm::kGroup;
+    if (split > G || G % split != 0 || split > 65535) return QMM_ESHAPE;
+    if (!aligned(A, 16) || !aligned(Wq, 16) || !aligned(partials, 16) || !aligned(scales, 16) ||
+        !aligned(biases, 16))
+        return QMM_EALIGN;
+    const qmm::Family fam = qmm::family_for(M);
+    if (ceil_div(M, fam.bm) > 65535) return QMM_ESHAPE;
+    const size_t need = static_cast<size_t>(split) * static_cast<size_t>(M) *
+                        static_cast<size_t>(Nout) * partial_elem_bytes(partial_dtype);
+    if (partials_bytes < need) return QMM_EWORKSPACE;
+    int rc = check_device();
+    if (rc != QMM_OK) return rc;
+    const int mode = partial_dtype == QMM_PARTIAL_F32 ? qmm::kOutF32 : qmm::kOutBf16;
+    return launched(qmm::launch_w4a16(fam, A, Wq, scales, biases, partials, mode, M, Kred, Nout,
+                                      split, stream));
+}
+
 int qmm_gemm_bf16_splitk(const void* A, const void* W, void* C, int M, int N, int K, int split,
                          void* workspace, size_t ws_bytes, void* stream) {
     if (!A || !W || !C || M < 1 || N < 1 || K < 1 || split < 1) return QMM_EINVAL;

@@ -92,6 +92,16 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity,
 
 // ---- TMA ----------------------------------------------------------------------
 
+// Orders the shared-memory accesses that happen before this point in the
+// generic proxy (ordinary loads and stores, including other threads' accesses
+// made visible through an mbarrier) before the async-proxy accesses this
+// thread issues next (TMA).  A stage read with ordinary loads needs it before
+// TMA refills the stage: the mbarrier hand-off alone does not order the two
+// proxies.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

@@ -254,6 +254,8 @@ __device__ __forceinline__ void tc_producer(const TcSmem& sm, const TcParams& p,
     for (uint32_t spin = 0; jw < nst || ja < nst; ++spin) {
         bool progress = false;
         if (jw < nst && mbar_probe(&sm.w_empty[sw], pw ^ 1)) {
+            // the dequantizers read this stage with ordinary loads
+            fence_proxy_async_smem();
             mbar_arrive_expect_tx(&sm.w_full[sw], C::W_STAGE);
             tma_load_3d(sm.w + sw * C::W_STAGE, wmap, &sm.w_full[sw], 0, n0, gbeg + jw * C::GPS);
             ++jw;
@@ -356,6 +358,8 @@ __device__ __forceinline__ void tc_dequant(const TcSmem& sm, const TcParams& p, 
         uint32_t w[64];
         dequant_row_group(wv, bf16_pair(s_cur), bf16_pair(b_cur), w);
         if (!mbar_wait_warp(&sm.a_empty[ab], ((i / C::A_STAGES) & 1) ^ 1, abort, p.status)) break;
+        // the stores below must follow the MMAs that read this buffer before
+        tc_fence_after();
         const uint32_t ta = tmem + lane_base + C::ACOL + ab * 64;
         tmem_st16(ta + 0, w);
         tmem_st16(ta + 16, w + 16);

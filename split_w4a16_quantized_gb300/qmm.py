@@ -54,6 +54,7 @@ _SIGS = {
     "qmm_w4a16_g128": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, ctypes.POINTER(qmm_policy),
                             _P, _SZ, _I, _P, ctypes.POINTER(_I)]),
     "qmm_splitk_reduce": (_I, [_P, _I, _I, _I, _I, _P, _P]),
+    "qmm_w4a16_g128_partition": (_I, [_P, _P, _P, _P, _P, _SZ, _I, _I, _I, _I, _I, _P]),
     "qmm_gemm_bf16_splitk": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _SZ, _P]),
     "qmm_gemm_workspace_bytes": (_SZ, [_I, _I, _I]),
     "qmm_unpack_probe": (_I, [_P, _I, _I, _P, _P]),
@@ -195,6 +196,25 @@ def qmm_w4a16_g128(A: torch.Tensor, Wq: torch.Tensor, scales: torch.Tensor,
         _stream(stream), ctypes.byref(used))
     _check(rc, "qmm_w4a16_g128")
     return used.value
+
+
+def qmm_w4a16_g128_partition(A: torch.Tensor, Wq: torch.Tensor, scales: torch.Tensor,
+                             biases: torch.Tensor, partials: torch.Tensor, split: int,
+                             partial_dtype: int = QMM_PARTIAL_BF16, stream=None) -> None:
+    """The partition kernel alone: partials [split, M, Nout] (bf16 or float32
+    to match partial_dtype) receives one rounded plane per partition."""
+    M, Kred = A.shape
+    Nout = Wq.shape[0]
+    if tuple(Wq.shape) != (Nout, Kred // 8) or \
+            tuple(scales.shape) != (Nout, Kred // 128) or tuple(biases.shape) != (Nout, Kred // 128):
+        raise ValueError("qmm_w4a16_g128_partition: inconsistent shapes")
+    want = (torch.float32,) if partial_dtype == QMM_PARTIAL_F32 else _BF16
+    rc = lib().qmm_w4a16_g128_partition(
+        _dev(A, _BF16, "A"), _dev(Wq, _WORDS, "Wq"), _dev(scales, _BF16, "scales"),
+        _dev(biases, _BF16, "biases"), _dev(partials, want, "partials"),
+        partials.numel() * partials.element_size(), M, Kred, Nout, split, partial_dtype,
+        _stream(stream))
+    _check(rc, "qmm_w4a16_g128_partition")
 
 
 def qmm_static_scratch_bytes() -> int:

@@ -330,6 +330,74 @@ def test_reduce_bit_exact(split, M, Nout, dt):
     assert np.array_equal(_bits(C), want)
 
 
+# ---- the partition kernel on its own: planes against the oracle -----------
+
+def _partition(d, M, Nout, split, dt):
+    tdt = torch.float32 if dt == Q.QMM_PARTIAL_F32 else torch.bfloat16
+    planes = torch.full((split, M, Nout), float("nan"), dtype=tdt, device="cuda")
+    Q.qmm_w4a16_g128_partition(d["A"], d["Wq"], d["scales"], d["biases"], planes, split, dt)
+    torch.cuda.synchronize()
+    return planes
+
+
+@pytest.mark.parametrize("M,Nout", [(40, 1000), (128, 256), (3, 136)])
+@pytest.mark.parametrize("split", [1, 2, 5, 20])
+@pytest.mark.parametrize("dt", [Q.QMM_PARTIAL_BF16, Q.QMM_PARTIAL_F32])
+def test_partition_planes(family, M, Nout, split, dt):
+    """Each plane is the partition's sum rounded once (BF16 or FP32) -- the
+    oracle's partition emulation of that plane.  The kernel accumulates in
+    FP32 in its own order, so a BF16 plane may sit one BF16 ulp away (the
+    FP32 sum and the exact one on either side of a rounding boundary); both
+    kinds also get 2^-10 * max(1, |plane|) for the FP32 accumulation.  A
+    dropped, doubled or misplaced 128-group moves a plane by far more."""
+    p = inputs.make_w4a16(M, 2560, Nout, seed=50 + split + M)
+    d = Q.to_device(p)
+    got = _partition(d, M, Nout, split, dt).float().cpu().numpy().astype(np.float64)
+    mode = 1 if dt == Q.QMM_PARTIAL_F32 else 0
+    _, want = oracle.qmm_partitioned(p["A"], p["Wq"], p["scales"], p["biases"], split, mode,
+                                     with_partials=True)
+    assert np.all(np.isfinite(got)), "a plane element was not written"
+    lim = 2.0 ** -10 * np.maximum(1.0, np.abs(want))
+    if dt == Q.QMM_PARTIAL_BF16:
+        lim = lim + _ulp_bf16(want)
+    err = np.abs(got - want)
+    bad = np.argwhere(err > lim)
+    assert bad.size == 0, "%d plane elements out of tolerance, first %s err %g lim %g" % (
+        len(bad), bad[0], err[tuple(bad[0])], lim[tuple(bad[0])])
+
+
+@pytest.mark.parametrize("name,M", [("k", 16), ("down", 128), ("ragged", 33)])
+@pytest.mark.parametrize("dt", [Q.QMM_PARTIAL_BF16, Q.QMM_PARTIAL_F32])
+def test_partition_then_reduce_is_the_call(family, name, M, dt):
+    """qmm_w4a16_g128 at a split s > 1 is the partition kernel followed by the
+    reduce on the same planes: bitwise the same C."""
+    Kred, Nout = inputs.PROJECTIONS[name] if name != "ragged" else inputs.RAGGED
+    p = inputs.make_w4a16(M, Kred, Nout, seed=60 + M)
+    d = Q.to_device(p)
+    pol = Q.qmm_policy_preset(Q.QMM_PRESET_GB300, M)
+    split = Q.qmm_splitk_plan(M, Kred, Nout, pol)
+    assert split > 1
+    whole, used = _run(d, M, Nout, 0, partial_dtype=dt)
+    assert used == split
+    planes = _partition(d, M, Nout, split, dt)
+    C = torch.empty((M, Nout), dtype=torch.bfloat16, device="cuda")
+    Q.qmm_splitk_reduce(planes, dt, split, M, Nout, C)
+    torch.cuda.synchronize()
+    assert np.array_equal(_bits(C), whole)
+
+
+def test_partition_argument_errors():
+    d = Q.to_device(inputs.make_w4a16(8, 256, 64, seed=1))
+    small = torch.empty((2, 8, 63), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(Q.QmmError) as e:
+        Q.qmm_w4a16_g128_partition(d["A"], d["Wq"], d["scales"], d["biases"], small, 2)
+    assert e.value.code == Q.QMM_EWORKSPACE
+    ok = torch.empty((3, 8, 64), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(Q.QmmError) as e:  # 3 does not divide G = 2
+        Q.qmm_w4a16_g128_partition(d["A"], d["Wq"], d["scales"], d["biases"], ok, 3)
+    assert e.value.code == Q.QMM_ESHAPE
+
+
 # ---- dense BF16 split-K GEMM -----------------------------------------------
 
 @pytest.fixture(scope="module")
