@@ -48,12 +48,19 @@ __global__ void __launch_bounds__(256) reduce_vec8(const T* __restrict__ partial
         float acc[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[j] = 0.f;
-#pragma unroll 4
-        for (int p = 0; p < split; ++p) {
-            float v[8];
-            load8(partials + p * plane + i * 8, v);
+        // up to eight planes' loads in flight at once, then added in
+        // ascending plane order (the sum's order does not change)
+        for (int p0 = 0; p0 < split; p0 += 8) {
+            float v[8][8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) acc[j] += v[j];
+            for (int q = 0; q < 8; ++q)
+                if (p0 + q < split) load8(partials + (p0 + q) * plane + i * 8, v[q]);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                if (p0 + q < split) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) acc[j] += v[q][j];
+                }
         }
         uint4 o;
         o.x = pack_bf16x2(acc[0], acc[1]);

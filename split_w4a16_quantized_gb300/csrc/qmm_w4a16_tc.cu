@@ -104,9 +104,7 @@ constexpr int kWGroup = kWRows * 64;   // packed weight bytes of one group
 constexpr int kMaxWStages = 16;
 constexpr int kMaxActStages = 16;
 constexpr int kMaxAStages = 8;
-constexpr int kDeqSets = 3;            // dequantizer warp sets (4 warps: one per lane quarter)
 constexpr int kCtlWarps = 4;           // producer, MMA issuers, allocator
-constexpr int kThreads = 32 * (kCtlWarps + 4 * kDeqSets);  // 512
 
 // Ring position of group i: stage j = i / gps, slot j % n, phase (j / n) & 1.
 // The divisions use multiply-high by a host-computed reciprocal (exact for
@@ -132,8 +130,13 @@ struct TcParams {
     void* out;
     int* status;
     int M, Kred, Nout, G, gpp, out_mode;
+    int tma_store;  // 1: the output tile leaves through a TMA store of a staged tile
+    int wtail;      // groups in the last weight stage when gpp % WGPS != 0, else 0
+    int atail;      // groups in the last activation stage when gpp % AGPS != 0, else 0
     Ring wr, ar;    // weight ring, activation ring (same groups per stage)
 };
+
+constexpr int ct_gcd(int a, int b) { return b == 0 ? a : ct_gcd(b, a % b); }
 
 template <int BNA>
 struct TcCfg {
@@ -142,29 +145,41 @@ struct TcCfg {
     static constexpr int ACT_GROUP = 2 * ACT_BOX;   // one 128-group
     // MMA issuers, each with its own accumulator: an issuing thread spends
     // tens of nanoseconds per tcgen05.mma, about the tensor time of an N = 128
-    // MMA, so narrower tiles spread the issue over threads
-    static constexpr int NACC = BNA <= 32 ? 3 : BNA <= 64 ? 2 : 1;
+    // MMA, so tiles up to N = 128 spread the issue over threads
+    static constexpr int NACC = BNA <= 32 ? 3 : BNA <= 128 ? 2 : 1;
+    // dequantizer warp sets of four warps (one per tensor-memory lane
+    // quarter); wide tiles spend more tensor time per group, so two sets keep
+    // up and leave tensor memory for two-deep A buffers per set
+    static constexpr int DSETS = BNA <= 64 ? 3 : 2;
+    static constexpr int THREADS = 32 * (kCtlWarps + 4 * DSETS);
     static constexpr int DCOLS = NACC * BNA;
     // tensor memory: accumulators in [0, DCOLS), then A buffers of 64 columns
     // (one 128-group of weights: 128 lanes x 128 k BF16)
     static constexpr int ACOL = DCOLS <= 64 ? 64 : (DCOLS + 63) / 64 * 64;
-    // Group i goes to A buffer i % A_STAGES, dequantizer set i % 3 and issuer
-    // i % NACC.  A_STAGES is a multiple of lcm(3, NACC), so every buffer has
-    // one writing set and one issuer, each of which passes every lap of its
-    // barriers: a parity wait is then never satisfied by a completion two laps
-    // old, which a buffer shared round-robin between sets would allow.
-    static constexpr int A_LCM = NACC == 2 ? 6 : 3;
+    // Group i goes to A buffer i % A_STAGES, dequantizer set i % DSETS and
+    // issuer i % NACC.  A_STAGES is a multiple of lcm(DSETS, NACC), so every
+    // buffer has one writing set and one issuer, each of which passes every
+    // lap of its barriers: a parity wait is then never satisfied by a
+    // completion two laps old, which a buffer shared round-robin between sets
+    // would allow.
+    static constexpr int A_LCM = DSETS / ct_gcd(DSETS, NACC) * NACC;
     static constexpr int A_AVAIL = (512 - ACOL) / 64 < 6 ? (512 - ACOL) / 64 : 6;
     static constexpr int A_STAGES = A_AVAIL / A_LCM * A_LCM;
     static constexpr int TMEM_COLS = 512;
     static constexpr uint32_t IDESC = idesc_bf16_f32(kWRows, BNA);
     // groups per TMA stage: one copy of several groups amortizes the
     // producer's barrier work over more bytes
-    static constexpr int GPS_LOG2 = BNA <= 32 ? 2 : BNA <= 128 ? 1 : 0;
-    static constexpr int GPS = 1 << GPS_LOG2;
-    static constexpr int W_STAGE = GPS * kWGroup;
-    static constexpr int ACT_STAGE = GPS * ACT_GROUP;
-    static_assert(A_STAGES >= 3 && A_STAGES <= kMaxAStages && A_STAGES % A_LCM == 0, "A ring");
+    // (weight stages of four groups: the producer's proxy fence and copy
+    // are paid once per four groups; activation stages are as small as the
+    // activation ring's depth needs)
+    static constexpr int WGPS_LOG2 = 2;
+    static constexpr int WGPS = 1 << WGPS_LOG2;
+    static constexpr int AGPS_LOG2 = BNA <= 32 ? 2 : BNA <= 64 ? 1 : 0;
+    static constexpr int AGPS = 1 << AGPS_LOG2;
+    static constexpr int W_STAGE = WGPS * kWGroup;
+    static constexpr int ACT_STAGE = AGPS * ACT_GROUP;
+    static_assert(A_STAGES >= DSETS && A_STAGES <= kMaxAStages && A_STAGES % A_LCM == 0,
+                  "A ring");
     static_assert(NACC <= kCtlWarps - 1, "issuer warps");
 };
 
@@ -237,35 +252,44 @@ __device__ __forceinline__ TcSmem carve(uint8_t* base, const TcParams& p) {
     return s;
 }
 
-// Producer (one thread): per stage, one 3-D TMA copy of GPS groups of packed
+// Producer (one thread): per stage, one 3-D TMA copy of WGPS groups of packed
 // weights into the weight ring (released by the dequantizers as soon as they
-// have read it) and one of the matching activation chunks into the
-// activation ring (released by the MMA commits).  Both rings are polled
-// without blocking, so neither waits behind the other.
+// have read it) and, per AGPS groups, one of the matching activation chunks
+// into the activation ring (released by the MMA commits).  Both rings are
+// polled without blocking, so neither waits behind the other.
 template <int BNA>
 __device__ __forceinline__ void tc_producer(const TcSmem& sm, const TcParams& p,
                                             const CUtensorMap* wmap, const CUtensorMap* amap,
+                                            const CUtensorMap* wmap_t, const CUtensorMap* amap_t,
                                             int n0, int m0, int gbeg, volatile int* abort) {
     using C = TcCfg<BNA>;
-    const int nst = (p.gpp + C::GPS - 1) >> C::GPS_LOG2;
+    const int nw = (p.gpp + C::WGPS - 1) >> C::WGPS_LOG2;
+    const int na = (p.gpp + C::AGPS - 1) >> C::AGPS_LOG2;
+    // a last stage of a ring's tail groups goes through its tail map, whose
+    // box holds exactly those groups: no bytes beyond the partition are loaded
+    const int wlast = p.wtail ? nw - 1 : nw;
+    const int alast = p.atail ? na - 1 : na;
     int jw = 0, ja = 0, sw = 0, sa = 0;
     uint32_t pw = 0, pa = 0;
     const unsigned long long t0 = globaltimer_ns();
-    for (uint32_t spin = 0; jw < nst || ja < nst; ++spin) {
+    for (uint32_t spin = 0; jw < nw || ja < na; ++spin) {
         bool progress = false;
-        if (jw < nst && mbar_probe(&sm.w_empty[sw], pw ^ 1)) {
+        if (jw < nw && mbar_probe(&sm.w_empty[sw], pw ^ 1)) {
             // the dequantizers read this stage with ordinary loads
             fence_proxy_async_smem();
-            mbar_arrive_expect_tx(&sm.w_full[sw], C::W_STAGE);
-            tma_load_3d(sm.w + sw * C::W_STAGE, wmap, &sm.w_full[sw], 0, n0, gbeg + jw * C::GPS);
+            const bool t = jw == wlast;
+            mbar_arrive_expect_tx(&sm.w_full[sw], t ? p.wtail * kWGroup : C::W_STAGE);
+            tma_load_3d(sm.w + sw * C::W_STAGE, t ? wmap_t : wmap, &sm.w_full[sw], 0, n0,
+                        gbeg + jw * C::WGPS);
             ++jw;
             if (++sw == p.wr.n) { sw = 0; pw ^= 1; }
             progress = true;
         }
-        if (ja < nst && mbar_probe(&sm.act_empty[sa], pa ^ 1)) {
-            mbar_arrive_expect_tx(&sm.act_full[sa], C::ACT_STAGE);
-            tma_load_3d(sm.act + sa * C::ACT_STAGE, amap, &sm.act_full[sa], 0, m0,
-                        (gbeg + ja * C::GPS) * 2);
+        if (ja < na && mbar_probe(&sm.act_empty[sa], pa ^ 1)) {
+            const bool t = ja == alast;
+            mbar_arrive_expect_tx(&sm.act_full[sa], t ? p.atail * C::ACT_GROUP : C::ACT_STAGE);
+            tma_load_3d(sm.act + sa * C::ACT_STAGE, t ? amap_t : amap, &sm.act_full[sa], 0, m0,
+                        (gbeg + ja * C::AGPS) * 2);
             ++ja;
             if (++sa == p.ar.n) { sa = 0; pa ^= 1; }
             progress = true;
@@ -287,11 +311,10 @@ __device__ __forceinline__ void tc_producer(const TcSmem& sm, const TcParams& p,
     }
 }
 
-// MMA issuer c (one warp, lane 0 issues): groups c, c + NACC, ... into
-// accumulator c.
+// MMA issuer c (one thread): groups c, c + NACC, ... into accumulator c.
 template <int BNA>
 __device__ __forceinline__ void tc_issuer(const TcSmem& sm, const TcParams& p, uint32_t tmem,
-                                          int c, int lane, volatile int* abort) {
+                                          int c, volatile int* abort) {
     using C = TcCfg<BNA>;
     const uint32_t d_tm = tmem + c * BNA;
     for (int i = c; i < p.gpp; i += C::NACC) {
@@ -299,28 +322,26 @@ __device__ __forceinline__ void tc_issuer(const TcSmem& sm, const TcParams& p, u
         uint32_t ph;
         ring_pos(p.ar, i, sa, ph, within);
         const int ab = i % C::A_STAGES;
-        if (!mbar_wait_warp(&sm.act_full[sa], ph, abort, p.status)) break;
-        if (!mbar_wait_warp(&sm.a_full[ab], (i / C::A_STAGES) & 1, abort, p.status)) break;
+        if (!mbar_wait(&sm.act_full[sa], ph, abort, p.status)) break;
+        if (!mbar_wait(&sm.a_full[ab], (i / C::A_STAGES) & 1, abort, p.status)) break;
         tc_fence_after();
-        if (lane == 0) {
-            const uint32_t a_tm = tmem + C::ACOL + ab * 64;
-            const uint32_t b_sm = smem_addr(sm.act + sa * C::ACT_STAGE + within * C::ACT_GROUP);
+        const uint32_t a_tm = tmem + C::ACOL + ab * 64;
+        const uint64_t b0 =
+            sdesc_kmajor_sw128(smem_addr(sm.act + sa * C::ACT_STAGE + within * C::ACT_GROUP));
+        const uint32_t acc = i != c;
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint64_t bdesc =
-                    sdesc_kmajor_sw128(b_sm + (kk >> 2) * C::ACT_BOX + (kk & 3) * 32);
-                umma_bf16_tmem_a(d_tm, a_tm + kk * 8, bdesc, C::IDESC, (i != c) || kk != 0);
-            }
-            umma_commit(&sm.act_empty[sa]);
-            umma_commit(&sm.a_empty[ab]);
-        }
-        __syncwarp();
+        for (int kk = 0; kk < 8; ++kk)  // k step of 16: +32 bytes in the swizzle atom
+            umma_bf16_tmem_a(d_tm, a_tm + kk * 8,
+                             b0 + ((((kk >> 2) * C::ACT_BOX) + (kk & 3) * 32) >> 4), C::IDESC,
+                             acc | (kk != 0));
+        umma_commit(&sm.act_empty[sa]);
+        umma_commit(&sm.a_empty[ab]);
     }
-    if (lane == 0) umma_commit(sm.acc_full);
+    umma_commit(sm.acc_full);
 }
 
 // Dequantizer warp of lane quarter `quarter` in set `set`: groups set,
-// set + kDeqSets, ...; weight row = 32 * quarter + lane.
+// set + DSETS, ...; weight row = 32 * quarter + lane.
 template <int BNA>
 __device__ __forceinline__ void tc_dequant(const TcSmem& sm, const TcParams& p, uint32_t tmem,
                                            int quarter, int set, int lane, int n0, int gbeg,
@@ -337,11 +358,11 @@ __device__ __forceinline__ void tc_dequant(const TcSmem& sm, const TcParams& p, 
         s_next = __ldg(p.scales + gp + set);
         b_next = __ldg(p.biases + gp + set);
     }
-    for (int i = set; i < p.gpp; i += kDeqSets) {
+    for (int i = set; i < p.gpp; i += C::DSETS) {
         const uint16_t s_cur = s_next, b_cur = b_next;
-        if (live && i + kDeqSets < p.gpp) {
-            s_next = __ldg(p.scales + gp + i + kDeqSets);
-            b_next = __ldg(p.biases + gp + i + kDeqSets);
+        if (live && i + C::DSETS < p.gpp) {
+            s_next = __ldg(p.scales + gp + i + C::DSETS);
+            b_next = __ldg(p.biases + gp + i + C::DSETS);
         }
         int sw, within;
         uint32_t ph;
@@ -373,50 +394,84 @@ __device__ __forceinline__ void tc_dequant(const TcSmem& sm, const TcParams& p, 
 }
 
 // Epilogue of one warp: columns (activation rows) in 16-column chunks c with
-// c % kDeqSets == set; the used accumulators are added in a fixed order.
+// c % DSETS == set; the used accumulators are added in a fixed order.  With
+// p.tma_store the tile is staged in shared memory as [m][n] (the activation
+// ring, idle once every MMA has completed) and leaves in one TMA store, which
+// also clips rows past M and columns past Nout; otherwise each thread stores
+// its column's values directly.
 template <int BNA>
 __device__ __forceinline__ void tc_epilogue(const TcSmem& sm, const TcParams& p, uint32_t tmem,
-                                            int quarter, int set, int lane, int n0, int m0,
-                                            int part, volatile int* abort) {
+                                            const CUtensorMap* omap, int quarter, int set,
+                                            int lane, int n0, int m0, int part,
+                                            volatile int* abort) {
     using C = TcCfg<BNA>;
-    if (!mbar_wait_warp(sm.acc_full, 0, abort, p.status)) return;
-    tc_fence_after();
-    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    const int n = n0 + quarter * 32 + lane;
-    const int nacc = p.gpp < C::NACC ? p.gpp : C::NACC;  // accumulators that received groups
-    const size_t plane = static_cast<size_t>(part) * p.M * p.Nout;
-    for (int c = set; c < BNA / 16; c += kDeqSets) {
-        uint32_t d[16];
-        tmem_ld16(tmem + lane_base + c * 16, d);
-        tmem_ld_wait();
-        float v[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(d[j]);
-        for (int a = 1; a < nacc; ++a) {
-            tmem_ld16(tmem + lane_base + a * BNA + c * 16, d);
+    const bool ok = mbar_wait_warp(sm.acc_full, 0, abort, p.status);
+    if (ok) {
+        tc_fence_after();
+        const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+        const int r = quarter * 32 + lane;  // row of the weight tile
+        const int n = n0 + r;
+        const int nacc = p.gpp < C::NACC ? p.gpp : C::NACC;  // accumulators that received groups
+        const size_t plane = static_cast<size_t>(part) * p.M * p.Nout;
+        for (int c = set; c < BNA / 16; c += C::DSETS) {
+            uint32_t d[16];
+            tmem_ld16(tmem + lane_base + c * 16, d);
             tmem_ld_wait();
+            float v[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] += __uint_as_float(d[j]);
-        }
-        if (n >= p.Nout) continue;
+            for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(d[j]);
+            for (int a = 1; a < nacc; ++a) {
+                tmem_ld16(tmem + lane_base + a * BNA + c * 16, d);
+                tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const int m = m0 + c * 16 + j;
-            if (m < p.M) {
-                const size_t o = plane + static_cast<size_t>(m) * p.Nout + n;
-                if (p.out_mode == kOutBf16)
-                    static_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(v[j]);
-                else
-                    static_cast<float*>(p.out)[o] = v[j];
+                for (int j = 0; j < 16; ++j) v[j] += __uint_as_float(d[j]);
             }
+            if (p.tma_store) {
+                if (p.out_mode == kOutBf16) {
+                    __nv_bfloat16* t = reinterpret_cast<__nv_bfloat16*>(sm.act);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        t[(c * 16 + j) * kWRows + r] = __float2bfloat16_rn(v[j]);
+                } else {
+                    float* t = reinterpret_cast<float*>(sm.act);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) t[(c * 16 + j) * kWRows + r] = v[j];
+                }
+                continue;
+            }
+            if (n >= p.Nout) continue;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int m = m0 + c * 16 + j;
+                if (m < p.M) {
+                    const size_t o = plane + static_cast<size_t>(m) * p.Nout + n;
+                    if (p.out_mode == kOutBf16)
+                        static_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(v[j]);
+                    else
+                        static_cast<float*>(p.out)[o] = v[j];
+                }
+            }
+        }
+    }
+    if (p.tma_store) {
+        // every epilogue warp reaches this barrier, with or without a tile
+        fence_proxy_async_smem();
+        asm volatile("bar.sync 3, %0;\n" ::"n"(128 * C::DSETS) : "memory");
+        if (ok && !*abort && set == 0 && quarter == 0 && lane == 0) {
+            tma_store_3d(omap, sm.act, n0, m0, part);
+            tma_store_commit();
+            tma_store_wait_all();
         }
     }
 }
 
 template <int BNA>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(TcCfg<BNA>::THREADS, 1)
     w4a16_tc_kernel(const __grid_constant__ CUtensorMap wmap,
-                    const __grid_constant__ CUtensorMap amap, const TcParams p) {
+                    const __grid_constant__ CUtensorMap amap,
+                    const __grid_constant__ CUtensorMap wmap_t,
+                    const __grid_constant__ CUtensorMap amap_t,
+                    const __grid_constant__ CUtensorMap omap, const TcParams p) {
     using C = TcCfg<BNA>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>(
@@ -434,11 +489,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         abort_flag = 0;
         for (int s = 0; s < p.wr.n; ++s) {
             mbar_init(&sm.w_full[s], 1);
-            mbar_init(&sm.w_empty[s], 4 * C::GPS);  // four dequant warps per group
+            mbar_init(&sm.w_empty[s], 4 * C::WGPS);  // four dequant warps per group
         }
         for (int s = 0; s < p.ar.n; ++s) {
             mbar_init(&sm.act_full[s], 1);
-            mbar_init(&sm.act_empty[s], C::GPS);  // one issuer commit per group
+            mbar_init(&sm.act_empty[s], C::AGPS);  // one issuer commit per group
         }
         for (int b = 0; b < C::A_STAGES; ++b) {
             mbar_init(&sm.a_full[b], 4);
@@ -449,15 +504,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_map(&wmap);
         tma_prefetch_map(&amap);
     }
+    if (warp == 0) {
+        // The packed weights are a read-only input: this CTA's share is pulled
+        // into L2 while the kernels before it on the stream finish.  L2 is the
+        // point of coherence, so the loads after the wait below still see
+        // anything those kernels wrote.
+        const int nw = (p.gpp + C::WGPS - 1) >> C::WGPS_LOG2;
+        const int wlast = p.wtail ? nw - 1 : nw;
+        for (int j = lane; j < nw; j += 32)
+            tma_prefetch_l2_3d(j == wlast ? &wmap_t : &wmap, 0, n0, gbeg + j * C::WGPS);
+    }
     pdl_wait();       // global memory is read only after the previous kernel is done
     __syncthreads();  // barriers initialized; the producer starts at once
     uint32_t tmem = 0;
     // warp 1 allocates tensor memory while the first copies are in flight and
     // hands the address to the issuers and dequantizers through named barrier 2
-    constexpr int kTmemBarThreads = 32 * C::NACC + 32 * 4 * kDeqSets;
+    constexpr int kTmemBarThreads = 32 * C::NACC + 32 * 4 * C::DSETS;
 
     if (warp == 0) {
-        if (lane == 0) tc_producer<BNA>(sm, p, &wmap, &amap, n0, m0, gbeg, abort);
+        if (lane == 0)
+            tc_producer<BNA>(sm, p, &wmap, &amap, &wmap_t, &amap_t, n0, m0, gbeg, abort);
     } else if (warp <= C::NACC) {
         if (warp == 1) {
             tmem_alloc(sm.tmem_slot, C::TMEM_COLS);
@@ -467,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("bar.sync 2, %0;\n" ::"n"(kTmemBarThreads) : "memory");
         tc_fence_after();
         tmem = *sm.tmem_slot;
-        tc_issuer<BNA>(sm, p, tmem, warp - 1, lane, abort);
+        if (lane == 0) tc_issuer<BNA>(sm, p, tmem, warp - 1, abort);
     } else if (warp >= kCtlWarps) {
         tc_fence_before();
         asm volatile("bar.sync 2, %0;\n" ::"n"(kTmemBarThreads) : "memory");
@@ -475,7 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem = *sm.tmem_slot;
         const int quarter = warp & 3, set = (warp - kCtlWarps) >> 2;
         tc_dequant<BNA>(sm, p, tmem, quarter, set, lane, n0, gbeg, abort);
-        tc_epilogue<BNA>(sm, p, tmem, quarter, set, lane, n0, m0, part, abort);
+        tc_epilogue<BNA>(sm, p, tmem, &omap, quarter, set, lane, n0, m0, part, abort);
     }
 
     // ---- teardown: every MMA has finished before tensor memory is freed ----
@@ -512,65 +578,97 @@ int launch_tc(const void* A, const uint32_t* Wq, const void* scales, const void*
     p.G = Kred / kGroup;
     p.gpp = p.G / split;
     p.out_mode = out_mode;
-    // ring depths (stages of GPS groups): the activation ring is shallow,
+    p.wtail = p.gpp % C::WGPS;
+    p.atail = p.gpp % C::AGPS;
+    // ring depths (stages of WGPS / AGPS groups): the activation ring is shallow,
     // its stages come from L2; the weight ring carries the HBM stream and
     // takes the rest of shared memory.  Both depths keep every slot's
     // consumers passing every lap (ring_laps_ok).
     const size_t fixed = 1024 + tc_bar_bytes() + 128;
-    const int nst = (p.gpp + C::GPS - 1) / C::GPS;
-    int ast = BNA <= 64 ? 4 : BNA <= 128 ? 3 : 2;
+    const int nst = (p.gpp + C::AGPS - 1) / C::AGPS;
+    int ast = BNA <= 64 ? 4 : BNA <= 128 ? 4 : 2;
     if (ast > nst + 1) ast = nst + 1 < 2 ? 2 : nst + 1;
     int wst = 0;
     for (; ast >= 2; --ast) {
-        if (!ring_laps_ok(ast, C::GPS, C::NACC)) continue;
+        if (!ring_laps_ok(ast, C::AGPS, C::NACC)) continue;
         const long room = static_cast<long>(limit) - static_cast<long>(fixed) -
                           static_cast<long>(ast) * C::ACT_STAGE;
         wst = room > 0 ? static_cast<int>(room / C::W_STAGE) : 0;
         if (wst > kMaxWStages) wst = kMaxWStages;
-        while (wst > 0 && !ring_laps_ok(wst, C::GPS, kDeqSets)) --wst;
+        while (wst > 0 && !ring_laps_ok(wst, C::WGPS, C::DSETS)) --wst;
         if (wst >= 3) break;
     }
     if (ast < 2 || wst < 3) return cudaErrorInvalidValue;
-    auto ring = [](int n) {
+    auto ring = [](int n, int gps_log2) {
         Ring r;
         r.n = n;
         r.magic = static_cast<uint32_t>((0x100000000ull + n - 1) / n);
-        r.gps_log2 = C::GPS_LOG2;
+        r.gps_log2 = gps_log2;
         return r;
     };
-    p.wr = ring(wst);
-    p.ar = ring(ast);
+    p.wr = ring(wst, C::WGPS_LOG2);
+    p.ar = ring(ast, C::AGPS_LOG2);
 
-    CUtensorMap wmap, amap;
-    // weights as [group][row][16 words] boxes of GPS groups x 128 rows (64-byte
+    // weights as [group][row][16 words] boxes of WGPS groups x 128 rows (64-byte
     // rows, 64-byte swizzle); activations as [64-k chunk][row][64] boxes of
-    // 2*GPS chunks x BNA rows (128-byte swizzle, the MMA's K-major layout)
+    // 2*AGPS chunks x BNA rows (128-byte swizzle, the MMA's K-major layout).
+    // The tail maps have boxes of the last stage's tail groups.
+    CUtensorMap wmap, amap, wmap_t, amap_t;
     {
         const cuuint64_t wdims[3] = {16, static_cast<cuuint64_t>(Nout),
                                      static_cast<cuuint64_t>(Kred / kGroup)};
         const cuuint64_t wstr[2] = {static_cast<cuuint64_t>(Kred) / 2, 64};
-        const cuuint32_t wbox[3] = {16, kWRows, static_cast<cuuint32_t>(C::GPS)};
         const cuuint64_t adims[3] = {64, static_cast<cuuint64_t>(M),
                                      static_cast<cuuint64_t>(Kred / 64)};
         const cuuint64_t astr[2] = {static_cast<cuuint64_t>(Kred) * 2, 128};
-        const cuuint32_t abox[3] = {64, static_cast<cuuint32_t>(BNA),
-                                    static_cast<cuuint32_t>(2 * C::GPS)};
-        if (!encode_tiled(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, Wq, wdims, wstr, wbox,
-                          CU_TENSOR_MAP_SWIZZLE_64B) ||
-            !encode_tiled(&amap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, A, adims, astr, abox,
-                          CU_TENSOR_MAP_SWIZZLE_128B))
-            return cudaErrorInvalidValue;
+        auto wenc = [&](CUtensorMap* m, int groups) {
+            const cuuint32_t box[3] = {16, kWRows, static_cast<cuuint32_t>(groups)};
+            return encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, Wq, wdims, wstr, box,
+                                CU_TENSOR_MAP_SWIZZLE_64B);
+        };
+        auto aenc = [&](CUtensorMap* m, int groups) {
+            const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(BNA),
+                                       static_cast<cuuint32_t>(2 * groups)};
+            return encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, A, adims, astr, box,
+                                CU_TENSOR_MAP_SWIZZLE_128B);
+        };
+        if (!wenc(&wmap, C::WGPS) || !aenc(&amap, C::AGPS)) return cudaErrorInvalidValue;
+        if (p.wtail ? !wenc(&wmap_t, p.wtail) : false) return cudaErrorInvalidValue;
+        if (p.atail ? !aenc(&amap_t, p.atail) : false) return cudaErrorInvalidValue;
+        if (!p.wtail) wmap_t = wmap;
+        if (!p.atail) amap_t = amap;
+    }
+    // output planes [split][M][Nout] as a 3-D map with a [BNA][128] box; a TMA
+    // store needs 16-byte row pitch, and the staged tile must fit the ring
+    CUtensorMap omap = wmap;
+    {
+        const int elem = out_mode == kOutBf16 ? 2 : 4;
+        const size_t tile = static_cast<size_t>(BNA) * kWRows * elem;
+        p.tma_store = (static_cast<size_t>(Nout) * elem) % 16 == 0 &&
+                      tile <= static_cast<size_t>(ast) * C::ACT_STAGE;
+        if (p.tma_store) {
+            const cuuint64_t odims[3] = {static_cast<cuuint64_t>(Nout), static_cast<cuuint64_t>(M),
+                                         static_cast<cuuint64_t>(split)};
+            const cuuint64_t ostr[2] = {static_cast<cuuint64_t>(Nout) * elem,
+                                        static_cast<cuuint64_t>(M) * Nout * elem};
+            const cuuint32_t obox[3] = {kWRows, static_cast<cuuint32_t>(BNA), 1};
+            if (!encode_tiled(&omap,
+                              out_mode == kOutBf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                   : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                              3, out, odims, ostr, obox, CU_TENSOR_MAP_SWIZZLE_NONE))
+                return cudaErrorInvalidValue;
+        }
     }
 
     cudaLaunchConfig_t cfg = {};
     LaunchAttrs la;
     apply_pdl(cfg, la);
     cfg.gridDim = dim3((Nout + kWRows - 1) / kWRows, (M + BNA - 1) / BNA, split);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(C::THREADS, 1, 1);
     cfg.dynamicSmemBytes = fixed + static_cast<size_t>(ast) * C::ACT_STAGE +
                            static_cast<size_t>(wst) * C::W_STAGE;
     cfg.stream = st;
-    return cudaLaunchKernelEx(&cfg, kern, wmap, amap, p);
+    return cudaLaunchKernelEx(&cfg, kern, wmap, amap, wmap_t, amap_t, omap, p);
 }
 
 }  // namespace
