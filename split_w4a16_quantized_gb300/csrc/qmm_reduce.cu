@@ -17,27 +17,44 @@
 namespace qmm {
 namespace {
 
-__device__ __forceinline__ void load8(const __nv_bfloat16* p, float v[8]) {
-    const uint4 u = __ldcs(reinterpret_cast<const uint4*>(p));
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        v[2 * i] = __uint_as_float(w[i] << 16);
-        v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+// Eight consecutive partial values of one plane: a 16-byte load (BF16) or two
+// (FP32), kept raw until the ordered sum.
+template <typename T>
+struct Raw8;
+template <>
+struct Raw8<__nv_bfloat16> {
+    uint4 u;
+    __device__ __forceinline__ void load(const __nv_bfloat16* p) {
+        u = __ldcs(reinterpret_cast<const uint4*>(p));
     }
-}
-
-__device__ __forceinline__ void load8(const float* p, float v[8]) {
-    const float4 a = __ldcs(reinterpret_cast<const float4*>(p));
-    const float4 b = __ldcs(reinterpret_cast<const float4*>(p) + 1);
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-}
+    __device__ __forceinline__ void add_to(float acc[8]) const {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            acc[2 * i] += __uint_as_float(w[i] << 16);
+            acc[2 * i + 1] += __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+    }
+};
+template <>
+struct Raw8<float> {
+    float4 a, b;
+    __device__ __forceinline__ void load(const float* p) {
+        a = __ldcs(reinterpret_cast<const float4*>(p));
+        b = __ldcs(reinterpret_cast<const float4*>(p) + 1);
+    }
+    __device__ __forceinline__ void add_to(float acc[8]) const {
+        acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+        acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+    }
+};
 
 __device__ __forceinline__ float load1(const __nv_bfloat16* p) { return __bfloat162float(*p); }
 __device__ __forceinline__ float load1(const float* p) { return *p; }
 
-template <typename T>
+// KC planes' loads are in flight at once (KC >= split where possible, so the
+// register footprint -- and the CTAs an SM holds -- follows the split).
+template <typename T, int KC>
 __global__ void __launch_bounds__(256) reduce_vec8(const T* __restrict__ partials, int split,
                                                    int64_t plane, __nv_bfloat16* __restrict__ C) {
     const int64_t nvec = plane / 8;
@@ -48,19 +65,16 @@ __global__ void __launch_bounds__(256) reduce_vec8(const T* __restrict__ partial
         float acc[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[j] = 0.f;
-        // up to eight planes' loads in flight at once, then added in
-        // ascending plane order (the sum's order does not change)
-        for (int p0 = 0; p0 < split; p0 += 8) {
-            float v[8][8];
+        // a chunk of KC planes' loads in flight at once, then the adds in
+        // ascending plane order
+        for (int p0 = 0; p0 < split; p0 += KC) {
+            Raw8<T> r[KC];
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-                if (p0 + q < split) load8(partials + (p0 + q) * plane + i * 8, v[q]);
+            for (int q = 0; q < KC; ++q)
+                if (p0 + q < split) r[q].load(partials + (p0 + q) * plane + i * 8);
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-                if (p0 + q < split) {
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) acc[j] += v[q][j];
-                }
+            for (int q = 0; q < KC; ++q)
+                if (p0 + q < split) r[q].add_to(acc);
         }
         uint4 o;
         o.x = pack_bf16x2(acc[0], acc[1]);
@@ -101,8 +115,9 @@ int launch_typed(const T* partials, int split, int64_t plane, __nv_bfloat16* C,
                  cudaStream_t stream) {
     const bool vec = plane % 8 == 0;
     const int64_t work = vec ? plane / 8 : plane;
+    // one thread per eight outputs (grid-stride beyond 16 CTAs per SM)
     int64_t blocks = (work + 255) / 256;
-    const int64_t max_blocks = static_cast<int64_t>(num_sms()) * 8;
+    const int64_t max_blocks = static_cast<int64_t>(num_sms()) * 16;
     if (blocks > max_blocks) blocks = max_blocks;
     cudaLaunchConfig_t cfg = {};
     LaunchAttrs la;
@@ -110,7 +125,14 @@ int launch_typed(const T* partials, int split, int64_t plane, __nv_bfloat16* C,
     cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
     cfg.blockDim = dim3(256, 1, 1);
     cfg.stream = stream;
-    if (vec) return cudaLaunchKernelEx(&cfg, reduce_vec8<T>, partials, split, plane, C);
+    if (vec) {
+        constexpr int kMax = sizeof(T) == 2 ? 16 : 8;
+        if (split <= 2) return cudaLaunchKernelEx(&cfg, reduce_vec8<T, 2>, partials, split, plane, C);
+        if (split <= 4) return cudaLaunchKernelEx(&cfg, reduce_vec8<T, 4>, partials, split, plane, C);
+        if (split <= 8 || kMax == 8)
+            return cudaLaunchKernelEx(&cfg, reduce_vec8<T, 8>, partials, split, plane, C);
+        return cudaLaunchKernelEx(&cfg, reduce_vec8<T, kMax>, partials, split, plane, C);
+    }
     return cudaLaunchKernelEx(&cfg, reduce_scalar<T>, partials, split, plane, C);
 }
 

@@ -150,9 +150,10 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void*
 __device__ __forceinline__ void tma_store_commit() {
     asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
 }
-// Wait until the committed stores are complete (their writes performed).
-__device__ __forceinline__ void tma_store_wait_all() {
-    asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory");
+// Wait until the committed stores have read their shared-memory source (the
+// global writes complete with the grid, before any dependent grid runs).
+__device__ __forceinline__ void tma_store_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
 }
 
 // ---- tensor memory ------------------------------------------------------------

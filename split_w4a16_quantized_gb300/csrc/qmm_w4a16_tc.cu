@@ -460,7 +460,7 @@ __device__ __forceinline__ void tc_epilogue(const TcSmem& sm, const TcParams& p,
         if (ok && !*abort && set == 0 && quarter == 0 && lane == 0) {
             tma_store_3d(omap, sm.act, n0, m0, part);
             tma_store_commit();
-            tma_store_wait_all();
+            tma_store_wait_read();
         }
     }
 }
@@ -514,21 +514,21 @@ __global__ void __launch_bounds__(TcCfg<BNA>::THREADS, 1)
         for (int j = lane; j < nw; j += 32)
             tma_prefetch_l2_3d(j == wlast ? &wmap_t : &wmap, 0, n0, gbeg + j * C::WGPS);
     }
+    if (warp == 1) {  // tensor memory is not global memory: allocated before the wait
+        tmem_alloc(sm.tmem_slot, C::TMEM_COLS);
+        tmem_relinquish();
+    }
     pdl_wait();       // global memory is read only after the previous kernel is done
     __syncthreads();  // barriers initialized; the producer starts at once
     uint32_t tmem = 0;
-    // warp 1 allocates tensor memory while the first copies are in flight and
-    // hands the address to the issuers and dequantizers through named barrier 2
+    // warp 1's tensor-memory address reaches the issuers and dequantizers
+    // through named barrier 2
     constexpr int kTmemBarThreads = 32 * C::NACC + 32 * 4 * C::DSETS;
 
     if (warp == 0) {
         if (lane == 0)
             tc_producer<BNA>(sm, p, &wmap, &amap, &wmap_t, &amap_t, n0, m0, gbeg, abort);
     } else if (warp <= C::NACC) {
-        if (warp == 1) {
-            tmem_alloc(sm.tmem_slot, C::TMEM_COLS);
-            tmem_relinquish();
-        }
         tc_fence_before();
         asm volatile("bar.sync 2, %0;\n" ::"n"(kTmemBarThreads) : "memory");
         tc_fence_after();
