@@ -101,6 +101,7 @@ namespace {
 
 constexpr int kWRows = 128;            // weight rows per CTA (MMA M)
 constexpr int kWGroup = kWRows * 64;   // packed weight bytes of one group
+constexpr int kWBox = 2 * kWGroup;     // one weight copy: 128 rows x two groups
 constexpr int kMaxWStages = 16;
 constexpr int kMaxActStages = 16;
 constexpr int kMaxAStages = 8;
@@ -252,23 +253,27 @@ __device__ __forceinline__ TcSmem carve(uint8_t* base, const TcParams& p) {
     return s;
 }
 
-// Producer (one thread): per stage, one 3-D TMA copy of WGPS groups of packed
-// weights into the weight ring (released by the dequantizers as soon as they
-// have read it) and, per AGPS groups, one of the matching activation chunks
-// into the activation ring (released by the MMA commits).  Both rings are
-// polled without blocking, so neither waits behind the other.
+// Producer (one thread): per weight stage, two 2-D TMA copies of two groups
+// each (128 rows x 128 bytes, the 128-byte swizzle) into the weight ring
+// (released by the dequantizers as soon as they have read it) and, per AGPS
+// groups, one copy of the matching activation chunks into the activation ring
+// (released by the MMA commits).  Both rings are polled without blocking, so
+// neither waits behind the other.  Weight rows of 128 bytes halve the TMA
+// requests of 64-byte rows; a box that runs past the end of a weight row is
+// zero-filled.
 template <int BNA>
 __device__ __forceinline__ void tc_producer(const TcSmem& sm, const TcParams& p,
                                             const CUtensorMap* wmap, const CUtensorMap* amap,
-                                            const CUtensorMap* wmap_t, const CUtensorMap* amap_t,
-                                            int n0, int m0, int gbeg, volatile int* abort) {
+                                            const CUtensorMap* amap_t, int n0, int m0, int gbeg,
+                                            volatile int* abort) {
     using C = TcCfg<BNA>;
     const int nw = (p.gpp + C::WGPS - 1) >> C::WGPS_LOG2;
     const int na = (p.gpp + C::AGPS - 1) >> C::AGPS_LOG2;
-    // a last stage of a ring's tail groups goes through its tail map, whose
-    // box holds exactly those groups: no bytes beyond the partition are loaded
-    const int wlast = p.wtail ? nw - 1 : nw;
+    // a last activation stage of a tail goes through the tail map, whose box
+    // holds exactly those groups; a last weight stage of one or two groups
+    // takes one two-group box
     const int alast = p.atail ? na - 1 : na;
+    const int wlast_boxes = p.wtail == 0 ? 2 : (p.wtail + 1) >> 1;
     int jw = 0, ja = 0, sw = 0, sa = 0;
     uint32_t pw = 0, pa = 0;
     const unsigned long long t0 = globaltimer_ns();
@@ -277,10 +282,12 @@ __device__ __forceinline__ void tc_producer(const TcSmem& sm, const TcParams& p,
         if (jw < nw && mbar_probe(&sm.w_empty[sw], pw ^ 1)) {
             // the dequantizers read this stage with ordinary loads
             fence_proxy_async_smem();
-            const bool t = jw == wlast;
-            mbar_arrive_expect_tx(&sm.w_full[sw], t ? p.wtail * kWGroup : C::W_STAGE);
-            tma_load_3d(sm.w + sw * C::W_STAGE, t ? wmap_t : wmap, &sm.w_full[sw], 0, n0,
-                        gbeg + jw * C::WGPS);
+            const int boxes = jw == nw - 1 ? wlast_boxes : 2;
+            const int x = (gbeg + jw * C::WGPS) * 16;  // 32-bit words
+            mbar_arrive_expect_tx(&sm.w_full[sw], boxes * kWBox);
+            tma_load_2d(sm.w + sw * C::W_STAGE, wmap, &sm.w_full[sw], x, n0);
+            if (boxes == 2)
+                tma_load_2d(sm.w + sw * C::W_STAGE + kWBox, wmap, &sm.w_full[sw], x + 32, n0);
             ++jw;
             if (++sw == p.wr.n) { sw = 0; pw ^= 1; }
             progress = true;
@@ -369,11 +376,14 @@ __device__ __forceinline__ void tc_dequant(const TcSmem& sm, const TcParams& p, 
         ring_pos(p.wr, i, sw, ph, within);
         const int ab = i % C::A_STAGES;
         if (!mbar_wait_warp(&sm.w_full[sw], ph, abort, p.status)) break;
-        const uint8_t* wr = sm.w + sw * C::W_STAGE + within * kWGroup + row * 64;
+        // box `within / 2`, row of 128 bytes, 16-byte chunks 4*(within % 2) ..
+        // +3 under the 128-byte swizzle (chunk k of row r at k ^ (r % 8))
+        const uint8_t* wr = sm.w + sw * C::W_STAGE + (within >> 1) * kWBox + row * 128;
         uint4 wv[4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c)  // 64-byte swizzle of the TMA box
-            wv[c] = *reinterpret_cast<const uint4*>(wr + ((c ^ ((row >> 1) & 3)) << 4));
+        for (int c = 0; c < 4; ++c)
+            wv[c] = *reinterpret_cast<const uint4*>(
+                wr + ((((within & 1) << 2) + c) ^ (row & 7)) * 16);
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.w_empty[sw]);
         uint32_t w[64];
@@ -469,7 +479,6 @@ template <int BNA>
 __global__ void __launch_bounds__(TcCfg<BNA>::THREADS, 1)
     w4a16_tc_kernel(const __grid_constant__ CUtensorMap wmap,
                     const __grid_constant__ CUtensorMap amap,
-                    const __grid_constant__ CUtensorMap wmap_t,
                     const __grid_constant__ CUtensorMap amap_t,
                     const __grid_constant__ CUtensorMap omap, const TcParams p) {
     using C = TcCfg<BNA>;
@@ -509,10 +518,8 @@ __global__ void __launch_bounds__(TcCfg<BNA>::THREADS, 1)
         // into L2 while the kernels before it on the stream finish.  L2 is the
         // point of coherence, so the loads after the wait below still see
         // anything those kernels wrote.
-        const int nw = (p.gpp + C::WGPS - 1) >> C::WGPS_LOG2;
-        const int wlast = p.wtail ? nw - 1 : nw;
-        for (int j = lane; j < nw; j += 32)
-            tma_prefetch_l2_3d(j == wlast ? &wmap_t : &wmap, 0, n0, gbeg + j * C::WGPS);
+        const int nbox = (p.gpp + 1) >> 1;
+        for (int j = lane; j < nbox; j += 32) tma_prefetch_l2_2d(&wmap, (gbeg + 2 * j) * 16, n0);
     }
     if (warp == 1) {  // tensor memory is not global memory: allocated before the wait
         tmem_alloc(sm.tmem_slot, C::TMEM_COLS);
@@ -527,7 +534,7 @@ __global__ void __launch_bounds__(TcCfg<BNA>::THREADS, 1)
 
     if (warp == 0) {
         if (lane == 0)
-            tc_producer<BNA>(sm, p, &wmap, &amap, &wmap_t, &amap_t, n0, m0, gbeg, abort);
+            tc_producer<BNA>(sm, p, &wmap, &amap, &amap_t, n0, m0, gbeg, abort);
     } else if (warp <= C::NACC) {
         tc_fence_before();
         asm volatile("bar.sync 2, %0;\n" ::"n"(kTmemBarThreads) : "memory");
@@ -609,33 +616,26 @@ int launch_tc(const void* A, const uint32_t* Wq, const void* scales, const void*
     p.wr = ring(wst, C::WGPS_LOG2);
     p.ar = ring(ast, C::AGPS_LOG2);
 
-    // weights as [group][row][16 words] boxes of WGPS groups x 128 rows (64-byte
-    // rows, 64-byte swizzle); activations as [64-k chunk][row][64] boxes of
+    // weights as 2-D [Nout][Kred/8 words] with boxes of 128 rows x 32 words (two
+    // groups, 128-byte swizzle); activations as [64-k chunk][row][64] boxes of
     // 2*AGPS chunks x BNA rows (128-byte swizzle, the MMA's K-major layout).
-    // The tail maps have boxes of the last stage's tail groups.
-    CUtensorMap wmap, amap, wmap_t, amap_t;
+    // The activation tail map has a box of the last stage's tail groups.
+    CUtensorMap wmap, amap, amap_t;
     {
-        const cuuint64_t wdims[3] = {16, static_cast<cuuint64_t>(Nout),
-                                     static_cast<cuuint64_t>(Kred / kGroup)};
-        const cuuint64_t wstr[2] = {static_cast<cuuint64_t>(Kred) / 2, 64};
         const cuuint64_t adims[3] = {64, static_cast<cuuint64_t>(M),
                                      static_cast<cuuint64_t>(Kred / 64)};
         const cuuint64_t astr[2] = {static_cast<cuuint64_t>(Kred) * 2, 128};
-        auto wenc = [&](CUtensorMap* m, int groups) {
-            const cuuint32_t box[3] = {16, kWRows, static_cast<cuuint32_t>(groups)};
-            return encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, Wq, wdims, wstr, box,
-                                CU_TENSOR_MAP_SWIZZLE_64B);
-        };
         auto aenc = [&](CUtensorMap* m, int groups) {
             const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(BNA),
                                        static_cast<cuuint32_t>(2 * groups)};
             return encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, A, adims, astr, box,
                                 CU_TENSOR_MAP_SWIZZLE_128B);
         };
-        if (!wenc(&wmap, C::WGPS) || !aenc(&amap, C::AGPS)) return cudaErrorInvalidValue;
-        if (p.wtail ? !wenc(&wmap_t, p.wtail) : false) return cudaErrorInvalidValue;
+        if (!encode_2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, Wq, Nout, Kred / 8, 4, kWRows, 32,
+                       CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !aenc(&amap, C::AGPS))
+            return cudaErrorInvalidValue;
         if (p.atail ? !aenc(&amap_t, p.atail) : false) return cudaErrorInvalidValue;
-        if (!p.wtail) wmap_t = wmap;
         if (!p.atail) amap_t = amap;
     }
     // output planes [split][M][Nout] as a 3-D map with a [BNA][128] box; a TMA
@@ -668,7 +668,7 @@ int launch_tc(const void* A, const uint32_t* Wq, const void* scales, const void*
     cfg.dynamicSmemBytes = fixed + static_cast<size_t>(ast) * C::ACT_STAGE +
                            static_cast<size_t>(wst) * C::W_STAGE;
     cfg.stream = st;
-    return cudaLaunchKernelEx(&cfg, kern, wmap, amap, wmap_t, amap_t, omap, p);
+    return cudaLaunchKernelEx(&cfg, kern, wmap, amap, amap_t, omap, p);
 }
 
 }  // namespace
