@@ -5,10 +5,13 @@
 //
 // One CTA = one 128 x 128 tile over one k slice.  Warp 0 (one thread) loads
 // 128 x 64 tiles of A and W by TMA (128-byte swizzle, K-major) into a
-// STAGES-deep ring; warp 1 allocates tensor memory and one of its threads
-// issues tcgen05.mma (A and B from shared memory, D = 128 x 128 FP32 in
-// tensor memory); warps 2-5 read D back with tcgen05.ld (lane = row of C)
-// and store it.  All waits are bounded (qmm_sm100.cuh).
+// STAGES-deep ring; warp 1 allocates tensor memory; one thread each of warps
+// 1 and 2 issues tcgen05.mma (A and B from shared memory) for alternate k
+// stages into its own 128 x 128 FP32 accumulator in tensor memory -- a single
+// issuing thread spends tens of ns per MMA, as much as the MMA's tensor time;
+// warps 3-6 read both accumulators back with tcgen05.ld (lane = row of C),
+// add them in a fixed order and store the sum.  All waits are bounded
+// (qmm_sm100.cuh).
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -24,7 +27,9 @@ namespace qmm {
 
 namespace {
 
-constexpr int kTile = 128, kKStep = 64, kThreadsG = 192, kMaxStagesG = 8;
+constexpr int kTile = 128, kKStep = 64, kMaxStagesG = 8;
+constexpr int kIssuers = 2;                       // MMA issuers, one accumulator each
+constexpr int kThreadsG = 32 * (1 + kIssuers + 4);  // producer, issuers, epilogue
 constexpr int kOpBytes = kTile * kKStep * 2;  // one operand tile per stage: 16 KB
 constexpr uint32_t kIdescG = idesc_bf16_f32(kTile, kTile);
 
@@ -74,13 +79,13 @@ __global__ void __launch_bounds__(kThreadsG, 1)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        mbar_init(acc_full, 1);
+        mbar_init(acc_full, kIssuers);
         mbar_fence_init();
         tma_prefetch_map(&amap);
         tma_prefetch_map(&bmap);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, kTile);
+        tmem_alloc(tmem_slot, kIssuers * kTile);
         tmem_relinquish();
     }
     pdl_wait();
@@ -105,8 +110,11 @@ __global__ void __launch_bounds__(kThreadsG, 1)
             for (int i = first; i < issued; ++i)
                 mbar_wait(&full[i % stages], (i / stages) & 1, nullptr, p.status);
         }
-    } else if (warp == 1 && lane == 0) {
-        for (int i = 0; i < nt; ++i) {
+    } else if (warp >= 1 && warp <= kIssuers) {
+      if (lane == 0) {
+        const int c = warp - 1;
+        const uint32_t dacc = tmem + c * kTile;
+        for (int i = c; i < nt; i += kIssuers) {
             const int s = i % stages;
             if (!mbar_wait(&full[s], (i / stages) & 1, abort, p.status)) break;
             tc_fence_after();
@@ -114,13 +122,16 @@ __global__ void __launch_bounds__(kThreadsG, 1)
             const uint32_t b_sm = a_sm + kOpBytes;
 #pragma unroll
             for (int kk = 0; kk < kKStep / 16; ++kk)
-                umma_bf16_ss(tmem, sdesc(a_sm + kk * 32), sdesc(b_sm + kk * 32), kIdescG,
-                             (i | kk) != 0);
+                umma_bf16_ss(dacc, sdesc(a_sm + kk * 32), sdesc(b_sm + kk * 32), kIdescG,
+                             (i != c) || kk != 0);
             umma_commit(&empty[s]);
         }
         umma_commit(acc_full);
-    } else if (warp >= 2) {
-        // epilogue: warp w reads tensor-memory lanes 32*(w%4).. = rows of C
+      }
+    } else if (warp > kIssuers) {
+        // epilogue (warps kIssuers+1 .. kIssuers+4, whole warps only: the
+        // warp-wide waits and tcgen05.ld need all 32 lanes): warp w reads
+        // tensor-memory lanes 32*(w%4).. = rows of C
         const int quarter = warp & 3;
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
         const int m = m0 + quarter * 32 + lane;
@@ -132,6 +143,15 @@ __global__ void __launch_bounds__(kThreadsG, 1)
                 uint32_t d[16];
                 tmem_ld16(tmem + lane_base + c * 16, d);
                 tmem_ld_wait();
+                static_assert(kIssuers == 2, "the epilogue adds two accumulators");
+                if (nt > 1) {  // the second accumulator received stages
+                    uint32_t e[16];
+                    tmem_ld16(tmem + lane_base + kTile + c * 16, e);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        d[j] = __float_as_uint(__uint_as_float(d[j]) + __uint_as_float(e[j]));
+                }
                 const int n = n0 + c * 16;
                 if (m >= p.M) continue;
                 const size_t o = plane + static_cast<size_t>(m) * p.N + n;
@@ -176,7 +196,7 @@ __global__ void __launch_bounds__(kThreadsG, 1)
         if (lane == 0 && *abort) mbar_wait(acc_full, 0, nullptr, p.status);
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem, kTile);
+        tmem_dealloc(tmem, kIssuers * kTile);
     }
 }
 
@@ -205,8 +225,13 @@ int launch_gemm_tc(const void* A, const void* W, void* out, int out_mode, int M,
     p.split = split;
     p.out_mode = out_mode;
     const size_t fixed = 1024 + (2 * kMaxStagesG + 1) * 8 + 16 + 128;
+    // stage s of the ring goes to issuer s % kIssuers; a multiple of kIssuers
+    // stages keeps each slot's laps with one issuer, so its parity waits are
+    // sound (a waiter that skipped a lap could take a two-laps-old completion)
     int stages = kMaxStagesG;
-    while (stages > 2 && fixed + stages * 2 * kOpBytes > static_cast<size_t>(limit)) --stages;
+    while (stages > kIssuers &&
+           (fixed + stages * 2 * kOpBytes > static_cast<size_t>(limit) || stages % kIssuers))
+        --stages;
     p.stages = stages;
     CUtensorMap amap, bmap;
     if (!encode_2d(&amap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, M, K, 2, kTile, kKStep,
