@@ -171,6 +171,20 @@ int qmm_unpack_probe(const uint32_t *Wq, int Nout, int Kred, uint8_t *q, void *s
 int qmm_dequant_probe(const uint32_t *Wq, const void *scales, const void *biases, int Nout,
                       int Kred, void *w, void *stream);
 
+/* Pipeline shape of the tcgen05 W4A16 kernel for a tile of bm activation rows
+ * (16, 32, 64, 128 or 256) and a partition of gpp 128-groups, under a dynamic
+ * shared-memory limit of smem_limit bytes (the per-block opt-in maximum minus
+ * the kernel's static shared memory; 232432 on GB300).  Host only, no CUDA
+ * calls: the same computation the launcher makes.  out (host, 9 ints)
+ * receives: MMA issuers, dequantizer sets, tensor-memory A buffers, groups
+ * per weight stage, groups per activation stage, activation ring stages,
+ * weight ring stages, threads per CTA, dynamic shared memory bytes.  The
+ * tiny-llm chapter has no counterpart: this call exists so tests can check
+ * the pipeline's synchronization rules on the configurations the kernel
+ * really uses.  Returns QMM_OK, QMM_EINVAL (bad bm, gpp, limit or null) or
+ * QMM_ESHAPE (nothing fits the limit). */
+int qmm_tc_pipeline_config(int bm, int gpp, int smem_limit, int *out);
+
 /* Kernel families used by qmm_w4a16_g128 (process-wide, thread-safe):
  *   QMM_KERNELS_DEFAULT   the tuned table: per M, the family measured fastest
  *   QMM_KERNELS_MMA_SYNC  register-dequant mma.sync kernels for every M

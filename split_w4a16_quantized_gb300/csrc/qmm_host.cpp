@@ -288,6 +288,18 @@ int qmm_gemm_bf16_splitk(const void* A, const void* W, void* C, int M, int N, in
     return rc;
 }
 
+int qmm_tc_pipeline_config(int bm, int gpp, int smem_limit, int* out) {
+    if (!out || gpp < 1 || smem_limit < 1) return QMM_EINVAL;
+    qmm::TcPipeline pl;
+    const int rc = qmm::tc_pipeline_config(bm, gpp, smem_limit, &pl);
+    if (rc < 0) return QMM_EINVAL;
+    if (rc > 0) return QMM_ESHAPE;
+    const int v[9] = {pl.nacc, pl.dsets, pl.a_stages, pl.wgps, pl.agps, pl.act_stages,
+                      pl.w_stages, pl.threads, static_cast<int>(pl.smem)};
+    for (int i = 0; i < 9; ++i) out[i] = v[i];
+    return QMM_OK;
+}
+
 int qmm_unpack_probe(const uint32_t* Wq, int Nout, int Kred, uint8_t* q, void* stream) {
     if (!Wq || !q || Nout < 1) return QMM_EINVAL;
     if (Kred < qmm::kGroup || Kred % qmm::kGroup) return QMM_ESHAPE;

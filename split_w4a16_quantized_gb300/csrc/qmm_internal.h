@@ -88,6 +88,14 @@ int launch_w4a16(const Family& fam, const void* A, const uint32_t* Wq, const voi
 int launch_w4a16_tc(int bm, const void* A, const uint32_t* Wq, const void* scales, const void* biases,
                     void* out, int out_mode, int M, int Kred, int Nout, int split, void* stream);
 int read_tc_status(int* out, bool clear);
+
+// Pipeline shape of the tcgen05 W4A16 kernel for one launch.
+struct TcPipeline {
+    int nacc, dsets, a_stages, wgps, agps, act_stages, w_stages, threads;
+    size_t smem;
+};
+// 0 = ok, 1 = does not fit the shared-memory limit, -1 = bad arguments.
+int tc_pipeline_config(int bm, int gpp, long smem_limit, TcPipeline* out);
 int launch_reduce(const void* partials, int partial_dtype, int split, int M, int Nout, void* C,
                   void* stream);
 int launch_gemm_tc(const void* A, const void* W, void* out, int out_mode, int M, int N, int K,

@@ -562,6 +562,42 @@ __global__ void __launch_bounds__(TcCfg<BNA>::THREADS, 1)
     }
 }
 
+// The pipeline shape of one launch: per-tile constants of TcCfg<BNA> and the
+// ring depths chosen for a partition of gpp groups under a dynamic shared
+// memory limit.  Ring depths (stages of WGPS / AGPS groups): the activation
+// ring is shallow, its stages come from L2; the weight ring carries the HBM
+// stream and takes the rest of shared memory.  Both depths keep every slot's
+// consumers passing every lap (ring_laps_ok).  Returns false if nothing fits.
+template <int BNA>
+bool tc_pipeline(int gpp, long limit, TcPipeline* out) {
+    using C = TcCfg<BNA>;
+    const size_t fixed = 1024 + tc_bar_bytes() + 128;
+    const int nst = (gpp + C::AGPS - 1) / C::AGPS;
+    int ast = BNA <= 64 ? 4 : BNA <= 128 ? 4 : 2;
+    if (ast > nst + 1) ast = nst + 1 < 2 ? 2 : nst + 1;
+    int wst = 0;
+    for (; ast >= 2; --ast) {
+        if (!ring_laps_ok(ast, C::AGPS, C::NACC)) continue;
+        const long room = limit - static_cast<long>(fixed) - static_cast<long>(ast) * C::ACT_STAGE;
+        wst = room > 0 ? static_cast<int>(room / C::W_STAGE) : 0;
+        if (wst > kMaxWStages) wst = kMaxWStages;
+        while (wst > 0 && !ring_laps_ok(wst, C::WGPS, C::DSETS)) --wst;
+        if (wst >= 3) break;
+    }
+    if (ast < 2 || wst < 3) return false;
+    out->nacc = C::NACC;
+    out->dsets = C::DSETS;
+    out->a_stages = C::A_STAGES;
+    out->wgps = C::WGPS;
+    out->agps = C::AGPS;
+    out->act_stages = ast;
+    out->w_stages = wst;
+    out->threads = C::THREADS;
+    out->smem = fixed + static_cast<size_t>(ast) * C::ACT_STAGE +
+                static_cast<size_t>(wst) * C::W_STAGE;
+    return true;
+}
+
 template <int BNA>
 int launch_tc(const void* A, const uint32_t* Wq, const void* scales, const void* biases,
               void* out, int out_mode, int M, int Kred, int Nout, int split, cudaStream_t st) {
@@ -587,25 +623,9 @@ int launch_tc(const void* A, const uint32_t* Wq, const void* scales, const void*
     p.out_mode = out_mode;
     p.wtail = p.gpp % C::WGPS;
     p.atail = p.gpp % C::AGPS;
-    // ring depths (stages of WGPS / AGPS groups): the activation ring is shallow,
-    // its stages come from L2; the weight ring carries the HBM stream and
-    // takes the rest of shared memory.  Both depths keep every slot's
-    // consumers passing every lap (ring_laps_ok).
-    const size_t fixed = 1024 + tc_bar_bytes() + 128;
-    const int nst = (p.gpp + C::AGPS - 1) / C::AGPS;
-    int ast = BNA <= 64 ? 4 : BNA <= 128 ? 4 : 2;
-    if (ast > nst + 1) ast = nst + 1 < 2 ? 2 : nst + 1;
-    int wst = 0;
-    for (; ast >= 2; --ast) {
-        if (!ring_laps_ok(ast, C::AGPS, C::NACC)) continue;
-        const long room = static_cast<long>(limit) - static_cast<long>(fixed) -
-                          static_cast<long>(ast) * C::ACT_STAGE;
-        wst = room > 0 ? static_cast<int>(room / C::W_STAGE) : 0;
-        if (wst > kMaxWStages) wst = kMaxWStages;
-        while (wst > 0 && !ring_laps_ok(wst, C::WGPS, C::DSETS)) --wst;
-        if (wst >= 3) break;
-    }
-    if (ast < 2 || wst < 3) return cudaErrorInvalidValue;
+    TcPipeline pl;
+    if (!tc_pipeline<BNA>(p.gpp, limit, &pl)) return cudaErrorInvalidValue;
+    const int ast = pl.act_stages, wst = pl.w_stages;
     auto ring = [](int n, int gps_log2) {
         Ring r;
         r.n = n;
@@ -665,13 +685,24 @@ int launch_tc(const void* A, const uint32_t* Wq, const void* scales, const void*
     apply_pdl(cfg, la);
     cfg.gridDim = dim3((Nout + kWRows - 1) / kWRows, (M + BNA - 1) / BNA, split);
     cfg.blockDim = dim3(C::THREADS, 1, 1);
-    cfg.dynamicSmemBytes = fixed + static_cast<size_t>(ast) * C::ACT_STAGE +
-                           static_cast<size_t>(wst) * C::W_STAGE;
+    cfg.dynamicSmemBytes = pl.smem;
     cfg.stream = st;
     return cudaLaunchKernelEx(&cfg, kern, wmap, amap, amap_t, omap, p);
 }
 
 }  // namespace
+
+int tc_pipeline_config(int bm, int gpp, long smem_limit, TcPipeline* out) {
+    if (gpp < 1 || !out) return -1;
+    switch (bm) {
+        case 16: return tc_pipeline<16>(gpp, smem_limit, out) ? 0 : 1;
+        case 32: return tc_pipeline<32>(gpp, smem_limit, out) ? 0 : 1;
+        case 64: return tc_pipeline<64>(gpp, smem_limit, out) ? 0 : 1;
+        case 128: return tc_pipeline<128>(gpp, smem_limit, out) ? 0 : 1;
+        case 256: return tc_pipeline<256>(gpp, smem_limit, out) ? 0 : 1;
+        default: return -1;
+    }
+}
 
 int launch_w4a16_tc(int bm, const void* A, const uint32_t* Wq, const void* scales,
                     const void* biases, void* out, int out_mode, int M, int Kred, int Nout,

@@ -66,6 +66,7 @@ _SIGS = {
     "qmm_w4a16_g128_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I,
                                     ctypes.POINTER(qmm_policy), _I, _P, ctypes.POINTER(_I)]),
     "qmm_static_scratch_bytes": (_SZ, []),
+    "qmm_tc_pipeline_config": (_I, [_I, _I, _I, ctypes.POINTER(_I)]),
 }
 
 
@@ -215,6 +216,17 @@ def qmm_w4a16_g128_partition(A: torch.Tensor, Wq: torch.Tensor, scales: torch.Te
         partials.numel() * partials.element_size(), M, Kred, Nout, split, partial_dtype,
         _stream(stream))
     _check(rc, "qmm_w4a16_g128_partition")
+
+
+TC_PIPELINE_FIELDS = ("issuers", "dequant_sets", "a_buffers", "weight_stage_groups",
+                      "act_stage_groups", "act_stages", "weight_stages", "threads", "smem")
+
+
+def qmm_tc_pipeline_config(bm: int, gpp: int, smem_limit: int = 232432) -> dict:
+    """The tcgen05 kernel's pipeline shape for a tile and partition (host only)."""
+    out = (_I * 9)()
+    _check(lib().qmm_tc_pipeline_config(bm, gpp, smem_limit, out), "qmm_tc_pipeline_config")
+    return dict(zip(TC_PIPELINE_FIELDS, list(out)))
 
 
 def qmm_static_scratch_bytes() -> int:
