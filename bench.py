@@ -290,6 +290,11 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.set_device(device)
     Q.qmm_set_kernels({"default": Q.QMM_KERNELS_DEFAULT, "mma": Q.QMM_KERNELS_MMA_SYNC,
                        "tc": Q.QMM_KERNELS_TCGEN05}[args.kernels])
+    # the workload's weights are loaded once and never written by a kernel on
+    # the stream, so the library may start weight work before the previous
+    # kernel finishes (qmm_set_weights_static); --weights dynamic turns it off
+    static_weights = args.weights == "static"
+    Q.qmm_set_weights_static(static_weights)
     props = torch.cuda.get_device_properties(device)
     l2 = int(getattr(props, "L2_cache_size", 128 << 20))
     sms = props.multi_processor_count
@@ -335,29 +340,38 @@ def run_gpu(args, rank, world, local_rank):
     if args.launch_list:
         return {"ms": ms, "wl": wl, "launch_list": True}
 
-    # the same step with programmatic dependent launch off, for comparison
-    prev = Q.qmm_set_pdl(False)
-    graphs_nopdl = []
-    with torch.cuda.stream(cap):
-        for r in range(wl.R):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=cap):
-                wl.step(r)
-            graphs_nopdl.append(g)
-    Q.qmm_set_pdl(prev)
-    torch.cuda.synchronize()
-    for k in range(args.warmup):
-        graphs_nopdl[k % wl.R].replay()
-    t0.record(stream)
-    for k in range(args.steps):
-        graphs_nopdl[k % wl.R].replay()
-    t1.record(stream)
-    torch.cuda.synchronize()
-    ms_nopdl = t0.elapsed_time(t1)
-    del graphs_nopdl
+    def time_variant(setter, value):
+        """The step re-captured with one library switch changed, same timing."""
+        prev = setter(value)
+        gs = []
+        with torch.cuda.stream(cap):
+            for r in range(wl.R):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=cap):
+                    wl.step(r)
+                gs.append(g)
+        setter(prev)
+        torch.cuda.synchronize()
+        for k in range(args.warmup):
+            gs[k % wl.R].replay()
+        t0.record(stream)
+        for k in range(args.steps):
+            gs[k % wl.R].replay()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1)
+
+    # the same step with programmatic dependent launch off, and with the
+    # static-weights promise flipped, for comparison
+    ms_nopdl = time_variant(Q.qmm_set_pdl, False)
+    ms_wflip = time_variant(Q.qmm_set_weights_static, not static_weights)
 
     # per call: policy split vs the unsplit control, each timed as a graph of
-    # back-to-back launches over copies of its inputs larger than L2
+    # back-to-back launches over copies of its inputs larger than L2.  These and
+    # the roofline's kernel timing run without the static-weights early start:
+    # back to back, a call whose grid leaves SMs free would otherwise overlap
+    # the next identical call, which measures the overlap, not the kernel
+    Q.qmm_set_weights_static(False)
     per_call = []
     dom = None
     for i, (name, M, Kred, Nout) in enumerate(wl.calls):
@@ -398,10 +412,11 @@ def run_gpu(args, rank, world, local_rank):
                     lambda j: Q.qmm_splitk_reduce(planes, Q.QMM_PARTIAL_BF16, s, M, Nout, C),
                     len(cps), stream)
         del cps
+    Q.qmm_set_weights_static(static_weights)
     sample = clocks.stop()
     dense = dense_sweep(Q, device, stream, sms, l2) if rank == 0 else None
     e2e = run_e2e(wl, Q, device, stream, min(args.steps, 20))
-    return {"ms": ms, "ms_nopdl": ms_nopdl, "per_call": per_call, "dom": dom,
+    return {"ms": ms, "ms_nopdl": ms_nopdl, "ms_wflip": ms_wflip, "per_call": per_call, "dom": dom,
             "clocks": sample, "wl": wl,
             "peaks": peaks,
             "peak_src": peak_src, "l2": l2, "sms": sms, "dense": dense, "e2e": e2e}
@@ -612,6 +627,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--launch-list", action="store_true",
                     help="only the timed graph steps (for a profiler's launch list)")
+    ap.add_argument("--weights", choices=["static", "dynamic"], default="static",
+                    help="static: promise that no kernel writes the weights during the run "
+                         "(qmm_set_weights_static), which lets weight work start early")
     ap.add_argument("--kernels", choices=["default", "mma", "tc"], default="default",
                     help="kernel table for the W4A16 calls (A/B comparisons)")
     ap.add_argument("--only", default=None, metavar="PROJ:M",
@@ -678,7 +696,8 @@ def main():
             "reduce_us": round(res["dom"].get("us_reduce", 0.0), 3),
             "timing": "CUDA events around replays of a graph of back-to-back launches of the "
                       "kernel alone, each launch on its own copy of the inputs (copies > 2.2x L2, "
-                      "weights read from HBM); programmatic dependent launch on"}
+                      "weights read from HBM); programmatic dependent launch on, no "
+                      "static-weights early start"}
     out = {"metric": METRIC, "value": round(value_us, 4), "unit": UNIT, "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": round(res["ms"] / args.steps, 6), "higher_is_better": False,
@@ -688,9 +707,15 @@ def main():
                       "l2": "inputs larger than L2: %d rotating input sets x %.0f MB (L2 %d MB)"
                             % (wl.R, wl.set_bytes / 2**20, res["l2"] >> 20),
                       "kernels": args.kernels,
+                      "weights": "static (qmm_set_weights_static: no kernel writes the "
+                                 "weights during the run; weight loads and dequant start "
+                                 "before the previous kernel ends)" if args.weights == "static"
+                                 else "dynamic (every kernel waits for the previous one)",
                       "graphs": "one CUDA graph per step, replayed", "parallelism":
                       "replicas x%d" % world, "sms": res["sms"]},
            "value_without_pdl": round(job_value_us(res["ms_nopdl"], 1, args.steps, ncalls), 4),
+           ("value_weights_dynamic" if args.weights == "static" else "value_weights_static"):
+               round(job_value_us(res["ms_wflip"], 1, args.steps, ncalls), 4),
            "roofline": roof, "gpu_launches": args.steps * wl.launches_per_step(),
            "clocks": res["clocks"], "e2e": res["e2e"], "per_call": res["per_call"],
            "dense_splitk_512x512x16384": res["dense"]}

@@ -205,6 +205,18 @@ int qmm_set_kernels(int which);
  * previous setting. */
 int qmm_set_pdl(int enable);
 
+/* Static weights (off by default).  enable = 1 promises that no kernel issued
+ * earlier on the same stream writes the packed weights, scales or biases of
+ * the matmuls that follow (true of inference weights loaded once).  The
+ * tcgen05 partition kernel then loads and dequantizes its first weight stages
+ * while the previous kernel on the stream is still running (programmatic
+ * dependent launch must be on); only its activation loads and its output
+ * writes wait for that kernel.  Weights written by copies or kernels ordered
+ * through events or stream synchronization are fine.  The tiny-llm chapter
+ * has no counterpart: this is launch-latency overlap on GB300.  Process-wide;
+ * returns the previous setting. */
+int qmm_set_weights_static(int enable);
+
 /* Status word of the tcgen05 kernels: 0 = ok, 1 = a bounded wait inside a
  * kernel ran out (the kernel stopped early; its output is not valid).
  * Synchronizes with the device (cudaMemcpyFromSymbol); clear != 0 resets the

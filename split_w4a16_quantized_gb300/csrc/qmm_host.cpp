@@ -46,6 +46,7 @@ size_t partial_elem_bytes(int dtype) { return dtype == QMM_PARTIAL_F32 ? 4 : 2; 
 
 std::atomic<int> g_kernels{QMM_KERNELS_DEFAULT};
 std::atomic<int> g_pdl{1};
+std::atomic<int> g_wstatic{0};
 
 template <size_t N>
 const qmm::Family& pick(const qmm::Family (&table)[N], int M) {
@@ -67,6 +68,8 @@ const Family& family_for(int M) {
 }
 
 bool pdl_enabled() { return g_pdl.load(std::memory_order_relaxed) != 0; }
+
+bool weights_static() { return g_wstatic.load(std::memory_order_relaxed) != 0; }
 
 bool gemm_uses_tc() { return g_kernels.load(std::memory_order_relaxed) != QMM_KERNELS_MMA_SYNC; }
 
@@ -105,6 +108,8 @@ int qmm_set_kernels(int which) {
 }
 
 int qmm_set_pdl(int enable) { return g_pdl.exchange(enable ? 1 : 0); }
+
+int qmm_set_weights_static(int enable) { return g_wstatic.exchange(enable ? 1 : 0); }
 
 int qmm_kernel_status(int* status, int clear) {
     if (!status) return QMM_EINVAL;

@@ -61,6 +61,8 @@ int set_max_dynamic_smem(const void* kernel);
 
 // Programmatic dependent launch of the library's kernels (qmm_set_pdl).
 bool pdl_enabled();
+// Weights not written by earlier kernels on the stream (qmm_set_weights_static).
+bool weights_static();
 struct LaunchAttrs {
     cudaLaunchAttribute attr[1];
 };

@@ -131,6 +131,7 @@ struct TcParams {
     void* out;
     int* status;
     int M, Kred, Nout, G, gpp, out_mode;
+    int weights_static;  // 1: only the activation copies wait for earlier kernels
     int tma_store;  // 1: the output tile leaves through a TMA store of a staged tile
     int wtail;      // groups in the last weight stage when gpp % WGPS != 0, else 0
     int atail;      // groups in the last activation stage when gpp % AGPS != 0, else 0
@@ -276,20 +277,30 @@ __device__ __forceinline__ void tc_producer(const TcSmem& sm, const TcParams& p,
     const int wlast_boxes = p.wtail == 0 ? 2 : (p.wtail + 1) >> 1;
     int jw = 0, ja = 0, sw = 0, sa = 0;
     uint32_t pw = 0, pa = 0;
+    auto issue_w = [&]() {
+        // the dequantizers read this stage with ordinary loads
+        fence_proxy_async_smem();
+        const int boxes = jw == nw - 1 ? wlast_boxes : 2;
+        const int x = (gbeg + jw * C::WGPS) * 16;  // 32-bit words
+        mbar_arrive_expect_tx(&sm.w_full[sw], boxes * kWBox);
+        tma_load_2d(sm.w + sw * C::W_STAGE, wmap, &sm.w_full[sw], x, n0);
+        if (boxes == 2)
+            tma_load_2d(sm.w + sw * C::W_STAGE + kWBox, wmap, &sm.w_full[sw], x + 32, n0);
+        ++jw;
+        if (++sw == p.wr.n) { sw = 0; pw ^= 1; }
+    };
+    if (p.weights_static) {
+        // static weights: every weight slot is filled (and dequantized by the
+        // sets) before the wait for the earlier kernels; only the activation
+        // copies come after it
+        while (jw < nw && jw < p.wr.n) issue_w();
+        pdl_wait();
+    }
     const unsigned long long t0 = globaltimer_ns();
     for (uint32_t spin = 0; jw < nw || ja < na; ++spin) {
         bool progress = false;
         if (jw < nw && mbar_probe(&sm.w_empty[sw], pw ^ 1)) {
-            // the dequantizers read this stage with ordinary loads
-            fence_proxy_async_smem();
-            const int boxes = jw == nw - 1 ? wlast_boxes : 2;
-            const int x = (gbeg + jw * C::WGPS) * 16;  // 32-bit words
-            mbar_arrive_expect_tx(&sm.w_full[sw], boxes * kWBox);
-            tma_load_2d(sm.w + sw * C::W_STAGE, wmap, &sm.w_full[sw], x, n0);
-            if (boxes == 2)
-                tma_load_2d(sm.w + sw * C::W_STAGE + kWBox, wmap, &sm.w_full[sw], x + 32, n0);
-            ++jw;
-            if (++sw == p.wr.n) { sw = 0; pw ^= 1; }
+            issue_w();
             progress = true;
         }
         if (ja < na && mbar_probe(&sm.act_empty[sa], pa ^ 1)) {
@@ -416,6 +427,7 @@ __device__ __forceinline__ void tc_epilogue(const TcSmem& sm, const TcParams& p,
                                             volatile int* abort) {
     using C = TcCfg<BNA>;
     const bool ok = mbar_wait_warp(sm.acc_full, 0, abort, p.status);
+    if (p.weights_static) pdl_wait();  // outputs: earlier kernels may read the planes
     if (ok) {
         tc_fence_after();
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
@@ -513,7 +525,7 @@ __global__ void __launch_bounds__(TcCfg<BNA>::THREADS, 1)
         tma_prefetch_map(&wmap);
         tma_prefetch_map(&amap);
     }
-    if (warp == 0) {
+    if (warp == 0 && !p.weights_static) {
         // The packed weights are a read-only input: this CTA's share is pulled
         // into L2 while the kernels before it on the stream finish.  L2 is the
         // point of coherence, so the loads after the wait below still see
@@ -525,7 +537,10 @@ __global__ void __launch_bounds__(TcCfg<BNA>::THREADS, 1)
         tmem_alloc(sm.tmem_slot, C::TMEM_COLS);
         tmem_relinquish();
     }
-    pdl_wait();       // global memory is read only after the previous kernel is done
+    // Global memory that earlier kernels on the stream may write is read (and
+    // outputs are written) only after the dependency wait.  With static
+    // weights only the activation copies (the producer) and the epilogue wait.
+    if (!p.weights_static) pdl_wait();
     __syncthreads();  // barriers initialized; the producer starts at once
     uint32_t tmem = 0;
     // warp 1's tensor-memory address reaches the issuers and dequantizers
@@ -621,6 +636,7 @@ int launch_tc(const void* A, const uint32_t* Wq, const void* scales, const void*
     p.G = Kred / kGroup;
     p.gpp = p.G / split;
     p.out_mode = out_mode;
+    p.weights_static = weights_static() && pdl_enabled() ? 1 : 0;
     p.wtail = p.gpp % C::WGPS;
     p.atail = p.gpp % C::AGPS;
     TcPipeline pl;

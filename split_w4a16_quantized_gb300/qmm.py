@@ -62,6 +62,7 @@ _SIGS = {
     "qmm_strerror": (ctypes.c_char_p, [_I]),
     "qmm_set_kernels": (_I, [_I]),
     "qmm_set_pdl": (_I, [_I]),
+    "qmm_set_weights_static": (_I, [_I]),
     "qmm_kernel_status": (_I, [ctypes.POINTER(_I), _I]),
     "qmm_w4a16_g128_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I,
                                     ctypes.POINTER(qmm_policy), _I, _P, ctypes.POINTER(_I)]),
@@ -137,6 +138,11 @@ def qmm_set_kernels(which: int) -> int:
 def qmm_set_pdl(enable: bool) -> int:
     """Programmatic dependent launch on/off; returns the previous setting."""
     return lib().qmm_set_pdl(int(bool(enable)))
+
+
+def qmm_set_weights_static(enable: bool) -> int:
+    """Promise that no earlier kernel on the stream writes the weights (see qmm.h)."""
+    return int(lib().qmm_set_weights_static(1 if enable else 0))
 
 
 def qmm_kernel_status(clear: bool = True) -> int:

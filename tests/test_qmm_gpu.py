@@ -398,6 +398,38 @@ def test_partition_argument_errors():
     assert e.value.code == Q.QMM_ESHAPE
 
 
+# ---- static weights: the early start overlaps the previous kernel -----------
+
+@pytest.mark.parametrize("pdl", [True, False])
+def test_weights_static_back_to_back(pdl):
+    """Calls launched back to back on one stream, with the static-weights
+    promise, so each partition kernel loads and dequantizes weights while
+    the kernel before it is still running.  Each result must match the
+    oracle exactly as without the promise."""
+    shapes = [("k", 16), ("gate", 32), ("down", 128), ("k", 16), ("ragged", 33)]
+    probs = []
+    for j, (name, M) in enumerate(shapes):
+        Kred, Nout = inputs.RAGGED if name == "ragged" else inputs.PROJECTIONS[name]
+        p = inputs.make_w4a16(M, Kred, Nout, seed=70 + j)
+        probs.append((p, Q.to_device(p), M, Nout))
+    prev_w, prev_p = Q.qmm_set_weights_static(True), Q.qmm_set_pdl(pdl)
+    try:
+        outs = []
+        for p, d, M, Nout in probs:
+            C, used = Q.w4a16_matmul(d["A"], d["Wq"], d["scales"], d["biases"])
+            outs.append((C, used))
+        torch.cuda.synchronize()
+        assert Q.qmm_kernel_status(clear=True) == 0
+    finally:
+        Q.qmm_set_weights_static(prev_w)
+        Q.qmm_set_pdl(prev_p)
+    rng = np.random.default_rng(5)
+    for (p, d, M, Nout), (C, used) in zip(probs, outs):
+        rows, cols = _sample(M, Nout, rng)
+        _check_sampled(p, _bits(C), used, Q.QMM_PARTIAL_BF16, rows, cols,
+                       "static weights M=%d Nout=%d" % (M, Nout))
+
+
 # ---- dense BF16 split-K GEMM -----------------------------------------------
 
 @pytest.fixture(scope="module")
