@@ -226,7 +226,10 @@ class Workload:
             s = Q.qmm_splitk_plan(M, Kred, Nout, pol)
             self.split.append(s)
             ws_max = max(ws_max, Q.qmm_splitk_workspace_bytes(M, Nout, s, Q.QMM_PARTIAL_BF16))
-        self.ws = torch.empty(ws_max, dtype=torch.uint8, device=device)
+        # one workspace for every call, zeroed, with room beyond the largest
+        # planes for the fused reduce's counter area (its last 32 KB), which
+        # planes therefore never touch
+        self.ws = torch.zeros(ws_max + (64 << 10), dtype=torch.uint8, device=device)
 
     def call(self, i, r, split_req=0):
         d = self.sets[r][i]
@@ -365,6 +368,7 @@ def run_gpu(args, rank, world, local_rank):
     # static-weights promise flipped, for comparison
     ms_nopdl = time_variant(Q.qmm_set_pdl, False)
     ms_wflip = time_variant(Q.qmm_set_weights_static, not static_weights)
+    ms_fused = time_variant(Q.qmm_set_reduce, Q.QMM_REDUCE_FUSED)
 
     # per call: policy split vs the unsplit control, each timed as a graph of
     # back-to-back launches over copies of its inputs larger than L2.  These and
@@ -416,7 +420,8 @@ def run_gpu(args, rank, world, local_rank):
     sample = clocks.stop()
     dense = dense_sweep(Q, device, stream, sms, l2) if rank == 0 else None
     e2e = run_e2e(wl, Q, device, stream, min(args.steps, 20))
-    return {"ms": ms, "ms_nopdl": ms_nopdl, "ms_wflip": ms_wflip, "per_call": per_call, "dom": dom,
+    return {"ms": ms, "ms_nopdl": ms_nopdl, "ms_wflip": ms_wflip, "ms_fused": ms_fused,
+            "per_call": per_call, "dom": dom,
             "clocks": sample, "wl": wl,
             "peaks": peaks,
             "peak_src": peak_src, "l2": l2, "sms": sms, "dense": dense, "e2e": e2e}
@@ -716,6 +721,7 @@ def main():
            "value_without_pdl": round(job_value_us(res["ms_nopdl"], 1, args.steps, ncalls), 4),
            ("value_weights_dynamic" if args.weights == "static" else "value_weights_static"):
                round(job_value_us(res["ms_wflip"], 1, args.steps, ncalls), 4),
+           "value_fused_reduce": round(job_value_us(res["ms_fused"], 1, args.steps, ncalls), 4),
            "roofline": roof, "gpu_launches": args.steps * wl.launches_per_step(),
            "clocks": res["clocks"], "e2e": res["e2e"], "per_call": res["per_call"],
            "dense_splitk_512x512x16384": res["dense"]}

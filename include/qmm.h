@@ -107,7 +107,9 @@ int qmm_kernel_tile(int M, int *bm, int *bn);
 int qmm_splitk_plan(int M, int Kred, int Nout, const qmm_policy *pol, int *split_out);
 
 /* Bytes of workspace the split path needs: split*M*Nout*(2 or 4), or 0 when
- * split <= 1.  Returns 0 for invalid arguments as well. */
+ * split <= 1; when the fused reduce applies (QMM_REDUCE_FUSED), the planes
+ * rounded up to 256 bytes, plus 256, plus QMM_FUSED_COUNTER_BYTES.  Returns 0 for
+ * invalid arguments as well. */
 size_t qmm_splitk_workspace_bytes(int M, int Nout, int split, int partial_dtype);
 
 /* C = A . W^T for the W4A16-g128 format (see the top of this header).
@@ -205,6 +207,29 @@ int qmm_set_kernels(int which);
  * previous setting. */
 int qmm_set_pdl(int enable);
 
+/* Where the split planes are added (process-wide, thread-safe):
+ *   QMM_REDUCE_KERNEL (default)  the chapter's design (Task 4): the partition
+ *       kernel writes the planes and a second kernel, qmm_splitk_reduce's,
+ *       adds them.
+ *   QMM_REDUCE_FUSED  a one-launch variant of Task 4 for the tcgen05 kernels:
+ *       the CTAs of one output tile count themselves in through a 32-bit
+ *       counter, and the last to finish adds the tile's planes (FP32,
+ *       ascending partition, one cast: the same C bit for bit) and resets the
+ *       counter.  The counters live in a fixed area: the last
+ *       QMM_FUSED_COUNTER_BYTES of the workspace passed to the call (one per
+ *       output tile; calls with more tiles, and the mma.sync family, use the
+ *       separate reduce).  qmm_splitk_workspace_bytes includes that area in
+ *       this mode.  The counter area must be zero when a workspace is first
+ *       used in this mode: zero the workspace once, pass the same workspace
+ *       (pointer and size) to every fused call, and zero it again after using
+ *       it in QMM_REDUCE_KERNEL mode.  Every call leaves the counters zero,
+ *       also when a bounded wait ran out.  Calls that share a workspace must
+ *       not overlap on the GPU.
+ * Returns the previous mode, or QMM_EINVAL for an unknown mode. */
+#define QMM_FUSED_COUNTER_BYTES 32768
+enum { QMM_REDUCE_KERNEL = 0, QMM_REDUCE_FUSED = 1 };
+int qmm_set_reduce(int mode);
+
 /* Static weights (off by default).  enable = 1 promises that no kernel issued
  * earlier on the same stream writes the packed weights, scales or biases of
  * the matmuls that follow (true of inference weights loaded once).  The
@@ -241,8 +266,10 @@ const char *qmm_strerror(int code);
  *     cudaGetSymbolAddress, with that device current, and caches it. Make
  *     that first call before any stream capture on the device.
  *   - Limit: a call whose planes (split * M * Nout * 2 bytes for BF16
- *     partials, * 4 for FP32) exceed qmm_static_scratch_bytes() returns
- *     QMM_EWORKSPACE and launches nothing.  The split is the policy's
+ *     partials, * 4 for FP32), rounded up to 256 bytes, exceed
+ *     qmm_static_scratch_bytes() - 256 - QMM_FUSED_COUNTER_BYTES returns
+ *     QMM_EWORKSPACE and launches nothing (the buffer's last bytes hold the
+ *     fused reduce's counters, zero from the start).  The split is the policy's
  *     (split_req = 0) or the forced one.  Unsplit calls (split 1) use none
  *     of the buffer.
  *   - Races: every call on a device shares the one buffer.  Two calls whose

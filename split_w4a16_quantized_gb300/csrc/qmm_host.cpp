@@ -44,9 +44,25 @@ int launched(int err) { return err == cudaSuccess ? QMM_OK : QMM_ECUDA; }
 
 size_t partial_elem_bytes(int dtype) { return dtype == QMM_PARTIAL_F32 ? 4 : 2; }
 
+// Fused reduce: one 32-bit counter per output tile in a fixed area at the end
+// of the caller's workspace (the last kFusedCounterBytes, 256-byte aligned),
+// so a workspace reused across shapes keeps its counters in one place.
+size_t fused_tiles(const qmm::Family& f, int M, int Nout) {
+    return static_cast<size_t>((M + f.bm - 1) / f.bm) * static_cast<size_t>((Nout + f.bn - 1) / f.bn);
+}
+uint32_t* fused_counters(void* workspace, size_t ws_bytes) {
+    const uintptr_t end = reinterpret_cast<uintptr_t>(workspace) + ws_bytes;
+    return reinterpret_cast<uint32_t*>((end - QMM_FUSED_COUNTER_BYTES) & ~static_cast<uintptr_t>(255));
+}
+bool fused_applies(const qmm::Family& f, int M, int Nout, int split) {
+    return qmm::reduce_fused() && f.kind == qmm::kKindTc && split > 1 &&
+           fused_tiles(f, M, Nout) * sizeof(uint32_t) <= QMM_FUSED_COUNTER_BYTES;
+}
+
 std::atomic<int> g_kernels{QMM_KERNELS_DEFAULT};
 std::atomic<int> g_pdl{1};
 std::atomic<int> g_wstatic{0};
+std::atomic<int> g_reduce{QMM_REDUCE_KERNEL};
 
 template <size_t N>
 const qmm::Family& pick(const qmm::Family (&table)[N], int M) {
@@ -70,6 +86,8 @@ const Family& family_for(int M) {
 bool pdl_enabled() { return g_pdl.load(std::memory_order_relaxed) != 0; }
 
 bool weights_static() { return g_wstatic.load(std::memory_order_relaxed) != 0; }
+
+bool reduce_fused() { return g_reduce.load(std::memory_order_relaxed) == QMM_REDUCE_FUSED; }
 
 bool gemm_uses_tc() { return g_kernels.load(std::memory_order_relaxed) != QMM_KERNELS_MMA_SYNC; }
 
@@ -110,6 +128,11 @@ int qmm_set_kernels(int which) {
 int qmm_set_pdl(int enable) { return g_pdl.exchange(enable ? 1 : 0); }
 
 int qmm_set_weights_static(int enable) { return g_wstatic.exchange(enable ? 1 : 0); }
+
+int qmm_set_reduce(int mode) {
+    if (mode != QMM_REDUCE_KERNEL && mode != QMM_REDUCE_FUSED) return QMM_EINVAL;
+    return g_reduce.exchange(mode);
+}
 
 int qmm_kernel_status(int* status, int clear) {
     if (!status) return QMM_EINVAL;
@@ -179,8 +202,11 @@ size_t qmm_splitk_workspace_bytes(int M, int Nout, int split, int partial_dtype)
     if (M < 1 || Nout < 1 || split < 1) return 0;
     if (partial_dtype != QMM_PARTIAL_BF16 && partial_dtype != QMM_PARTIAL_F32) return 0;
     if (split == 1) return 0;
-    return static_cast<size_t>(split) * static_cast<size_t>(M) * static_cast<size_t>(Nout) *
-           partial_elem_bytes(partial_dtype);
+    const size_t planes = static_cast<size_t>(split) * static_cast<size_t>(M) *
+                          static_cast<size_t>(Nout) * partial_elem_bytes(partial_dtype);
+    if (!fused_applies(qmm::family_for(M), M, Nout, split)) return planes;
+    // planes, then the fixed counter area (with 256 bytes of alignment slack)
+    return (planes + 255) / 256 * 256 + 256 + QMM_FUSED_COUNTER_BYTES;
 }
 
 size_t qmm_gemm_workspace_bytes(int M, int N, int split) {
@@ -238,10 +264,17 @@ int qmm_w4a16_g128(const void* A, const uint32_t* Wq, const void* scales, const 
         if (!workspace || ws_bytes < need) return QMM_EWORKSPACE;
         if (!aligned(workspace, 16)) return QMM_EALIGN;
         const int mode = partial_dtype == QMM_PARTIAL_F32 ? qmm::kOutF32 : qmm::kOutBf16;
-        rc = launched(qmm::launch_w4a16(fam, A, Wq, scales, biases, workspace, mode, M, Kred,
-                                        Nout, split, stream));
-        if (rc == QMM_OK)
-            rc = launched(qmm::launch_reduce(workspace, partial_dtype, split, M, Nout, C, stream));
+        if (fused_applies(fam, M, Nout, split)) {
+            // one launch: the last CTA of each output tile adds the planes
+            rc = launched(qmm::launch_w4a16_tc(fam.bm, A, Wq, scales, biases, workspace, mode, M,
+                                               Kred, Nout, split, stream, C,
+                                               fused_counters(workspace, ws_bytes)));
+        } else {
+            rc = launched(qmm::launch_w4a16(fam, A, Wq, scales, biases, workspace, mode, M, Kred,
+                                            Nout, split, stream));
+            if (rc == QMM_OK)
+                rc = launched(qmm::launch_reduce(workspace, partial_dtype, split, M, Nout, C, stream));
+        }
     }
     if (rc == QMM_OK && split_used) *split_used = split;
     return rc;

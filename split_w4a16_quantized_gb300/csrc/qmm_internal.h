@@ -63,6 +63,8 @@ int set_max_dynamic_smem(const void* kernel);
 bool pdl_enabled();
 // Weights not written by earlier kernels on the stream (qmm_set_weights_static).
 bool weights_static();
+// Fused last-CTA reduce of the tcgen05 kernels (qmm_set_reduce).
+bool reduce_fused();
 struct LaunchAttrs {
     cudaLaunchAttribute attr[1];
 };
@@ -88,7 +90,8 @@ int launch_w4a16(const Family& fam, const void* A, const uint32_t* Wq, const voi
                  const void* biases, void* out, int out_mode, int M, int Kred, int Nout,
                  int split, void* stream);
 int launch_w4a16_tc(int bm, const void* A, const uint32_t* Wq, const void* scales, const void* biases,
-                    void* out, int out_mode, int M, int Kred, int Nout, int split, void* stream);
+                    void* out, int out_mode, int M, int Kred, int Nout, int split, void* stream,
+                    void* fused_C = nullptr, uint32_t* counters = nullptr);
 int read_tc_status(int* out, bool clear);
 
 // Pipeline shape of the tcgen05 W4A16 kernel for one launch.

@@ -70,7 +70,13 @@ int qmm_w4a16_g128_noalloc(const void* A, const uint32_t* Wq, const void* scales
     } else if (split > G || G % split != 0) {
         return QMM_ESHAPE;
     }
-    if (qmm_splitk_workspace_bytes(M, Nout, split, partial_dtype) > qmm::kStaticScratchBytes)
+    // the last QMM_FUSED_COUNTER_BYTES (and 256 bytes of slack) are kept for
+    // the fused reduce's counters in every mode, so no planes ever land there
+    // and the counters stay zero from the module's load on
+    const size_t planes = static_cast<size_t>(split) * static_cast<size_t>(M) *
+                          static_cast<size_t>(Nout) * (partial_dtype == QMM_PARTIAL_F32 ? 4 : 2);
+    if (split > 1 && (planes + 255) / 256 * 256 + 256 + QMM_FUSED_COUNTER_BYTES >
+                         qmm::kStaticScratchBytes)
         return QMM_EWORKSPACE;
     void* scratch = qmm::scratch_on_current_device();
     if (!scratch) return QMM_ECUDA;

@@ -132,6 +132,9 @@ struct TcParams {
     int* status;
     int M, Kred, Nout, G, gpp, out_mode;
     int weights_static;  // 1: only the activation copies wait for earlier kernels
+    int fused;           // 1: the last CTA of an output tile adds its planes into C
+    void* C;             // BF16 [M, Nout] (fused reduce)
+    uint32_t* counters;  // one per output tile (fused reduce), zero between calls
     int tma_store;  // 1: the output tile leaves through a TMA store of a staged tile
     int wtail;      // groups in the last weight stage when gpp % WGPS != 0, else 0
     int atail;      // groups in the last activation stage when gpp % AGPS != 0, else 0
@@ -414,6 +417,100 @@ __device__ __forceinline__ void tc_dequant(const TcSmem& sm, const TcParams& p, 
     }
 }
 
+// Fused reduce of one output tile by its last-arriving CTA: C[m, n] = BF16 of
+// the FP32 sum of the split planes in ascending order (the same arithmetic as
+// the separate reduce kernel, so the same bits).  Threads take items of eight
+// consecutive outputs; two items' loads of four planes each are in flight at
+// once, kept raw until the adds.  Not inlined: its registers stay out of the
+// main loop's allocation.
+template <typename T>
+struct Raw8p;
+template <>
+struct Raw8p<__nv_bfloat16> {
+    uint4 u;
+    __device__ __forceinline__ void load(const __nv_bfloat16* p) {
+        u = __ldcg(reinterpret_cast<const uint4*>(p));
+    }
+    __device__ __forceinline__ void add_to(float acc[8]) const {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            acc[2 * i] += __uint_as_float(w[i] << 16);
+            acc[2 * i + 1] += __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+    }
+};
+template <>
+struct Raw8p<float> {
+    float4 a, b;
+    __device__ __forceinline__ void load(const float* p) {
+        a = __ldcg(reinterpret_cast<const float4*>(p));
+        b = __ldcg(reinterpret_cast<const float4*>(p) + 1);
+    }
+    __device__ __forceinline__ void add_to(float acc[8]) const {
+        acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+        acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+    }
+};
+__device__ __forceinline__ float plane_load(const __nv_bfloat16* p) { return __bfloat162float(__ldcg(p)); }
+__device__ __forceinline__ float plane_load(const float* p) { return __ldcg(p); }
+
+template <typename T>
+__device__ __noinline__ void reduce_tile(const T* planes, __nv_bfloat16* C, int M, int Nout,
+                                         int split, int m0, int rows, int n0, int cols, int t,
+                                         int nthreads) {
+    const size_t plane = static_cast<size_t>(M) * Nout;
+    if (Nout % 8 == 0) {  // cols is then a multiple of 8 and items are 16-byte aligned
+        const int per_row = cols / 8;
+        const int items = rows * per_row;
+        for (int i0 = t; i0 < items; i0 += 2 * nthreads) {
+            float acc[2][8];
+            size_t off[2];
+            bool live[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int i = i0 + u * nthreads;
+                live[u] = i < items;
+                const int ii = live[u] ? i : 0;
+                off[u] = static_cast<size_t>(m0 + ii / per_row) * Nout + n0 + (ii % per_row) * 8;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[u][j] = 0.f;
+            }
+            for (int p0 = 0; p0 < split; p0 += 4) {
+                Raw8p<T> r[4][2];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+#pragma unroll
+                    for (int u = 0; u < 2; ++u)
+                        if (live[u] && p0 + q < split) r[q][u].load(planes + (p0 + q) * plane + off[u]);
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+#pragma unroll
+                    for (int u = 0; u < 2; ++u)
+                        if (live[u] && p0 + q < split) r[q][u].add_to(acc[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+                if (live[u]) {
+                    uint4 o;
+                    o.x = pack_bf16x2(acc[u][0], acc[u][1]);
+                    o.y = pack_bf16x2(acc[u][2], acc[u][3]);
+                    o.z = pack_bf16x2(acc[u][4], acc[u][5]);
+                    o.w = pack_bf16x2(acc[u][6], acc[u][7]);
+                    *reinterpret_cast<uint4*>(C + off[u]) = o;
+                }
+        }
+    } else {
+        const int items = rows * cols;
+        for (int i = t; i < items; i += nthreads) {
+            const size_t o = static_cast<size_t>(m0 + i / cols) * Nout + n0 + i % cols;
+            float acc = 0.f;
+            for (int p = 0; p < split; ++p) acc += plane_load(planes + p * plane + o);
+            C[o] = __float2bfloat16_rn(acc);
+        }
+    }
+}
+
 // Epilogue of one warp: columns (activation rows) in 16-column chunks c with
 // c % DSETS == set; the used accumulators are added in a fixed order.  With
 // p.tma_store the tile is staged in shared memory as [m][n] (the activation
@@ -473,6 +570,39 @@ __device__ __forceinline__ void tc_epilogue(const TcSmem& sm, const TcParams& p,
                         static_cast<float*>(p.out)[o] = v[j];
                 }
             }
+        }
+    }
+    if (p.fused) {
+        // Count this CTA's plane in.  Every epilogue thread's plane stores are
+        // made visible (fence) before the elected thread's increment; the
+        // CTA that brings the count to the split adds the tile's planes.  A CTA
+        // whose wait ran out still counts in (its planes are invalid, and so is
+        // C, which the status word reports), so the counter always returns to
+        // zero.
+        __shared__ int last;
+        __threadfence();
+        asm volatile("bar.sync 3, %0;\n" ::"n"(128 * C::DSETS) : "memory");
+        if (set == 0 && quarter == 0 && lane == 0) {
+            const unsigned tile = blockIdx.y * gridDim.x + blockIdx.x;
+            const unsigned prev = atomicAdd(&p.counters[tile], 1u);
+            last = prev == gridDim.z - 1;
+            if (last) {
+                p.counters[tile] = 0;
+                __threadfence();
+            }
+        }
+        asm volatile("bar.sync 3, %0;\n" ::"n"(128 * C::DSETS) : "memory");
+        if (last) {
+            const int rows = p.M - m0 < BNA ? p.M - m0 : BNA;
+            const int cols = p.Nout - n0 < kWRows ? p.Nout - n0 : kWRows;
+            const int t = (set * 4 + quarter) * 32 + lane;
+            if (p.out_mode == kOutBf16)
+                reduce_tile(static_cast<const __nv_bfloat16*>(p.out),
+                            static_cast<__nv_bfloat16*>(p.C), p.M, p.Nout, gridDim.z, m0, rows,
+                            n0, cols, t, 128 * C::DSETS);
+            else
+                reduce_tile(static_cast<const float*>(p.out), static_cast<__nv_bfloat16*>(p.C),
+                            p.M, p.Nout, gridDim.z, m0, rows, n0, cols, t, 128 * C::DSETS);
         }
     }
     if (p.tma_store) {
@@ -615,7 +745,8 @@ bool tc_pipeline(int gpp, long limit, TcPipeline* out) {
 
 template <int BNA>
 int launch_tc(const void* A, const uint32_t* Wq, const void* scales, const void* biases,
-              void* out, int out_mode, int M, int Kred, int Nout, int split, cudaStream_t st) {
+              void* out, int out_mode, int M, int Kred, int Nout, int split, void* fused_C,
+              uint32_t* counters, cudaStream_t st) {
     using C = TcCfg<BNA>;
     auto kern = w4a16_tc_kernel<BNA>;
     static int limit = -1;
@@ -637,6 +768,9 @@ int launch_tc(const void* A, const uint32_t* Wq, const void* scales, const void*
     p.gpp = p.G / split;
     p.out_mode = out_mode;
     p.weights_static = weights_static() && pdl_enabled() ? 1 : 0;
+    p.fused = fused_C != nullptr && counters != nullptr && split > 1 ? 1 : 0;
+    p.C = fused_C;
+    p.counters = counters;
     p.wtail = p.gpp % C::WGPS;
     p.atail = p.gpp % C::AGPS;
     TcPipeline pl;
@@ -680,7 +814,9 @@ int launch_tc(const void* A, const uint32_t* Wq, const void* scales, const void*
     {
         const int elem = out_mode == kOutBf16 ? 2 : 4;
         const size_t tile = static_cast<size_t>(BNA) * kWRows * elem;
-        p.tma_store = (static_cast<size_t>(Nout) * elem) % 16 == 0 &&
+        // (the fused reduce reads planes that other CTAs wrote, so its plane
+        // stores stay in the generic proxy)
+        p.tma_store = !p.fused && (static_cast<size_t>(Nout) * elem) % 16 == 0 &&
                       tile <= static_cast<size_t>(ast) * C::ACT_STAGE;
         if (p.tma_store) {
             const cuuint64_t odims[3] = {static_cast<cuuint64_t>(Nout), static_cast<cuuint64_t>(M),
@@ -722,14 +858,14 @@ int tc_pipeline_config(int bm, int gpp, long smem_limit, TcPipeline* out) {
 
 int launch_w4a16_tc(int bm, const void* A, const uint32_t* Wq, const void* scales,
                     const void* biases, void* out, int out_mode, int M, int Kred, int Nout,
-                    int split, void* stream) {
+                    int split, void* stream, void* fused_C, uint32_t* counters) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     switch (bm) {
-        case 16: return launch_tc<16>(A, Wq, scales, biases, out, out_mode, M, Kred, Nout, split, st);
-        case 32: return launch_tc<32>(A, Wq, scales, biases, out, out_mode, M, Kred, Nout, split, st);
-        case 64: return launch_tc<64>(A, Wq, scales, biases, out, out_mode, M, Kred, Nout, split, st);
-        case 128: return launch_tc<128>(A, Wq, scales, biases, out, out_mode, M, Kred, Nout, split, st);
-        case 256: return launch_tc<256>(A, Wq, scales, biases, out, out_mode, M, Kred, Nout, split, st);
+        case 16: return launch_tc<16>(A, Wq, scales, biases, out, out_mode, M, Kred, Nout, split, fused_C, counters, st);
+        case 32: return launch_tc<32>(A, Wq, scales, biases, out, out_mode, M, Kred, Nout, split, fused_C, counters, st);
+        case 64: return launch_tc<64>(A, Wq, scales, biases, out, out_mode, M, Kred, Nout, split, fused_C, counters, st);
+        case 128: return launch_tc<128>(A, Wq, scales, biases, out, out_mode, M, Kred, Nout, split, fused_C, counters, st);
+        case 256: return launch_tc<256>(A, Wq, scales, biases, out, out_mode, M, Kred, Nout, split, fused_C, counters, st);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -63,6 +63,7 @@ _SIGS = {
     "qmm_set_kernels": (_I, [_I]),
     "qmm_set_pdl": (_I, [_I]),
     "qmm_set_weights_static": (_I, [_I]),
+    "qmm_set_reduce": (_I, [_I]),
     "qmm_kernel_status": (_I, [ctypes.POINTER(_I), _I]),
     "qmm_w4a16_g128_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I,
                                     ctypes.POINTER(qmm_policy), _I, _P, ctypes.POINTER(_I)]),
@@ -138,6 +139,17 @@ def qmm_set_kernels(which: int) -> int:
 def qmm_set_pdl(enable: bool) -> int:
     """Programmatic dependent launch on/off; returns the previous setting."""
     return lib().qmm_set_pdl(int(bool(enable)))
+
+
+QMM_REDUCE_KERNEL, QMM_REDUCE_FUSED = 0, 1
+
+
+def qmm_set_reduce(mode: int) -> int:
+    """Separate reduce kernel (default) or the fused last-CTA reduce (see qmm.h)."""
+    prev = lib().qmm_set_reduce(mode)
+    if prev < 0:
+        raise QmmError(prev, "qmm_set_reduce")
+    return prev
 
 
 def qmm_set_weights_static(enable: bool) -> int:

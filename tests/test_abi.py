@@ -123,3 +123,22 @@ def test_argument_errors_before_any_cuda_work():
     assert lib.qmm_splitk_reduce(a, 0, 2, 16, 16, P(0x50008), None) == Q.QMM_EALIGN
     assert lib.qmm_gemm_bf16_splitk(a, w, c, 512, 512, 1000, 2, None, 0, None) == Q.QMM_ESHAPE
     assert lib.qmm_gemm_bf16_splitk(a, w, c, 512, 512, 1024, 17, None, 0, None) == Q.QMM_ESHAPE
+
+
+def test_fused_reduce_workspace_holds_the_counters():
+    from split_w4a16_quantized_gb300 import qmm as Q
+    prev_k = Q.qmm_set_kernels(Q.QMM_KERNELS_TCGEN05)
+    prev = Q.qmm_set_reduce(Q.QMM_REDUCE_FUSED)
+    try:
+        # planes, rounded up to 256 bytes, 256 bytes of slack, the fixed counter area
+        planes = 4 * 128 * 2560 * 2
+        assert Q.qmm_splitk_workspace_bytes(128, 2560, 4, Q.QMM_PARTIAL_BF16) == \
+            (planes + 255) // 256 * 256 + 256 + 32768
+        assert Q.qmm_splitk_workspace_bytes(128, 2560, 1, Q.QMM_PARTIAL_BF16) == 0
+        Q.qmm_set_kernels(Q.QMM_KERNELS_MMA_SYNC)  # the separate reduce: planes only
+        assert Q.qmm_splitk_workspace_bytes(128, 2560, 4, Q.QMM_PARTIAL_BF16) == planes
+        with pytest.raises(Q.QmmError):
+            Q.qmm_set_reduce(7)
+    finally:
+        Q.qmm_set_reduce(prev)
+        Q.qmm_set_kernels(prev_k)

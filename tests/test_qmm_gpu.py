@@ -487,3 +487,62 @@ def test_error_codes_on_device():
                             ctypes.c_void_p(d["scales"].data_ptr()), ctypes.c_void_p(d["biases"].data_ptr()),
                             ctypes.c_void_p(C.data_ptr()), M, Kred, Nout, 1, None, None, 0, 0, None, None)
     assert rc == Q.QMM_EALIGN
+
+
+# ---- fused last-CTA reduce: the same C as the separate reduce ---------------
+
+def _call_with(d, M, Nout, split, dt, ws):
+    C = torch.full((M, Nout), float("nan"), dtype=torch.bfloat16, device="cuda")
+    used = Q.qmm_w4a16_g128(d["A"], d["Wq"], d["scales"], d["biases"], C, split_req=split,
+                            workspace=ws, partial_dtype=dt)
+    torch.cuda.synchronize()
+    assert used == split
+    return _bits(C)
+
+
+@pytest.mark.parametrize("name,M,split", [("k", 16, 10), ("gate", 32, 2), ("down", 128, 4),
+                                          ("ragged", 33, 10), ("odd", 5, 2), ("k", 300, 4)])
+@pytest.mark.parametrize("dt", [Q.QMM_PARTIAL_BF16, Q.QMM_PARTIAL_F32])
+def test_fused_reduce_bitwise_equals_kernel_reduce(name, M, split, dt):
+    """QMM_REDUCE_FUSED adds the planes in the partition kernel's last CTA of
+    each tile: same planes, same FP32 ascending sum, so the same bits as the
+    separate reduce.  Three calls on one workspace also check that every call
+    leaves the tile counters at zero."""
+    if name == "odd":
+        Kred, Nout = 256, 77          # scalar path of the fused reduce
+    else:
+        Kred, Nout = inputs.RAGGED if name == "ragged" else inputs.PROJECTIONS[name]
+    d = Q.to_device(inputs.make_w4a16(M, Kred, Nout, seed=90 + M))
+    prev_k = Q.qmm_set_kernels(Q.QMM_KERNELS_TCGEN05)
+    try:
+        prev = Q.qmm_set_reduce(Q.QMM_REDUCE_KERNEL)
+        nb = Q.qmm_splitk_workspace_bytes(M, Nout, split, dt)
+        ref = _call_with(d, M, Nout, split, dt, torch.empty(max(nb, 16), dtype=torch.uint8,
+                                                            device="cuda"))
+        Q.qmm_set_reduce(Q.QMM_REDUCE_FUSED)
+        nbf = Q.qmm_splitk_workspace_bytes(M, Nout, split, dt)
+        assert nbf > nb  # the counters follow the planes
+        ws = torch.zeros(nbf, dtype=torch.uint8, device="cuda")
+        for _ in range(3):
+            got = _call_with(d, M, Nout, split, dt, ws)
+            assert np.array_equal(got, ref)
+        assert Q.qmm_kernel_status(clear=True) == 0
+    finally:
+        Q.qmm_set_reduce(prev)
+        Q.qmm_set_kernels(prev_k)
+
+
+def test_fused_reduce_with_the_static_scratch():
+    d = Q.to_device(inputs.make_w4a16(32, 2560, 1024, seed=99))
+    prev = Q.qmm_set_reduce(Q.QMM_REDUCE_KERNEL)
+    try:
+        C1 = torch.empty((32, 1024), dtype=torch.bfloat16, device="cuda")
+        C2 = torch.empty_like(C1)
+        Q.qmm_w4a16_g128_noalloc(d["A"], d["Wq"], d["scales"], d["biases"], C1, split_req=10)
+        Q.qmm_set_reduce(Q.QMM_REDUCE_FUSED)
+        for _ in range(2):
+            Q.qmm_w4a16_g128_noalloc(d["A"], d["Wq"], d["scales"], d["biases"], C2, split_req=10)
+            torch.cuda.synchronize()
+            assert np.array_equal(_bits(C1), _bits(C2))
+    finally:
+        Q.qmm_set_reduce(prev)
