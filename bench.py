@@ -416,6 +416,7 @@ def run_gpu(args, rank, world, local_rank):
                     lambda j: Q.qmm_splitk_reduce(planes, Q.QMM_PARTIAL_BF16, s, M, Nout, C),
                     len(cps), stream)
         del cps
+    prefill = prefill_sweep(Q, device, stream, l2, peaks) if rank == 0 else None
     Q.qmm_set_weights_static(static_weights)
     sample = clocks.stop()
     dense = dense_sweep(Q, device, stream, sms, l2) if rank == 0 else None
@@ -424,7 +425,38 @@ def run_gpu(args, rank, world, local_rank):
             "per_call": per_call, "dom": dom,
             "clocks": sample, "wl": wl,
             "peaks": peaks,
-            "peak_src": peak_src, "l2": l2, "sms": sms, "dense": dense, "e2e": e2e}
+            "peak_src": peak_src, "l2": l2, "sms": sms, "dense": dense, "e2e": e2e,
+            "prefill": prefill}
+
+
+def prefill_sweep(Q, device, stream, l2, peaks):
+    """The prefill regime (M = 2048) of each projection shape: the policy's
+    split (the unsplit kernel wherever the base grid already fills the GPU),
+    graphs of back-to-back calls over input copies larger than L2, tensor
+    throughput against the measured dense BF16 peak.  Informational."""
+    out = []
+    ws = torch.zeros(64 << 20, dtype=torch.uint8, device=device)
+    for name in PROJ:
+        Kred, Nout = inputs.PROJECTIONS[name]
+        M = 2048
+        d = Q.to_device(inputs.make_w4a16(M, Kred, Nout, seed=0), device)
+        pol = Q.qmm_policy_preset(Q.QMM_PRESET_GB300, M)
+        split = Q.qmm_splitk_plan(M, Kred, Nout, pol)
+        cps = cold_copies(d, l2)
+        C = torch.empty((M, Nout), dtype=torch.bfloat16, device=device)
+
+        def call(j):
+            c = cps[j]
+            Q.qmm_w4a16_g128(c["A"], c["Wq"], c["scales"], c["biases"], C, workspace=ws)
+        us = graph_us_per_launch(call, len(cps), stream)
+        fl = 2.0 * M * Nout * Kred
+        bm, bn = Q.qmm_kernel_tile(M)
+        out.append({"proj": name, "M": M, "split": split,
+                    "ctas": -(-M // bm) * -(-Nout // bn) * split, "us": round(us, 3),
+                    "tflops": round(fl / us / 1e6, 1),
+                    "frac_of_bf16_peak": round(fl / us / 1e6 / peaks["bf16_tflops"], 3)})
+        del cps, d
+    return out
 
 
 def dense_sweep(Q, device, stream, sms, l2):
@@ -724,7 +756,7 @@ def main():
            "value_fused_reduce": round(job_value_us(res["ms_fused"], 1, args.steps, ncalls), 4),
            "roofline": roof, "gpu_launches": args.steps * wl.launches_per_step(),
            "clocks": res["clocks"], "e2e": res["e2e"], "per_call": res["per_call"],
-           "dense_splitk_512x512x16384": res["dense"]}
+           "dense_splitk_512x512x16384": res["dense"], "prefill_M2048": res["prefill"]}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(wl.host)
     if rank == 0:
