@@ -176,8 +176,11 @@ struct TcCfg {
     // producer's barrier work over more bytes
     // (weight stages of four groups: the producer's proxy fence and copy
     // are paid once per four groups; activation stages are as small as the
-    // activation ring's depth needs)
-    static constexpr int WGPS_LOG2 = 2;
+    // activation ring's depth needs.  The 256-row tile is the exception: its
+    // activations are 64 KB a group against 8 KB of weights, so its weight
+    // stages hold two groups and the shared memory goes to a third
+    // activation stage)
+    static constexpr int WGPS_LOG2 = BNA == 256 ? 1 : 2;
     static constexpr int WGPS = 1 << WGPS_LOG2;
     static constexpr int AGPS_LOG2 = BNA <= 32 ? 2 : BNA <= 64 ? 1 : 0;
     static constexpr int AGPS = 1 << AGPS_LOG2;
@@ -276,14 +279,15 @@ __device__ __forceinline__ void tc_producer(const TcSmem& sm, const TcParams& p,
     // a last activation stage of a tail goes through the tail map, whose box
     // holds exactly those groups; a last weight stage of one or two groups
     // takes one two-group box
+    constexpr int kBoxes = C::WGPS / 2;  // two-group boxes per weight stage
     const int alast = p.atail ? na - 1 : na;
-    const int wlast_boxes = p.wtail == 0 ? 2 : (p.wtail + 1) >> 1;
+    const int wlast_boxes = p.wtail == 0 ? kBoxes : (p.wtail + 1) >> 1;
     int jw = 0, ja = 0, sw = 0, sa = 0;
     uint32_t pw = 0, pa = 0;
     auto issue_w = [&]() {
         // the dequantizers read this stage with ordinary loads
         fence_proxy_async_smem();
-        const int boxes = jw == nw - 1 ? wlast_boxes : 2;
+        const int boxes = jw == nw - 1 ? wlast_boxes : kBoxes;
         const int x = (gbeg + jw * C::WGPS) * 16;  // 32-bit words
         mbar_arrive_expect_tx(&sm.w_full[sw], boxes * kWBox);
         tma_load_2d(sm.w + sw * C::W_STAGE, wmap, &sm.w_full[sw], x, n0);
@@ -718,7 +722,9 @@ bool tc_pipeline(int gpp, long limit, TcPipeline* out) {
     using C = TcCfg<BNA>;
     const size_t fixed = 1024 + tc_bar_bytes() + 128;
     const int nst = (gpp + C::AGPS - 1) / C::AGPS;
-    int ast = BNA <= 64 ? 4 : BNA <= 128 ? 4 : 2;
+    int ast = BNA <= 128 ? 4 : 3;
+    // weight stages at least: three of four groups, or two of two
+    const int wmin = C::WGPS >= 4 ? 3 : 2;
     if (ast > nst + 1) ast = nst + 1 < 2 ? 2 : nst + 1;
     int wst = 0;
     for (; ast >= 2; --ast) {
@@ -727,9 +733,9 @@ bool tc_pipeline(int gpp, long limit, TcPipeline* out) {
         wst = room > 0 ? static_cast<int>(room / C::W_STAGE) : 0;
         if (wst > kMaxWStages) wst = kMaxWStages;
         while (wst > 0 && !ring_laps_ok(wst, C::WGPS, C::DSETS)) --wst;
-        if (wst >= 3) break;
+        if (wst >= wmin) break;
     }
-    if (ast < 2 || wst < 3) return false;
+    if (ast < 2 || wst < wmin) return false;
     out->nacc = C::NACC;
     out->dsets = C::DSETS;
     out->a_stages = C::A_STAGES;
