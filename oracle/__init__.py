@@ -69,6 +69,7 @@ def _load():
             "oracle_qmm_partitioned_sampled": [P, P, P, P, I64, I64, I64, P, I64, P, I64, I, I,
                                                P, P, I],
             "oracle_splitk_plan": [I64, I64, I64, I64, I64, I64, I64, I64, P],
+            "oracle_splitk_plan_near_equal": [I64, I64, I64, I64, I64, I64, I64, I64, P],
             "oracle_waves": [I64, I64, I64],
             "oracle_gemm": [P, P, I64, I64, I64, P, I],
             "oracle_gemm_partitioned": [P, P, I64, I64, I64, I64, I, P, I],
@@ -165,7 +166,9 @@ def qmm_sampled(A, Wq, scales, biases, rows, cols, threads: int | None = None) -
 
 def qmm_partitioned(A, Wq, scales, biases, split: int, partial_mode: int = 0,
                     with_partials: bool = False, threads: int | None = None):
-    """Partition emulation: returns (C bf16 bits [M,Nout], partial planes or None)."""
+    """Partition emulation: returns (C bf16 bits [M,Nout], partial planes or None).
+    A split that does not divide Kred/128 takes near-equal partitions (the first
+    G mod split ones hold one group more)."""
     A, Wq = _c(A, np.uint16), _c(Wq, np.uint32)
     scales, biases = _c(scales, np.uint16), _c(biases, np.uint16)
     M, Kred = A.shape
@@ -203,6 +206,14 @@ def splitk_plan(M, Kred, Nout, bm, bn, target, cap, min_k=128) -> int:
     s = ctypes.c_int(0)
     _check(_load().oracle_splitk_plan(M, Kred, Nout, bm, bn, target, cap, min_k,
                                       ctypes.byref(s)), "splitk_plan")
+    return s.value
+
+
+def splitk_plan_near_equal(M, Kred, Nout, bm, bn, target, cap, min_k=128) -> int:
+    """The plan without the divisibility step (near-equal partitions)."""
+    s = ctypes.c_int(0)
+    _check(_load().oracle_splitk_plan_near_equal(M, Kred, Nout, bm, bn, target, cap, min_k,
+                                                 ctypes.byref(s)), "splitk_plan_near_equal")
     return s.value
 
 

@@ -211,10 +211,12 @@ static int emulate_element(const double *am, const double *wn, int64_t Kred, int
         if (planes) planes[0] = exact;
         return bf16_round(exact, c);
     }
-    int64_t span = (Kred / QO_GROUP / split) * QO_GROUP;
+    int64_t G = Kred / QO_GROUP, g0 = 0;
     float acc = 0.0f; /* the reduce adds the planes in FP32 */
     for (int p = 0; p < split; ++p) {
-        double exact = dot(am, wn, p * span, (p + 1) * span);
+        int64_t ng = G / split + (p < G % split ? 1 : 0); /* groups in partition p */
+        double exact = dot(am, wn, g0 * QO_GROUP, (g0 + ng) * QO_GROUP);
+        g0 += ng;
         double plane;
         if (partial_mode == 0) {
             uint16_t pb;
@@ -231,7 +233,11 @@ static int emulate_element(const double *am, const double *wn, int64_t Kred, int
 
 /* Partition emulation [TL, Task 2 and Task 4].  With split s dividing
  * G = Kred/128, partition p covers groups [p*G/s, (p+1)*G/s): equal length,
- * starting and ending on group boundaries.  Each partition's fp64 sum is
+ * starting and ending on group boundaries.  A split that does not divide G
+ * (1 < s <= G) cuts the groups into s slices as equal as whole groups allow,
+ * in order, the first G mod s slices one group longer [SK, Concept: split-K
+ * slices the reduction axis; the same rule as the dense GEMM below].
+ * With s dividing G that is the equal cut.  Each partition's fp64 sum is
  * rounded to the partial-plane type (partial_mode 0: BF16, 1: FP32) and
  * stored in its own plane partial[p, m, n]; the planes are then added in
  * FP32 in ascending p and the sum is rounded once to BF16.  With s = 1 there
@@ -243,7 +249,7 @@ int oracle_qmm_partitioned(const uint16_t *A, const uint32_t *Wq, const uint16_t
                            int nthreads) {
     if (M < 1 || Nout < 1 || Kred < QO_GROUP || Kred % QO_GROUP || nthreads < 1) return -1;
     int64_t G = Kred / QO_GROUP;
-    if (split < 1 || split > 4096 || G % split || (partial_mode != 0 && partial_mode != 1))
+    if (split < 1 || split > 4096 || split > G || (partial_mode != 0 && partial_mode != 1))
         return -1;
     double *w = dequant_all(Wq, scales, biases, Nout, Kred, nthreads);
     double *a = bf16_matrix(A, M, Kred, nthreads);
@@ -275,7 +281,7 @@ int oracle_qmm_partitioned_sampled(const uint16_t *A, const uint32_t *Wq, const 
                                    double *planes, int nthreads) {
     if (M < 1 || Nout < 1 || Kred < QO_GROUP || Kred % QO_GROUP || nthreads < 1) return -1;
     int64_t G = Kred / QO_GROUP;
-    if (split < 1 || G % split || (partial_mode != 0 && partial_mode != 1)) return -1;
+    if (split < 1 || split > G || (partial_mode != 0 && partial_mode != 1)) return -1;
     for (int64_t i = 0; i < nr; ++i) if (rows[i] < 0 || rows[i] >= M) return -1;
     for (int64_t j = 0; j < nc; ++j) if (cols[j] < 0 || cols[j] >= Nout) return -1;
     double *w = (double *)malloc(sizeof(double) * (size_t)(nc * Kred));
@@ -322,6 +328,25 @@ int oracle_splitk_plan(int64_t M, int64_t Kred, int64_t Nout, int64_t bm, int64_
     return 0;
 }
 
+/* The plan without the divisibility step, for near-equal slices: the
+ * largest s within the three bounds of [TL, Task 3] (cap, floor(target/base),
+ * floor(Kred/min_k)); s <= 1 means the unsplit kernel.  With target = one
+ * wave of blocks this is the split the model of [SK, Maths, Split-K] picks,
+ * the largest one whose blocks still fit a single wave; there the slices
+ * need not divide k (its A100 example takes s = 6 of 256 k-tiles). */
+int oracle_splitk_plan_near_equal(int64_t M, int64_t Kred, int64_t Nout, int64_t bm, int64_t bn,
+                                  int64_t target, int64_t cap, int64_t min_k, int *split) {
+    if (M < 1 || Nout < 1 || Kred < QO_GROUP || Kred % QO_GROUP) return -1;
+    if (bm < 1 || bn < 1 || target < 0 || cap < 1 || min_k < QO_GROUP || min_k % QO_GROUP) return -1;
+    int64_t base = ((M + bm - 1) / bm) * ((Nout + bn - 1) / bn);
+    int64_t s = cap;
+    if (target / base < s) s = target / base;
+    if (Kred / min_k < s) s = Kred / min_k;
+    if (s <= 1) s = 1;
+    *split = (int)s;
+    return 0;
+}
+
 /* [SK, Maths, Split-K]: tiles*s blocks run in ceil(tiles*s / SMs) waves. */
 int64_t oracle_waves(int64_t tiles, int64_t split, int64_t sms) {
     if (tiles < 1 || split < 1 || sms < 1) return -1;
@@ -345,8 +370,8 @@ int oracle_gemm(const uint16_t *A, const uint16_t *W, int64_t M, int64_t N, int6
     return 0;
 }
 
-/* Split-K with k cut into T = K/ktile tiles [SK, Concept: "cuts the k
- * dimension into s slices"].  When s does not divide T the slices are as
+/* Split-K with k cut into T = K/ktile tiles, grouped into s slices [SK,
+ * Concept: split-K].  When s does not divide T the slices are as
  * equal as whole tiles allow: the first T mod s slices get one extra tile.
  * Partial sums are FP32 planes [s, M, N] [SK, Maths: 4-byte partials];
  * the second pass adds them in FP32, ascending slice, and rounds to BF16. */

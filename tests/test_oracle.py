@@ -234,10 +234,53 @@ def test_partitioned_sampled_matches_full():
         assert np.array_equal(Ps, np.moveaxis(P, 0, 2)[np.ix_(rows, cols)])
 
 
-def test_partitioned_rejects_nondividing_split():
+def test_partitioned_rejects_split_beyond_the_groups():
     p = inputs.make_w4a16(1, 2560, 4, seed=12)
     with pytest.raises(ValueError):
-        oracle.qmm_partitioned(p["A"], p["Wq"], p["scales"], p["biases"], 3, 0)
+        oracle.qmm_partitioned(p["A"], p["Wq"], p["scales"], p["biases"], 21, 0)
+    with pytest.raises(ValueError):
+        oracle.qmm_partitioned(p["A"], p["Wq"], p["scales"], p["biases"], 0, 0)
+
+
+@pytest.mark.parametrize("G,s", [(10, 3), (10, 4), (10, 7), (11, 2), (20, 6), (7, 7), (20, 13)])
+def test_near_equal_partition_boundaries(G, s):
+    # a split that does not divide G: slices in order, the first G mod s one
+    # group longer; activations nonzero only in group g light up one plane
+    lengths = [G // s + 1] * (G % s) + [G // s] * (s - G % s)
+    owner = [i for i, n in enumerate(lengths) for _ in range(n)]
+    assert len(owner) == G
+    p = inputs.make_w4a16(2, 128 * G, 8, seed=17)
+    for g in range(G):
+        a = np.zeros((2, 128 * G), np.uint16)
+        a[:, g * 128:(g + 1) * 128] = p["A"][:, g * 128:(g + 1) * 128]
+        _, P = oracle.qmm_partitioned(a, p["Wq"], p["scales"], p["biases"], s, 1,
+                                      with_partials=True)
+        nonzero = [bool(np.any(P[i] != 0)) for i in range(s)]
+        assert nonzero == [i == owner[g] for i in range(s)], (g, nonzero)
+
+
+@pytest.mark.parametrize("split", list(range(1, 12)))
+def test_near_equal_partitions_cover_every_group(split):
+    # integer weights (scale 1, bias 0) and integer activations: every plane is
+    # an exact FP32 sum, so the planes add up to C64 exactly and C = BF16(C64);
+    # a dropped or doubled group breaks the first equality
+    rng = np.random.default_rng(18)
+    G = 11
+    M, Kred, Nout = 3, 128 * G, 5
+    q = rng.integers(0, 16, (Nout, Kred)).astype(np.uint32)
+    Wq = np.zeros((Nout, Kred // 8), np.uint32)
+    for j in range(8):
+        Wq |= q[:, j::8] << (4 * j)
+    scales = np.full((Nout, G), _bf16_bits(1.0), np.uint16)
+    biases = np.zeros((Nout, G), np.uint16)
+    A = inputs.f32_to_bf16_bits(rng.integers(-2, 3, (M, Kred)).astype(np.float32))
+    C64 = oracle.qmm(A, Wq, scales, biases, threads=2)
+    assert np.array_equal(C64, _bits_to_f64(A) @ q.T.astype(np.float64))
+    C, P = oracle.qmm_partitioned(A, Wq, scales, biases, split, 1, with_partials=True)
+    if split > 1:
+        assert np.array_equal(P.sum(axis=0), C64)
+        assert all(np.any(P[i] != 0) for i in range(split))
+    assert np.array_equal(C, oracle.bf16_round(C64))
 
 
 # ---- policy and waves ------------------------------------------------------
@@ -271,6 +314,50 @@ def test_plan_matches_divisor_formulation():
         min_k = 128 * int(rng.integers(1, 9))
         assert oracle.splitk_plan(M, Kred, Nout, bm, bn, target, cap, min_k) == \
             _plan_property(M, Kred, Nout, bm, bn, target, cap, min_k)
+
+
+def _plan_near_equal_property(M, Kred, Nout, bm, bn, target, cap, min_k):
+    """The largest s >= 2 within every bound (no divisibility), else 1."""
+    base = math.ceil(M / bm) * math.ceil(Nout / bn)
+    ok = [s for s in range(2, Kred // 128 + 1)
+          if s <= cap and s * base <= target and s * min_k <= Kred]
+    return max(ok) if ok else 1
+
+
+def test_plan_near_equal_fuzz():
+    rng = np.random.default_rng(19)
+    agree = 0
+    for _ in range(3000):
+        M = int(rng.integers(1, 3000))
+        Kred = 128 * int(rng.integers(1, 101))
+        Nout = int(rng.integers(1, 12000))
+        bm, bn = int(rng.choice([8, 16, 32, 64, 128])), int(rng.choice([32, 64, 128, 256]))
+        target = int(rng.integers(0, 2000))
+        cap = int(rng.integers(1, 33))
+        min_k = 128 * int(rng.integers(1, 9))
+        s = oracle.splitk_plan_near_equal(M, Kred, Nout, bm, bn, target, cap, min_k)
+        assert s == _plan_near_equal_property(M, Kred, Nout, bm, bn, target, cap, min_k)
+        d = oracle.splitk_plan(M, Kred, Nout, bm, bn, target, cap, min_k)
+        # the divisor rule never splits further, and agrees when s divides G
+        assert d <= s
+        if (Kred // 128) % s == 0:
+            assert d == s
+            agree += 1
+    assert agree > 100
+
+
+def test_plan_near_equal_takes_the_models_best_one_wave_split():
+    # the Split-K page's model: 16 output tiles, the largest split whose
+    # blocks fit one wave -- 6 on 108 SMs, 8 on 132 -- for k = 16384 (128
+    # groups), which 6 does not divide
+    gold = _golden("splitk_waves_model.json")
+    M, Nout = gold["output"]
+    bm, bn = gold["tile"]
+    for arch in ("a100", "h100"):
+        s = oracle.splitk_plan_near_equal(M, 16384, Nout, bm, bn, gold[arch]["sms"], 16)
+        assert s == gold[arch]["best_split_one_wave"]
+    # the divisor rule stops at 4 on the A100 (128 groups)
+    assert oracle.splitk_plan(M, 16384, Nout, bm, bn, gold["a100"]["sms"], 16) == 4
 
 
 def test_waves_model_table():
