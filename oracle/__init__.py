@@ -210,7 +210,8 @@ def splitk_plan(M, Kred, Nout, bm, bn, target, cap, min_k=128) -> int:
 
 
 def splitk_plan_near_equal(M, Kred, Nout, bm, bn, target, cap, min_k=128) -> int:
-    """The plan without the divisibility step (near-equal partitions)."""
+    """The plan for near-equal partitions: the fewest partitions that reach the
+    shortest longest partition within the policy's bounds."""
     s = ctypes.c_int(0)
     _check(_load().oracle_splitk_plan_near_equal(M, Kred, Nout, bm, bn, target, cap, min_k,
                                                  ctypes.byref(s)), "splitk_plan_near_equal")

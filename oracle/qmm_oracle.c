@@ -328,22 +328,31 @@ int oracle_splitk_plan(int64_t M, int64_t Kred, int64_t Nout, int64_t bm, int64_
     return 0;
 }
 
-/* The plan without the divisibility step, for near-equal slices: the
- * largest s within the three bounds of [TL, Task 3] (cap, floor(target/base),
- * floor(Kred/min_k)); s <= 1 means the unsplit kernel.  With target = one
- * wave of blocks this is the split the model of [SK, Maths, Split-K] picks,
- * the largest one whose blocks still fit a single wave; there the slices
- * need not divide k (its A100 example takes s = 6 of 256 k-tiles). */
+/* The plan for near-equal slices (no divisibility step).  B = min(cap,
+ * floor(target/base), floor(Kred/min_k)) bounds the split as in [TL, Task 3];
+ * B <= 1 means the unsplit kernel.  The longest slice holds ceil(G/s) groups,
+ * and no split within the bound makes it shorter than L = ceil(G/B); the plan
+ * takes the fewest slices that reach L, s = ceil(G/L).  That is the model of
+ * [SK, Maths, Split-K]: the time falls with the work of the longest slice
+ * while the blocks fit one wave, and more slices than needed only add partial
+ * planes to reduce.  There the slices need not divide k: its A100 example
+ * takes s = 6 of 256 k-tiles.  When B divides G the plan is B, the divisor
+ * rule's split. */
 int oracle_splitk_plan_near_equal(int64_t M, int64_t Kred, int64_t Nout, int64_t bm, int64_t bn,
                                   int64_t target, int64_t cap, int64_t min_k, int *split) {
     if (M < 1 || Nout < 1 || Kred < QO_GROUP || Kred % QO_GROUP) return -1;
     if (bm < 1 || bn < 1 || target < 0 || cap < 1 || min_k < QO_GROUP || min_k % QO_GROUP) return -1;
+    int64_t G = Kred / QO_GROUP;
     int64_t base = ((M + bm - 1) / bm) * ((Nout + bn - 1) / bn);
-    int64_t s = cap;
-    if (target / base < s) s = target / base;
-    if (Kred / min_k < s) s = Kred / min_k;
-    if (s <= 1) s = 1;
-    *split = (int)s;
+    int64_t B = cap;
+    if (target / base < B) B = target / base;
+    if (Kred / min_k < B) B = Kred / min_k;
+    if (B <= 1) {
+        *split = 1;
+        return 0;
+    }
+    int64_t L = (G + B - 1) / B; /* shortest reachable longest slice */
+    *split = (int)((G + L - 1) / L);
     return 0;
 }
 

@@ -317,11 +317,14 @@ def test_plan_matches_divisor_formulation():
 
 
 def _plan_near_equal_property(M, Kred, Nout, bm, bn, target, cap, min_k):
-    """The largest s >= 2 within every bound (no divisibility), else 1."""
+    """Among the splits within every bound (no divisibility), those whose
+    longest partition, ceil(G/s) groups, is shortest; the smallest of them."""
+    G = Kred // 128
     base = math.ceil(M / bm) * math.ceil(Nout / bn)
-    ok = [s for s in range(2, Kred // 128 + 1)
-          if s <= cap and s * base <= target and s * min_k <= Kred]
-    return max(ok) if ok else 1
+    ok = [s for s in range(1, G + 1)
+          if s == 1 or (s <= cap and s * base <= target and s * min_k <= Kred)]
+    best = min(-(-G // s) for s in ok)
+    return min(s for s in ok if -(-G // s) == best)
 
 
 def test_plan_near_equal_fuzz():
