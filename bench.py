@@ -76,9 +76,9 @@ def partition_algorithmic(M, Kred, Nout, split, partial_bytes=2):
 NCU_TRAFFIC = {
     # python bench.py --only down:128 --launch-list --steps 1 --warmup 3 under
     # ncu --set full -k regex:w4a16_tc -s 2 -c 1: dram__bytes_read.sum + _write.sum
-    ("down", 128, 4): (15788544, "4009c99ebdbc020e"),
+    ("down", 128, 4): (15788544, "4226552ed820491b"),
     # the same for --only gate:32
-    ("gate", 32, 2): (13462016, "4009c99ebdbc020e"),
+    ("gate", 32, 2): (13462016, "4226552ed820491b"),
 }
 TC_SOURCES = ("qmm_w4a16_tc.cu", "qmm_sm100.cuh", "qmm_device.cuh", "qmm_internal.h")
 
@@ -219,13 +219,16 @@ class Workload:
                                for _ in range(self.R - 1)]
         self.C = [[torch.empty((M, Nout), dtype=torch.bfloat16, device=device)
                    for (_, M, _, Nout) in self.calls] for _ in range(self.R)]
-        self.split = []
+        self.split, self.split_ne = [], []
         ws_max = 16
         for (_, M, Kred, Nout) in self.calls:
             pol = Q.qmm_policy_preset(Q.QMM_PRESET_GB300, M)
             s = Q.qmm_splitk_plan(M, Kred, Nout, pol)
+            # the near-equal rule's split (qmm_set_partitions), never smaller
+            s_ne = Q.qmm_splitk_plan_near_equal(M, Kred, Nout, pol)
             self.split.append(s)
-            ws_max = max(ws_max, Q.qmm_splitk_workspace_bytes(M, Nout, s, Q.QMM_PARTIAL_BF16))
+            self.split_ne.append(s_ne)
+            ws_max = max(ws_max, Q.qmm_splitk_workspace_bytes(M, Nout, s_ne, Q.QMM_PARTIAL_BF16))
         # one workspace for every call, zeroed, with room beyond the largest
         # planes for the fused reduce's counter area (its last 32 KB), which
         # planes therefore never touch
@@ -369,6 +372,7 @@ def run_gpu(args, rank, world, local_rank):
     ms_nopdl = time_variant(Q.qmm_set_pdl, False)
     ms_wflip = time_variant(Q.qmm_set_weights_static, not static_weights)
     ms_fused = time_variant(Q.qmm_set_reduce, Q.QMM_REDUCE_FUSED)
+    ms_ne = time_variant(Q.qmm_set_partitions, Q.QMM_PARTITIONS_NEAR_EQUAL)
 
     # per call: policy split vs the unsplit control, each timed as a graph of
     # back-to-back launches over copies of its inputs larger than L2.  These and
@@ -389,6 +393,15 @@ def run_gpu(args, rank, world, local_rank):
                              workspace=wl.ws)
         us_s = graph_us_per_launch(lambda j: call(j, 0), len(cps), stream)
         us_1 = graph_us_per_launch(lambda j: call(j, 1), len(cps), stream) if s > 1 else us_s
+        s_ne = wl.split_ne[i]
+        if s_ne != s:
+            prev_pr = Q.qmm_set_partitions(Q.QMM_PARTITIONS_NEAR_EQUAL)
+            us_ne = graph_us_per_launch(lambda j: call(j, 0), len(cps), stream)
+            Q.qmm_set_partitions(prev_pr)
+        else:
+            us_ne = us_s
+        nb_ne, fl_ne = algorithmic(M, Kred, Nout, s_ne)
+        t_roof_ne, _ = roofline_time_s(nb_ne, fl_ne, peaks)
         nb, fl = algorithmic(M, Kred, Nout, s)
         nb1, _ = algorithmic(M, Kred, Nout, 1)
         t_roof, bound = roofline_time_s(nb, fl, peaks)
@@ -399,7 +412,10 @@ def run_gpu(args, rank, world, local_rank):
                          "roof_frac_split": round(t_roof * 1e6 / us_s, 4),
                          "roof_frac_unsplit": round(t_roof1 * 1e6 / us_1, 4),
                          "tbps_split": round(nb / us_s / 1e6, 3),
-                         "tflops_split": round(fl / us_s / 1e6, 2), "copies": len(cps)})
+                         "tflops_split": round(fl / us_s / 1e6, 2),
+                         "split_near_equal": s_ne, "us_near_equal": round(us_ne, 3),
+                         "roof_frac_near_equal": round(t_roof_ne * 1e6 / us_ne, 4),
+                         "copies": len(cps)})
         if dom is None or us_s > per_call[dom["index"]]["us_split"]:
             dom = {"index": i, "split": s}
             # the call's partition kernel on its own (the roofline's kernel) and
@@ -422,6 +438,7 @@ def run_gpu(args, rank, world, local_rank):
     dense = dense_sweep(Q, device, stream, sms, l2) if rank == 0 else None
     e2e = run_e2e(wl, Q, device, stream, min(args.steps, 20))
     return {"ms": ms, "ms_nopdl": ms_nopdl, "ms_wflip": ms_wflip, "ms_fused": ms_fused,
+            "ms_ne": ms_ne,
             "per_call": per_call, "dom": dom,
             "clocks": sample, "wl": wl,
             "peaks": peaks,
@@ -754,6 +771,7 @@ def main():
            ("value_weights_dynamic" if args.weights == "static" else "value_weights_static"):
                round(job_value_us(res["ms_wflip"], 1, args.steps, ncalls), 4),
            "value_fused_reduce": round(job_value_us(res["ms_fused"], 1, args.steps, ncalls), 4),
+           "value_near_equal": round(job_value_us(res["ms_ne"], 1, args.steps, ncalls), 4),
            "roofline": roof, "gpu_launches": args.steps * wl.launches_per_step(),
            "clocks": res["clocks"], "e2e": res["e2e"], "per_call": res["per_call"],
            "dense_splitk_512x512x16384": res["dense"], "prefill_M2048": res["prefill"]}

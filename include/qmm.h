@@ -21,7 +21,9 @@
  * `split` partitions of equal length that start and end on 128-group
  * boundaries; partition p writes its own partial plane [M, Nout] of the
  * workspace (no atomics); a second kernel adds the planes in FP32, in
- * ascending p, and rounds once to BF16.
+ * ascending p, and rounds once to BF16.  An opt-in rule
+ * (qmm_set_partitions) also takes splits that do not divide the group count,
+ * with near-equal partitions.
  *
  * Conventions for every entry point:
  *   - Device pointers are CUDA device memory owned by the caller; the
@@ -52,7 +54,7 @@ extern "C" {
 enum {
     QMM_OK = 0,
     QMM_EINVAL = -1,     /* null pointer, non-positive size, unknown enum value */
-    QMM_ESHAPE = -2,     /* Kred not a multiple of 128, split not dividing Kred/128, size overflow */
+    QMM_ESHAPE = -2,     /* Kred not a multiple of 128, split the partition rule rejects, size overflow */
     QMM_EWORKSPACE = -3, /* workspace missing or smaller than qmm_splitk_workspace_bytes() */
     QMM_ECUDA = -4,      /* a CUDA call or kernel launch failed */
     QMM_EALIGN = -5,     /* a pointer breaks the alignment rules above */
@@ -106,6 +108,18 @@ int qmm_kernel_tile(int M, int *bm, int *bn);
  * QMM_ESHAPE (Kred not a positive multiple of 128). */
 int qmm_splitk_plan(int M, int Kred, int Nout, const qmm_policy *pol, int *split_out);
 
+/* The occupancy rule above without its divisibility step, for near-equal
+ * partitions (the longest holds ceil(G/split) of the G = Kred/128 groups):
+ *   bound = min(cap, floor(target_blocks/base), floor(Kred/min_k_per_split));
+ *   bound <= 1 selects the unsplit kernel; otherwise
+ *   longest = ceil(G/bound), the shortest longest partition within the bound,
+ *   split = ceil(G/longest), the fewest partitions that reach it (more would
+ *   only add partial planes to the reduce).
+ * The split the policy takes under QMM_PARTITIONS_NEAR_EQUAL.  It is never
+ * smaller than qmm_splitk_plan's and equals it whenever bound divides G.
+ * Pure host function; same arguments and returns as qmm_splitk_plan. */
+int qmm_splitk_plan_near_equal(int M, int Kred, int Nout, const qmm_policy *pol, int *split_out);
+
 /* Bytes of workspace the split path needs: split*M*Nout*(2 or 4), or 0 when
  * split <= 1; when the fused reduce applies (QMM_REDUCE_FUSED), the planes
  * rounded up to 256 bytes, plus 256, plus QMM_FUSED_COUNTER_BYTES.  Returns 0 for
@@ -113,9 +127,12 @@ int qmm_splitk_plan(int M, int Kred, int Nout, const qmm_policy *pol, int *split
 size_t qmm_splitk_workspace_bytes(int M, int Nout, int split, int partial_dtype);
 
 /* C = A . W^T for the W4A16-g128 format (see the top of this header).
- *   split_req  0: split from the policy; 1: the unsplit kernel (the
- *              control, writes C directly); s > 1: forced split, must
- *              divide Kred/128 (QMM_ESHAPE otherwise).
+ *   split_req  0: split from the policy (qmm_splitk_plan, or
+ *              qmm_splitk_plan_near_equal under QMM_PARTITIONS_NEAR_EQUAL);
+ *              1: the unsplit kernel (the control, writes C directly);
+ *              s > 1: forced split, which must divide Kred/128 under
+ *              QMM_PARTITIONS_EQUAL and be at most Kred/128 under
+ *              QMM_PARTITIONS_NEAR_EQUAL (QMM_ESHAPE otherwise).
  *   pol        policy used when split_req == 0; NULL = QMM_PRESET_GB300
  *              for this M on the current device.
  *   workspace  device buffer for the partial planes [split, M, Nout] of
@@ -135,9 +152,12 @@ int qmm_w4a16_g128(const void *A, const uint32_t *Wq, const void *scales, const 
  * Task 2: grid z = partition, each partition writes its own plane, no
  * atomics): partials[p, m, n] = round(sum over the groups of partition p of
  * A[m, k] * w[n, k]), FP32 accumulation rounded once to partial_dtype (RNE).
- * Partition p covers groups [p*G/split, (p+1)*G/split), G = Kred/128.
- *   split      1 <= split <= G, must divide G (QMM_ESHAPE otherwise); no
- *              policy is applied (take it from qmm_splitk_plan).
+ * Partition p covers groups [p*G/split, (p+1)*G/split), G = Kred/128; under
+ * QMM_PARTITIONS_NEAR_EQUAL a split that does not divide G gives partition p
+ * floor(G/split) groups, one more for p < G mod split, in order.
+ *   split      1 <= split <= G; under QMM_PARTITIONS_EQUAL it must divide G
+ *              (QMM_ESHAPE otherwise).  No policy is applied (take it from
+ *              the plan of the current rule).
  *   partials   device buffer [split, M, Nout] of partial_dtype, planes
  *              contiguous, of at least split*M*Nout*(2 or 4) bytes
  *              (partials_bytes; QMM_EWORKSPACE when smaller).
@@ -229,6 +249,26 @@ int qmm_set_pdl(int enable);
 #define QMM_FUSED_COUNTER_BYTES 32768
 enum { QMM_REDUCE_KERNEL = 0, QMM_REDUCE_FUSED = 1 };
 int qmm_set_reduce(int mode);
+
+/* Partition rule of the W4A16 calls (process-wide, thread-safe):
+ *   QMM_PARTITIONS_EQUAL (default)  the chapter's rule (Task 2, Task 3):
+ *       a split divides G = Kred/128, every partition holds G/split groups,
+ *       and the policy lowers its split until it divides G
+ *       (qmm_splitk_plan).
+ *   QMM_PARTITIONS_NEAR_EQUAL  any split 1 <= s <= G.  Partition p holds
+ *       floor(G/s) groups, one more for p < G mod s, in order: the cut the
+ *       dense GEMM above takes for its k-tiles.  The policy takes
+ *       qmm_splitk_plan_near_equal (gpu-kernels-explained, "Split-K, streams
+ *       and overlap", Maths: the time falls with the slice length while the
+ *       blocks fit one wave).  Down-type shapes (76 groups) then split 7 ways
+ *       instead of 4.
+ * Applies to qmm_w4a16_g128, qmm_w4a16_g128_partition and
+ * qmm_w4a16_g128_noalloc.  With a split that divides G both rules cut the
+ * same partitions and give the same bits.  Size workspaces with the split
+ * the call will use (qmm_splitk_plan_near_equal's is an upper bound for both
+ * rules).  Returns the previous rule, or QMM_EINVAL for an unknown value. */
+enum { QMM_PARTITIONS_EQUAL = 0, QMM_PARTITIONS_NEAR_EQUAL = 1 };
+int qmm_set_partitions(int mode);
 
 /* Static weights (off by default).  enable = 1 promises that no kernel issued
  * earlier on the same stream writes the packed weights, scales or biases of

@@ -63,6 +63,23 @@ std::atomic<int> g_kernels{QMM_KERNELS_DEFAULT};
 std::atomic<int> g_pdl{1};
 std::atomic<int> g_wstatic{0};
 std::atomic<int> g_reduce{QMM_REDUCE_KERNEL};
+std::atomic<int> g_partitions{QMM_PARTITIONS_EQUAL};
+
+// a split the current partition rule accepts for G groups (grid z <= 65535)
+bool split_fits(int64_t G, int64_t split) {
+    if (split < 1 || split > G || split > 65535) return false;
+    return qmm::partitions_near_equal() || G % split == 0;
+}
+
+// the three bounds of the occupancy rule: min(cap, floor(target/base),
+// floor(Kred/min_k)); pol and the shape already checked
+int64_t plan_bound(int M, int Kred, int Nout, const qmm_policy* pol) {
+    const int64_t base = ceil_div(M, pol->bm) * ceil_div(Nout, pol->bn);
+    int64_t bound = pol->cap;
+    if (pol->target_blocks / base < bound) bound = pol->target_blocks / base;
+    if (Kred / pol->min_k_per_split < bound) bound = Kred / pol->min_k_per_split;
+    return bound;
+}
 
 template <size_t N>
 const qmm::Family& pick(const qmm::Family (&table)[N], int M) {
@@ -88,6 +105,26 @@ bool pdl_enabled() { return g_pdl.load(std::memory_order_relaxed) != 0; }
 bool weights_static() { return g_wstatic.load(std::memory_order_relaxed) != 0; }
 
 bool reduce_fused() { return g_reduce.load(std::memory_order_relaxed) == QMM_REDUCE_FUSED; }
+
+bool partitions_near_equal() {
+    return g_partitions.load(std::memory_order_relaxed) == QMM_PARTITIONS_NEAR_EQUAL;
+}
+
+int choose_split(int M, int Kred, int Nout, int split_req, const qmm_policy* pol, int* split) {
+    if (split_req == 0) {
+        qmm_policy local;
+        if (!pol) {
+            const int rc = qmm_policy_preset(QMM_PRESET_GB300, M, 0, &local);
+            if (rc != QMM_OK) return rc;
+            pol = &local;
+        }
+        return partitions_near_equal() ? qmm_splitk_plan_near_equal(M, Kred, Nout, pol, split)
+                                       : qmm_splitk_plan(M, Kred, Nout, pol, split);
+    }
+    if (!split_fits(Kred / kGroup, split_req)) return QMM_ESHAPE;
+    *split = split_req;
+    return QMM_OK;
+}
 
 bool gemm_uses_tc() { return g_kernels.load(std::memory_order_relaxed) != QMM_KERNELS_MMA_SYNC; }
 
@@ -132,6 +169,11 @@ int qmm_set_weights_static(int enable) { return g_wstatic.exchange(enable ? 1 : 
 int qmm_set_reduce(int mode) {
     if (mode != QMM_REDUCE_KERNEL && mode != QMM_REDUCE_FUSED) return QMM_EINVAL;
     return g_reduce.exchange(mode);
+}
+
+int qmm_set_partitions(int mode) {
+    if (mode != QMM_PARTITIONS_EQUAL && mode != QMM_PARTITIONS_NEAR_EQUAL) return QMM_EINVAL;
+    return g_partitions.exchange(mode);
 }
 
 int qmm_kernel_status(int* status, int clear) {
@@ -187,14 +229,30 @@ int qmm_splitk_plan(int M, int Kred, int Nout, const qmm_policy* pol, int* split
     if (!split_out || !policy_ok(pol) || M < 1 || Nout < 1) return QMM_EINVAL;
     if (Kred < qmm::kGroup || Kred % qmm::kGroup) return QMM_ESHAPE;
     const int64_t G = Kred / qmm::kGroup;
-    const int64_t base = ceil_div(M, pol->bm) * ceil_div(Nout, pol->bn);
-    int64_t bound = pol->cap;
-    if (pol->target_blocks / base < bound) bound = pol->target_blocks / base;
-    if (Kred / pol->min_k_per_split < bound) bound = Kred / pol->min_k_per_split;
+    const int64_t bound = plan_bound(M, Kred, Nout, pol);
     int best = 1;
     for (int64_t d = 2; d <= bound && d <= G; ++d)
         if (G % d == 0) best = static_cast<int>(d);
     *split_out = best;
+    return QMM_OK;
+}
+
+// The same three bounds with no divisibility step.  A partition's work is set
+// by the longest one, ceil(G/s) groups, which no split within the bound takes
+// below ceil(G/bound); the plan is the fewest partitions that reach it, since
+// more would only add partial planes.  floor(Kred/min_k) <= G, so every
+// partition keeps at least one group.
+int qmm_splitk_plan_near_equal(int M, int Kred, int Nout, const qmm_policy* pol, int* split_out) {
+    if (!split_out || !policy_ok(pol) || M < 1 || Nout < 1) return QMM_EINVAL;
+    if (Kred < qmm::kGroup || Kred % qmm::kGroup) return QMM_ESHAPE;
+    const int64_t G = Kred / qmm::kGroup;
+    const int64_t bound = plan_bound(M, Kred, Nout, pol);
+    if (bound <= 1) {
+        *split_out = 1;
+        return QMM_OK;
+    }
+    const int64_t longest = ceil_div(G, bound);
+    *split_out = static_cast<int>(ceil_div(G, longest));
     return QMM_OK;
 }
 
@@ -241,20 +299,9 @@ int qmm_w4a16_g128(const void* A, const uint32_t* Wq, const void* scales, const 
     int rc = check_device();
     if (rc != QMM_OK) return rc;
 
-    const int G = Kred / qmm::kGroup;
-    int split = split_req;
-    if (split_req == 0) {
-        qmm_policy local;
-        if (!pol) {
-            rc = qmm_policy_preset(QMM_PRESET_GB300, M, 0, &local);
-            if (rc != QMM_OK) return rc;
-            pol = &local;
-        }
-        rc = qmm_splitk_plan(M, Kred, Nout, pol, &split);
-        if (rc != QMM_OK) return rc;
-    } else if (split > G || G % split != 0 || split > 65535) {
-        return QMM_ESHAPE;
-    }
+    int split = 1;
+    rc = qmm::choose_split(M, Kred, Nout, split_req, pol, &split);
+    if (rc != QMM_OK) return rc;
 
     if (split == 1) {
         rc = launched(qmm::launch_w4a16(fam, A, Wq, scales, biases, C, qmm::kOutBf16, M, Kred,
@@ -287,8 +334,7 @@ int qmm_w4a16_g128_partition(const void* A, const uint32_t* Wq, const void* scal
         return QMM_EINVAL;
     if (partial_dtype != QMM_PARTIAL_BF16 && partial_dtype != QMM_PARTIAL_F32) return QMM_EINVAL;
     if (Kred < qmm::kGroup || Kred % qmm::kGroup) return QMM_ESHAPE;
-    const int G = Kred / qmm::kGroup;
-    if (split > G || G % split != 0 || split > 65535) return QMM_ESHAPE;
+    if (!split_fits(Kred / qmm::kGroup, split)) return QMM_ESHAPE;
     if (!aligned(A, 16) || !aligned(Wq, 16) || !aligned(partials, 16) || !aligned(scales, 16) ||
         !aligned(biases, 16))
         return QMM_EALIGN;

@@ -7,6 +7,8 @@
 #include <cstddef>
 #include <cstdint>
 
+#include "qmm.h"
+
 namespace qmm {
 
 constexpr int kGroup = 128;  // quantization group length along the reduction axis
@@ -65,6 +67,13 @@ bool pdl_enabled();
 bool weights_static();
 // Fused last-CTA reduce of the tcgen05 kernels (qmm_set_reduce).
 bool reduce_fused();
+// Near-equal partitions for splits that do not divide the groups (qmm_set_partitions).
+bool partitions_near_equal();
+// The split a matmul call dispatches: the policy's (split_req 0, pol NULL =
+// the GB300 preset) under the current partition rule, or the forced split if
+// that rule accepts it (QMM_ESHAPE otherwise).  Shape and policy checked by
+// the caller; returns a QMM_* code.
+int choose_split(int M, int Kred, int Nout, int split_req, const qmm_policy* pol, int* split);
 struct LaunchAttrs {
     cudaLaunchAttribute attr[1];
 };

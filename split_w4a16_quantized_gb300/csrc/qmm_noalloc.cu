@@ -15,6 +15,7 @@
 #include <mutex>
 
 #include "qmm.h"
+#include "qmm_internal.h"
 
 namespace qmm {
 namespace {
@@ -55,21 +56,10 @@ int qmm_w4a16_g128_noalloc(const void* A, const uint32_t* Wq, const void* scales
         return QMM_EINVAL;
     if (partial_dtype != QMM_PARTIAL_BF16 && partial_dtype != QMM_PARTIAL_F32) return QMM_EINVAL;
     if (Kred < 128 || Kred % 128) return QMM_ESHAPE;
-    const int G = Kred / 128;
     // the split this call will use, to size its partial planes
-    int split = split_req;
-    if (split == 0) {
-        qmm_policy local;
-        if (!pol) {
-            const int rc = qmm_policy_preset(QMM_PRESET_GB300, M, 0, &local);
-            if (rc != QMM_OK) return rc;
-            pol = &local;
-        }
-        const int rc = qmm_splitk_plan(M, Kred, Nout, pol, &split);
-        if (rc != QMM_OK) return rc;
-    } else if (split > G || G % split != 0) {
-        return QMM_ESHAPE;
-    }
+    int split = 1;
+    const int rc = qmm::choose_split(M, Kred, Nout, split_req, pol, &split);
+    if (rc != QMM_OK) return rc;
     // the last QMM_FUSED_COUNTER_BYTES (and 256 bytes of slack) are kept for
     // the fused reduce's counters in every mode, so no planes ever land there
     // and the counters stay zero from the module's load on

@@ -4,7 +4,9 @@
 // weight rows = output columns) over one partition of the reduction axis:
 // groups [p*gpp, (p+1)*gpp) with gpp = (Kred/128)/split (tiny-llm book,
 // "Week 2 Day 7: Split-K Prefill", Task 2: equal partitions on 128-group
-// boundaries, grid z = partition).  With split = 1 it writes C directly (the
+// boundaries, grid z = partition); a split that does not divide the group
+// count takes near-equal partitions, the first G mod split one group
+// longer.  With split = 1 it writes C directly (the
 // unsplit control); otherwise it writes its own partial plane [M, Nout] of
 // the workspace with no atomics.
 //
@@ -49,7 +51,9 @@ struct W4Params {
     const uint16_t* scales;  // BF16 bits [Nout, G]
     const uint16_t* biases;  // BF16 bits [Nout, G]
     void* out;               // BF16 or FP32 planes [split, M, Nout]
-    int M, Kred, Nout, G, gpp;
+    int M, Kred, Nout, G;
+    int gpp;     // groups in the longest partition (sizes shared memory)
+    int gq, gr;  // G / split, G % split: partition p holds gq + (p < gr) groups
     int out_mode;
 };
 
@@ -88,7 +92,8 @@ __global__ void __launch_bounds__(C::THREADS) w4a16_kernel(const W4Params p) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g8 = lane >> 2, t4 = lane & 3;
     const int n0 = blockIdx.x * BN, m0 = blockIdx.y * BM, part = blockIdx.z;
-    const int ngrp = p.gpp, gbeg = part * p.gpp;
+    const int ngrp = p.gq + (part < p.gr ? 1 : 0);
+    const int gbeg = part * p.gq + (part < p.gr ? part : p.gr);
     const size_t wrow = static_cast<size_t>(p.Kred) / 8;  // words per weight row
     pdl_trigger();
     pdl_wait();
@@ -347,7 +352,9 @@ int launch_w4a16(const Family& fam, const void* A, const uint32_t* Wq, const voi
     p.Kred = Kred;
     p.Nout = Nout;
     p.G = Kred / kGroup;
-    p.gpp = p.G / split;
+    p.gq = p.G / split;
+    p.gr = p.G % split;
+    p.gpp = p.gq + (p.gr ? 1 : 0);
     p.out_mode = out_mode;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     switch (fam.bm) {

@@ -5,7 +5,9 @@
 // rows (m0..m0+BNA-1) over one partition of the reduction axis (tiny-llm
 // book, "Week 2 Day 7: Split-K Prefill", Task 2: grid z = partition, equal
 // partitions on 128-group boundaries, each writes its own partial plane, no
-// atomics).  The product is computed transposed, C^T tile = W . A^T:
+// atomics).  A split that does not divide the group count takes near-equal
+// partitions, the first G mod split one group longer.  The product is
+// computed transposed, C^T tile = W . A^T:
 //   - MMA A operand = dequantized weights, 128 rows x 16 k, held in TENSOR
 //     MEMORY (lane = weight row).  The weights go packed HBM -> shared memory
 //     (TMA) -> registers (unpack + dequant) -> tensor memory (tcgen05.st);
@@ -130,14 +132,14 @@ struct TcParams {
     const uint16_t* biases;
     void* out;
     int* status;
-    int M, Kred, Nout, G, gpp, out_mode;
+    int M, Kred, Nout, G, out_mode;
+    int gpp;        // groups in the longest partition (sizes the rings)
+    int gq, gr;     // G / split, G % split: partition p holds gq + (p < gr) groups
     int weights_static;  // 1: only the activation copies wait for earlier kernels
     int fused;           // 1: the last CTA of an output tile adds its planes into C
     void* C;             // BF16 [M, Nout] (fused reduce)
     uint32_t* counters;  // one per output tile (fused reduce), zero between calls
     int tma_store;  // 1: the output tile leaves through a TMA store of a staged tile
-    int wtail;      // groups in the last weight stage when gpp % WGPS != 0, else 0
-    int atail;      // groups in the last activation stage when gpp % AGPS != 0, else 0
     Ring wr, ar;    // weight ring, activation ring (same groups per stage)
 };
 
@@ -267,21 +269,22 @@ __device__ __forceinline__ TcSmem carve(uint8_t* base, const TcParams& p) {
 // (released by the MMA commits).  Both rings are polled without blocking, so
 // neither waits behind the other.  Weight rows of 128 bytes halve the TMA
 // requests of 64-byte rows; a box that runs past the end of a weight row is
-// zero-filled.
+// zero-filled.  The partition holds gpp groups from group gbeg on.
 template <int BNA>
 __device__ __forceinline__ void tc_producer(const TcSmem& sm, const TcParams& p,
                                             const CUtensorMap* wmap, const CUtensorMap* amap,
-                                            const CUtensorMap* amap_t, int n0, int m0, int gbeg,
-                                            volatile int* abort) {
+                                            const CUtensorMap* amap_1, int n0, int m0, int gbeg,
+                                            int gpp, volatile int* abort) {
     using C = TcCfg<BNA>;
-    const int nw = (p.gpp + C::WGPS - 1) >> C::WGPS_LOG2;
-    const int na = (p.gpp + C::AGPS - 1) >> C::AGPS_LOG2;
-    // a last activation stage of a tail goes through the tail map, whose box
-    // holds exactly those groups; a last weight stage of one or two groups
-    // takes one two-group box
+    const int nw = (gpp + C::WGPS - 1) >> C::WGPS_LOG2;
+    const int na = (gpp + C::AGPS - 1) >> C::AGPS_LOG2;
+    // a last activation stage of fewer than AGPS groups is filled one group
+    // at a time through the one-group map; a last weight stage of one or two
+    // groups takes one two-group box
     constexpr int kBoxes = C::WGPS / 2;  // two-group boxes per weight stage
-    const int alast = p.atail ? na - 1 : na;
-    const int wlast_boxes = p.wtail == 0 ? kBoxes : (p.wtail + 1) >> 1;
+    const int wtail = gpp & (C::WGPS - 1), atail = gpp & (C::AGPS - 1);
+    const int alast = atail ? na - 1 : na;
+    const int wlast_boxes = wtail == 0 ? kBoxes : (wtail + 1) >> 1;
     int jw = 0, ja = 0, sw = 0, sa = 0;
     uint32_t pw = 0, pa = 0;
     auto issue_w = [&]() {
@@ -311,10 +314,17 @@ __device__ __forceinline__ void tc_producer(const TcSmem& sm, const TcParams& p,
             progress = true;
         }
         if (ja < na && mbar_probe(&sm.act_empty[sa], pa ^ 1)) {
-            const bool t = ja == alast;
-            mbar_arrive_expect_tx(&sm.act_full[sa], t ? p.atail * C::ACT_GROUP : C::ACT_STAGE);
-            tma_load_3d(sm.act + sa * C::ACT_STAGE, t ? amap_t : amap, &sm.act_full[sa], 0, m0,
-                        (gbeg + ja * C::AGPS) * 2);
+            const int g = gbeg + ja * C::AGPS;
+            uint8_t* dst = sm.act + sa * C::ACT_STAGE;
+            if (ja == alast) {
+                mbar_arrive_expect_tx(&sm.act_full[sa], atail * C::ACT_GROUP);
+                for (int t = 0; t < atail; ++t)
+                    tma_load_3d(dst + t * C::ACT_GROUP, amap_1, &sm.act_full[sa], 0, m0,
+                                (g + t) * 2);
+            } else {
+                mbar_arrive_expect_tx(&sm.act_full[sa], C::ACT_STAGE);
+                tma_load_3d(dst, amap, &sm.act_full[sa], 0, m0, g * 2);
+            }
             ++ja;
             if (++sa == p.ar.n) { sa = 0; pa ^= 1; }
             progress = true;
@@ -339,10 +349,10 @@ __device__ __forceinline__ void tc_producer(const TcSmem& sm, const TcParams& p,
 // MMA issuer c (one thread): groups c, c + NACC, ... into accumulator c.
 template <int BNA>
 __device__ __forceinline__ void tc_issuer(const TcSmem& sm, const TcParams& p, uint32_t tmem,
-                                          int c, volatile int* abort) {
+                                          int c, int gpp, volatile int* abort) {
     using C = TcCfg<BNA>;
     const uint32_t d_tm = tmem + c * BNA;
-    for (int i = c; i < p.gpp; i += C::NACC) {
+    for (int i = c; i < gpp; i += C::NACC) {
         int sa, within;
         uint32_t ph;
         ring_pos(p.ar, i, sa, ph, within);
@@ -370,7 +380,7 @@ __device__ __forceinline__ void tc_issuer(const TcSmem& sm, const TcParams& p, u
 template <int BNA>
 __device__ __forceinline__ void tc_dequant(const TcSmem& sm, const TcParams& p, uint32_t tmem,
                                            int quarter, int set, int lane, int n0, int gbeg,
-                                           volatile int* abort) {
+                                           int gpp, volatile int* abort) {
     using C = TcCfg<BNA>;
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
@@ -379,13 +389,13 @@ __device__ __forceinline__ void tc_dequant(const TcSmem& sm, const TcParams& p, 
     const bool live = n0 + row < p.Nout;
     const size_t gp = static_cast<size_t>(live ? n0 + row : 0) * p.G + gbeg;
     uint16_t s_next = 0, b_next = 0;
-    if (live && set < p.gpp) {
+    if (live && set < gpp) {
         s_next = __ldg(p.scales + gp + set);
         b_next = __ldg(p.biases + gp + set);
     }
-    for (int i = set; i < p.gpp; i += C::DSETS) {
+    for (int i = set; i < gpp; i += C::DSETS) {
         const uint16_t s_cur = s_next, b_cur = b_next;
-        if (live && i + C::DSETS < p.gpp) {
+        if (live && i + C::DSETS < gpp) {
             s_next = __ldg(p.scales + gp + i + C::DSETS);
             b_next = __ldg(p.biases + gp + i + C::DSETS);
         }
@@ -524,7 +534,7 @@ __device__ __noinline__ void reduce_tile(const T* planes, __nv_bfloat16* C, int 
 template <int BNA>
 __device__ __forceinline__ void tc_epilogue(const TcSmem& sm, const TcParams& p, uint32_t tmem,
                                             const CUtensorMap* omap, int quarter, int set,
-                                            int lane, int n0, int m0, int part,
+                                            int lane, int n0, int m0, int part, int gpp,
                                             volatile int* abort) {
     using C = TcCfg<BNA>;
     const bool ok = mbar_wait_warp(sm.acc_full, 0, abort, p.status);
@@ -534,7 +544,7 @@ __device__ __forceinline__ void tc_epilogue(const TcSmem& sm, const TcParams& p,
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
         const int r = quarter * 32 + lane;  // row of the weight tile
         const int n = n0 + r;
-        const int nacc = p.gpp < C::NACC ? p.gpp : C::NACC;  // accumulators that received groups
+        const int nacc = gpp < C::NACC ? gpp : C::NACC;  // accumulators that received groups
         const size_t plane = static_cast<size_t>(part) * p.M * p.Nout;
         for (int c = set; c < BNA / 16; c += C::DSETS) {
             uint32_t d[16];
@@ -625,7 +635,7 @@ template <int BNA>
 __global__ void __launch_bounds__(TcCfg<BNA>::THREADS, 1)
     w4a16_tc_kernel(const __grid_constant__ CUtensorMap wmap,
                     const __grid_constant__ CUtensorMap amap,
-                    const __grid_constant__ CUtensorMap amap_t,
+                    const __grid_constant__ CUtensorMap amap_1,
                     const __grid_constant__ CUtensorMap omap, const TcParams p) {
     using C = TcCfg<BNA>;
     extern __shared__ uint8_t smem_raw[];
@@ -637,7 +647,10 @@ __global__ void __launch_bounds__(TcCfg<BNA>::THREADS, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n0 = blockIdx.x * kWRows, m0 = blockIdx.y * BNA, part = blockIdx.z;
-    const int gbeg = part * p.gpp;
+    // partition `part`: groups [gbeg, gbeg + gpp), the first G mod split
+    // partitions one group longer
+    const int gpp = p.gq + (part < p.gr ? 1 : 0);
+    const int gbeg = part * p.gq + (part < p.gr ? part : p.gr);
 
     pdl_trigger();
     if (tid == 0) {
@@ -664,7 +677,7 @@ __global__ void __launch_bounds__(TcCfg<BNA>::THREADS, 1)
         // into L2 while the kernels before it on the stream finish.  L2 is the
         // point of coherence, so the loads after the wait below still see
         // anything those kernels wrote.
-        const int nbox = (p.gpp + 1) >> 1;
+        const int nbox = (gpp + 1) >> 1;
         for (int j = lane; j < nbox; j += 32) tma_prefetch_l2_2d(&wmap, (gbeg + 2 * j) * 16, n0);
     }
     if (warp == 1) {  // tensor memory is not global memory: allocated before the wait
@@ -683,21 +696,21 @@ __global__ void __launch_bounds__(TcCfg<BNA>::THREADS, 1)
 
     if (warp == 0) {
         if (lane == 0)
-            tc_producer<BNA>(sm, p, &wmap, &amap, &amap_t, n0, m0, gbeg, abort);
+            tc_producer<BNA>(sm, p, &wmap, &amap, &amap_1, n0, m0, gbeg, gpp, abort);
     } else if (warp <= C::NACC) {
         tc_fence_before();
         asm volatile("bar.sync 2, %0;\n" ::"n"(kTmemBarThreads) : "memory");
         tc_fence_after();
         tmem = *sm.tmem_slot;
-        if (lane == 0) tc_issuer<BNA>(sm, p, tmem, warp - 1, abort);
+        if (lane == 0) tc_issuer<BNA>(sm, p, tmem, warp - 1, gpp, abort);
     } else if (warp >= kCtlWarps) {
         tc_fence_before();
         asm volatile("bar.sync 2, %0;\n" ::"n"(kTmemBarThreads) : "memory");
         tc_fence_after();
         tmem = *sm.tmem_slot;
         const int quarter = warp & 3, set = (warp - kCtlWarps) >> 2;
-        tc_dequant<BNA>(sm, p, tmem, quarter, set, lane, n0, gbeg, abort);
-        tc_epilogue<BNA>(sm, p, tmem, &omap, quarter, set, lane, n0, m0, part, abort);
+        tc_dequant<BNA>(sm, p, tmem, quarter, set, lane, n0, gbeg, gpp, abort);
+        tc_epilogue<BNA>(sm, p, tmem, &omap, quarter, set, lane, n0, m0, part, gpp, abort);
     }
 
     // ---- teardown: every MMA has finished before tensor memory is freed ----
@@ -771,14 +784,17 @@ int launch_tc(const void* A, const uint32_t* Wq, const void* scales, const void*
     p.Kred = Kred;
     p.Nout = Nout;
     p.G = Kred / kGroup;
-    p.gpp = p.G / split;
+    p.gq = p.G / split;
+    p.gr = p.G % split;
+    p.gpp = p.gq + (p.gr ? 1 : 0);
     p.out_mode = out_mode;
     p.weights_static = weights_static() && pdl_enabled() ? 1 : 0;
     p.fused = fused_C != nullptr && counters != nullptr && split > 1 ? 1 : 0;
     p.C = fused_C;
     p.counters = counters;
-    p.wtail = p.gpp % C::WGPS;
-    p.atail = p.gpp % C::AGPS;
+    // a partition whose last activation stage holds fewer than AGPS groups
+    // fills it through a one-group map
+    const bool atails = p.gq % C::AGPS != 0 || (p.gr && (p.gq + 1) % C::AGPS != 0);
     TcPipeline pl;
     if (!tc_pipeline<BNA>(p.gpp, limit, &pl)) return cudaErrorInvalidValue;
     const int ast = pl.act_stages, wst = pl.w_stages;
@@ -795,8 +811,8 @@ int launch_tc(const void* A, const uint32_t* Wq, const void* scales, const void*
     // weights as 2-D [Nout][Kred/8 words] with boxes of 128 rows x 32 words (two
     // groups, 128-byte swizzle); activations as [64-k chunk][row][64] boxes of
     // 2*AGPS chunks x BNA rows (128-byte swizzle, the MMA's K-major layout).
-    // The activation tail map has a box of the last stage's tail groups.
-    CUtensorMap wmap, amap, amap_t;
+    // The one-group map (box of one group) fills short last stages.
+    CUtensorMap wmap, amap, amap_1;
     {
         const cuuint64_t adims[3] = {64, static_cast<cuuint64_t>(M),
                                      static_cast<cuuint64_t>(Kred / 64)};
@@ -811,8 +827,8 @@ int launch_tc(const void* A, const uint32_t* Wq, const void* scales, const void*
                        CU_TENSOR_MAP_SWIZZLE_128B) ||
             !aenc(&amap, C::AGPS))
             return cudaErrorInvalidValue;
-        if (p.atail ? !aenc(&amap_t, p.atail) : false) return cudaErrorInvalidValue;
-        if (!p.atail) amap_t = amap;
+        if (atails ? !aenc(&amap_1, 1) : false) return cudaErrorInvalidValue;
+        if (!atails) amap_1 = amap;
     }
     // output planes [split][M][Nout] as a 3-D map with a [BNA][128] box; a TMA
     // store needs 16-byte row pitch, and the staged tile must fit the ring
@@ -845,7 +861,7 @@ int launch_tc(const void* A, const uint32_t* Wq, const void* scales, const void*
     cfg.blockDim = dim3(C::THREADS, 1, 1);
     cfg.dynamicSmemBytes = pl.smem;
     cfg.stream = st;
-    return cudaLaunchKernelEx(&cfg, kern, wmap, amap, amap_t, omap, p);
+    return cudaLaunchKernelEx(&cfg, kern, wmap, amap, amap_1, omap, p);
 }
 
 }  // namespace

@@ -50,6 +50,8 @@ _SIGS = {
     "qmm_policy_preset": (_I, [_I, _I, _I, ctypes.POINTER(qmm_policy)]),
     "qmm_kernel_tile": (_I, [_I, ctypes.POINTER(_I), ctypes.POINTER(_I)]),
     "qmm_splitk_plan": (_I, [_I, _I, _I, ctypes.POINTER(qmm_policy), ctypes.POINTER(_I)]),
+    "qmm_splitk_plan_near_equal": (_I, [_I, _I, _I, ctypes.POINTER(qmm_policy),
+                                        ctypes.POINTER(_I)]),
     "qmm_splitk_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "qmm_w4a16_g128": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, ctypes.POINTER(qmm_policy),
                             _P, _SZ, _I, _P, ctypes.POINTER(_I)]),
@@ -64,6 +66,7 @@ _SIGS = {
     "qmm_set_pdl": (_I, [_I]),
     "qmm_set_weights_static": (_I, [_I]),
     "qmm_set_reduce": (_I, [_I]),
+    "qmm_set_partitions": (_I, [_I]),
     "qmm_kernel_status": (_I, [ctypes.POINTER(_I), _I]),
     "qmm_w4a16_g128_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I,
                                     ctypes.POINTER(qmm_policy), _I, _P, ctypes.POINTER(_I)]),
@@ -152,6 +155,17 @@ def qmm_set_reduce(mode: int) -> int:
     return prev
 
 
+QMM_PARTITIONS_EQUAL, QMM_PARTITIONS_NEAR_EQUAL = 0, 1
+
+
+def qmm_set_partitions(mode: int) -> int:
+    """Equal partitions (default) or near-equal ones for any split (see qmm.h)."""
+    prev = lib().qmm_set_partitions(mode)
+    if prev < 0:
+        raise QmmError(prev, "qmm_set_partitions")
+    return prev
+
+
 def qmm_set_weights_static(enable: bool) -> int:
     """Promise that no earlier kernel on the stream writes the weights (see qmm.h)."""
     return int(lib().qmm_set_weights_static(1 if enable else 0))
@@ -174,6 +188,13 @@ def qmm_splitk_plan(M: int, Kred: int, Nout: int, pol: qmm_policy) -> int:
     s = _I(0)
     _check(lib().qmm_splitk_plan(M, Kred, Nout, ctypes.byref(pol), ctypes.byref(s)),
            "qmm_splitk_plan")
+    return s.value
+
+
+def qmm_splitk_plan_near_equal(M: int, Kred: int, Nout: int, pol: qmm_policy) -> int:
+    s = _I(0)
+    _check(lib().qmm_splitk_plan_near_equal(M, Kred, Nout, ctypes.byref(pol), ctypes.byref(s)),
+           "qmm_splitk_plan_near_equal")
     return s.value
 
 
@@ -326,7 +347,8 @@ def w4a16_matmul(A, Wq, scales, biases, split_req: int = 0, pol=None,
     if split_req == 0:
         if pol is None:
             pol = qmm_policy_preset(QMM_PRESET_GB300, M)
-        split = qmm_splitk_plan(M, Kred, Nout, pol)
+        # the near-equal plan's split bounds the one either partition rule takes
+        split = qmm_splitk_plan_near_equal(M, Kred, Nout, pol)
     else:
         split = split_req
     C = torch.empty((M, Nout), dtype=torch.bfloat16, device=A.device)

@@ -85,6 +85,51 @@ def test_plan_bit_exact_against_oracle_fuzz():
             oracle.splitk_plan(M, Kred, Nout, *pol.as_tuple())
 
 
+def test_plan_near_equal_bit_exact_against_oracle():
+    for pol in _policies():
+        for M in M_LIST:
+            for Kred, Nout in SHAPES:
+                got = Q.qmm_splitk_plan_near_equal(M, Kred, Nout, pol)
+                assert got == oracle.splitk_plan_near_equal(M, Kred, Nout, *pol.as_tuple())
+                assert got >= Q.qmm_splitk_plan(M, Kred, Nout, pol)
+    rng = np.random.default_rng(22)
+    for _ in range(20000):
+        M = int(rng.integers(1, 5000))
+        Kred = 128 * int(rng.integers(1, 129))
+        Nout = int(rng.integers(1, 20000))
+        pol = Q.qmm_policy(int(rng.integers(1, 257)), int(rng.integers(1, 257)),
+                           int(rng.integers(0, 5000)), int(rng.integers(1, 65)),
+                           128 * int(rng.integers(1, 17)))
+        assert Q.qmm_splitk_plan_near_equal(M, Kred, Nout, pol) == \
+            oracle.splitk_plan_near_equal(M, Kred, Nout, *pol.as_tuple())
+
+
+def test_gb300_near_equal_splits_of_the_workload():
+    # 152 SMs, one CTA each: the divisor rule leaves o and down at 4 ways
+    # (80 CTAs); near-equal partitions take 7 (140 CTAs, the longest
+    # partition 11 of 76 groups instead of 19, and 5 of 32 instead of 8).
+    # k/v stay at 10: 16 partitions of 20 groups still leave one of 2.
+    got = {}
+    for M in (32, 128):
+        pol = Q.qmm_policy_preset(Q.QMM_PRESET_GB300, M, 152)
+        for name, (Kred, Nout) in inputs.PROJECTIONS.items():
+            got[name, M] = (Q.qmm_splitk_plan(M, Kred, Nout, pol),
+                            Q.qmm_splitk_plan_near_equal(M, Kred, Nout, pol))
+    for M in (32, 128):
+        assert got["down", M] == (4, 7) and got["o", M] == (4, 7)
+        assert got["k", M] == (10, 10) and got["v", M] == (10, 10)
+        assert got["q", M] == (4, 4) and got["gate", M] == (2, 2) and got["up", M] == (2, 2)
+
+
+def test_partition_rule_switch():
+    assert Q.qmm_set_partitions(Q.QMM_PARTITIONS_NEAR_EQUAL) == Q.QMM_PARTITIONS_EQUAL
+    assert Q.qmm_set_partitions(Q.QMM_PARTITIONS_EQUAL) == Q.QMM_PARTITIONS_NEAR_EQUAL
+    assert Q.lib().qmm_set_partitions(2) == Q.QMM_EINVAL
+    assert Q.lib().qmm_set_partitions(-1) == Q.QMM_EINVAL
+    with pytest.raises(Q.QmmError):
+        Q.qmm_set_partitions(5)
+
+
 def test_plan_errors():
     pol = Q.qmm_policy_preset(Q.QMM_PRESET_PAGES)
     s = ctypes.c_int(0)
@@ -94,6 +139,12 @@ def test_plan_errors():
     assert lib.qmm_splitk_plan(16, 2560, 1024, None, ctypes.byref(s)) == Q.QMM_EINVAL
     bad = Q.qmm_policy(32, 32, 320, 16, 100)
     assert lib.qmm_splitk_plan(16, 2560, 1024, ctypes.byref(bad), ctypes.byref(s)) == Q.QMM_EINVAL
+    for plan in (lib.qmm_splitk_plan_near_equal,):
+        assert plan(16, 2500, 1024, ctypes.byref(pol), ctypes.byref(s)) == Q.QMM_ESHAPE
+        assert plan(0, 2560, 1024, ctypes.byref(pol), ctypes.byref(s)) == Q.QMM_EINVAL
+        assert plan(16, 2560, 1024, None, ctypes.byref(s)) == Q.QMM_EINVAL
+        assert plan(16, 2560, 1024, ctypes.byref(bad), ctypes.byref(s)) == Q.QMM_EINVAL
+        assert plan(16, 2560, 1024, ctypes.byref(pol), None) == Q.QMM_EINVAL
 
 
 def test_workspace_bytes():

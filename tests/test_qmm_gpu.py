@@ -123,12 +123,14 @@ def _check_sampled(p, got_bits, split, dt, rows, cols, what=""):
         _assert_close(got, ref, TOL_F32, what)
 
 
-def _run(d, M, Nout, split_req=0, pol=None, partial_dtype=Q.QMM_PARTIAL_BF16):
-    """Call qmm_w4a16_g128 into a NaN-filled C with a canary tail; returns (C bits, split)."""
+def _run(d, M, Nout, split_req=0, pol=None, partial_dtype=Q.QMM_PARTIAL_BF16,
+         plan=Q.qmm_splitk_plan):
+    """Call qmm_w4a16_g128 into a NaN-filled C with a canary tail; returns (C bits, split).
+    plan: the split plan of the partition rule in force."""
     Kred = d["A"].shape[1]
     if split_req == 0:
         p = pol or Q.qmm_policy_preset(Q.QMM_PRESET_GB300, M)
-        split = Q.qmm_splitk_plan(M, Kred, Nout, p)
+        split = plan(M, Kred, Nout, p)
     else:
         split = split_req
     nbytes = Q.qmm_splitk_workspace_bytes(M, Nout, split, partial_dtype)
@@ -396,6 +398,16 @@ def test_partition_argument_errors():
     with pytest.raises(Q.QmmError) as e:  # 3 does not divide G = 2
         Q.qmm_w4a16_g128_partition(d["A"], d["Wq"], d["scales"], d["biases"], ok, 3)
     assert e.value.code == Q.QMM_ESHAPE
+    prev = Q.qmm_set_partitions(Q.QMM_PARTITIONS_NEAR_EQUAL)
+    try:
+        with pytest.raises(Q.QmmError) as e:  # near-equal: 3 > G = 2 is still refused
+            Q.qmm_w4a16_g128_partition(d["A"], d["Wq"], d["scales"], d["biases"], ok, 3)
+        assert e.value.code == Q.QMM_ESHAPE
+        d3 = Q.to_device(inputs.make_w4a16(8, 640, 64, seed=1))  # G = 5: split 3 is fine
+        Q.qmm_w4a16_g128_partition(d3["A"], d3["Wq"], d3["scales"], d3["biases"], ok, 3)
+        torch.cuda.synchronize()
+    finally:
+        Q.qmm_set_partitions(prev)
 
 
 # ---- static weights: the early start overlaps the previous kernel -----------
@@ -546,3 +558,153 @@ def test_fused_reduce_with_the_static_scratch():
             assert np.array_equal(_bits(C1), _bits(C2))
     finally:
         Q.qmm_set_reduce(prev)
+
+
+# ---- near-equal partitions (QMM_PARTITIONS_NEAR_EQUAL) ----------------------
+
+NE_PLAN = Q.qmm_splitk_plan_near_equal
+
+
+@pytest.fixture
+def near_equal():
+    prev = Q.qmm_set_partitions(Q.QMM_PARTITIONS_NEAR_EQUAL)
+    try:
+        yield
+    finally:
+        Q.qmm_set_partitions(prev)
+
+
+@pytest.mark.parametrize("M", [16, 128])
+@pytest.mark.parametrize("name,splits", [("k", [3, 6, 7, 9, 13, 16, 19]), ("o", [3, 5, 7, 9, 31]),
+                                         ("down", [3, 5, 7, 9, 13, 75])])
+def test_near_equal_forced_splits(family, near_equal, name, splits, M):
+    """Splits that do not divide the group count: the first G mod s partitions
+    hold one group more.  Against the oracle's emulation of that cut."""
+    Kred, Nout = inputs.PROJECTIONS[name]
+    p = inputs.make_w4a16(M, Kred, Nout, seed=110 + M)
+    d = Q.to_device(p)
+    C64 = oracle.qmm(p["A"], p["Wq"], p["scales"], p["biases"])
+    for s in splits:
+        for dt in (Q.QMM_PARTIAL_BF16, Q.QMM_PARTIAL_F32):
+            got, used = _run(d, M, Nout, s, partial_dtype=dt, plan=NE_PLAN)
+            _check_full(p, got, s, dt, C64, "%s M=%d s=%d dt=%d" % (name, M, s, dt))
+
+
+@pytest.mark.parametrize("M", [1, 9, 17, 33, 65, 129, 300])
+def test_near_equal_families_ragged(family, near_equal, M):
+    # G = 10 and Nout = 1000: every short last stage (one to three groups on
+    # the narrow tiles) and a partial last column tile
+    Kred, Nout = 1280, 1000
+    p = inputs.make_w4a16(M, Kred, Nout, seed=120 + M)
+    d = Q.to_device(p)
+    C64 = oracle.qmm(p["A"], p["Wq"], p["scales"], p["biases"])
+    for split_req in (0, 3, 4, 6, 7, 9):
+        got, s = _run(d, M, Nout, split_req, plan=NE_PLAN)
+        _check_full(p, got, s, Q.QMM_PARTIAL_BF16, C64, "M=%d req=%d" % (M, split_req))
+
+
+@pytest.mark.parametrize("M", [16, 32, 64, 128])
+@pytest.mark.parametrize("name", list(inputs.PROJECTIONS) + ["ragged"])
+def test_near_equal_policy_full_size_sampled(near_equal, name, M):
+    Kred, Nout = inputs.RAGGED if name == "ragged" else inputs.PROJECTIONS[name]
+    p = inputs.make_w4a16(M, Kred, Nout, seed=0)
+    d = Q.to_device(p)
+    pol = Q.qmm_policy_preset(Q.QMM_PRESET_GB300, M)
+    got, s = _run(d, M, Nout, 0, plan=NE_PLAN)
+    assert s == NE_PLAN(M, Kred, Nout, pol) >= Q.qmm_splitk_plan(M, Kred, Nout, pol)
+    rows, cols = _sample(M, Nout, np.random.default_rng(M * 11 + Nout))
+    _check_sampled(p, got, s, Q.QMM_PARTIAL_BF16, rows, cols, "near-equal policy s=%d" % s)
+
+
+@pytest.mark.parametrize("name,M,splits", [("k", 32, [2, 5, 10]), ("down", 128, [2, 4]),
+                                           ("ragged", 33, [4, 10])])
+def test_near_equal_dividing_split_is_the_equal_cut(family, name, M, splits):
+    """With a split that divides G both rules cut the same partitions: the
+    same bits from either mode."""
+    Kred, Nout = inputs.RAGGED if name == "ragged" else inputs.PROJECTIONS[name]
+    d = Q.to_device(inputs.make_w4a16(M, Kred, Nout, seed=130 + M))
+    for s in splits:
+        a, _ = _run(d, M, Nout, s)
+        prev = Q.qmm_set_partitions(Q.QMM_PARTITIONS_NEAR_EQUAL)
+        try:
+            b, _ = _run(d, M, Nout, s, plan=NE_PLAN)
+        finally:
+            Q.qmm_set_partitions(prev)
+        assert np.array_equal(a, b), "s=%d" % s
+
+
+@pytest.mark.parametrize("M,Nout", [(40, 1000), (3, 136)])
+@pytest.mark.parametrize("split", [3, 7, 13])
+@pytest.mark.parametrize("dt", [Q.QMM_PARTIAL_BF16, Q.QMM_PARTIAL_F32])
+def test_near_equal_partition_planes(family, near_equal, M, Nout, split, dt):
+    """Each plane against the oracle's plane of the near-equal cut (the
+    tolerance of test_partition_planes)."""
+    p = inputs.make_w4a16(M, 2560, Nout, seed=140 + split + M)
+    d = Q.to_device(p)
+    got = _partition(d, M, Nout, split, dt).float().cpu().numpy().astype(np.float64)
+    mode = 1 if dt == Q.QMM_PARTIAL_F32 else 0
+    _, want = oracle.qmm_partitioned(p["A"], p["Wq"], p["scales"], p["biases"], split, mode,
+                                     with_partials=True)
+    assert np.all(np.isfinite(got)), "a plane element was not written"
+    lim = 2.0 ** -10 * np.maximum(1.0, np.abs(want))
+    if dt == Q.QMM_PARTIAL_BF16:
+        lim = lim + _ulp_bf16(want)
+    err = np.abs(got - want)
+    bad = np.argwhere(err > lim)
+    assert bad.size == 0, "%d plane elements out of tolerance, first %s err %g lim %g" % (
+        len(bad), bad[0], err[tuple(bad[0])], lim[tuple(bad[0])])
+
+
+@pytest.mark.parametrize("name,M,split", [("k", 32, 16), ("down", 128, 7), ("ragged", 33, 7)])
+def test_near_equal_fused_reduce_and_static_scratch(near_equal, name, M, split):
+    """The fused last-CTA reduce and the allocation-free entry point under
+    the near-equal rule: the same bits as the separate reduce with a caller
+    workspace."""
+    Kred, Nout = inputs.RAGGED if name == "ragged" else inputs.PROJECTIONS[name]
+    dt = Q.QMM_PARTIAL_BF16
+    d = Q.to_device(inputs.make_w4a16(M, Kred, Nout, seed=150 + M))
+    prev_k = Q.qmm_set_kernels(Q.QMM_KERNELS_TCGEN05)
+    prev = Q.qmm_set_reduce(Q.QMM_REDUCE_KERNEL)
+    try:
+        nb = Q.qmm_splitk_workspace_bytes(M, Nout, split, dt)
+        ref = _call_with(d, M, Nout, split, dt, torch.empty(nb, dtype=torch.uint8, device="cuda"))
+        C = torch.empty((M, Nout), dtype=torch.bfloat16, device="cuda")
+        used = Q.qmm_w4a16_g128_noalloc(d["A"], d["Wq"], d["scales"], d["biases"], C,
+                                        split_req=split)
+        torch.cuda.synchronize()
+        assert used == split and np.array_equal(_bits(C), ref)
+        Q.qmm_set_reduce(Q.QMM_REDUCE_FUSED)
+        ws = torch.zeros(Q.qmm_splitk_workspace_bytes(M, Nout, split, dt), dtype=torch.uint8,
+                         device="cuda")
+        for _ in range(2):
+            assert np.array_equal(_call_with(d, M, Nout, split, dt, ws), ref)
+        assert Q.qmm_kernel_status(clear=True) == 0
+    finally:
+        Q.qmm_set_reduce(prev)
+        Q.qmm_set_kernels(prev_k)
+
+
+def test_near_equal_weights_static_back_to_back(near_equal):
+    """Back-to-back policy calls with the static-weights early start under
+    the near-equal rule (o and down split 7 ways)."""
+    shapes = [("k", 32), ("down", 128), ("o", 32), ("k", 128), ("ragged", 33)]
+    probs = []
+    for j, (name, M) in enumerate(shapes):
+        Kred, Nout = inputs.RAGGED if name == "ragged" else inputs.PROJECTIONS[name]
+        p = inputs.make_w4a16(M, Kred, Nout, seed=160 + j)
+        probs.append((p, Q.to_device(p), M, Nout))
+    prev_w = Q.qmm_set_weights_static(True)
+    try:
+        outs = [Q.w4a16_matmul(d["A"], d["Wq"], d["scales"], d["biases"])
+                for p, d, M, Nout in probs]
+        torch.cuda.synchronize()
+        assert Q.qmm_kernel_status(clear=True) == 0
+    finally:
+        Q.qmm_set_weights_static(prev_w)
+    rng = np.random.default_rng(6)
+    for (p, d, M, Nout), (C, used) in zip(probs, outs):
+        pol = Q.qmm_policy_preset(Q.QMM_PRESET_GB300, M)
+        assert used == NE_PLAN(M, p["A"].shape[1], Nout, pol)
+        rows, cols = _sample(M, Nout, rng)
+        _check_sampled(p, _bits(C), used, Q.QMM_PARTIAL_BF16, rows, cols,
+                       "near-equal static weights M=%d Nout=%d" % (M, Nout))
