@@ -77,6 +77,8 @@ NCU_TRAFFIC = {
     # python bench.py --only down:128 --launch-list --steps 1 --warmup 3 under
     # ncu --set full -k regex:w4a16_tc -s 2 -c 1: dram__bytes_read.sum + _write.sum
     ("down", 128, 4): (15788544, "4226552ed820491b"),
+    # the same with --partitions near-equal (split 7)
+    ("down", 128, 7): (15788288, "4226552ed820491b"),
     # the same for --only gate:32
     ("gate", 32, 2): (13462016, "4226552ed820491b"),
 }
@@ -204,7 +206,7 @@ class ClockSampler:
 class Workload:
     """Device buffers for R rotating copies of the 14-call step."""
 
-    def __init__(self, device, Q, l2_bytes):
+    def __init__(self, device, Q, l2_bytes, near_equal=False):
         self.Q = Q
         self.device = device
         self.calls = calls()
@@ -219,15 +221,16 @@ class Workload:
                                for _ in range(self.R - 1)]
         self.C = [[torch.empty((M, Nout), dtype=torch.bfloat16, device=device)
                    for (_, M, _, Nout) in self.calls] for _ in range(self.R)]
-        self.split, self.split_ne = [], []
+        # split of each call under the partition rule in force, and under the
+        # other rule (qmm_set_partitions); the near-equal one is never smaller
+        self.split, self.split_alt = [], []
         ws_max = 16
         for (_, M, Kred, Nout) in self.calls:
             pol = Q.qmm_policy_preset(Q.QMM_PRESET_GB300, M)
-            s = Q.qmm_splitk_plan(M, Kred, Nout, pol)
-            # the near-equal rule's split (qmm_set_partitions), never smaller
+            s_eq = Q.qmm_splitk_plan(M, Kred, Nout, pol)
             s_ne = Q.qmm_splitk_plan_near_equal(M, Kred, Nout, pol)
-            self.split.append(s)
-            self.split_ne.append(s_ne)
+            self.split.append(s_ne if near_equal else s_eq)
+            self.split_alt.append(s_eq if near_equal else s_ne)
             ws_max = max(ws_max, Q.qmm_splitk_workspace_bytes(M, Nout, s_ne, Q.QMM_PARTIAL_BF16))
         # one workspace for every call, zeroed, with room beyond the largest
         # planes for the fused reduce's counter area (its last 32 KB), which
@@ -301,11 +304,15 @@ def run_gpu(args, rank, world, local_rank):
     # kernel finishes (qmm_set_weights_static); --weights dynamic turns it off
     static_weights = args.weights == "static"
     Q.qmm_set_weights_static(static_weights)
+    near_equal = args.partitions == "near-equal"
+    rule = Q.QMM_PARTITIONS_NEAR_EQUAL if near_equal else Q.QMM_PARTITIONS_EQUAL
+    alt_rule = Q.QMM_PARTITIONS_EQUAL if near_equal else Q.QMM_PARTITIONS_NEAR_EQUAL
+    Q.qmm_set_partitions(rule)
     props = torch.cuda.get_device_properties(device)
     l2 = int(getattr(props, "L2_cache_size", 128 << 20))
     sms = props.multi_processor_count
     peaks, peak_src = load_peaks()
-    wl = Workload(device, Q, l2)
+    wl = Workload(device, Q, l2, near_equal)
     stream = torch.cuda.current_stream()
 
     # warm-up: eager step per set (first calls set kernel attributes), then graphs
@@ -372,7 +379,7 @@ def run_gpu(args, rank, world, local_rank):
     ms_nopdl = time_variant(Q.qmm_set_pdl, False)
     ms_wflip = time_variant(Q.qmm_set_weights_static, not static_weights)
     ms_fused = time_variant(Q.qmm_set_reduce, Q.QMM_REDUCE_FUSED)
-    ms_ne = time_variant(Q.qmm_set_partitions, Q.QMM_PARTITIONS_NEAR_EQUAL)
+    ms_alt = time_variant(Q.qmm_set_partitions, alt_rule)
 
     # per call: policy split vs the unsplit control, each timed as a graph of
     # back-to-back launches over copies of its inputs larger than L2.  These and
@@ -393,15 +400,16 @@ def run_gpu(args, rank, world, local_rank):
                              workspace=wl.ws)
         us_s = graph_us_per_launch(lambda j: call(j, 0), len(cps), stream)
         us_1 = graph_us_per_launch(lambda j: call(j, 1), len(cps), stream) if s > 1 else us_s
-        s_ne = wl.split_ne[i]
-        if s_ne != s:
-            prev_pr = Q.qmm_set_partitions(Q.QMM_PARTITIONS_NEAR_EQUAL)
-            us_ne = graph_us_per_launch(lambda j: call(j, 0), len(cps), stream)
-            Q.qmm_set_partitions(prev_pr)
+        s_alt = wl.split_alt[i]
+        if s_alt != s:
+            Q.qmm_set_partitions(alt_rule)
+            us_alt = graph_us_per_launch(lambda j: call(j, 0), len(cps), stream)
+            Q.qmm_set_partitions(rule)
         else:
-            us_ne = us_s
-        nb_ne, fl_ne = algorithmic(M, Kred, Nout, s_ne)
-        t_roof_ne, _ = roofline_time_s(nb_ne, fl_ne, peaks)
+            us_alt = us_s
+        nb_alt, fl_alt = algorithmic(M, Kred, Nout, s_alt)
+        t_roof_alt, _ = roofline_time_s(nb_alt, fl_alt, peaks)
+        alt = "equal" if near_equal else "near_equal"
         nb, fl = algorithmic(M, Kred, Nout, s)
         nb1, _ = algorithmic(M, Kred, Nout, 1)
         t_roof, bound = roofline_time_s(nb, fl, peaks)
@@ -413,8 +421,8 @@ def run_gpu(args, rank, world, local_rank):
                          "roof_frac_unsplit": round(t_roof1 * 1e6 / us_1, 4),
                          "tbps_split": round(nb / us_s / 1e6, 3),
                          "tflops_split": round(fl / us_s / 1e6, 2),
-                         "split_near_equal": s_ne, "us_near_equal": round(us_ne, 3),
-                         "roof_frac_near_equal": round(t_roof_ne * 1e6 / us_ne, 4),
+                         "split_" + alt: s_alt, "us_" + alt: round(us_alt, 3),
+                         "roof_frac_" + alt: round(t_roof_alt * 1e6 / us_alt, 4),
                          "copies": len(cps)})
         if dom is None or us_s > per_call[dom["index"]]["us_split"]:
             dom = {"index": i, "split": s}
@@ -431,6 +439,18 @@ def run_gpu(args, rank, world, local_rank):
                 dom["us_reduce"] = graph_us_per_launch(
                     lambda j: Q.qmm_splitk_reduce(planes, Q.QMM_PARTIAL_BF16, s, M, Nout, C),
                     len(cps), stream)
+            # and under the other partition rule, when that splits it otherwise
+            if s_alt > 1 and s_alt != s:
+                planes_alt = wl.ws[:s_alt * M * Nout * 2].view(torch.bfloat16).view(s_alt, M, Nout)
+
+                def part_alt(j):
+                    d = cps[j]
+                    Q.qmm_w4a16_g128_partition(d["A"], d["Wq"], d["scales"], d["biases"],
+                                               planes_alt, s_alt)
+                Q.qmm_set_partitions(alt_rule)
+                dom["split_alt"] = s_alt
+                dom["us_partition_alt"] = graph_us_per_launch(part_alt, len(cps), stream)
+                Q.qmm_set_partitions(rule)
         del cps
     prefill = prefill_sweep(Q, device, stream, l2, peaks) if rank == 0 else None
     Q.qmm_set_weights_static(static_weights)
@@ -438,7 +458,7 @@ def run_gpu(args, rank, world, local_rank):
     dense = dense_sweep(Q, device, stream, sms, l2) if rank == 0 else None
     e2e = run_e2e(wl, Q, device, stream, min(args.steps, 20))
     return {"ms": ms, "ms_nopdl": ms_nopdl, "ms_wflip": ms_wflip, "ms_fused": ms_fused,
-            "ms_ne": ms_ne,
+            "ms_alt": ms_alt,
             "per_call": per_call, "dom": dom,
             "clocks": sample, "wl": wl,
             "peaks": peaks,
@@ -686,6 +706,8 @@ def main():
                          "(qmm_set_weights_static), which lets weight work start early")
     ap.add_argument("--kernels", choices=["default", "mma", "tc"], default="default",
                     help="kernel table for the W4A16 calls (A/B comparisons)")
+    ap.add_argument("--partitions", choices=["equal", "near-equal"], default="equal",
+                    help="partition rule of the W4A16 calls (qmm_set_partitions)")
     ap.add_argument("--only", default=None, metavar="PROJ:M",
                     help="restrict the step to one call, e.g. gate:128 (profiling aid)")
     args = ap.parse_args()
@@ -752,6 +774,22 @@ def main():
                       "kernel alone, each launch on its own copy of the inputs (copies > 2.2x L2, "
                       "weights read from HBM); programmatic dependent launch on, no "
                       "static-weights early start"}
+    roof_alt = None
+    if "us_partition_alt" in res["dom"]:
+        # the same kernel and call under the other partition rule
+        s_alt = res["dom"]["split_alt"]
+        nb_a, fl_a = partition_algorithmic(dc["M"], dc["Kred"], dc["Nout"], s_alt)
+        us_a = res["dom"]["us_partition_alt"]
+        ach_a = nb_a / us_a / 1e3 if bound == "hbm" else fl_a / us_a / 1e6
+        key_a = (dc["proj"], dc["M"], s_alt)
+        tr_a = NCU_TRAFFIC[key_a][0] if (args.kernels != "mma" and key_a in NCU_TRAFFIC and
+                                         NCU_TRAFFIC[key_a][1] == tc_source_hash()) else None
+        roof_alt = {"partitions": "near-equal" if args.partitions == "equal" else "equal",
+                    "split": s_alt, "grid": "%d x %d x %d" % (-(-dc["Nout"] // bn),
+                                                            -(-dc["M"] // bm), s_alt),
+                    "achieved": round(ach_a, 2), "peak": peak, "unit": unit,
+                    "frac": round(ach_a / peak, 4), "traffic": tr_a,
+                    "per_launch": {"algorithmic_bytes": nb_a, "flops": fl_a, "us": round(us_a, 3)}}
     out = {"metric": METRIC, "value": round(value_us, 4), "unit": UNIT, "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": round(res["ms"] / args.steps, 6), "higher_is_better": False,
@@ -761,6 +799,10 @@ def main():
                       "l2": "inputs larger than L2: %d rotating input sets x %.0f MB (L2 %d MB)"
                             % (wl.R, wl.set_bytes / 2**20, res["l2"] >> 20),
                       "kernels": args.kernels,
+                      "partitions": "equal (the split divides the groups; the chapter's rule)"
+                                    if args.partitions == "equal" else
+                                    "near-equal (qmm_set_partitions: any split, the first "
+                                    "G mod s partitions one group longer)",
                       "weights": "static (qmm_set_weights_static: no kernel writes the "
                                  "weights during the run; weight loads and dequant start "
                                  "before the previous kernel ends)" if args.weights == "static"
@@ -771,8 +813,10 @@ def main():
            ("value_weights_dynamic" if args.weights == "static" else "value_weights_static"):
                round(job_value_us(res["ms_wflip"], 1, args.steps, ncalls), 4),
            "value_fused_reduce": round(job_value_us(res["ms_fused"], 1, args.steps, ncalls), 4),
-           "value_near_equal": round(job_value_us(res["ms_ne"], 1, args.steps, ncalls), 4),
-           "roofline": roof, "gpu_launches": args.steps * wl.launches_per_step(),
+           ("value_near_equal" if args.partitions == "equal" else "value_equal_partitions"):
+               round(job_value_us(res["ms_alt"], 1, args.steps, ncalls), 4),
+           "roofline": roof, "roofline_other_partitions": roof_alt,
+           "gpu_launches": args.steps * wl.launches_per_step(),
            "clocks": res["clocks"], "e2e": res["e2e"], "per_call": res["per_call"],
            "dense_splitk_512x512x16384": res["dense"], "prefill_M2048": res["prefill"]}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
