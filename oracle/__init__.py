@@ -7,7 +7,8 @@ fp64); this module compiles it with gcc and wraps it with ctypes.
 
 Sources the oracle follows (cited per function in the C file):
   * tiny-llm book, "Week 2 Day 7: Split-K Prefill" (Tasks 2-4)
-  * gpu-kernels-explained, "Split-K, streams and overlap" (Maths; A100 table)
+  * gpu-kernels-explained, "Split-K, streams and overlap" (Concept sections;
+    Maths, Overlap and Split-K; A100 table)
   * "Optimize Prefill vs Decode Kernels" (Required reasoning process, step 5)
 
 Parity pins: every function here is checked by ``tests/test_oracle.py``
@@ -71,6 +72,7 @@ def _load():
             "oracle_splitk_plan": [I64, I64, I64, I64, I64, I64, I64, I64, P],
             "oracle_splitk_plan_near_equal": [I64, I64, I64, I64, I64, I64, I64, I64, P],
             "oracle_waves": [I64, I64, I64],
+            "oracle_overlap_schedule": [I64, I64, P, P, P, I, P, P],
             "oracle_gemm": [P, P, I64, I64, I64, P, I],
             "oracle_gemm_partitioned": [P, P, I64, I64, I64, I64, I, P, I],
         }
@@ -223,6 +225,22 @@ def waves(tiles, split, sms) -> int:
     if r < 0:
         raise ValueError("waves: bad arguments")
     return int(r)
+
+
+def overlap_schedule(n, buffers, t_load, t_comp, t_store, out_reuse=False,
+                     with_events=False):
+    """Finish time of n tiles through copy-in, compute and copy-out engines with
+    `buffers` buffers; times are scalars (every tile alike) or length-n arrays.
+    with_events also returns the [n, 6] start/end times."""
+    t = [np.ascontiguousarray(np.broadcast_to(np.asarray(x, np.float64), (n,)))
+         for x in (t_load, t_comp, t_store)]
+    T = ctypes.c_double(0.0)
+    ev = np.empty((n, 6), np.float64) if with_events else None
+    _check(_load().oracle_overlap_schedule(n, buffers, _ptr(t[0]), _ptr(t[1]), _ptr(t[2]),
+                                           int(bool(out_reuse)), ctypes.byref(T),
+                                           _ptr(ev) if ev is not None else None),
+           "overlap_schedule")
+    return (T.value, ev) if with_events else T.value
 
 
 # ---- dense BF16 GEMM -----------------------------------------------------

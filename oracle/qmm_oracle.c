@@ -10,7 +10,9 @@
  *        for Each Partition; Task 3: Choose Partitions From Occupancy;
  *        Task 4: Reduce and Verify)
  *   [SK] gpu-kernels-explained, "Split-K, streams and overlap"
- *        (second Concept section; Maths, "Split-K"; the A100 model table)
+ *        (first Concept section: copy-in / compute / copy-out engines and
+ *        buffers; second Concept section; Maths, "Overlap" and "Split-K";
+ *        the A100 model table)
  *   [PD] "Optimize Prefill vs Decode Kernels" (Required reasoning process,
  *        step 5: at least ~512 reduction elements per split)
  * The weight format (w = scale*q + bias, q in 0..15, eight nibbles per
@@ -412,4 +414,47 @@ int oracle_gemm_partitioned(const uint16_t *A, const uint16_t *W, int64_t M, int
     free(a);
     free(w);
     return bad ? -1 : 0;
+}
+
+/* ---- copy / compute overlap schedule ----------------------------------- */
+
+/* [SK, first Concept section and Maths, Overlap]: n tiles pass three engines
+ * in tile order -- copy in (load), compute, copy out (store) -- each engine
+ * working on one tile at a time.  With b buffers, tile i's load needs a free
+ * buffer: it starts when tile i-1's load has ended and tile i-b's compute has
+ * ended.  Tile i's compute starts when its load and tile i-1's compute have
+ * ended; its store when its compute and tile i-1's store have ended.  The
+ * schedule is built tile by tile from these rules (event by event, as the
+ * page's model does) and T is the end of the last store.
+ * out_reuse = 1 adds a rule the page's model leaves out: the outputs also sit
+ * in b buffers, so tile i's compute also waits for tile i-b's store.
+ * Per-tile times t_load[i], t_comp[i], t_store[i] >= 0.  events (nullable)
+ * receives [n][6]: load start/end, compute start/end, store start/end. */
+int oracle_overlap_schedule(int64_t n, int64_t b, const double *t_load, const double *t_comp,
+                            const double *t_store, int out_reuse, double *T, double *events) {
+    if (n < 1 || b < 1 || !t_load || !t_comp || !t_store || !T) return -1;
+    if (out_reuse != 0 && out_reuse != 1) return -1;
+    double *ev = (double *)malloc(sizeof(double) * (size_t)(6 * n));
+    if (!ev) return -4;
+    for (int64_t i = 0; i < n; ++i) {
+        if (t_load[i] < 0 || t_comp[i] < 0 || t_store[i] < 0) { free(ev); return -1; }
+        double *e = ev + 6 * i;
+        double ls = i > 0 ? ev[6 * (i - 1) + 1] : 0.0;        /* previous load ended */
+        if (i >= b && ev[6 * (i - b) + 3] > ls) ls = ev[6 * (i - b) + 3]; /* buffer free */
+        e[0] = ls;
+        e[1] = ls + t_load[i];
+        double cs = e[1];                                      /* own load ended */
+        if (i > 0 && ev[6 * (i - 1) + 3] > cs) cs = ev[6 * (i - 1) + 3];
+        if (out_reuse && i >= b && ev[6 * (i - b) + 5] > cs) cs = ev[6 * (i - b) + 5];
+        e[2] = cs;
+        e[3] = cs + t_comp[i];
+        double ss = e[3];                                      /* own compute ended */
+        if (i > 0 && ev[6 * (i - 1) + 5] > ss) ss = ev[6 * (i - 1) + 5];
+        e[4] = ss;
+        e[5] = ss + t_store[i];
+    }
+    *T = ev[6 * (n - 1) + 5];
+    if (events) memcpy(events, ev, sizeof(double) * (size_t)(6 * n));
+    free(ev);
+    return 0;
 }
