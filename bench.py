@@ -457,13 +457,14 @@ def run_gpu(args, rank, world, local_rank):
     sample = clocks.stop()
     dense = dense_sweep(Q, device, stream, sms, l2) if rank == 0 else None
     e2e = run_e2e(wl, Q, device, stream, min(args.steps, 20))
+    overlap = overlap_sweep(wl, Q, device) if rank == 0 else None
     return {"ms": ms, "ms_nopdl": ms_nopdl, "ms_wflip": ms_wflip, "ms_fused": ms_fused,
             "ms_alt": ms_alt,
             "per_call": per_call, "dom": dom,
             "clocks": sample, "wl": wl,
             "peaks": peaks,
             "peak_src": peak_src, "l2": l2, "sms": sms, "dense": dense, "e2e": e2e,
-            "prefill": prefill}
+            "prefill": prefill, "overlap": overlap}
 
 
 def prefill_sweep(Q, device, stream, l2, peaks):
@@ -512,6 +513,82 @@ def dense_sweep(Q, device, stream, sms, l2):
             stream)
         out.append({"split": s, "blocks": 16 * s, "waves": -(-16 * s // sms), "us": round(us, 3),
                     "tflops": round(2 * 512 * 512 * 16384 / us / 1e6, 2)})
+    return out
+
+
+def overlap_sweep(wl, Q, device, reps=10):
+    """The copy-in / compute / copy-out pipeline (qmm_w4a16_g128_stream) on the
+    step's 14 calls: activations from pinned host memory, weights resident,
+    outputs back to pinned host memory.  Per-chunk engine times are measured
+    engine by engine (each engine's 14 chunks back to back on one stream,
+    events between chunks); the pipeline's end-to-end time is measured for 1,
+    2 and 3 buffers on three streams and set beside the schedule model's
+    prediction from the measured engine times (qmm_overlap_schedule, output
+    buffers reused as the executor does).  Every timed sequence is enqueued
+    behind a short device-side delay (torch.cuda._sleep, a bounded clock
+    loop), so the GPU runs it back to back instead of at the host's launch
+    pace."""
+    n = len(wl.calls)
+    chunks = []
+    for p, d in zip(wl.host, wl.sets[0]):
+        M, Nout = p["A"].shape[0], p["Wq"].shape[0]
+        chunks.append({"A": torch.from_numpy(p["A"].view(np.int16)).view(torch.bfloat16)
+                       .pin_memory(),
+                       "C": torch.empty((M, Nout), dtype=torch.bfloat16).pin_memory(),
+                       "Wq": d["Wq"], "scales": d["scales"], "biases": d["biases"],
+                       "A_dev": d["A"]})
+    calls = Q.stream_calls(chunks)
+    s_in, s_comp, s_out = (torch.cuda.Stream(device=device) for _ in range(3))
+    arena = torch.zeros(Q.qmm_stream_arena_bytes(calls, 3), dtype=torch.uint8, device=device)
+    C_dev = [torch.empty_like(c["C"], device=device) for c in chunks]
+
+    hold = int(2e-3 * 2.0e9)  # about 2 ms of SM clocks: time to enqueue a sequence
+
+    def engine_times(enqueue, st):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+        acc = np.zeros(n)
+        for r in range(reps + 2):
+            with torch.cuda.stream(st):
+                torch.cuda._sleep(hold)
+                ev[0].record(st)
+                for i in range(n):
+                    enqueue(i)
+                    ev[i + 1].record(st)
+            st.synchronize()
+            if r >= 2:
+                acc += [ev[i].elapsed_time(ev[i + 1]) * 1e3 for i in range(n)]
+        return acc / reps
+
+    t_load = engine_times(lambda i: chunks[i]["A_dev"].copy_(chunks[i]["A"], non_blocking=True),
+                          s_in)
+    t_comp = engine_times(lambda i: Q.qmm_w4a16_g128(
+        chunks[i]["A_dev"], chunks[i]["Wq"], chunks[i]["scales"], chunks[i]["biases"], C_dev[i],
+        workspace=wl.ws, stream=s_comp), s_comp)
+    t_store = engine_times(lambda i: chunks[i]["C"].copy_(C_dev[i], non_blocking=True), s_out)
+    out = {"chunks": n, "engine_us_per_step": {"load": round(float(t_load.sum()), 2),
+                                               "compute": round(float(t_comp.sum()), 2),
+                                               "store": round(float(t_store.sum()), 2)},
+           "measured_us": {}, "model_us": {}}
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for b in (1, 2, 3):
+        total = 0.0
+        for r in range(reps + 2):
+            with torch.cuda.stream(s_in):
+                torch.cuda._sleep(hold)
+            t0.record(s_in)
+            Q.qmm_w4a16_g128_stream(calls, b, arena, s_in, s_comp, s_out)
+            t1.record(s_out)
+            torch.cuda.synchronize()
+            if r >= 2:
+                total += t0.elapsed_time(t1) * 1e3
+        out["measured_us"][str(b)] = round(total / reps, 2)
+        out["model_us"][str(b)] = round(Q.qmm_overlap_schedule(n, b, t_load, t_comp, t_store,
+                                                                out_reuse=True), 2)
+    out["speedup_2_buffers"] = {"measured": round(out["measured_us"]["1"] /
+                                                  out["measured_us"]["2"], 3),
+                                "model": round(out["model_us"]["1"] / out["model_us"]["2"], 3)}
+    out["note"] = ("weights resident; per chunk the activations come in and the output goes "
+                   "out through pinned host memory; reps=%d" % reps)
     return out
 
 
@@ -818,7 +895,8 @@ def main():
            "roofline": roof, "roofline_other_partitions": roof_alt,
            "gpu_launches": args.steps * wl.launches_per_step(),
            "clocks": res["clocks"], "e2e": res["e2e"], "per_call": res["per_call"],
-           "dense_splitk_512x512x16384": res["dense"], "prefill_M2048": res["prefill"]}
+           "dense_splitk_512x512x16384": res["dense"], "prefill_M2048": res["prefill"],
+           "overlap_stream": res["overlap"]}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(wl.host)
     if rank == 0:

@@ -328,6 +328,67 @@ int qmm_w4a16_g128_noalloc(const void *A, const uint32_t *Wq, const void *scales
 /* Size in bytes of the fixed partial-plane buffer of qmm_w4a16_g128_noalloc. */
 size_t qmm_static_scratch_bytes(void);
 
+/* ---- streaming host activations through the matmul ----------------------
+ *
+ * gpu-kernels-explained, "Split-K, streams and overlap" (first Concept
+ * section; Maths, Overlap): copies and kernels run on separate engines, so a
+ * host-to-device copy, a kernel and a device-to-host copy of different chunks
+ * can run at once.  With b device buffers, chunk i's copy in waits for chunk
+ * i-b's compute to free its buffer; after the pipeline fills it runs at the
+ * pace of its slowest engine.
+ *
+ * One chunk: a W4A16 call whose activations and output live in host memory
+ * and whose weights are already on the device. */
+typedef struct {
+    const void *A_host;     /* host BF16 [M, Kred]; pinned memory to overlap */
+    void *C_host;           /* host BF16 [M, Nout]; pinned memory to overlap */
+    const uint32_t *Wq;     /* device, as qmm_w4a16_g128 */
+    const void *scales;     /* device */
+    const void *biases;     /* device */
+    int M, Kred, Nout;
+} qmm_stream_call;
+
+/* Device bytes qmm_w4a16_g128_stream needs for these calls and `buffers`
+ * buffers: per buffer, room for the largest A and C (each rounded up to 256
+ * bytes), plus one workspace for the largest split of any call under the
+ * current partition rule and reduce mode (computes run one at a time).
+ * Returns 0 for invalid arguments.  Host only. */
+size_t qmm_stream_arena_bytes(const qmm_stream_call *calls, int n, int buffers);
+
+/* Run n calls as a three-stage pipeline: for chunk i, buffer i % buffers,
+ *   stream_in:       wait for chunk i-buffers' compute, copy A_host in;
+ *   stream_compute:  wait for that copy and for chunk i-buffers' copy out,
+ *                    run qmm_w4a16_g128 (policy split, current rules);
+ *   stream_out:      wait for the compute, copy C out to C_host.
+ * The waits use events the library creates once per device and reuses.  The
+ * streams may be equal (the stages then serialize).  arena: device memory of
+ * at least qmm_stream_arena_bytes(calls, n, buffers) bytes (arena_bytes),
+ * 256-byte aligned; its contents on return are unspecified (under
+ * QMM_REDUCE_FUSED zero it before its first use, as any fused-reduce
+ * workspace).  splits_used (host, nullable, n ints) receives each call's
+ * split.  Asynchronous: synchronize stream_out before reading C_host.
+ * Each call's result is bitwise what qmm_w4a16_g128 gives for it.
+ * Returns QMM_OK, QMM_EINVAL (null calls/arena, n < 1, buffers < 1, a chunk
+ * with null pointers or bad sizes), QMM_ESHAPE, QMM_EALIGN, QMM_EWORKSPACE
+ * (arena too small) or QMM_ECUDA.  Arguments of every chunk are checked
+ * before anything is enqueued. */
+int qmm_w4a16_g128_stream(const qmm_stream_call *calls, int n, int buffers, void *arena,
+                          size_t arena_bytes, void *stream_in, void *stream_compute,
+                          void *stream_out, int *splits_used);
+
+/* The schedule model of that pipeline (the Split-K page's, Maths: Overlap),
+ * for planning: n chunks with per-chunk engine times t_load[i], t_comp[i],
+ * t_store[i] >= 0 (host arrays, any unit).  Each engine takes the chunks in
+ * order, one at a time; chunk i's load starts after chunk i-1's load and
+ * chunk i-buffers' compute; its compute after its load and chunk i-1's
+ * compute (and, with out_reuse = 1, after chunk i-buffers' store, the rule
+ * the executor above adds for its output buffers); its store after its
+ * compute and chunk i-1's store.  *T receives the end of the last store;
+ * events (host, nullable, [n][6]) the start and end of each chunk's load,
+ * compute and store.  Returns QMM_OK or QMM_EINVAL.  Host only. */
+int qmm_overlap_schedule(int n, int buffers, const double *t_load, const double *t_comp,
+                         const double *t_store, int out_reuse, double *T, double *events);
+
 #ifdef __cplusplus
 }
 #endif

@@ -42,6 +42,14 @@ class QmmError(RuntimeError):
         super().__init__("%s: %s (%d)" % (what, qmm_strerror(code), code))
 
 
+class qmm_stream_call(ctypes.Structure):
+    """One chunk of qmm_w4a16_g128_stream (see qmm.h)."""
+    _fields_ = [("A_host", ctypes.c_void_p), ("C_host", ctypes.c_void_p),
+                ("Wq", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("biases", ctypes.c_void_p), ("M", ctypes.c_int), ("Kred", ctypes.c_int),
+                ("Nout", ctypes.c_int)]
+
+
 _lock = threading.Lock()
 _lib = None
 
@@ -72,6 +80,13 @@ _SIGS = {
                                     ctypes.POINTER(qmm_policy), _I, _P, ctypes.POINTER(_I)]),
     "qmm_static_scratch_bytes": (_SZ, []),
     "qmm_tc_pipeline_config": (_I, [_I, _I, _I, ctypes.POINTER(_I)]),
+    "qmm_stream_arena_bytes": (_SZ, [ctypes.POINTER(qmm_stream_call), _I, _I]),
+    "qmm_w4a16_g128_stream": (_I, [ctypes.POINTER(qmm_stream_call), _I, _I, _P, _SZ, _P, _P, _P,
+                                   ctypes.POINTER(_I)]),
+    "qmm_overlap_schedule": (_I, [_I, _I, ctypes.POINTER(ctypes.c_double),
+                                  ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double),
+                                  _I, ctypes.POINTER(ctypes.c_double),
+                                  ctypes.POINTER(ctypes.c_double)]),
 }
 
 
@@ -353,7 +368,9 @@ def w4a16_matmul(A, Wq, scales, biases, split_req: int = 0, pol=None,
         split = split_req
     C = torch.empty((M, Nout), dtype=torch.bfloat16, device=A.device)
     nbytes = qmm_splitk_workspace_bytes(M, Nout, split, partial_dtype)
-    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=A.device) if nbytes else None
+    # zeroed: under QMM_REDUCE_FUSED the workspace's tail holds tile counters
+    # that must start at zero
+    ws = torch.zeros(max(nbytes, 16), dtype=torch.uint8, device=A.device) if nbytes else None
     used = qmm_w4a16_g128(A, Wq, scales, biases, C, split_req=split_req, pol=pol, workspace=ws,
                           partial_dtype=partial_dtype, stream=stream)
     return C, used
@@ -374,3 +391,62 @@ def to_device(problem: dict, device="cuda") -> dict:
         "scales": bf16(problem["scales"]),
         "biases": bf16(problem["biases"]),
     }
+
+
+# ---- streaming host activations (copy in / compute / copy out) -------------
+
+def _host(t: torch.Tensor, name: str) -> int:
+    if not isinstance(t, torch.Tensor) or t.is_cuda or t.dtype != torch.bfloat16:
+        raise TypeError("%s must be a host BF16 tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return t.data_ptr()
+
+
+def stream_calls(chunks) -> "ctypes.Array":
+    """chunks: sequence of dicts with host A and C (BF16, pinned to overlap) and
+    device Wq, scales, biases.  Returns the qmm_stream_call array."""
+    arr = (qmm_stream_call * len(chunks))()
+    for i, c in enumerate(chunks):
+        M, Kred = c["A"].shape
+        Nout = c["Wq"].shape[0]
+        if tuple(c["C"].shape) != (M, Nout):
+            raise ValueError("chunk %d: C must be [M, Nout]" % i)
+        arr[i] = qmm_stream_call(_host(c["A"], "A"), _host(c["C"], "C"),
+                                 _dev(c["Wq"], _WORDS, "Wq").value,
+                                 _dev(c["scales"], _BF16, "scales").value,
+                                 _dev(c["biases"], _BF16, "biases").value, M, Kred, Nout)
+    return arr
+
+
+def qmm_stream_arena_bytes(calls, buffers: int) -> int:
+    return int(lib().qmm_stream_arena_bytes(calls, len(calls), buffers))
+
+
+def qmm_w4a16_g128_stream(calls, buffers: int, arena: torch.Tensor, stream_in=None,
+                          stream_compute=None, stream_out=None):
+    """Enqueue the copy-in / compute / copy-out pipeline; returns the splits used.
+    Synchronize stream_out before reading the host outputs."""
+    n = len(calls)
+    used = (_I * n)()
+    _check(lib().qmm_w4a16_g128_stream(calls, n, buffers, _dev(arena, (torch.uint8,), "arena"),
+                                       arena.numel(), _stream(stream_in),
+                                       _stream(stream_compute), _stream(stream_out), used),
+           "qmm_w4a16_g128_stream")
+    return list(used)
+
+
+def qmm_overlap_schedule(n: int, buffers: int, t_load, t_comp, t_store, out_reuse=False,
+                         with_events=False):
+    """The pipeline's schedule model: end of the last store (and the [n, 6] events)."""
+    import numpy as np
+    t = [np.ascontiguousarray(np.broadcast_to(np.asarray(x, np.float64), (n,)))
+         for x in (t_load, t_comp, t_store)]
+    D = ctypes.POINTER(ctypes.c_double)
+    T = ctypes.c_double(0.0)
+    ev = np.empty((n, 6), np.float64) if with_events else None
+    _check(lib().qmm_overlap_schedule(n, buffers, *(a.ctypes.data_as(D) for a in t),
+                                      int(bool(out_reuse)), ctypes.byref(T),
+                                      ev.ctypes.data_as(D) if ev is not None else None),
+           "qmm_overlap_schedule")
+    return (T.value, ev) if with_events else T.value

@@ -176,6 +176,60 @@ def test_argument_errors_before_any_cuda_work():
     assert lib.qmm_gemm_bf16_splitk(a, w, c, 512, 512, 1024, 17, None, 0, None) == Q.QMM_ESHAPE
 
 
+def test_overlap_schedule_bit_exact_against_oracle():
+    rng = np.random.default_rng(26)
+    for _ in range(2000):
+        n = int(rng.integers(1, 30))
+        b = int(rng.integers(1, 6))
+        t = [rng.random(n) * float(rng.choice([1.0, 10.0, 100.0])) for _ in range(3)]
+        if rng.random() < 0.3:
+            t = [np.full(n, float(rng.integers(0, 9))) for _ in range(3)]
+        for out_reuse in (False, True):
+            T, ev = Q.qmm_overlap_schedule(n, b, *t, out_reuse=out_reuse, with_events=True)
+            To, evo = oracle.overlap_schedule(n, b, *t, out_reuse=out_reuse, with_events=True)
+            assert T == To and np.array_equal(ev, evo)
+
+
+def test_overlap_schedule_errors():
+    lib = Q.lib()
+    D = ctypes.POINTER(ctypes.c_double)
+    one = (ctypes.c_double * 1)(1.0)
+    neg = (ctypes.c_double * 1)(-1.0)
+    T = ctypes.c_double()
+    assert lib.qmm_overlap_schedule(0, 1, one, one, one, 0, ctypes.byref(T), None) == Q.QMM_EINVAL
+    assert lib.qmm_overlap_schedule(1, 0, one, one, one, 0, ctypes.byref(T), None) == Q.QMM_EINVAL
+    assert lib.qmm_overlap_schedule(1, 1, neg, one, one, 0, ctypes.byref(T), None) == Q.QMM_EINVAL
+    assert lib.qmm_overlap_schedule(1, 1, one, one, one, 2, ctypes.byref(T), None) == Q.QMM_EINVAL
+    assert lib.qmm_overlap_schedule(1, 1, None, one, one, 0, ctypes.byref(T), None) == Q.QMM_EINVAL
+    assert lib.qmm_overlap_schedule(1, 1, one, one, one, 0, None, None) == Q.QMM_EINVAL
+    assert lib.qmm_overlap_schedule(1, 1, one, one, one, 0, ctypes.byref(T), None) == Q.QMM_OK
+    assert T.value == 3.0
+
+
+def test_stream_executor_argument_errors_before_any_cuda_work():
+    lib = Q.lib()
+    P = ctypes.c_void_p
+    ok = Q.qmm_stream_call(0x1000, 0x2000, 0x30000, 0x40000, 0x50000, 16, 2560, 1024)
+    calls = (Q.qmm_stream_call * 1)(ok)
+    arena = P(0x100000)
+    run = lambda c, n, b, a: lib.qmm_w4a16_g128_stream(c, n, b, a, 1 << 30, None, None, None,
+                                                       None)
+    assert run(None, 1, 2, arena) == Q.QMM_EINVAL
+    assert run(calls, 0, 2, arena) == Q.QMM_EINVAL
+    assert run(calls, 1, 0, arena) == Q.QMM_EINVAL
+    assert run(calls, 1, 2, None) == Q.QMM_EINVAL
+    assert run(calls, 1, 2, P(0x100010)) == Q.QMM_EALIGN
+    bad = (Q.qmm_stream_call * 2)(ok, Q.qmm_stream_call(0x1000, 0x2000, 0x30000, 0x40000,
+                                                          0x50000, 16, 2500, 1024))
+    assert run(bad, 2, 2, arena) == Q.QMM_ESHAPE          # the second chunk's Kred
+    bad[1] = Q.qmm_stream_call(0x1000, None, 0x30000, 0x40000, 0x50000, 16, 2560, 1024)
+    assert run(bad, 2, 2, arena) == Q.QMM_EINVAL
+    bad[1] = Q.qmm_stream_call(0x1000, 0x2000, 0x30004, 0x40000, 0x50000, 16, 2560, 1024)
+    assert run(bad, 2, 2, arena) == Q.QMM_EALIGN
+    assert lib.qmm_stream_arena_bytes(None, 1, 1) == 0
+    assert lib.qmm_stream_arena_bytes(calls, 1, 0) == 0
+
+
 def test_fused_reduce_workspace_holds_the_counters():
     from split_w4a16_quantized_gb300 import qmm as Q
     prev_k = Q.qmm_set_kernels(Q.QMM_KERNELS_TCGEN05)

@@ -708,3 +708,103 @@ def test_near_equal_weights_static_back_to_back(near_equal):
         rows, cols = _sample(M, Nout, rng)
         _check_sampled(p, _bits(C), used, Q.QMM_PARTIAL_BF16, rows, cols,
                        "near-equal static weights M=%d Nout=%d" % (M, Nout))
+
+
+# ---- streaming host activations (qmm_w4a16_g128_stream) ---------------------
+
+STREAM_SHAPES = [("k", 16), ("down", 128), ("ragged", 33), ("gate", 32), ("k", 300), ("o", 64)]
+
+
+def _stream_chunks(seed0):
+    chunks, probs = [], []
+    for j, (name, M) in enumerate(STREAM_SHAPES):
+        Kred, Nout = inputs.RAGGED if name == "ragged" else inputs.PROJECTIONS[name]
+        p = inputs.make_w4a16(M, Kred, Nout, seed=seed0 + j)
+        d = Q.to_device(p)
+        A_host = torch.from_numpy(p["A"].view(np.int16)).view(torch.bfloat16).pin_memory()
+        C_host = torch.full((M, Nout), float("nan"), dtype=torch.bfloat16).pin_memory()
+        chunks.append({"A": A_host, "C": C_host, "Wq": d["Wq"], "scales": d["scales"],
+                       "biases": d["biases"]})
+        probs.append((p, d, M, Nout))
+    return chunks, probs
+
+
+@pytest.mark.parametrize("buffers", [1, 2, 3, 8])
+@pytest.mark.parametrize("streams", ["three", "one"])
+def test_stream_executor_equals_the_calls(buffers, streams):
+    """Each chunk's host output is bitwise the output of qmm_w4a16_g128 on the
+    same inputs, for any buffer count, on three streams or on one; a second
+    run on the same arena (and the library's reused events) gives the same."""
+    chunks, probs = _stream_chunks(170)
+    calls = Q.stream_calls(chunks)
+    nbytes = Q.qmm_stream_arena_bytes(calls, buffers)
+    assert nbytes > 0
+    arena = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    if streams == "three":
+        s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    else:
+        s_in = s_comp = s_out = torch.cuda.current_stream()
+    refs = []
+    for p, d, M, Nout in probs:
+        C, used = Q.w4a16_matmul(d["A"], d["Wq"], d["scales"], d["biases"])
+        refs.append((_bits(C), used))
+    for rep in range(2):
+        for c in chunks:
+            c["C"].fill_(float("nan"))
+        used = Q.qmm_w4a16_g128_stream(calls, buffers, arena, s_in, s_comp, s_out)
+        s_out.synchronize()
+        torch.cuda.synchronize()
+        for j, (c, (ref, ref_used)) in enumerate(zip(chunks, refs)):
+            assert used[j] == ref_used
+            assert np.array_equal(c["C"].view(torch.int16).numpy().view(np.uint16), ref), \
+                "chunk %d rep %d" % (j, rep)
+    # and one chunk against the oracle directly
+    p, d, M, Nout = probs[1]
+    rows, cols = _sample(M, Nout, np.random.default_rng(7))
+    got = chunks[1]["C"].view(torch.int16).numpy().view(np.uint16)
+    _check_sampled(p, got, used[1], Q.QMM_PARTIAL_BF16, rows, cols, "streamed down M=128")
+    assert Q.qmm_kernel_status(clear=True) == 0
+
+
+def test_stream_executor_under_near_equal_and_fused_reduce():
+    """Near-equal partitions and the fused reduce inside the pipeline: the same
+    bits as the separate reduce's calls (the arena zeroed once, as a fused
+    workspace must be)."""
+    chunks, probs = _stream_chunks(180)
+    prev_p = Q.qmm_set_partitions(Q.QMM_PARTITIONS_NEAR_EQUAL)
+    prev_k = Q.qmm_set_kernels(Q.QMM_KERNELS_TCGEN05)
+    prev_r = Q.qmm_set_reduce(Q.QMM_REDUCE_KERNEL)
+    try:
+        refs = []
+        for p, d, M, Nout in probs:
+            C, used = Q.w4a16_matmul(d["A"], d["Wq"], d["scales"], d["biases"])
+            refs.append((_bits(C), used))
+        Q.qmm_set_reduce(Q.QMM_REDUCE_FUSED)
+        calls = Q.stream_calls(chunks)
+        arena = torch.zeros(Q.qmm_stream_arena_bytes(calls, 2), dtype=torch.uint8, device="cuda")
+        used = Q.qmm_w4a16_g128_stream(calls, 2, arena, torch.cuda.Stream(), torch.cuda.Stream(),
+                                       torch.cuda.Stream())
+        torch.cuda.synchronize()
+        for j, (c, (ref, ref_used)) in enumerate(zip(chunks, refs)):
+            assert used[j] == ref_used
+            assert np.array_equal(c["C"].view(torch.int16).numpy().view(np.uint16), ref), j
+        assert Q.qmm_kernel_status(clear=True) == 0
+    finally:
+        Q.qmm_set_kernels(prev_k)
+        Q.qmm_set_reduce(prev_r)
+        Q.qmm_set_partitions(prev_p)
+
+
+def test_stream_executor_refuses_a_small_arena():
+    chunks, _ = _stream_chunks(190)
+    calls = Q.stream_calls(chunks[:2])
+    nbytes = Q.qmm_stream_arena_bytes(calls, 2)
+    # one more buffer adds one slot: the largest A and C, each rounded to 256 bytes
+    r256 = lambda x: -(-x // 256) * 256
+    slot = r256(max(c["A"].numel() * 2 for c in chunks[:2])) + \
+        r256(max(c["C"].numel() * 2 for c in chunks[:2]))
+    assert nbytes - Q.qmm_stream_arena_bytes(calls, 1) == slot
+    small = torch.empty(nbytes - 256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(Q.QmmError) as e:
+        Q.qmm_w4a16_g128_stream(calls, 2, small)
+    assert e.value.code == Q.QMM_EWORKSPACE
