@@ -381,6 +381,32 @@ def run_gpu(args, rank, world, local_rank):
     ms_fused = time_variant(Q.qmm_set_reduce, Q.QMM_REDUCE_FUSED)
     ms_alt = time_variant(Q.qmm_set_partitions, alt_rule)
 
+    # the same 14 calls as one grouped call per step (qmm_w4a16_g128_grouped):
+    # one partition launch per tile width and one reduce launch
+    group_arrays = [Q.group_calls([dict(wl.sets[r][i], C=wl.C[r][i])
+                                   for i in range(len(wl.calls))]) for r in range(wl.R)]
+    gws = torch.zeros(max(Q.qmm_group_workspace_bytes(group_arrays[0]), 16), dtype=torch.uint8,
+                      device=device)
+    gs = []
+    with torch.cuda.stream(cap):
+        for r in range(wl.R):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cap):
+                Q.qmm_w4a16_g128_grouped(group_arrays[r], gws)
+            gs.append(g)
+    torch.cuda.synchronize()
+    for k in range(args.warmup):
+        gs[k % wl.R].replay()
+    t0.record(stream)
+    for k in range(args.steps):
+        gs[k % wl.R].replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms_grouped = t0.elapsed_time(t1)
+    tile_widths = len({Q.qmm_kernel_tile(M)[0] for (_, M, _, _) in wl.calls})
+    grouped_launches = tile_widths + (1 if any(s > 1 for s in wl.split) else 0)
+    del gs
+
     # per call: policy split vs the unsplit control, each timed as a graph of
     # back-to-back launches over copies of its inputs larger than L2.  These and
     # the roofline's kernel timing run without the static-weights early start:
@@ -459,7 +485,7 @@ def run_gpu(args, rank, world, local_rank):
     e2e = run_e2e(wl, Q, device, stream, min(args.steps, 20))
     overlap = overlap_sweep(wl, Q, device) if rank == 0 else None
     return {"ms": ms, "ms_nopdl": ms_nopdl, "ms_wflip": ms_wflip, "ms_fused": ms_fused,
-            "ms_alt": ms_alt,
+            "ms_alt": ms_alt, "ms_grouped": ms_grouped, "grouped_launches": grouped_launches,
             "per_call": per_call, "dom": dom,
             "clocks": sample, "wl": wl,
             "peaks": peaks,
@@ -892,6 +918,8 @@ def main():
            "value_fused_reduce": round(job_value_us(res["ms_fused"], 1, args.steps, ncalls), 4),
            ("value_near_equal" if args.partitions == "equal" else "value_equal_partitions"):
                round(job_value_us(res["ms_alt"], 1, args.steps, ncalls), 4),
+           "value_grouped": round(job_value_us(res["ms_grouped"], 1, args.steps, ncalls), 4),
+           "grouped_launches_per_step": res["grouped_launches"],
            "roofline": roof, "roofline_other_partitions": roof_alt,
            "gpu_launches": args.steps * wl.launches_per_step(),
            "clocks": res["clocks"], "e2e": res["e2e"], "per_call": res["per_call"],

@@ -328,6 +328,46 @@ int qmm_w4a16_g128_noalloc(const void *A, const uint32_t *Wq, const void *scales
 /* Size in bytes of the fixed partial-plane buffer of qmm_w4a16_g128_noalloc. */
 size_t qmm_static_scratch_bytes(void);
 
+/* ---- several independent calls in few launches ---------------------------
+ *
+ * gpu-kernels-explained, "Split-K, streams and overlap" (second Concept
+ * section): a partial wave leaves SMs idle, and Stream-K balances the work
+ * over the SMs instead; "Optimize Prefill vs Decode Kernels" counts some
+ * microseconds per launch.  A model
+ * step has independent projections (q, k and v of one layer; gate and up)
+ * whose calls can share launches: their CTAs fill each other's partial waves
+ * and the launch and prologue costs are paid once.
+ *
+ * One call of a group: the arguments of qmm_w4a16_g128 (device pointers). */
+typedef struct {
+    const void *A;          /* BF16 [M, Kred] */
+    const uint32_t *Wq;     /* [Nout, Kred/8] */
+    const void *scales;     /* BF16 [Nout, Kred/128] */
+    const void *biases;     /* BF16 [Nout, Kred/128] */
+    void *C;                /* BF16 [M, Nout]; no call's C may alias any input or other C */
+    int M, Kred, Nout;
+} qmm_group_call;
+
+/* Workspace bytes qmm_w4a16_g128_grouped needs: the partial planes of every
+ * call whose policy split is > 1, each rounded up to 256 bytes.  0 when no
+ * call splits, or for invalid arguments.  Queries the device for the policy
+ * (as qmm_policy_preset with num_sms <= 0). */
+size_t qmm_group_workspace_bytes(const qmm_group_call *calls, int n, int partial_dtype);
+
+/* The n calls, each with its policy split under the current partition rule
+ * (split_req 0 and the GB300 preset of qmm_w4a16_g128), in few launches:
+ * the tcgen05 calls of one tile width share one partition launch (up to 16
+ * calls per launch), and every split call's planes are added by one reduce
+ * launch per 16 split calls.  Calls served by the mma.sync family
+ * (qmm_set_kernels) are launched one by one.  The reduce is always the
+ * separate kernel (QMM_REDUCE_FUSED does not apply).  Each C is bitwise the C
+ * that qmm_w4a16_g128 gives for the call.  The calls must be independent: no
+ * call reads another's C.  splits_used (host, nullable, n ints) receives
+ * each call's split.  Returns the codes of qmm_w4a16_g128; every call is
+ * checked before anything is launched. */
+int qmm_w4a16_g128_grouped(const qmm_group_call *calls, int n, void *workspace, size_t ws_bytes,
+                           int partial_dtype, void *stream, int *splits_used);
+
 /* ---- streaming host activations through the matmul ----------------------
  *
  * gpu-kernels-explained, "Split-K, streams and overlap" (first Concept

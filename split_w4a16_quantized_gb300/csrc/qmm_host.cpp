@@ -2,10 +2,12 @@
 // dispatch of the W4A16 matmul, the reduce and the dense split-K GEMM.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <climits>
 #include <cstdint>
 #include <mutex>
+#include <vector>
 
 #include "qmm.h"
 #include "qmm_internal.h"
@@ -348,6 +350,138 @@ int qmm_w4a16_g128_partition(const void* A, const uint32_t* Wq, const void* scal
     const int mode = partial_dtype == QMM_PARTIAL_F32 ? qmm::kOutF32 : qmm::kOutBf16;
     return launched(qmm::launch_w4a16(fam, A, Wq, scales, biases, partials, mode, M, Kred, Nout,
                                       split, stream));
+}
+
+namespace {
+
+// Checks one grouped call like qmm_w4a16_g128 checks its arguments (host only).
+int check_group_call(const qmm_group_call& c) {
+    if (!c.A || !c.Wq || !c.scales || !c.biases || !c.C || c.M < 1 || c.Nout < 1)
+        return QMM_EINVAL;
+    if (c.Kred < qmm::kGroup || c.Kred % qmm::kGroup) return QMM_ESHAPE;
+    if (!aligned(c.A, 16) || !aligned(c.Wq, 16) || !aligned(c.C, 16) || !aligned(c.scales, 16) ||
+        !aligned(c.biases, 16))
+        return QMM_EALIGN;
+    if (ceil_div(c.M, qmm::family_for(c.M).bm) > 65535) return QMM_ESHAPE;
+    return QMM_OK;
+}
+
+// Every call's arguments, then its split and the offset of its planes in the
+// workspace (256-byte aligned); *ws_need receives the total.
+int plan_group(const qmm_group_call* calls, int n, int partial_dtype, std::vector<int>* splits,
+               std::vector<size_t>* offsets, size_t* ws_need) {
+    if (!calls || n < 1) return QMM_EINVAL;
+    if (partial_dtype != QMM_PARTIAL_BF16 && partial_dtype != QMM_PARTIAL_F32) return QMM_EINVAL;
+    for (int i = 0; i < n; ++i) {
+        const int rc = check_group_call(calls[i]);
+        if (rc != QMM_OK) return rc;
+    }
+    splits->assign(static_cast<size_t>(n), 1);
+    offsets->assign(static_cast<size_t>(n), 0);
+    size_t off = 0;
+    for (int i = 0; i < n; ++i) {
+        const qmm_group_call& c = calls[i];
+        int& s = (*splits)[static_cast<size_t>(i)];
+        const int rc = qmm::choose_split(c.M, c.Kred, c.Nout, 0, nullptr, &s);
+        if (rc != QMM_OK) return rc;
+        if (s > 1) {
+            (*offsets)[static_cast<size_t>(i)] = off;
+            const size_t planes = static_cast<size_t>(s) * static_cast<size_t>(c.M) *
+                                  static_cast<size_t>(c.Nout) * partial_elem_bytes(partial_dtype);
+            off += (planes + 255) / 256 * 256;
+        }
+    }
+    *ws_need = off;
+    return QMM_OK;
+}
+
+}  // namespace
+
+size_t qmm_group_workspace_bytes(const qmm_group_call* calls, int n, int partial_dtype) {
+    std::vector<int> splits;
+    std::vector<size_t> offsets;
+    size_t need = 0;
+    if (plan_group(calls, n, partial_dtype, &splits, &offsets, &need) != QMM_OK) return 0;
+    return need;
+}
+
+int qmm_w4a16_g128_grouped(const qmm_group_call* calls, int n, void* workspace, size_t ws_bytes,
+                           int partial_dtype, void* stream, int* splits_used) {
+    std::vector<int> splits;
+    std::vector<size_t> offsets;
+    size_t need = 0;
+    int rc = plan_group(calls, n, partial_dtype, &splits, &offsets, &need);
+    if (rc != QMM_OK) return rc;
+    if (need > 0) {
+        if (!workspace || ws_bytes < need) return QMM_EWORKSPACE;
+        if (!aligned(workspace, 16)) return QMM_EALIGN;
+    }
+    rc = check_device();
+    if (rc != QMM_OK) return rc;
+    const int mode = partial_dtype == QMM_PARTIAL_F32 ? qmm::kOutF32 : qmm::kOutBf16;
+    auto out_of = [&](int i) -> void* {
+        return splits[i] > 1 ? static_cast<uint8_t*>(workspace) + offsets[i] : calls[i].C;
+    };
+    // partition launches: tcgen05 calls bucketed by tile width, up to
+    // kMaxGroupCalls per launch; mma.sync calls one by one.  Within a launch
+    // the calls with the longest partitions come first: blocks are dispatched
+    // in index order, so the long CTAs start early and the short ones fill in
+    // behind them (longest-first list scheduling) instead of leaving a tail.
+    std::vector<int> order(static_cast<size_t>(n));
+    for (int i = 0; i < n; ++i) order[i] = i;
+    auto longest = [&](int i) {
+        const int G = calls[i].Kred / qmm::kGroup;
+        return G / splits[i] + (G % splits[i] ? 1 : 0);
+    };
+    std::stable_sort(order.begin(), order.end(),
+                     [&](int a, int b) { return longest(a) > longest(b); });
+    std::vector<qmm::GroupCall> bucket;
+    for (const int bm : {16, 32, 64, 128, 256}) {
+        bucket.clear();
+        for (const int i : order) {
+            if (rc != QMM_OK) break;
+            const qmm::Family fam = qmm::family_for(calls[i].M);
+            if (fam.kind != qmm::kKindTc || fam.bm != bm) continue;
+            const qmm_group_call& c = calls[i];
+            bucket.push_back({c.A, c.Wq, c.scales, c.biases, out_of(i),
+                              splits[i] > 1 ? mode : static_cast<int>(qmm::kOutBf16), c.M, c.Kred,
+                              c.Nout, splits[i]});
+            if (static_cast<int>(bucket.size()) == qmm::kMaxGroupCalls) {
+                rc = launched(qmm::launch_w4a16_tc_group(bm, bucket.data(),
+                                                         static_cast<int>(bucket.size()), stream));
+                bucket.clear();
+            }
+        }
+        if (rc == QMM_OK && !bucket.empty())
+            rc = launched(qmm::launch_w4a16_tc_group(bm, bucket.data(),
+                                                     static_cast<int>(bucket.size()), stream));
+        if (rc != QMM_OK) return rc;
+    }
+    for (int i = 0; i < n && rc == QMM_OK; ++i) {
+        const qmm::Family fam = qmm::family_for(calls[i].M);
+        if (fam.kind == qmm::kKindTc) continue;
+        const qmm_group_call& c = calls[i];
+        rc = launched(qmm::launch_w4a16(fam, c.A, c.Wq, c.scales, c.biases, out_of(i),
+                                        splits[i] > 1 ? mode : qmm::kOutBf16, c.M, c.Kred, c.Nout,
+                                        splits[i], stream));
+    }
+    // the planes of every split call, one reduce launch per kMaxGroupCalls
+    std::vector<qmm::ReduceCall> red;
+    for (int i = 0; i < n && rc == QMM_OK; ++i) {
+        if (splits[i] <= 1) continue;
+        red.push_back({out_of(i), calls[i].C, splits[i], calls[i].M, calls[i].Nout});
+        if (static_cast<int>(red.size()) == qmm::kMaxGroupCalls) {
+            rc = launched(qmm::launch_reduce_group(red.data(), static_cast<int>(red.size()),
+                                                   partial_dtype, stream));
+            red.clear();
+        }
+    }
+    if (rc == QMM_OK && !red.empty())
+        rc = launched(qmm::launch_reduce_group(red.data(), static_cast<int>(red.size()),
+                                               partial_dtype, stream));
+    if (rc == QMM_OK && splits_used)
+        for (int i = 0; i < n; ++i) splits_used[i] = splits[i];
+    return rc;
 }
 
 int qmm_gemm_bf16_splitk(const void* A, const void* W, void* C, int M, int N, int K, int split,

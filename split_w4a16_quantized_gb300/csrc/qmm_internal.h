@@ -103,6 +103,28 @@ int launch_w4a16_tc(int bm, const void* A, const uint32_t* Wq, const void* scale
                     void* fused_C = nullptr, uint32_t* counters = nullptr);
 int read_tc_status(int* out, bool clear);
 
+// Grouped launches: independent calls in one kernel launch (at most
+// kMaxGroupCalls per launch; the caller cuts longer lists).
+constexpr int kMaxGroupCalls = 16;
+struct GroupCall {
+    const void* A;
+    const uint32_t* Wq;
+    const void* scales;
+    const void* biases;
+    void* out;     // C (split 1) or the call's partial planes
+    int out_mode;  // OutMode
+    int M, Kred, Nout, split;
+};
+// One partition launch of the tcgen05 kernel of tile width bm for n calls.
+int launch_w4a16_tc_group(int bm, const GroupCall* calls, int n, void* stream);
+struct ReduceCall {
+    const void* partials;  // [split, M, Nout] planes
+    void* C;               // BF16 [M, Nout]
+    int split, M, Nout;
+};
+// One reduce launch for n calls' planes (all of partial_dtype).
+int launch_reduce_group(const ReduceCall* calls, int n, int partial_dtype, void* stream);
+
 // Pipeline shape of the tcgen05 W4A16 kernel for one launch.
 struct TcPipeline {
     int nacc, dsets, a_stages, wgps, agps, act_stages, w_stages, threads;

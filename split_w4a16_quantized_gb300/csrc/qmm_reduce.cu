@@ -98,6 +98,63 @@ __global__ void __launch_bounds__(256) reduce_scalar(const T* __restrict__ parti
     }
 }
 
+// Several calls' reduces in one launch.  Work item w of the launch belongs to
+// the call whose [begin, next begin) range holds it; a call with planes a
+// multiple of eight long takes items of eight outputs, the others one.  Each
+// output is the same ascending FP32 sum as in the kernels above.
+struct RedItem {
+    const void* partials;
+    __nv_bfloat16* C;
+    int64_t plane;  // M * Nout
+    int64_t begin;  // first work item of the call
+    int split;
+    int vec;        // 1: items of eight outputs
+};
+struct RedGroup {
+    int n;
+    int64_t total;
+    RedItem item[kMaxGroupCalls];
+};
+
+template <typename T>
+__global__ void __launch_bounds__(256) reduce_group(const __grid_constant__ RedGroup g) {
+    constexpr int KC = 8;
+    pdl_trigger();
+    pdl_wait();
+    for (int64_t w = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; w < g.total;
+         w += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        int c = 0;
+        while (c + 1 < g.n && w >= g.item[c + 1].begin) ++c;
+        const RedItem& it = g.item[c];
+        const T* P = static_cast<const T*>(it.partials);
+        const int64_t i = w - it.begin;
+        if (it.vec) {
+            float acc[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+            for (int p0 = 0; p0 < it.split; p0 += KC) {
+                Raw8<T> r[KC];
+#pragma unroll
+                for (int q = 0; q < KC; ++q)
+                    if (p0 + q < it.split) r[q].load(P + (p0 + q) * it.plane + i * 8);
+#pragma unroll
+                for (int q = 0; q < KC; ++q)
+                    if (p0 + q < it.split) r[q].add_to(acc);
+            }
+            uint4 o;
+            o.x = pack_bf16x2(acc[0], acc[1]);
+            o.y = pack_bf16x2(acc[2], acc[3]);
+            o.z = pack_bf16x2(acc[4], acc[5]);
+            o.w = pack_bf16x2(acc[6], acc[7]);
+            *reinterpret_cast<uint4*>(it.C + i * 8) = o;
+        } else {
+            float acc = 0.f;
+            for (int p = 0; p < it.split; ++p) acc += load1(P + p * it.plane + i);
+            it.C[i] = __float2bfloat16_rn(acc);
+        }
+    }
+}
+
 int num_sms() {
     static int sms = 0;
     static std::once_flag once;
@@ -137,6 +194,35 @@ int launch_typed(const T* partials, int split, int64_t plane, __nv_bfloat16* C,
 }
 
 }  // namespace
+
+int launch_reduce_group(const ReduceCall* calls, int n, int partial_dtype, void* stream) {
+    if (n < 1 || n > kMaxGroupCalls) return cudaErrorInvalidValue;
+    RedGroup g;
+    g.n = n;
+    int64_t total = 0;
+    for (int i = 0; i < n; ++i) {
+        RedItem& it = g.item[i];
+        it.partials = calls[i].partials;
+        it.C = static_cast<__nv_bfloat16*>(calls[i].C);
+        it.plane = static_cast<int64_t>(calls[i].M) * calls[i].Nout;
+        it.split = calls[i].split;
+        it.vec = it.plane % 8 == 0 ? 1 : 0;
+        it.begin = total;
+        total += it.vec ? it.plane / 8 : it.plane;
+    }
+    g.total = total;
+    int64_t blocks = (total + 255) / 256;
+    const int64_t max_blocks = static_cast<int64_t>(num_sms()) * 16;
+    if (blocks > max_blocks) blocks = max_blocks;
+    cudaLaunchConfig_t cfg = {};
+    LaunchAttrs la;
+    apply_pdl(cfg, la);
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    if (partial_dtype == QMM_PARTIAL_F32) return cudaLaunchKernelEx(&cfg, reduce_group<float>, g);
+    return cudaLaunchKernelEx(&cfg, reduce_group<__nv_bfloat16>, g);
+}
 
 int launch_reduce(const void* partials, int partial_dtype, int split, int M, int Nout, void* C,
                   void* stream) {

@@ -36,6 +36,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <mutex>
 
@@ -134,6 +135,7 @@ struct TcParams {
     int* status;
     int M, Kred, Nout, G, out_mode;
     int gpp;        // groups in the longest partition (sizes the rings)
+    int split;      // partitions of the reduction axis
     int gq, gr;     // G / split, G % split: partition p holds gq + (p < gr) groups
     int weights_static;  // 1: only the activation copies wait for earlier kernels
     int fused;           // 1: the last CTA of an output tile adds its planes into C
@@ -597,9 +599,10 @@ __device__ __forceinline__ void tc_epilogue(const TcSmem& sm, const TcParams& p,
         __threadfence();
         asm volatile("bar.sync 3, %0;\n" ::"n"(128 * C::DSETS) : "memory");
         if (set == 0 && quarter == 0 && lane == 0) {
-            const unsigned tile = blockIdx.y * gridDim.x + blockIdx.x;
+            const unsigned tile = static_cast<unsigned>(m0 / BNA) * ((p.Nout + kWRows - 1) / kWRows) +
+                                  static_cast<unsigned>(n0 / kWRows);
             const unsigned prev = atomicAdd(&p.counters[tile], 1u);
-            last = prev == gridDim.z - 1;
+            last = prev == static_cast<unsigned>(p.split) - 1;
             if (last) {
                 p.counters[tile] = 0;
                 __threadfence();
@@ -612,11 +615,11 @@ __device__ __forceinline__ void tc_epilogue(const TcSmem& sm, const TcParams& p,
             const int t = (set * 4 + quarter) * 32 + lane;
             if (p.out_mode == kOutBf16)
                 reduce_tile(static_cast<const __nv_bfloat16*>(p.out),
-                            static_cast<__nv_bfloat16*>(p.C), p.M, p.Nout, gridDim.z, m0, rows,
+                            static_cast<__nv_bfloat16*>(p.C), p.M, p.Nout, p.split, m0, rows,
                             n0, cols, t, 128 * C::DSETS);
             else
                 reduce_tile(static_cast<const float*>(p.out), static_cast<__nv_bfloat16*>(p.C),
-                            p.M, p.Nout, gridDim.z, m0, rows, n0, cols, t, 128 * C::DSETS);
+                            p.M, p.Nout, p.split, m0, rows, n0, cols, t, 128 * C::DSETS);
         }
     }
     if (p.tma_store) {
@@ -631,12 +634,16 @@ __device__ __forceinline__ void tc_epilogue(const TcSmem& sm, const TcParams& p,
     }
 }
 
+// One CTA: the output tile (n0.., m0..) over partition `part` of the call
+// described by p and its tensor maps.
 template <int BNA>
-__global__ void __launch_bounds__(TcCfg<BNA>::THREADS, 1)
-    w4a16_tc_kernel(const __grid_constant__ CUtensorMap wmap,
-                    const __grid_constant__ CUtensorMap amap,
-                    const __grid_constant__ CUtensorMap amap_1,
-                    const __grid_constant__ CUtensorMap omap, const TcParams p) {
+__device__ __forceinline__ void tc_cta(const TcParams& p, const CUtensorMap* wmap_,
+                                       const CUtensorMap* amap_, const CUtensorMap* amap_1_,
+                                       const CUtensorMap* omap_, int n0, int m0, int part) {
+    const CUtensorMap& wmap = *wmap_;
+    const CUtensorMap& amap = *amap_;
+    const CUtensorMap& amap_1 = *amap_1_;
+    const CUtensorMap& omap = *omap_;
     using C = TcCfg<BNA>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>(
@@ -646,7 +653,6 @@ __global__ void __launch_bounds__(TcCfg<BNA>::THREADS, 1)
     volatile int* abort = &abort_flag;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int n0 = blockIdx.x * kWRows, m0 = blockIdx.y * BNA, part = blockIdx.z;
     // partition `part`: groups [gbeg, gbeg + gpp), the first G mod split
     // partitions one group longer
     const int gpp = p.gq + (part < p.gr ? 1 : 0);
@@ -724,6 +730,51 @@ __global__ void __launch_bounds__(TcCfg<BNA>::THREADS, 1)
     }
 }
 
+template <int BNA>
+__global__ void __launch_bounds__(TcCfg<BNA>::THREADS, 1)
+    w4a16_tc_kernel(const __grid_constant__ CUtensorMap wmap,
+                    const __grid_constant__ CUtensorMap amap,
+                    const __grid_constant__ CUtensorMap amap_1,
+                    const __grid_constant__ CUtensorMap omap, const TcParams p) {
+    tc_cta<BNA>(p, &wmap, &amap, &amap_1, &omap, blockIdx.x * kWRows, blockIdx.y * BNA,
+                blockIdx.z);
+}
+
+// Several independent calls of one tile width in one launch: the CTAs of call
+// c are the linear block indices [cta_begin, next call's cta_begin), in the
+// order (column tile, row tile, partition) of a single call's grid.  Each CTA
+// copies its call's parameters to shared memory and runs the same CTA body.
+struct TcCall {
+    CUtensorMap wmap, amap, amap_1, omap;
+    TcParams p;
+    int n_tiles, m_tiles;
+    int cta_begin;
+};
+struct TcGroup {
+    int ncalls;
+    TcCall call[kMaxGroupCalls];
+};
+
+template <int BNA>
+__global__ void __launch_bounds__(TcCfg<BNA>::THREADS, 1)
+    w4a16_tc_group_kernel(const __grid_constant__ TcGroup g) {
+    static_assert(sizeof(TcParams) % 4 == 0, "parameter copy");
+    __shared__ TcParams sp;
+    int c = 0;
+    while (c + 1 < g.ncalls && static_cast<int>(blockIdx.x) >= g.call[c + 1].cta_begin) ++c;
+    const TcCall& call = g.call[c];
+    if (threadIdx.x < sizeof(TcParams) / 4)
+        reinterpret_cast<int*>(&sp)[threadIdx.x] =
+            reinterpret_cast<const int*>(&call.p)[threadIdx.x];
+    __syncthreads();
+    int t = static_cast<int>(blockIdx.x) - call.cta_begin;
+    const int nx = t % call.n_tiles;
+    t /= call.n_tiles;
+    const int my = t % call.m_tiles;
+    tc_cta<BNA>(sp, &call.wmap, &call.amap, &call.amap_1, &call.omap, nx * kWRows, my * BNA,
+                t / call.m_tiles);
+}
+
 // The pipeline shape of one launch: per-tile constants of TcCfg<BNA> and the
 // ring depths chosen for a partition of gpp groups under a dynamic shared
 // memory limit.  Ring depths (stages of WGPS / AGPS groups): the activation
@@ -762,20 +813,14 @@ bool tc_pipeline(int gpp, long limit, TcPipeline* out) {
     return true;
 }
 
+// Parameters and tensor maps of one call, for a launch whose rings pl describes.
 template <int BNA>
-int launch_tc(const void* A, const uint32_t* Wq, const void* scales, const void* biases,
-              void* out, int out_mode, int M, int Kred, int Nout, int split, void* fused_C,
-              uint32_t* counters, cudaStream_t st) {
+bool setup_call(const void* A, const uint32_t* Wq, const void* scales, const void* biases,
+                void* out, int out_mode, int M, int Kred, int Nout, int split, void* fused_C,
+                uint32_t* counters, const TcPipeline& pl, int* status, TcParams* pp,
+                CUtensorMap* wmap, CUtensorMap* amap, CUtensorMap* amap_1, CUtensorMap* omap) {
     using C = TcCfg<BNA>;
-    auto kern = w4a16_tc_kernel<BNA>;
-    static int limit = -1;
-    static std::once_flag once;
-    std::call_once(once, [&] { limit = set_max_dynamic_smem(reinterpret_cast<const void*>(kern)); });
-    if (limit < 0) return cudaErrorInvalidValue;
-    int* status = tc_status_ptr();
-    if (!status) return cudaErrorInvalidSymbol;
-
-    TcParams p;
+    TcParams& p = *pp;
     p.scales = static_cast<const uint16_t*>(scales);
     p.biases = static_cast<const uint16_t*>(biases);
     p.out = out;
@@ -784,6 +829,7 @@ int launch_tc(const void* A, const uint32_t* Wq, const void* scales, const void*
     p.Kred = Kred;
     p.Nout = Nout;
     p.G = Kred / kGroup;
+    p.split = split;
     p.gq = p.G / split;
     p.gr = p.G % split;
     p.gpp = p.gq + (p.gr ? 1 : 0);
@@ -795,8 +841,6 @@ int launch_tc(const void* A, const uint32_t* Wq, const void* scales, const void*
     // a partition whose last activation stage holds fewer than AGPS groups
     // fills it through a one-group map
     const bool atails = p.gq % C::AGPS != 0 || (p.gr && (p.gq + 1) % C::AGPS != 0);
-    TcPipeline pl;
-    if (!tc_pipeline<BNA>(p.gpp, limit, &pl)) return cudaErrorInvalidValue;
     const int ast = pl.act_stages, wst = pl.w_stages;
     auto ring = [](int n, int gps_log2) {
         Ring r;
@@ -812,7 +856,6 @@ int launch_tc(const void* A, const uint32_t* Wq, const void* scales, const void*
     // groups, 128-byte swizzle); activations as [64-k chunk][row][64] boxes of
     // 2*AGPS chunks x BNA rows (128-byte swizzle, the MMA's K-major layout).
     // The one-group map (box of one group) fills short last stages.
-    CUtensorMap wmap, amap, amap_1;
     {
         const cuuint64_t adims[3] = {64, static_cast<cuuint64_t>(M),
                                      static_cast<cuuint64_t>(Kred / 64)};
@@ -823,16 +866,16 @@ int launch_tc(const void* A, const uint32_t* Wq, const void* scales, const void*
             return encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, A, adims, astr, box,
                                 CU_TENSOR_MAP_SWIZZLE_128B);
         };
-        if (!encode_2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, Wq, Nout, Kred / 8, 4, kWRows, 32,
+        if (!encode_2d(wmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, Wq, Nout, Kred / 8, 4, kWRows, 32,
                        CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !aenc(&amap, C::AGPS))
-            return cudaErrorInvalidValue;
-        if (atails ? !aenc(&amap_1, 1) : false) return cudaErrorInvalidValue;
-        if (!atails) amap_1 = amap;
+            !aenc(amap, C::AGPS))
+            return false;
+        if (atails ? !aenc(amap_1, 1) : false) return false;
+        if (!atails) *amap_1 = *amap;
     }
     // output planes [split][M][Nout] as a 3-D map with a [BNA][128] box; a TMA
     // store needs 16-byte row pitch, and the staged tile must fit the ring
-    CUtensorMap omap = wmap;
+    *omap = *wmap;
     {
         const int elem = out_mode == kOutBf16 ? 2 : 4;
         const size_t tile = static_cast<size_t>(BNA) * kWRows * elem;
@@ -846,14 +889,36 @@ int launch_tc(const void* A, const uint32_t* Wq, const void* scales, const void*
             const cuuint64_t ostr[2] = {static_cast<cuuint64_t>(Nout) * elem,
                                         static_cast<cuuint64_t>(M) * Nout * elem};
             const cuuint32_t obox[3] = {kWRows, static_cast<cuuint32_t>(BNA), 1};
-            if (!encode_tiled(&omap,
+            if (!encode_tiled(omap,
                               out_mode == kOutBf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                    : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
                               3, out, odims, ostr, obox, CU_TENSOR_MAP_SWIZZLE_NONE))
-                return cudaErrorInvalidValue;
+                return false;
         }
     }
+    return true;
+}
 
+template <int BNA>
+int launch_tc(const void* A, const uint32_t* Wq, const void* scales, const void* biases,
+              void* out, int out_mode, int M, int Kred, int Nout, int split, void* fused_C,
+              uint32_t* counters, cudaStream_t st) {
+    using C = TcCfg<BNA>;
+    auto kern = w4a16_tc_kernel<BNA>;
+    static int limit = -1;
+    static std::once_flag once;
+    std::call_once(once, [&] { limit = set_max_dynamic_smem(reinterpret_cast<const void*>(kern)); });
+    if (limit < 0) return cudaErrorInvalidValue;
+    int* status = tc_status_ptr();
+    if (!status) return cudaErrorInvalidSymbol;
+    const int G = Kred / kGroup;
+    TcPipeline pl;
+    if (!tc_pipeline<BNA>(G / split + (G % split ? 1 : 0), limit, &pl)) return cudaErrorInvalidValue;
+    TcParams p;
+    CUtensorMap wmap, amap, amap_1, omap;
+    if (!setup_call<BNA>(A, Wq, scales, biases, out, out_mode, M, Kred, Nout, split, fused_C,
+                         counters, pl, status, &p, &wmap, &amap, &amap_1, &omap))
+        return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     LaunchAttrs la;
     apply_pdl(cfg, la);
@@ -862,6 +927,56 @@ int launch_tc(const void* A, const uint32_t* Wq, const void* scales, const void*
     cfg.dynamicSmemBytes = pl.smem;
     cfg.stream = st;
     return cudaLaunchKernelEx(&cfg, kern, wmap, amap, amap_1, omap, p);
+}
+
+// Up to kMaxGroupCalls calls of tile width BNA in one launch.  The rings are
+// sized for the longest partition of any call; ring depth changes neither the
+// groups an accumulator receives nor their order, so every call's result is
+// the one its own launch gives.
+template <int BNA>
+int launch_tc_group(const GroupCall* calls, int n, cudaStream_t st) {
+    using C = TcCfg<BNA>;
+    if (n < 1 || n > kMaxGroupCalls) return cudaErrorInvalidValue;
+    auto kern = w4a16_tc_group_kernel<BNA>;
+    static int limit = -1;
+    static std::once_flag once;
+    std::call_once(once, [&] { limit = set_max_dynamic_smem(reinterpret_cast<const void*>(kern)); });
+    if (limit < 0) return cudaErrorInvalidValue;
+    int* status = tc_status_ptr();
+    if (!status) return cudaErrorInvalidSymbol;
+    int gpp_max = 1;
+    for (int i = 0; i < n; ++i) {
+        const int G = calls[i].Kred / kGroup;
+        gpp_max = std::max(gpp_max, G / calls[i].split + (G % calls[i].split ? 1 : 0));
+    }
+    TcPipeline pl;
+    if (!tc_pipeline<BNA>(gpp_max, limit, &pl)) return cudaErrorInvalidValue;
+    static TcGroup g;  // large: built on the host once per launch, under a lock
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lock(mu);
+    g.ncalls = n;
+    long long ctas = 0;
+    for (int i = 0; i < n; ++i) {
+        const GroupCall& c = calls[i];
+        TcCall& tc = g.call[i];
+        if (!setup_call<BNA>(c.A, c.Wq, c.scales, c.biases, c.out, c.out_mode, c.M, c.Kred, c.Nout,
+                             c.split, nullptr, nullptr, pl, status, &tc.p, &tc.wmap, &tc.amap,
+                             &tc.amap_1, &tc.omap))
+            return cudaErrorInvalidValue;
+        tc.n_tiles = (c.Nout + kWRows - 1) / kWRows;
+        tc.m_tiles = (c.M + BNA - 1) / BNA;
+        tc.cta_begin = static_cast<int>(ctas);
+        ctas += static_cast<long long>(tc.n_tiles) * tc.m_tiles * c.split;
+        if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
+    }
+    cudaLaunchConfig_t cfg = {};
+    LaunchAttrs la;
+    apply_pdl(cfg, la);
+    cfg.gridDim = dim3(static_cast<unsigned>(ctas), 1, 1);
+    cfg.blockDim = dim3(C::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = pl.smem;
+    cfg.stream = st;
+    return cudaLaunchKernelEx(&cfg, kern, g);
 }
 
 }  // namespace
@@ -888,6 +1003,18 @@ int launch_w4a16_tc(int bm, const void* A, const uint32_t* Wq, const void* scale
         case 64: return launch_tc<64>(A, Wq, scales, biases, out, out_mode, M, Kred, Nout, split, fused_C, counters, st);
         case 128: return launch_tc<128>(A, Wq, scales, biases, out, out_mode, M, Kred, Nout, split, fused_C, counters, st);
         case 256: return launch_tc<256>(A, Wq, scales, biases, out, out_mode, M, Kred, Nout, split, fused_C, counters, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+int launch_w4a16_tc_group(int bm, const GroupCall* calls, int n, void* stream) {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    switch (bm) {
+        case 16: return launch_tc_group<16>(calls, n, st);
+        case 32: return launch_tc_group<32>(calls, n, st);
+        case 64: return launch_tc_group<64>(calls, n, st);
+        case 128: return launch_tc_group<128>(calls, n, st);
+        case 256: return launch_tc_group<256>(calls, n, st);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -50,6 +50,13 @@ class qmm_stream_call(ctypes.Structure):
                 ("Nout", ctypes.c_int)]
 
 
+class qmm_group_call(ctypes.Structure):
+    """One call of qmm_w4a16_g128_grouped (see qmm.h)."""
+    _fields_ = [("A", ctypes.c_void_p), ("Wq", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("biases", ctypes.c_void_p), ("C", ctypes.c_void_p), ("M", ctypes.c_int),
+                ("Kred", ctypes.c_int), ("Nout", ctypes.c_int)]
+
+
 _lock = threading.Lock()
 _lib = None
 
@@ -80,6 +87,9 @@ _SIGS = {
                                     ctypes.POINTER(qmm_policy), _I, _P, ctypes.POINTER(_I)]),
     "qmm_static_scratch_bytes": (_SZ, []),
     "qmm_tc_pipeline_config": (_I, [_I, _I, _I, ctypes.POINTER(_I)]),
+    "qmm_group_workspace_bytes": (_SZ, [ctypes.POINTER(qmm_group_call), _I, _I]),
+    "qmm_w4a16_g128_grouped": (_I, [ctypes.POINTER(qmm_group_call), _I, _P, _SZ, _I, _P,
+                                    ctypes.POINTER(_I)]),
     "qmm_stream_arena_bytes": (_SZ, [ctypes.POINTER(qmm_stream_call), _I, _I]),
     "qmm_w4a16_g128_stream": (_I, [ctypes.POINTER(qmm_stream_call), _I, _I, _P, _SZ, _P, _P, _P,
                                    ctypes.POINTER(_I)]),
@@ -450,3 +460,41 @@ def qmm_overlap_schedule(n: int, buffers: int, t_load, t_comp, t_store, out_reus
                                       ev.ctypes.data_as(D) if ev is not None else None),
            "qmm_overlap_schedule")
     return (T.value, ev) if with_events else T.value
+
+
+# ---- several independent calls in few launches ----------------------------
+
+def group_calls(calls) -> "ctypes.Array":
+    """calls: sequence of dicts of device tensors A, Wq, scales, biases, C.
+    Returns the qmm_group_call array (shapes checked here)."""
+    arr = (qmm_group_call * len(calls))()
+    for i, c in enumerate(calls):
+        M, Kred = c["A"].shape
+        Nout = c["Wq"].shape[0]
+        if tuple(c["Wq"].shape) != (Nout, Kred // 8) or tuple(c["C"].shape) != (M, Nout) or \
+                tuple(c["scales"].shape) != (Nout, Kred // 128) or \
+                tuple(c["biases"].shape) != (Nout, Kred // 128):
+            raise ValueError("group call %d: inconsistent shapes" % i)
+        arr[i] = qmm_group_call(_dev(c["A"], _BF16, "A").value, _dev(c["Wq"], _WORDS, "Wq").value,
+                                _dev(c["scales"], _BF16, "scales").value,
+                                _dev(c["biases"], _BF16, "biases").value,
+                                _dev(c["C"], _BF16, "C").value, M, Kred, Nout)
+    return arr
+
+
+def qmm_group_workspace_bytes(calls, partial_dtype: int = QMM_PARTIAL_BF16) -> int:
+    return int(lib().qmm_group_workspace_bytes(calls, len(calls), partial_dtype))
+
+
+def qmm_w4a16_g128_grouped(calls, workspace: torch.Tensor | None = None,
+                           partial_dtype: int = QMM_PARTIAL_BF16, stream=None):
+    """Every call's C with its policy split, in few launches; returns the splits."""
+    n = len(calls)
+    used = (_I * n)()
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr = _dev(workspace, (workspace.dtype,), "workspace")
+        ws_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().qmm_w4a16_g128_grouped(calls, n, ws_ptr, ws_bytes, partial_dtype,
+                                        _stream(stream), used), "qmm_w4a16_g128_grouped")
+    return list(used)

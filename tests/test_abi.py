@@ -230,6 +230,29 @@ def test_stream_executor_argument_errors_before_any_cuda_work():
     assert lib.qmm_stream_arena_bytes(calls, 1, 0) == 0
 
 
+def test_grouped_argument_errors_before_any_cuda_work():
+    lib = Q.lib()
+    P = ctypes.c_void_p
+    ok = Q.qmm_group_call(0x10000, 0x20000, 0x30000, 0x40000, 0x50000, 16, 2560, 1024)
+    run = lambda c, n, dt=0: lib.qmm_w4a16_g128_grouped(c, n, P(0x100000), 1 << 30, dt, None,
+                                                         None)
+    one = (Q.qmm_group_call * 1)(ok)
+    assert run(None, 1) == Q.QMM_EINVAL
+    assert run(one, 0) == Q.QMM_EINVAL
+    assert run(one, 1, 7) == Q.QMM_EINVAL
+    two = (Q.qmm_group_call * 2)(ok, Q.qmm_group_call(0x10000, 0x20000, 0x30000, 0x40000,
+                                                      0x50000, 16, 2500, 1024))
+    assert run(two, 2) == Q.QMM_ESHAPE                    # the second call's Kred
+    two[1] = Q.qmm_group_call(0x10000, 0x20000, 0x30000, 0x40000, None, 16, 2560, 1024)
+    assert run(two, 2) == Q.QMM_EINVAL
+    two[1] = Q.qmm_group_call(0x10002, 0x20000, 0x30000, 0x40000, 0x50000, 16, 2560, 1024)
+    assert run(two, 2) == Q.QMM_EALIGN
+    two[1] = Q.qmm_group_call(0x10000, 0x20000, 0x30000, 0x40000, 0x50000, 0, 2560, 1024)
+    assert run(two, 2) == Q.QMM_EINVAL
+    assert lib.qmm_group_workspace_bytes(None, 1, 0) == 0
+    assert lib.qmm_group_workspace_bytes(two, 2, 0) == 0
+
+
 def test_fused_reduce_workspace_holds_the_counters():
     from split_w4a16_quantized_gb300 import qmm as Q
     prev_k = Q.qmm_set_kernels(Q.QMM_KERNELS_TCGEN05)

@@ -808,3 +808,110 @@ def test_stream_executor_refuses_a_small_arena():
     with pytest.raises(Q.QmmError) as e:
         Q.qmm_w4a16_g128_stream(calls, 2, small)
     assert e.value.code == Q.QMM_EWORKSPACE
+
+
+# ---- several independent calls in few launches (qmm_w4a16_g128_grouped) -----
+
+def _group_problems(shapes, seed0):
+    probs = []
+    for j, (name, M) in enumerate(shapes):
+        if name == "odd":
+            Kred, Nout = 256, 77
+        else:
+            Kred, Nout = inputs.RAGGED if name == "ragged" else inputs.PROJECTIONS[name]
+        p = inputs.make_w4a16(M, Kred, Nout, seed=seed0 + j)
+        d = Q.to_device(p)
+        d["C"] = torch.full((M, Nout), float("nan"), dtype=torch.bfloat16, device="cuda")
+        probs.append((p, d))
+    return probs
+
+
+def _grouped_vs_calls(probs, dt=Q.QMM_PARTIAL_BF16):
+    refs = []
+    for p, d in probs:
+        M, Nout = d["C"].shape
+        C = torch.empty((M, Nout), dtype=torch.bfloat16, device="cuda")
+        nb = Q.qmm_splitk_workspace_bytes(M, Nout, 16, dt)  # room for any split
+        ws = torch.zeros(max(nb, 16) + (64 << 10), dtype=torch.uint8, device="cuda")
+        used = Q.qmm_w4a16_g128(d["A"], d["Wq"], d["scales"], d["biases"], C, workspace=ws,
+                                partial_dtype=dt)
+        refs.append((_bits(C), used))
+    calls = Q.group_calls([d for _, d in probs])
+    nb = Q.qmm_group_workspace_bytes(calls, dt)
+    ws = torch.full((max(nb, 16) // 2 + 8,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    used = Q.qmm_w4a16_g128_grouped(calls, ws if nb else None, dt)
+    torch.cuda.synchronize()
+    assert Q.qmm_kernel_status(clear=True) == 0
+    for j, ((p, d), (ref, ref_used)) in enumerate(zip(probs, refs)):
+        assert used[j] == ref_used, j
+        assert np.array_equal(_bits(d["C"]), ref), "call %d" % j
+    return used
+
+
+GROUP_SHAPES = [(n, M) for M in (32, 128) for n in inputs.PROJECTIONS] + \
+    [("ragged", 33), ("odd", 5), ("k", 16), ("down", 300), ("q", 8), ("ragged", 1)]
+
+
+@pytest.mark.parametrize("rule", ["equal", "near-equal"])
+@pytest.mark.parametrize("dt", [Q.QMM_PARTIAL_BF16, Q.QMM_PARTIAL_F32])
+def test_grouped_equals_the_calls(family, rule, dt):
+    """Each C of the grouped call is bitwise its own call's C: the same CTA
+    body, ring depth aside, and the same ordered FP32 reduce."""
+    prev = Q.qmm_set_partitions(Q.QMM_PARTITIONS_NEAR_EQUAL if rule == "near-equal"
+                                else Q.QMM_PARTITIONS_EQUAL)
+    try:
+        probs = _group_problems(GROUP_SHAPES, 200)
+        used = _grouped_vs_calls(probs, dt)
+        assert max(used) > 1 and min(used) == 1
+    finally:
+        Q.qmm_set_partitions(prev)
+    # and one call against the oracle directly
+    p, d = probs[13]  # down M=128
+    M, Nout = d["C"].shape
+    rows, cols = _sample(M, Nout, np.random.default_rng(8))
+    _check_sampled(p, _bits(d["C"]), used[13], dt, rows, cols, "grouped down M=128")
+
+
+def test_grouped_more_calls_than_one_launch_holds():
+    # 20 calls of one tile width: two partition launches and two reduce launches
+    shapes = [("k", 32), ("v", 32), ("q", 32), ("odd", 20), ("ragged", 31)] * 4
+    probs = _group_problems(shapes, 230)
+    _grouped_vs_calls(probs)
+
+
+@pytest.mark.parametrize("pdl", [True, False])
+def test_grouped_with_static_weights(pdl):
+    prev_w, prev_p = Q.qmm_set_weights_static(True), Q.qmm_set_pdl(pdl)
+    try:
+        probs = _group_problems(GROUP_SHAPES, 260)
+        _grouped_vs_calls(probs)
+        # twice back to back on one stream: the second group's early weight
+        # work overlaps the first group's last kernel
+        calls = Q.group_calls([d for _, d in probs])
+        ws = torch.zeros(Q.qmm_group_workspace_bytes(calls), dtype=torch.uint8, device="cuda")
+        first = [_bits(d["C"]) for _, d in probs]
+        for _ in range(3):
+            Q.qmm_w4a16_g128_grouped(calls, ws)
+        torch.cuda.synchronize()
+        assert all(np.array_equal(_bits(d["C"]), f) for (_, d), f in zip(probs, first))
+    finally:
+        Q.qmm_set_weights_static(prev_w)
+        Q.qmm_set_pdl(prev_p)
+
+
+def test_grouped_argument_errors():
+    probs = _group_problems([("k", 32), ("down", 128)], 290)
+    calls = Q.group_calls([d for _, d in probs])
+    nb = Q.qmm_group_workspace_bytes(calls)
+    assert nb > 0
+    with pytest.raises(Q.QmmError) as e:
+        Q.qmm_w4a16_g128_grouped(calls, torch.empty(nb - 256, dtype=torch.uint8, device="cuda"))
+    assert e.value.code == Q.QMM_EWORKSPACE
+    with pytest.raises(Q.QmmError) as e:
+        Q.qmm_w4a16_g128_grouped(calls, None)
+    assert e.value.code == Q.QMM_EWORKSPACE
+    # only unsplit calls need no workspace
+    big = _group_problems([("gate", 2048)], 295)
+    c1 = Q.group_calls([d for _, d in big])
+    assert Q.qmm_group_workspace_bytes(c1) == 0
+    assert Q.qmm_w4a16_g128_grouped(c1, None) == [1]
