@@ -9,7 +9,8 @@ Sources the oracle follows (cited per function in the C file):
   * tiny-llm book, "Week 2 Day 7: Split-K Prefill" (Tasks 2-4)
   * gpu-kernels-explained, "Split-K, streams and overlap" (Concept sections;
     Maths, Overlap and Split-K; A100 table)
-  * "Optimize Prefill vs Decode Kernels" (Required reasoning process, step 5)
+  * "Optimize Prefill vs Decode Kernels" (Required reasoning process, steps 4
+    and 5; Correctness requirements: the split-KV log-sum-exp merge)
 
 Parity pins: every function here is checked by ``tests/test_oracle.py``
 against values the pages print, closed forms, exact rational brute force on
@@ -73,6 +74,11 @@ def _load():
             "oracle_splitk_plan_near_equal": [I64, I64, I64, I64, I64, I64, I64, I64, P],
             "oracle_waves": [I64, I64, I64],
             "oracle_overlap_schedule": [I64, I64, P, P, P, I, P, P],
+            "oracle_decode_attention": [P, P, P, P, I64, I64, I64, I64, I64, ctypes.c_double, P,
+                                        I],
+            "oracle_decode_attention_split": [P, P, P, P, I64, I64, I64, I64, I64,
+                                              ctypes.c_double, I64, I, P, I],
+            "oracle_attention_splits": [I64, I64, I64, I64, I64, I64, P],
             "oracle_gemm": [P, P, I64, I64, I64, P, I],
             "oracle_gemm_partitioned": [P, P, I64, I64, I64, I64, I, P, I],
         }
@@ -241,6 +247,50 @@ def overlap_schedule(n, buffers, t_load, t_comp, t_store, out_reuse=False,
                                            _ptr(ev) if ev is not None else None),
            "overlap_schedule")
     return (T.value, ev) if with_events else T.value
+
+
+# ---- split-KV decode attention -----------------------------------------------
+
+def _attn_args(q, K, V, lens):
+    q, K, V = _c(q, np.uint16), _c(K, np.uint16), _c(V, np.uint16)
+    lens = _c(lens, np.int32)
+    B, Hq, D = q.shape
+    _, Hkv, Lmax, _ = K.shape
+    assert K.shape == V.shape == (B, Hkv, Lmax, D) and lens.shape == (B,)
+    return q, K, V, lens, B, Hq, Hkv, Lmax, D
+
+
+def decode_attention(q, K, V, lens, scale=None, threads: int | None = None) -> np.ndarray:
+    """fp64 O [B, Hq, D] of one query token per sequence over its KV history
+    (K, V BF16 bits [B, Hkv, Lmax, D]; lens [B]); scale defaults to 1/sqrt(D)."""
+    q, K, V, lens, B, Hq, Hkv, Lmax, D = _attn_args(q, K, V, lens)
+    O = np.empty((B, Hq, D), np.float64)
+    sc = 1.0 / np.sqrt(D) if scale is None else float(scale)
+    _check(_load().oracle_decode_attention(_ptr(q), _ptr(K), _ptr(V), _ptr(lens), B, Hq, Hkv,
+                                           Lmax, D, sc, _ptr(O), threads or default_threads()),
+           "decode_attention")
+    return O
+
+
+def decode_attention_split(q, K, V, lens, chunk: int, merge: str = "lse", scale=None,
+                           threads: int | None = None) -> np.ndarray:
+    """The split-KV algorithm in fp64: chunks of `chunk` positions merged with
+    the log-sum-exp correction (merge="lse") or naively ("naive")."""
+    q, K, V, lens, B, Hq, Hkv, Lmax, D = _attn_args(q, K, V, lens)
+    O = np.empty((B, Hq, D), np.float64)
+    sc = 1.0 / np.sqrt(D) if scale is None else float(scale)
+    _check(_load().oracle_decode_attention_split(
+        _ptr(q), _ptr(K), _ptr(V), _ptr(lens), B, Hq, Hkv, Lmax, D, sc, chunk,
+        {"lse": 0, "naive": 1}[merge], _ptr(O), threads or default_threads()),
+        "decode_attention_split")
+    return O
+
+
+def attention_splits(B, Hkv, Lmax, sms, blocks_per_sm, min_chunk) -> int:
+    s = ctypes.c_int(0)
+    _check(_load().oracle_attention_splits(B, Hkv, Lmax, sms, blocks_per_sm, min_chunk,
+                                           ctypes.byref(s)), "attention_splits")
+    return s.value
 
 
 # ---- dense BF16 GEMM -----------------------------------------------------

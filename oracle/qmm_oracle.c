@@ -14,7 +14,9 @@
  *        buffers; second Concept section; Maths, "Overlap" and "Split-K";
  *        the A100 model table)
  *   [PD] "Optimize Prefill vs Decode Kernels" (Required reasoning process,
- *        step 5: at least ~512 reduction elements per split)
+ *        steps 4 and 5: split-K for decode matmuls, at least ~512 reduction
+ *        elements per split, split-KV decode attention; Correctness
+ *        requirements: the FP32 log-sum-exp merge)
  * The weight format (w = scale*q + bias, q in 0..15, eight nibbles per
  * uint32 low nibble first, BF16 scale and bias per 128-group along the
  * reduction axis) is the MLX-style affine "w4a16_g128" format [TL] checks
@@ -456,5 +458,149 @@ int oracle_overlap_schedule(int64_t n, int64_t b, const double *t_load, const do
     *T = ev[6 * (n - 1) + 5];
     if (events) memcpy(events, ev, sizeof(double) * (size_t)(6 * n));
     free(ev);
+    return 0;
+}
+
+/* ---- split-KV decode attention ----------------------------------------- */
+
+/* [PD, step 4 (decode attention), step 5 and Correctness requirements]:
+ * one query token per sequence attends to its whole KV history.  q is BF16
+ * [B, Hq, D]; K and V are BF16 [B, Hkv, Lmax, D] (head-major, contiguous
+ * along the sequence); sequence b has lens[b] valid positions (1 <= lens[b]
+ * <= Lmax).  Query head h reads KV head h / (Hq / Hkv) (grouped-query
+ * attention; Hq a multiple of Hkv).
+ *   O[b, h, :] = sum_{l < lens[b]} softmax_l(scale * q[b, h] . K[b, g, l]) V[b, g, l]
+ * computed in fp64: the scores, their maximum, exp(s - max), their sum and
+ * the weighted sum of V rows, then one division.  O is fp64 [B, Hq, D]. */
+static int attn_check(int64_t B, int64_t Hq, int64_t Hkv, int64_t Lmax, int64_t D,
+                      const int32_t *lens) {
+    if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || Lmax < 1 || D < 1 || !lens) return -1;
+    for (int64_t b = 0; b < B; ++b)
+        if (lens[b] < 1 || lens[b] > Lmax) return -1;
+    return 0;
+}
+
+/* scores of one (b, h) over positions [l0, l1): s[l - l0] (fp64) */
+static void attn_scores(const uint16_t *q, const uint16_t *K, int64_t b, int64_t h, int64_t Hq,
+                        int64_t Hkv, int64_t Lmax, int64_t D, double scale, int64_t l0,
+                        int64_t l1, double *s) {
+    int64_t g = h / (Hq / Hkv);
+    const uint16_t *qv = q + (b * Hq + h) * D;
+    for (int64_t l = l0; l < l1; ++l) {
+        const uint16_t *kv = K + ((b * Hkv + g) * Lmax + l) * D;
+        double acc = 0.0;
+        for (int64_t d = 0; d < D; ++d) acc += bf16_value(qv[d]) * bf16_value(kv[d]);
+        s[l - l0] = scale * acc;
+    }
+}
+
+int oracle_decode_attention(const uint16_t *q, const uint16_t *K, const uint16_t *V,
+                            const int32_t *lens, int64_t B, int64_t Hq, int64_t Hkv, int64_t Lmax,
+                            int64_t D, double scale, double *O, int nthreads) {
+    if (!q || !K || !V || !O || nthreads < 1 || attn_check(B, Hq, Hkv, Lmax, D, lens)) return -1;
+    int bad = 0;
+#pragma omp parallel for num_threads(nthreads) schedule(dynamic) collapse(2) reduction(| : bad)
+    for (int64_t b = 0; b < B; ++b)
+        for (int64_t h = 0; h < Hq; ++h) {
+            int64_t L = lens[b], g = h / (Hq / Hkv);
+            double *s = (double *)malloc(sizeof(double) * (size_t)L);
+            if (!s) { bad = 1; continue; }
+            attn_scores(q, K, b, h, Hq, Hkv, Lmax, D, scale, 0, L, s);
+            double mx = s[0];
+            for (int64_t l = 1; l < L; ++l) if (s[l] > mx) mx = s[l];
+            double sum = 0.0;
+            for (int64_t l = 0; l < L; ++l) { s[l] = exp(s[l] - mx); sum += s[l]; }
+            double *o = O + (b * Hq + h) * D;
+            for (int64_t d = 0; d < D; ++d) o[d] = 0.0;
+            for (int64_t l = 0; l < L; ++l) {
+                const uint16_t *vv = V + ((b * Hkv + g) * Lmax + l) * D;
+                for (int64_t d = 0; d < D; ++d) o[d] += s[l] * bf16_value(vv[d]);
+            }
+            for (int64_t d = 0; d < D; ++d) o[d] /= sum;
+            free(s);
+        }
+    return bad ? -4 : 0;
+}
+
+/* The split-KV algorithm [PD, step 4, step 5 and Correctness requirements],
+ * in fp64: the positions of sequence b are cut into chunks of `chunk`
+ * positions; chunk c gives a partial softmax state -- its maximum m_c, its
+ * sum l_c of exp(s - m_c) and its unnormalized output o_c = sum exp(s - m_c)
+ * V -- and the states are merged with the log-sum-exp correction:
+ * M = max_c m_c, O = sum_c exp(m_c - M) o_c / sum_c exp(m_c - M) l_c
+ * (merge 0).  merge 1 is the naive combine the page warns about: the mean
+ * of the chunks' normalized outputs o_c / l_c, with no correction.  O is fp64
+ * [B, Hq, D]. */
+int oracle_decode_attention_split(const uint16_t *q, const uint16_t *K, const uint16_t *V,
+                                  const int32_t *lens, int64_t B, int64_t Hq, int64_t Hkv,
+                                  int64_t Lmax, int64_t D, double scale, int64_t chunk, int merge,
+                                  double *O, int nthreads) {
+    if (!q || !K || !V || !O || nthreads < 1 || chunk < 1 || (merge != 0 && merge != 1) ||
+        attn_check(B, Hq, Hkv, Lmax, D, lens))
+        return -1;
+    int bad = 0;
+#pragma omp parallel for num_threads(nthreads) schedule(dynamic) collapse(2) reduction(| : bad)
+    for (int64_t b = 0; b < B; ++b)
+        for (int64_t h = 0; h < Hq; ++h) {
+            int64_t L = lens[b], g = h / (Hq / Hkv), nc = (L + chunk - 1) / chunk;
+            double *s = (double *)malloc(sizeof(double) * (size_t)chunk);
+            double *m = (double *)malloc(sizeof(double) * (size_t)nc);
+            double *l = (double *)malloc(sizeof(double) * (size_t)nc);
+            double *oc = (double *)malloc(sizeof(double) * (size_t)(nc * D));
+            if (!s || !m || !l || !oc) { bad = 1; free(s); free(m); free(l); free(oc); continue; }
+            for (int64_t c = 0; c < nc; ++c) {
+                int64_t l0 = c * chunk, l1 = l0 + chunk < L ? l0 + chunk : L;
+                attn_scores(q, K, b, h, Hq, Hkv, Lmax, D, scale, l0, l1, s);
+                double mx = s[0];
+                for (int64_t t = 1; t < l1 - l0; ++t) if (s[t] > mx) mx = s[t];
+                m[c] = mx;
+                l[c] = 0.0;
+                for (int64_t d = 0; d < D; ++d) oc[c * D + d] = 0.0;
+                for (int64_t t = 0; t < l1 - l0; ++t) {
+                    double p = exp(s[t] - mx);
+                    l[c] += p;
+                    const uint16_t *vv = V + ((b * Hkv + g) * Lmax + l0 + t) * D;
+                    for (int64_t d = 0; d < D; ++d) oc[c * D + d] += p * bf16_value(vv[d]);
+                }
+            }
+            double *o = O + (b * Hq + h) * D;
+            if (merge == 0) {
+                double M = m[0];
+                for (int64_t c = 1; c < nc; ++c) if (m[c] > M) M = m[c];
+                double den = 0.0;
+                for (int64_t d = 0; d < D; ++d) o[d] = 0.0;
+                for (int64_t c = 0; c < nc; ++c) {
+                    double w = exp(m[c] - M);
+                    den += w * l[c];
+                    for (int64_t d = 0; d < D; ++d) o[d] += w * oc[c * D + d];
+                }
+                for (int64_t d = 0; d < D; ++d) o[d] /= den;
+            } else {
+                for (int64_t d = 0; d < D; ++d) {
+                    double acc = 0.0;
+                    for (int64_t c = 0; c < nc; ++c) acc += oc[c * D + d] / l[c];
+                    o[d] = acc / (double)nc;
+                }
+            }
+            free(s); free(m); free(l); free(oc);
+        }
+    return bad ? -4 : 0;
+}
+
+/* [PD, step 5]: the split-KV factor.  S = ceil(SMs * blocks_per_sm /
+ * (B * Hkv)) blocks of work per (sequence, KV head), at least 1, clamped so
+ * every split keeps at least min_chunk positions of the longest sequence:
+ * S <= max(1, floor(Lmax / min_chunk)). */
+int oracle_attention_splits(int64_t B, int64_t Hkv, int64_t Lmax, int64_t sms,
+                            int64_t blocks_per_sm, int64_t min_chunk, int *splits) {
+    if (B < 1 || Hkv < 1 || Lmax < 1 || sms < 1 || blocks_per_sm < 1 || min_chunk < 1 || !splits)
+        return -1;
+    int64_t work = B * Hkv;
+    int64_t S = (sms * blocks_per_sm + work - 1) / work;
+    int64_t cap = Lmax / min_chunk;
+    if (cap < 1) cap = 1;
+    if (S > cap) S = cap;
+    if (S < 1) S = 1;
+    *splits = (int)S;
     return 0;
 }

@@ -467,6 +467,114 @@ def test_overlap_more_buffers_never_hurt_and_help_only_with_varying_times():
     assert helped  # some varying-time schedule gains from a third buffer
 
 
+# ---- split-KV decode attention ---------------------------------------------
+
+def _attn_problem(B, Hq, Hkv, Lmax, D, seed, lens=None):
+    rng = np.random.default_rng(seed)
+    q = inputs.f32_to_bf16_bits(rng.standard_normal((B, Hq, D)).astype(np.float32))
+    K = inputs.f32_to_bf16_bits(rng.standard_normal((B, Hkv, Lmax, D)).astype(np.float32))
+    V = inputs.f32_to_bf16_bits(rng.standard_normal((B, Hkv, Lmax, D)).astype(np.float32))
+    if lens is None:
+        lens = rng.integers(1, Lmax + 1, B)
+    return q, K, V, np.asarray(lens, np.int32)
+
+
+def test_attention_matches_a_library_softmax():
+    from scipy.special import softmax
+    for (B, Hq, Hkv, Lmax, D) in [(1, 1, 1, 1, 8), (2, 4, 2, 9, 16), (3, 8, 1, 33, 32)]:
+        q, K, V, lens = _attn_problem(B, Hq, Hkv, Lmax, D, seed=B + Lmax)
+        O = oracle.decode_attention(q, K, V, lens, threads=2)
+        qf, Kf, Vf = _bits_to_f64(q), _bits_to_f64(K), _bits_to_f64(V)
+        for b in range(B):
+            for h in range(Hq):
+                g = h // (Hq // Hkv)
+                L = lens[b]
+                p = softmax(Kf[b, g, :L] @ qf[b, h] / np.sqrt(D))
+                assert np.allclose(O[b, h], p @ Vf[b, g, :L], rtol=0, atol=1e-12)
+
+
+def test_attention_closed_forms():
+    B, Hq, Hkv, Lmax, D = 2, 4, 2, 40, 16
+    q, K, V, lens = _attn_problem(B, Hq, Hkv, Lmax, D, seed=30, lens=[40, 23])
+    Vf = _bits_to_f64(V)
+    # every key of a sequence equal: uniform weights, the mean of the valid V rows
+    Ku = np.repeat(K[:, :, :1, :], Lmax, axis=2)
+    O = oracle.decode_attention(q, Ku, V, lens, threads=2)
+    for b in range(B):
+        for h in range(Hq):
+            g = h // 2
+            assert np.allclose(O[b, h], Vf[b, g, :lens[b]].mean(axis=0), rtol=0, atol=1e-12)
+    # a constant V per KV head: every query head reads its own group's value
+    Vc = np.zeros_like(V)
+    for g in range(Hkv):
+        Vc[:, g] = _bf16_bits(float(g + 1))
+    O = oracle.decode_attention(q, K, Vc, lens, threads=2)
+    for h in range(Hq):
+        assert np.all(O[:, h] == h // (Hq // Hkv) + 1)
+    # one key aligned with the query and far longer wins: O -> that key's V row
+    qs = np.full((1, 1, D), _bf16_bits(1.0), np.uint16)
+    Kd = np.zeros((1, 1, 16, D), np.uint16)
+    Kd[0, 0, 5] = _bf16_bits(8.0)            # score 8 * D / sqrt(D) = 32; the rest 0
+    Vd = V[:1, :1, :16]
+    O = oracle.decode_attention(qs, Kd, Vd, [16], threads=1)
+    bound = 15 * np.exp(-32.0) * np.abs(_bits_to_f64(Vd)).max() * 2
+    assert np.all(np.abs(O[0, 0] - _bits_to_f64(Vd)[0, 0, 5]) <= bound)
+
+
+def test_attention_ignores_positions_past_the_length():
+    q, K, V, lens = _attn_problem(3, 4, 4, 30, 16, seed=31, lens=[30, 7, 1])
+    O = oracle.decode_attention(q, K, V, lens, threads=2)
+    K2, V2 = K.copy(), V.copy()
+    for b, L in enumerate(lens):
+        K2[b, :, L:] = _bf16_bits(100.0)
+        V2[b, :, L:] = _bf16_bits(-1000.0)
+    assert np.array_equal(O, oracle.decode_attention(q, K2, V2, lens, threads=2))
+
+
+def test_attention_shift_invariance():
+    # adding one vector t to every key shifts all scores of a query by q.t:
+    # the softmax, and O, stay the same (integer values keep K + t exact)
+    rng = np.random.default_rng(32)
+    B, H, L, D = 2, 3, 25, 16
+    q = inputs.f32_to_bf16_bits(rng.integers(-3, 4, (B, H, D)).astype(np.float32))
+    Kf = rng.integers(-3, 4, (B, H, L, D)).astype(np.float32)
+    K = inputs.f32_to_bf16_bits(Kf)
+    K2 = inputs.f32_to_bf16_bits(Kf + rng.integers(-5, 6, (1, 1, 1, D)).astype(np.float32))
+    V = inputs.f32_to_bf16_bits(rng.standard_normal((B, H, L, D)).astype(np.float32))
+    lens = np.array([25, 11], np.int32)
+    O1 = oracle.decode_attention(q, K, V, lens, scale=0.1, threads=2)
+    O2 = oracle.decode_attention(q, K2, V, lens, scale=0.1, threads=2)
+    assert np.allclose(O1, O2, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("chunk", [1, 3, 7, 16, 64, 1000])
+def test_split_kv_lse_merge_is_exact_and_the_naive_merge_is_not(chunk):
+    q, K, V, lens = _attn_problem(3, 8, 2, 64, 32, seed=33, lens=[64, 45, 9])
+    O = oracle.decode_attention(q, K, V, lens, threads=2)
+    Os = oracle.decode_attention_split(q, K, V, lens, chunk, "lse", threads=2)
+    assert np.allclose(Os, O, rtol=0, atol=1e-12)
+    On = oracle.decode_attention_split(q, K, V, lens, chunk, "naive", threads=2)
+    if chunk < 64:  # more than one chunk somewhere: the naive mean is wrong
+        assert np.abs(On - O).max() > 1e-3
+    else:
+        assert np.allclose(On, O, rtol=0, atol=1e-12)
+
+
+def test_attention_split_factor():
+    rng = np.random.default_rng(34)
+    for _ in range(2000):
+        B, Hkv = int(rng.integers(1, 65)), int(rng.integers(1, 17))
+        Lmax, sms = int(rng.integers(1, 40000)), int(rng.integers(1, 200))
+        bps, mc = int(rng.integers(1, 5)), int(rng.integers(1, 2049))
+        S = oracle.attention_splits(B, Hkv, Lmax, sms, bps, mc)
+        # the smallest S whose grid reaches the target, unless the chunk floor binds
+        cap = max(1, Lmax // mc)
+        want = next(s for s in range(1, 10 ** 6) if s * B * Hkv >= sms * bps)
+        assert S == min(want, cap) and S >= 1
+        if S > 1:
+            assert Lmax // S >= mc
+
+
 # ---- dense GEMM ------------------------------------------------------------
 
 def test_gemm_exact_brute_force():
