@@ -484,13 +484,14 @@ def run_gpu(args, rank, world, local_rank):
     dense = dense_sweep(Q, device, stream, sms, l2) if rank == 0 else None
     e2e = run_e2e(wl, Q, device, stream, min(args.steps, 20))
     overlap = overlap_sweep(wl, Q, device) if rank == 0 else None
+    attention = attention_bench(Q, device, stream, peaks, l2) if rank == 0 else None
     return {"ms": ms, "ms_nopdl": ms_nopdl, "ms_wflip": ms_wflip, "ms_fused": ms_fused,
             "ms_alt": ms_alt, "ms_grouped": ms_grouped, "grouped_launches": grouped_launches,
             "per_call": per_call, "dom": dom,
             "clocks": sample, "wl": wl,
             "peaks": peaks,
             "peak_src": peak_src, "l2": l2, "sms": sms, "dense": dense, "e2e": e2e,
-            "prefill": prefill, "overlap": overlap}
+            "prefill": prefill, "overlap": overlap, "attention": attention}
 
 
 def prefill_sweep(Q, device, stream, l2, peaks):
@@ -540,6 +541,75 @@ def dense_sweep(Q, device, stream, sms, l2):
         out.append({"split": s, "blocks": 16 * s, "waves": -(-16 * s // sms), "us": round(us, 3),
                     "tflops": round(2 * 512 * 512 * 16384 / us / 1e6, 2)})
     return out
+
+
+def attention_bench(Q, device, stream, peaks, l2):
+    """Split-KV decode attention (qmm_decode_attention) on the Qwen3-4B heads
+    (32 query, 8 KV, dim 128): 32 sequences with lengths mixed uniformly in
+    [1024, 8192].  The KV history (about 0.6 GB) is far larger than L2, so
+    each call reads it from HBM.  Timed as a graph of back-to-back calls, for
+    the plan's split and a few forced ones; the roofline is the HBM copy
+    bandwidth over the bytes a call must move (the valid K and V rows, q, O
+    and, when split, the partial states written and read back)."""
+    h = inputs.ATTENTION_HEADS
+    B, Lmax = 32, 8192
+    prob = inputs.make_attention(B, h["Hq"], h["Hkv"], Lmax, h["D"], seed=0, lmin=1024)
+    d = Q.attention_to_device(prob, device)
+    O = torch.empty((B, h["Hq"], h["D"]), dtype=torch.bfloat16, device=device)
+    plan = Q.qmm_decode_attention_splits(B, h["Hq"], h["Hkv"], Lmax)
+    ws = torch.empty(max(Q.qmm_decode_attention_workspace_bytes(B, h["Hq"], h["D"], 16), 16),
+                     dtype=torch.uint8, device=device)
+    kv_bytes = int(prob["lens"].sum()) * h["Hkv"] * h["D"] * 2 * 2
+    qo_bytes = 2 * B * h["Hq"] * h["D"] * 2
+    out = {"workload": "Qwen3-4B heads (Hq 32, Hkv 8, D 128), B=32, lens U[1024, 8192] "
+                       "(seed 0), K/V BF16 head-major",
+           "kv_bytes": kv_bytes, "plan_split": plan, "splits": []}
+    calls_per_graph = max(4, -(-3 * l2 // kv_bytes))
+    for S in sorted({plan, 1, 2, 4, 8, 16}):
+        us = graph_us_per_launch(
+            lambda j: Q.qmm_decode_attention(d["q"], d["K"], d["V"], d["lens"], O,
+                                             splits_req=S, workspace=ws),
+            calls_per_graph, stream)
+        part = 2 * B * h["Hq"] * S * (h["D"] + 2) * 4 if S > 1 else 0
+        nbytes = kv_bytes + qo_bytes + part
+        gbs = nbytes / us / 1e3
+        out["splits"].append({"split": S, "ctas": S * B * h["Hkv"], "us": round(us, 3),
+                              "gbs": round(gbs, 1),
+                              "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4)})
+    best = min(out["splits"], key=lambda r: r["us"])
+    out["plan"] = next(r for r in out["splits"] if r["split"] == plan)
+    out["best"] = best
+    return out
+
+
+def run_attention_only(args):
+    """--attention-only: W warm-up and K timed decode-attention calls of the
+    bench's attention workload at the plan's split, one JSON line."""
+    from split_w4a16_quantized_gb300 import build as qbuild
+    qbuild.build()
+    from split_w4a16_quantized_gb300 import qmm as Q
+    device = torch.device("cuda", 0)
+    h = inputs.ATTENTION_HEADS
+    B, Lmax = 32, 8192
+    prob = inputs.make_attention(B, h["Hq"], h["Hkv"], Lmax, h["D"], seed=0, lmin=1024)
+    d = Q.attention_to_device(prob, device)
+    O = torch.empty((B, h["Hq"], h["D"]), dtype=torch.bfloat16, device=device)
+    S = Q.qmm_decode_attention_splits(B, h["Hq"], h["Hkv"], Lmax)
+    ws = torch.empty(max(Q.qmm_decode_attention_workspace_bytes(B, h["Hq"], h["D"], S), 16),
+                     dtype=torch.uint8, device=device)
+    run = lambda: Q.qmm_decode_attention(d["q"], d["K"], d["V"], d["lens"], O, workspace=ws)
+    for _ in range(args.warmup):
+        run()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(args.steps):
+        run()
+    t1.record()
+    torch.cuda.synchronize()
+    print(json.dumps({"attention_only": True, "split": S, "calls": args.steps,
+                      "us_per_call": round(t0.elapsed_time(t1) * 1e3 / args.steps, 3),
+                      "status": Q.qmm_kernel_status(clear=True)}), flush=True)
 
 
 def overlap_sweep(wl, Q, device, reps=10):
@@ -813,6 +883,8 @@ def main():
                     help="partition rule of the W4A16 calls (qmm_set_partitions)")
     ap.add_argument("--only", default=None, metavar="PROJ:M",
                     help="restrict the step to one call, e.g. gate:128 (profiling aid)")
+    ap.add_argument("--attention-only", action="store_true",
+                    help="only the decode-attention calls at the plan's split (profiling aid)")
     args = ap.parse_args()
     if args.only:
         global ONLY
@@ -831,6 +903,8 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    if args.attention_only:
+        return run_attention_only(args)
     res = run_gpu(args, rank, world, local_rank)
     wl = res["wl"]
     ncalls = len(wl.calls)
@@ -924,7 +998,7 @@ def main():
            "gpu_launches": args.steps * wl.launches_per_step(),
            "clocks": res["clocks"], "e2e": res["e2e"], "per_call": res["per_call"],
            "dense_splitk_512x512x16384": res["dense"], "prefill_M2048": res["prefill"],
-           "overlap_stream": res["overlap"]}
+           "overlap_stream": res["overlap"], "decode_attention": res["attention"]}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(wl.host)
     if rank == 0:

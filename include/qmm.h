@@ -368,6 +368,52 @@ size_t qmm_group_workspace_bytes(const qmm_group_call *calls, int n, int partial
 int qmm_w4a16_g128_grouped(const qmm_group_call *calls, int n, void *workspace, size_t ws_bytes,
                            int partial_dtype, void *stream, int *splits_used);
 
+/* ---- split-KV decode attention -------------------------------------------
+ *
+ * "Optimize Prefill vs Decode Kernels" (Required reasoning process, steps 4
+ * and 5; Correctness requirements): in decode one query token per sequence
+ * attends to its whole KV history, an HBM-bound read of every K and V byte.
+ * The history of each (sequence, KV head) is split into S parts (split-KV);
+ * each part's partial softmax state -- maximum, sum of exponentials,
+ * unnormalized output -- is kept in FP32 and the parts are merged with the
+ * log-sum-exp correction.
+ *   q     BF16 [B, Hq, D], one query token per sequence
+ *   K, V  BF16 [B, Hkv, Lmax, D], head-major (each head's positions contiguous)
+ *   lens  device int32 [B]: sequence b uses positions 0 .. lens[b]-1, with
+ *         1 <= lens[b] <= Lmax (values outside are clamped into [0, Lmax];
+ *         a length of 0 gives NaN outputs for that sequence)
+ *   O     BF16 [B, Hq, D]:
+ *         O[b,h] = sum_l softmax_l(scale * q[b,h] . K[b,h/QG,l]) V[b,h/QG,l]
+ *         with QG = Hq / Hkv query heads per KV head (grouped-query attention)
+ * D is 64 or 128; QG is 1, 2, 4 or 8. */
+
+/* The split factor the page prescribes (step 5): S = ceil(num_sms * 4 /
+ * (B * Hkv)) -- a grid of 4 blocks per SM, two waves of the kernel's two
+ * resident CTAs, within the page's 2-4 -- clamped to [1, max(1,
+ * floor(Lmax / 512))] so every split keeps at least 512 positions of the
+ * longest sequence.  num_sms <= 0 queries the device.  Returns QMM_OK,
+ * QMM_EINVAL or QMM_ENODEV.  Host only. */
+int qmm_decode_attention_splits(int B, int Hq, int Hkv, int Lmax, int num_sms, int *splits);
+
+/* Workspace bytes of the partial states for `splits` splits:
+ * B * Hq * splits * (D + 2) * 4, or 0 when splits <= 1. */
+size_t qmm_decode_attention_workspace_bytes(int B, int Hq, int D, int splits);
+
+/* O = decode attention of q over K, V (above).  splits_req 0 takes
+ * qmm_decode_attention_splits; s >= 1 forces s splits (splits past the
+ * longest sequence's positions are empty and cost a little).  scale <= 0
+ * means 1/sqrt(D).  workspace: device, 16-byte aligned, at least
+ * qmm_decode_attention_workspace_bytes bytes when the split used is > 1.
+ * One launch (split 1) or the split kernel and the merge kernel on `stream`.
+ * splits_used (host, nullable) receives the split.  Returns QMM_OK,
+ * QMM_EINVAL (null pointers, sizes < 1, Hq not a multiple of Hkv),
+ * QMM_ESHAPE (D not 64 or 128, QG not 1/2/4/8, a grid dimension past 65535,
+ * splits_req past 65535), QMM_EALIGN, QMM_EWORKSPACE, QMM_ENODEV or
+ * QMM_ECUDA. */
+int qmm_decode_attention(const void *q, const void *K, const void *V, const int *lens, void *O,
+                         int B, int Hq, int Hkv, int Lmax, int D, float scale, int splits_req,
+                         void *workspace, size_t ws_bytes, void *stream, int *splits_used);
+
 /* ---- streaming host activations through the matmul ----------------------
  *
  * gpu-kernels-explained, "Split-K, streams and overlap" (first Concept

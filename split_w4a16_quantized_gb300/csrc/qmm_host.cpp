@@ -5,6 +5,7 @@
 #include <algorithm>
 #include <atomic>
 #include <climits>
+#include <cmath>
 #include <cstdint>
 #include <mutex>
 #include <vector>
@@ -503,6 +504,64 @@ int qmm_gemm_bf16_splitk(const void* A, const void* W, void* C, int M, int N, in
                       : qmm::launch_gemm(A, W, workspace, qmm::kOutF32, M, N, K, split, stream));
     if (rc == QMM_OK)
         rc = launched(qmm::launch_reduce(workspace, QMM_PARTIAL_F32, split, M, N, C, stream));
+    return rc;
+}
+
+int qmm_decode_attention_splits(int B, int Hq, int Hkv, int Lmax, int num_sms, int* splits) {
+    if (!splits || B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || Lmax < 1) return QMM_EINVAL;
+    if (num_sms <= 0) {
+        const int rc = device_sms(&num_sms);
+        if (rc != QMM_OK) return rc;
+    }
+    // grid target: two waves of the kernel's two resident CTAs per SM, the
+    // page's "2-4 blocks per SM"; a mix of sequence lengths balances better
+    // over more than one wave
+    constexpr int kBlocksPerSm = 4;
+    const int64_t work = static_cast<int64_t>(B) * Hkv;
+    const int64_t target = static_cast<int64_t>(num_sms) * kBlocksPerSm;
+    int64_t S = ceil_div(target, work);
+    int64_t cap = Lmax / 512;
+    if (cap < 1) cap = 1;
+    if (S > cap) S = cap;
+    *splits = static_cast<int>(S < 1 ? 1 : S);
+    return QMM_OK;
+}
+
+size_t qmm_decode_attention_workspace_bytes(int B, int Hq, int D, int splits) {
+    if (B < 1 || Hq < 1 || D < 1 || splits <= 1) return 0;
+    return static_cast<size_t>(B) * Hq * splits * (D + 2) * sizeof(float);
+}
+
+int qmm_decode_attention(const void* q, const void* K, const void* V, const int* lens, void* O,
+                         int B, int Hq, int Hkv, int Lmax, int D, float scale, int splits_req,
+                         void* workspace, size_t ws_bytes, void* stream, int* splits_used) {
+    if (!q || !K || !V || !lens || !O || B < 1 || Hq < 1 || Hkv < 1 || Lmax < 1 ||
+        splits_req < 0 || Hq % Hkv)
+        return QMM_EINVAL;
+    const int qg = Hq / Hkv;
+    if ((D != 64 && D != 128) || (qg != 1 && qg != 2 && qg != 4 && qg != 8)) return QMM_ESHAPE;
+    if (B > 65535 || Hkv > 65535 || splits_req > 65535 ||
+        static_cast<int64_t>(B) * Hq > 0x7fffffffLL)
+        return QMM_ESHAPE;
+    if (!aligned(q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) ||
+        !aligned(lens, 4))
+        return QMM_EALIGN;
+    int rc = check_device();
+    if (rc != QMM_OK) return rc;
+    int S = splits_req;
+    if (S == 0) {
+        rc = qmm_decode_attention_splits(B, Hq, Hkv, Lmax, 0, &S);
+        if (rc != QMM_OK) return rc;
+    }
+    if (S > 1) {
+        if (!workspace || ws_bytes < qmm_decode_attention_workspace_bytes(B, Hq, D, S))
+            return QMM_EWORKSPACE;
+        if (!aligned(workspace, 16)) return QMM_EALIGN;
+    }
+    const float sc = scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(D));
+    rc = launched(qmm::launch_decode_attention(q, K, V, lens, O, static_cast<float*>(workspace), B,
+                                               Hq, Hkv, Lmax, D, sc, S, stream));
+    if (rc == QMM_OK && splits_used) *splits_used = S;
     return rc;
 }
 

@@ -102,6 +102,14 @@ int launch_w4a16_tc(int bm, const void* A, const uint32_t* Wq, const void* scale
                     void* out, int out_mode, int M, int Kred, int Nout, int split, void* stream,
                     void* fused_C = nullptr, uint32_t* counters = nullptr);
 int read_tc_status(int* out, bool clear);
+// Device address of the status word the tcgen05 and attention kernels share.
+int* tc_status_ptr();
+
+// Split-KV decode attention (qmm_attention.cu): S splits per (sequence, KV
+// head); ws holds the partial states when S > 1 (B*Hq*S*(D+2) floats).
+int launch_decode_attention(const void* q, const void* K, const void* V, const int* lens, void* O,
+                            float* ws, int B, int Hq, int Hkv, int Lmax, int D, float scale,
+                            int S, void* stream);
 
 // Grouped launches: independent calls in one kernel launch (at most
 // kMaxGroupCalls per launch; the caller cuts longer lists).

@@ -90,3 +90,25 @@ def make_dense(M: int, N: int, K: int, seed: int = 0) -> dict:
     a = rng.standard_normal((M, K), dtype=np.float32)
     w = rng.standard_normal((N, K), dtype=np.float32)
     return {"A": f32_to_bf16_bits(a), "W": f32_to_bf16_bits(w), "M": M, "N": N, "K": K}
+
+
+# Qwen3-4B attention: 32 query heads, 8 KV heads (grouped-query, 4 per KV
+# head), head dim 128.
+ATTENTION_HEADS = {"Hq": 32, "Hkv": 8, "D": 128}
+
+
+def make_attention(B: int, Hq: int, Hkv: int, Lmax: int, D: int, seed: int = 0,
+                   lens=None, lmin: int = 1) -> dict:
+    """One seeded decode-attention problem: q [B,Hq,D], K and V [B,Hkv,Lmax,D]
+    (BF16 bits, ~ N(0, 1)) and per-sequence lengths lens [B] (int32), drawn
+    uniformly from [lmin, Lmax] unless given -- a mix of context lengths, as a
+    decode batch of requests has.  Draw order: q, K, V, lens."""
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((B, Hq, D), dtype=np.float32)
+    K = rng.standard_normal((B, Hkv, Lmax, D), dtype=np.float32)
+    V = rng.standard_normal((B, Hkv, Lmax, D), dtype=np.float32)
+    if lens is None:
+        lens = rng.integers(lmin, Lmax + 1, size=B)
+    return {"q": f32_to_bf16_bits(q), "K": f32_to_bf16_bits(K), "V": f32_to_bf16_bits(V),
+            "lens": np.asarray(lens, dtype=np.int32), "B": B, "Hq": Hq, "Hkv": Hkv,
+            "Lmax": Lmax, "D": D}

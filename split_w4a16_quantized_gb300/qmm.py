@@ -12,6 +12,7 @@ import ctypes
 import os
 import threading
 
+import numpy as np
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -87,6 +88,10 @@ _SIGS = {
                                     ctypes.POINTER(qmm_policy), _I, _P, ctypes.POINTER(_I)]),
     "qmm_static_scratch_bytes": (_SZ, []),
     "qmm_tc_pipeline_config": (_I, [_I, _I, _I, ctypes.POINTER(_I)]),
+    "qmm_decode_attention_splits": (_I, [_I, _I, _I, _I, _I, ctypes.POINTER(_I)]),
+    "qmm_decode_attention_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
+    "qmm_decode_attention": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, ctypes.c_float, _I,
+                                  _P, _SZ, _P, ctypes.POINTER(_I)]),
     "qmm_group_workspace_bytes": (_SZ, [ctypes.POINTER(qmm_group_call), _I, _I]),
     "qmm_w4a16_g128_grouped": (_I, [ctypes.POINTER(qmm_group_call), _I, _P, _SZ, _I, _P,
                                     ctypes.POINTER(_I)]),
@@ -498,3 +503,48 @@ def qmm_w4a16_g128_grouped(calls, workspace: torch.Tensor | None = None,
     _check(lib().qmm_w4a16_g128_grouped(calls, n, ws_ptr, ws_bytes, partial_dtype,
                                         _stream(stream), used), "qmm_w4a16_g128_grouped")
     return list(used)
+
+
+# ---- split-KV decode attention ---------------------------------------------
+
+def qmm_decode_attention_splits(B: int, Hq: int, Hkv: int, Lmax: int, num_sms: int = 0) -> int:
+    s = _I(0)
+    _check(lib().qmm_decode_attention_splits(B, Hq, Hkv, Lmax, num_sms, ctypes.byref(s)),
+           "qmm_decode_attention_splits")
+    return s.value
+
+
+def qmm_decode_attention_workspace_bytes(B: int, Hq: int, D: int, splits: int) -> int:
+    return int(lib().qmm_decode_attention_workspace_bytes(B, Hq, D, splits))
+
+
+def qmm_decode_attention(q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, lens: torch.Tensor,
+                         O: torch.Tensor, scale: float = 0.0, splits_req: int = 0,
+                         workspace: torch.Tensor | None = None, stream=None) -> int:
+    """O = split-KV decode attention (see qmm.h); returns the split used.
+    q [B, Hq, D], K/V [B, Hkv, Lmax, D] bf16, lens int32 [B] (device), O [B, Hq, D] bf16."""
+    B, Hq, D = q.shape
+    _, Hkv, Lmax, _ = K.shape
+    if tuple(K.shape) != (B, Hkv, Lmax, D) or tuple(V.shape) != tuple(K.shape) or \
+            tuple(O.shape) != (B, Hq, D) or tuple(lens.shape) != (B,):
+        raise ValueError("qmm_decode_attention: inconsistent shapes")
+    used = _I(0)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr = _dev(workspace, (workspace.dtype,), "workspace")
+        ws_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().qmm_decode_attention(_dev(q, _BF16, "q"), _dev(K, _BF16, "K"),
+                                      _dev(V, _BF16, "V"), _dev(lens, (torch.int32,), "lens"),
+                                      _dev(O, _BF16, "O"), B, Hq, Hkv, Lmax, D, float(scale),
+                                      splits_req, ws_ptr, ws_bytes, _stream(stream),
+                                      ctypes.byref(used)), "qmm_decode_attention")
+    return used.value
+
+
+def attention_to_device(problem: dict, device="cuda") -> dict:
+    """Upload an inputs.make_attention problem: q, K, V as bf16, lens as int32."""
+    def bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16) \
+            .to(device)
+    return {"q": bf16(problem["q"]), "K": bf16(problem["K"]), "V": bf16(problem["V"]),
+            "lens": torch.from_numpy(problem["lens"]).to(device)}

@@ -253,6 +253,42 @@ def test_grouped_argument_errors_before_any_cuda_work():
     assert lib.qmm_group_workspace_bytes(two, 2, 0) == 0
 
 
+def test_attention_splits_bit_exact_against_oracle():
+    rng = np.random.default_rng(27)
+    for _ in range(5000):
+        B, Hkv = int(rng.integers(1, 65)), int(rng.choice([1, 2, 4, 8, 16]))
+        qg = int(rng.choice([1, 2, 4, 8]))
+        Lmax, sms = int(rng.integers(1, 40000)), int(rng.integers(1, 200))
+        got = Q.qmm_decode_attention_splits(B, Hkv * qg, Hkv, Lmax, sms)
+        want = oracle.attention_splits(B, Hkv, Lmax, sms, 4, 512)
+        assert got == want
+    # the workload: 32 sequences x 8 KV heads on 152 SMs, 4 blocks per SM
+    assert Q.qmm_decode_attention_splits(32, 32, 8, 8192, 152) == 3
+    assert Q.qmm_decode_attention_workspace_bytes(32, 32, 128, 2) == 32 * 32 * 2 * 130 * 4
+    assert Q.qmm_decode_attention_workspace_bytes(32, 32, 128, 1) == 0
+
+
+def test_attention_argument_errors_before_any_cuda_work():
+    lib = Q.lib()
+    P = ctypes.c_void_p
+    q, k, v, ln, o = P(0x10000), P(0x20000), P(0x30000), P(0x40000), P(0x50000)
+    run = lambda *a: lib.qmm_decode_attention(*a)
+    ok = (q, k, v, ln, o, 2, 32, 8, 100, 128, 0.0, 0, None, 0, None, None)
+    bad = lambda i, x: tuple(x if j == i else a for j, a in enumerate(ok))
+    assert run(*bad(0, None)) == Q.QMM_EINVAL
+    assert run(*bad(3, None)) == Q.QMM_EINVAL
+    assert run(*bad(5, 0)) == Q.QMM_EINVAL
+    assert run(*bad(6, 30)) == Q.QMM_EINVAL          # Hq not a multiple of Hkv
+    assert run(*bad(9, 96)) == Q.QMM_ESHAPE          # D
+    assert run(*bad(6, 48)) == Q.QMM_ESHAPE          # 6 query heads per KV head
+    assert run(*bad(11, -1)) == Q.QMM_EINVAL
+    assert run(*bad(0, P(0x10008))) == Q.QMM_EALIGN
+    assert run(*bad(3, P(0x40002))) == Q.QMM_EALIGN
+    s = ctypes.c_int()
+    assert lib.qmm_decode_attention_splits(0, 32, 8, 100, 152, ctypes.byref(s)) == Q.QMM_EINVAL
+    assert lib.qmm_decode_attention_splits(1, 30, 8, 100, 152, ctypes.byref(s)) == Q.QMM_EINVAL
+
+
 def test_fused_reduce_workspace_holds_the_counters():
     from split_w4a16_quantized_gb300 import qmm as Q
     prev_k = Q.qmm_set_kernels(Q.QMM_KERNELS_TCGEN05)

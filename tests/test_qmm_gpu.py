@@ -915,3 +915,103 @@ def test_grouped_argument_errors():
     c1 = Q.group_calls([d for _, d in big])
     assert Q.qmm_group_workspace_bytes(c1) == 0
     assert Q.qmm_w4a16_g128_grouped(c1, None) == [1]
+
+
+# ---- split-KV decode attention (qmm_decode_attention) ------------------------
+#
+# Tolerance, per element: |O_gpu - O64| <= 2^-8 |O64| + 1e-4.  The GPU forms
+# scores, weights and sums in FP32 (relative error ~1e-6 here) and rounds O
+# to BF16 once (2^-9 relative); 1e-4 covers the FP32 sums of up to ~10^4
+# weighted rows for the small |O| of long, flat softmaxes.
+
+def _attention(prob, splits_req=0, scale=0.0):
+    d = Q.attention_to_device(prob)
+    B, Hq, D = prob["q"].shape
+    O = torch.full((B, Hq, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    S = splits_req or Q.qmm_decode_attention_splits(B, Hq, prob["K"].shape[1], prob["K"].shape[2])
+    nb = Q.qmm_decode_attention_workspace_bytes(B, Hq, D, S)
+    ws = torch.full((max(nb, 16) // 4,), float("nan"), dtype=torch.float32, device="cuda")
+    used = Q.qmm_decode_attention(d["q"], d["K"], d["V"], d["lens"], O, scale, splits_req,
+                                  ws if nb else None)
+    torch.cuda.synchronize()
+    assert used == S
+    assert Q.qmm_kernel_status(clear=True) == 0
+    return _bits(O).reshape(B, Hq, D), used
+
+
+def _assert_attention(got_bits, O64, what=""):
+    got = _val(got_bits)
+    assert np.all(np.isfinite(got)), "non-finite output " + what
+    lim = 2.0 ** -8 * np.abs(O64) + 1e-4
+    err = np.abs(got - O64)
+    bad = np.argwhere(err > lim)
+    assert bad.size == 0, "%s: %d elements out of tolerance, first %s err %g lim %g" % (
+        what, len(bad), bad[0], err[tuple(bad[0])], lim[tuple(bad[0])])
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Lmax,D", [(1, 1, 1, 1, 64), (2, 4, 2, 100, 128),
+                                             (3, 32, 8, 777, 128), (4, 8, 1, 64, 64),
+                                             (2, 16, 8, 2049, 128), (5, 8, 4, 300, 64)])
+def test_attention_splits_against_oracle(B, Hq, Hkv, Lmax, D):
+    """Split factors 1, 2, 4, 8, a non-power-of-two one and the plan's, on
+    ragged lengths, against the fp64 definition."""
+    prob = inputs.make_attention(B, Hq, Hkv, Lmax, D, seed=300 + Lmax)
+    O64 = oracle.decode_attention(prob["q"], prob["K"], prob["V"], prob["lens"])
+    for S in (0, 1, 2, 3, 4, 7, 8):
+        got, used = _attention(prob, S)
+        _assert_attention(got, O64, "S=%d (used %d)" % (S, used))
+
+
+def test_attention_edge_lengths_and_scale():
+    # single positions, full length, a length just past a tile, empty splits
+    B, Hq, Hkv, Lmax, D = 6, 8, 2, 200, 128
+    prob = inputs.make_attention(B, Hq, Hkv, Lmax, D, seed=310,
+                                 lens=[1, 200, 65, 64, 63, 129])
+    for scale in (0.0, 0.05):
+        O64 = oracle.decode_attention(prob["q"], prob["K"], prob["V"], prob["lens"],
+                                      scale=scale or None)
+        for S in (1, 2, 5, 16):  # 16 splits of 200 positions: most are empty
+            got, _ = _attention(prob, S, scale)
+            _assert_attention(got, O64, "scale=%g S=%d" % (scale, S))
+
+
+def test_attention_dominant_key_and_uniform_keys():
+    # closed forms through the GPU path: a dominant key returns its V row,
+    # equal keys return the mean of the valid V rows
+    B, Hq, Hkv, Lmax, D = 2, 4, 4, 300, 128
+    prob = inputs.make_attention(B, Hq, Hkv, Lmax, D, seed=320, lens=[300, 150])
+    prob["K"][:] = prob["K"][:, :, :1, :]
+    O64 = oracle.decode_attention(prob["q"], prob["K"], prob["V"], prob["lens"])
+    Vf = _val(prob["V"])
+    for b, L in enumerate(prob["lens"]):
+        assert np.allclose(O64[b], Vf[b, :, :L].mean(axis=1), atol=1e-12)
+    for S in (1, 3):
+        got, _ = _attention(prob, S)
+        _assert_attention(got, O64, "uniform S=%d" % S)
+
+
+def test_attention_workload_full_size():
+    """The bench workload: Qwen3-4B heads (32 query, 8 KV, dim 128), 32
+    sequences with lengths mixed in [1024, 8192], the plan's split."""
+    h = inputs.ATTENTION_HEADS
+    prob = inputs.make_attention(32, h["Hq"], h["Hkv"], 8192, h["D"], seed=0, lmin=1024)
+    O64 = oracle.decode_attention(prob["q"], prob["K"], prob["V"], prob["lens"])
+    got, used = _attention(prob, 0)
+    assert used == Q.qmm_decode_attention_splits(32, 32, 8, 8192)
+    _assert_attention(got, O64, "workload S=%d" % used)
+    again, _ = _attention(prob, 0)
+    assert np.array_equal(got, again), "not deterministic"
+
+
+def test_attention_errors_on_device():
+    prob = inputs.make_attention(2, 8, 2, 100, 128, seed=330)
+    d = Q.attention_to_device(prob)
+    O = torch.empty((2, 8, 128), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(Q.QmmError) as e:
+        Q.qmm_decode_attention(d["q"], d["K"], d["V"], d["lens"], O, splits_req=4)
+    assert e.value.code == Q.QMM_EWORKSPACE
+    small = torch.empty(64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(Q.QmmError) as e:
+        Q.qmm_decode_attention(d["q"], d["K"], d["V"], d["lens"], O, splits_req=4,
+                               workspace=small)
+    assert e.value.code == Q.QMM_EWORKSPACE
