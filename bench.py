@@ -76,19 +76,24 @@ def partition_algorithmic(M, Kred, Nout, split, partial_bytes=2):
 NCU_TRAFFIC = {
     # python bench.py --only down:128 --launch-list --steps 1 --warmup 3 under
     # ncu --set full -k regex:w4a16_tc -s 2 -c 1: dram__bytes_read.sum + _write.sum
-    ("down", 128, 4): (15788544, "4226552ed820491b"),
+    ("down", 128, 4): (15788288, "c9ba71336c950b3c"),
     # the same with --partitions near-equal (split 7)
-    ("down", 128, 7): (15788288, "4226552ed820491b"),
+    ("down", 128, 7): (15788544, "c9ba71336c950b3c"),
     # the same for --only gate:32
-    ("gate", 32, 2): (13462016, "4226552ed820491b"),
+    ("gate", 32, 2): (13462016, "c9ba71336c950b3c"),
 }
 TC_SOURCES = ("qmm_w4a16_tc.cu", "qmm_sm100.cuh", "qmm_device.cuh", "qmm_internal.h")
+# The same for the decode-attention split kernel at the workload's planned
+# split (python bench.py --attention-only --steps 2 --warmup 3 under
+# ncu --set full -k regex:attn_split -s 3 -c 1), keyed by the split.
+ATTN_TRAFFIC = {3: (670844928, "a33acebd2b95854e")}
+ATTN_SOURCES = ("qmm_attention.cu", "qmm_sm100.cuh", "qmm_device.cuh", "qmm_internal.h")
 
 
-def tc_source_hash():
+def tc_source_hash(sources=TC_SOURCES):
     import hashlib
     h = hashlib.sha256()
-    for name in TC_SOURCES:
+    for name in sources:
         with open(os.path.join(ROOT, "split_w4a16_quantized_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -579,6 +584,10 @@ def attention_bench(Q, device, stream, peaks, l2):
     best = min(out["splits"], key=lambda r: r["us"])
     out["plan"] = next(r for r in out["splits"] if r["split"] == plan)
     out["best"] = best
+    # ncu DRAM bytes of one launch of the split kernel at the plan's split,
+    # while the kernel's sources are the ones captured (else null)
+    tr = ATTN_TRAFFIC.get(plan)
+    out["plan"]["traffic"] = tr[0] if tr and tr[1] == tc_source_hash(ATTN_SOURCES) else None
     return out
 
 
