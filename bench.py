@@ -484,6 +484,7 @@ def run_gpu(args, rank, world, local_rank):
                 Q.qmm_set_partitions(rule)
         del cps
     prefill = prefill_sweep(Q, device, stream, l2, peaks) if rank == 0 else None
+    sweep = shape_sweep(Q, device, stream, l2, peaks) if rank == 0 else None
     Q.qmm_set_weights_static(static_weights)
     sample = clocks.stop()
     dense = dense_sweep(Q, device, stream, sms, l2) if rank == 0 else None
@@ -496,7 +497,7 @@ def run_gpu(args, rank, world, local_rank):
             "clocks": sample, "wl": wl,
             "peaks": peaks,
             "peak_src": peak_src, "l2": l2, "sms": sms, "dense": dense, "e2e": e2e,
-            "prefill": prefill, "overlap": overlap, "attention": attention}
+            "prefill": prefill, "sweep": sweep, "overlap": overlap, "attention": attention}
 
 
 def prefill_sweep(Q, device, stream, l2, peaks):
@@ -527,6 +528,62 @@ def prefill_sweep(Q, device, stream, l2, peaks):
                     "frac_of_bf16_peak": round(fl / us / 1e6 / peaks["bf16_tflops"], 3)})
         del cps, d
     return out
+
+
+def shape_sweep(Q, device, stream, l2, peaks):
+    """The policy's split against its control on every shape of the workload
+    configs that the 14-call step does not hold:
+    - the M = 16 K-projection (the small case);
+    - M in {16, 64} on the seven projections;
+    - the ragged shape (Kred 2560, Nout 1000) at M in {16, 32, 64, 128, 2048};
+    - M = 2048 on the seven projections;
+    - the decode regime, M in {1, 4, 8} on k, o and down (the policy then keeps
+      at least 512 reduction elements per partition).
+    The control is the unsplit kernel where the policy splits.  Where the
+    policy keeps the unsplit kernel because the base grid fills the GPU, the
+    control is a forced split of 2, so the row shows whether not splitting was
+    the faster choice.  Each side is a graph of back-to-back calls over input
+    copies larger than L2, without the static-weights early start."""
+    shapes = []
+    for M in (16, 64, 2048):
+        shapes += [(name, M) for name in PROJ]
+    shapes += [("ragged", M) for M in (16, 32, 64, 128, 2048)]
+    shapes += [(name, M) for M in (1, 4, 8) for name in ("k", "o", "down")]
+    rows = []
+    for name, M in shapes:
+        Kred, Nout = inputs.RAGGED if name == "ragged" else inputs.PROJECTIONS[name]
+        d = Q.to_device(inputs.make_w4a16(M, Kred, Nout, seed=0), device)
+        pol = Q.qmm_policy_preset(Q.QMM_PRESET_GB300, M)
+        split = Q.qmm_splitk_plan(M, Kred, Nout, pol)
+        control = 1 if split > 1 else 2
+        ws = torch.empty(max(16, Q.qmm_splitk_workspace_bytes(M, Nout, max(split, control),
+                                                               Q.QMM_PARTIAL_BF16)),
+                         dtype=torch.uint8, device=device)
+        cps = cold_copies(d, l2)
+        C = torch.empty((M, Nout), dtype=torch.bfloat16, device=device)
+
+        def call(j, split_req):
+            c = cps[j]
+            Q.qmm_w4a16_g128(c["A"], c["Wq"], c["scales"], c["biases"], C,
+                             split_req=split_req, workspace=ws)
+        us = graph_us_per_launch(lambda j: call(j, 0), len(cps), stream)
+        us_c = graph_us_per_launch(lambda j: call(j, control), len(cps), stream)
+        nb, fl = algorithmic(M, Kred, Nout, split)
+        t_roof, bound = roofline_time_s(nb, fl, peaks)
+        bm, bn = Q.qmm_kernel_tile(M)
+        rows.append({"proj": name, "M": M, "Kred": Kred, "Nout": Nout, "split": split,
+                     "base_ctas": -(-M // bm) * -(-Nout // bn), "us": round(us, 3),
+                     "control_split": control, "control_us": round(us_c, 3),
+                     "speedup_vs_control": round(us_c / us, 3), "bound": bound,
+                     "roofline_frac": round(t_roof * 1e6 / us, 4)})
+        del cps, d, ws
+    split_rows = [r for r in rows if r["split"] > 1]
+    kept = [r for r in rows if r["split"] == 1]
+    summary = {"shapes": len(rows), "policy_splits": len(split_rows),
+               "split_beats_unsplit": sum(r["us"] < r["control_us"] for r in split_rows),
+               "policy_unsplit": len(kept),
+               "unsplit_beats_split_2": sum(r["us"] < r["control_us"] for r in kept)}
+    return {"summary": summary, "rows": rows}
 
 
 def dense_sweep(Q, device, stream, sms, l2):
@@ -1007,6 +1064,7 @@ def main():
            "gpu_launches": args.steps * wl.launches_per_step(),
            "clocks": res["clocks"], "e2e": res["e2e"], "per_call": res["per_call"],
            "dense_splitk_512x512x16384": res["dense"], "prefill_M2048": res["prefill"],
+           "split_vs_control": res["sweep"],
            "overlap_stream": res["overlap"], "decode_attention": res["attention"]}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(wl.host)
