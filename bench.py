@@ -76,11 +76,11 @@ def partition_algorithmic(M, Kred, Nout, split, partial_bytes=2):
 NCU_TRAFFIC = {
     # python bench.py --only down:128 --launch-list --steps 1 --warmup 3 under
     # ncu --set full -k regex:w4a16_tc -s 2 -c 1: dram__bytes_read.sum + _write.sum
-    ("down", 128, 4): (15788288, "c9ba71336c950b3c"),
+    ("down", 128, 4): (15788544, "5c9ab83fbb61e35e"),
     # the same with --partitions near-equal (split 7)
-    ("down", 128, 7): (15788544, "c9ba71336c950b3c"),
+    ("down", 128, 7): (15788288, "5c9ab83fbb61e35e"),
     # the same for --only gate:32
-    ("gate", 32, 2): (13462016, "c9ba71336c950b3c"),
+    ("gate", 32, 2): (13462016, "5c9ab83fbb61e35e"),
 }
 TC_SOURCES = ("qmm_w4a16_tc.cu", "qmm_sm100.cuh", "qmm_device.cuh", "qmm_internal.h")
 # The same for the decode-attention split kernel at the workload's planned
@@ -392,25 +392,33 @@ def run_gpu(args, rank, world, local_rank):
                                    for i in range(len(wl.calls))]) for r in range(wl.R)]
     gws = torch.zeros(max(Q.qmm_group_workspace_bytes(group_arrays[0]), 16), dtype=torch.uint8,
                       device=device)
-    gs = []
-    with torch.cuda.stream(cap):
-        for r in range(wl.R):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=cap):
-                Q.qmm_w4a16_g128_grouped(group_arrays[r], gws)
-            gs.append(g)
-    torch.cuda.synchronize()
-    for k in range(args.warmup):
-        gs[k % wl.R].replay()
-    t0.record(stream)
-    for k in range(args.steps):
-        gs[k % wl.R].replay()
-    t1.record(stream)
-    torch.cuda.synchronize()
-    ms_grouped = t0.elapsed_time(t1)
+
+    def time_grouped():
+        gs = []
+        with torch.cuda.stream(cap):
+            for r in range(wl.R):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=cap):
+                    Q.qmm_w4a16_g128_grouped(group_arrays[r], gws)
+                gs.append(g)
+        torch.cuda.synchronize()
+        for k in range(args.warmup):
+            gs[k % wl.R].replay()
+        t0.record(stream)
+        for k in range(args.steps):
+            gs[k % wl.R].replay()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        del gs
+        return t0.elapsed_time(t1)
+    ms_grouped = time_grouped()
+    # the same grouped step under the persistent schedule (one CTA per SM
+    # walking the tiles of each partition launch)
+    prev_sched = Q.qmm_set_grouped_schedule(Q.QMM_GROUPED_PERSISTENT)
+    ms_grouped_persistent = time_grouped()
+    Q.qmm_set_grouped_schedule(prev_sched)
     tile_widths = len({Q.qmm_kernel_tile(M)[0] for (_, M, _, _) in wl.calls})
     grouped_launches = tile_widths + (1 if any(s > 1 for s in wl.split) else 0)
-    del gs
 
     # per call: policy split vs the unsplit control, each timed as a graph of
     # back-to-back launches over copies of its inputs larger than L2.  These and
@@ -492,7 +500,8 @@ def run_gpu(args, rank, world, local_rank):
     overlap = overlap_sweep(wl, Q, device) if rank == 0 else None
     attention = attention_bench(Q, device, stream, peaks, l2) if rank == 0 else None
     return {"ms": ms, "ms_nopdl": ms_nopdl, "ms_wflip": ms_wflip, "ms_fused": ms_fused,
-            "ms_alt": ms_alt, "ms_grouped": ms_grouped, "grouped_launches": grouped_launches,
+            "ms_alt": ms_alt, "ms_grouped": ms_grouped,
+            "ms_grouped_persistent": ms_grouped_persistent, "grouped_launches": grouped_launches,
             "per_call": per_call, "dom": dom,
             "clocks": sample, "wl": wl,
             "peaks": peaks,
@@ -1059,6 +1068,8 @@ def main():
            ("value_near_equal" if args.partitions == "equal" else "value_equal_partitions"):
                round(job_value_us(res["ms_alt"], 1, args.steps, ncalls), 4),
            "value_grouped": round(job_value_us(res["ms_grouped"], 1, args.steps, ncalls), 4),
+           "value_grouped_persistent": round(job_value_us(res["ms_grouped_persistent"], 1,
+                                                          args.steps, ncalls), 4),
            "grouped_launches_per_step": res["grouped_launches"],
            "roofline": roof, "roofline_other_partitions": roof_alt,
            "gpu_launches": args.steps * wl.launches_per_step(),

@@ -207,6 +207,15 @@ int qmm_dequant_probe(const uint32_t *Wq, const void *scales, const void *biases
  * QMM_ESHAPE (nothing fits the limit). */
 int qmm_tc_pipeline_config(int bm, int gpp, int smem_limit, int *out);
 
+/* The same for the persistent grouped launch (QMM_GROUPED_PERSISTENT), whose
+ * rings keep two activation stages and give the rest of shared memory to
+ * weight stages; gpp is the longest partition of the launch's calls and
+ * smem_limit the opt-in maximum minus that kernel's static shared memory
+ * (its call table: 231408 on GB300).  Same outputs and return codes.  The
+ * tiny-llm chapter has no counterpart: this call exists so tests can check
+ * the persistent pipeline's synchronization on its real configurations. */
+int qmm_tc_persistent_pipeline_config(int bm, int gpp, int smem_limit, int *out);
+
 /* Kernel families used by qmm_w4a16_g128 (process-wide, thread-safe):
  *   QMM_KERNELS_DEFAULT   the tuned table: per M, the family measured fastest
  *   QMM_KERNELS_MMA_SYNC  register-dequant mma.sync kernels for every M
@@ -367,6 +376,22 @@ size_t qmm_group_workspace_bytes(const qmm_group_call *calls, int n, int partial
  * checked before anything is launched. */
 int qmm_w4a16_g128_grouped(const qmm_group_call *calls, int n, void *workspace, size_t ws_bytes,
                            int partial_dtype, void *stream, int *splits_used);
+
+/* Schedule of the grouped call's tcgen05 partition launches (process-wide,
+ * thread-safe):
+ *   QMM_GROUPED_TILES (default)  one CTA per output tile and partition.
+ *   QMM_GROUPED_PERSISTENT  for the launches of tiles up to 64 activation
+ *       rows (calls with M <= 64): min(tiles, SMs) CTAs, each walking a list
+ *       of the launch's tiles (gpu-kernels-explained, "Split-K, streams and
+ *       overlap": a persistent schedule keeps every SM busy rather than
+ *       launching one block per tile).  The tiles stay whole.  Each CTA pays
+ *       its prologue once, and its copies of the next tile's weights and
+ *       activations run while the current tile drains.  Wider tiles keep one
+ *       CTA per tile, which measured faster for them.  Each C is bitwise the
+ *       C of QMM_GROUPED_TILES.
+ * Returns the previous schedule, or QMM_EINVAL for an unknown value. */
+enum { QMM_GROUPED_TILES = 0, QMM_GROUPED_PERSISTENT = 1 };
+int qmm_set_grouped_schedule(int mode);
 
 /* ---- split-KV decode attention -------------------------------------------
  *

@@ -67,6 +67,7 @@ std::atomic<int> g_pdl{1};
 std::atomic<int> g_wstatic{0};
 std::atomic<int> g_reduce{QMM_REDUCE_KERNEL};
 std::atomic<int> g_partitions{QMM_PARTITIONS_EQUAL};
+std::atomic<int> g_grouped{QMM_GROUPED_TILES};
 
 // a split the current partition rule accepts for G groups (grid z <= 65535)
 bool split_fits(int64_t G, int64_t split) {
@@ -111,6 +112,10 @@ bool reduce_fused() { return g_reduce.load(std::memory_order_relaxed) == QMM_RED
 
 bool partitions_near_equal() {
     return g_partitions.load(std::memory_order_relaxed) == QMM_PARTITIONS_NEAR_EQUAL;
+}
+
+bool grouped_persistent() {
+    return g_grouped.load(std::memory_order_relaxed) == QMM_GROUPED_PERSISTENT;
 }
 
 int choose_split(int M, int Kred, int Nout, int split_req, const qmm_policy* pol, int* split) {
@@ -177,6 +182,11 @@ int qmm_set_reduce(int mode) {
 int qmm_set_partitions(int mode) {
     if (mode != QMM_PARTITIONS_EQUAL && mode != QMM_PARTITIONS_NEAR_EQUAL) return QMM_EINVAL;
     return g_partitions.exchange(mode);
+}
+
+int qmm_set_grouped_schedule(int mode) {
+    if (mode != QMM_GROUPED_TILES && mode != QMM_GROUPED_PERSISTENT) return QMM_EINVAL;
+    return g_grouped.exchange(mode);
 }
 
 int qmm_kernel_status(int* status, int clear) {
@@ -565,16 +575,24 @@ int qmm_decode_attention(const void* q, const void* K, const void* V, const int*
     return rc;
 }
 
-int qmm_tc_pipeline_config(int bm, int gpp, int smem_limit, int* out) {
+static int pipeline_config(int bm, int gpp, int smem_limit, int* out, bool persistent) {
     if (!out || gpp < 1 || smem_limit < 1) return QMM_EINVAL;
     qmm::TcPipeline pl;
-    const int rc = qmm::tc_pipeline_config(bm, gpp, smem_limit, &pl);
+    const int rc = qmm::tc_pipeline_config(bm, gpp, smem_limit, &pl, persistent);
     if (rc < 0) return QMM_EINVAL;
     if (rc > 0) return QMM_ESHAPE;
     const int v[9] = {pl.nacc, pl.dsets, pl.a_stages, pl.wgps, pl.agps, pl.act_stages,
                       pl.w_stages, pl.threads, static_cast<int>(pl.smem)};
     for (int i = 0; i < 9; ++i) out[i] = v[i];
     return QMM_OK;
+}
+
+int qmm_tc_pipeline_config(int bm, int gpp, int smem_limit, int* out) {
+    return pipeline_config(bm, gpp, smem_limit, out, false);
+}
+
+int qmm_tc_persistent_pipeline_config(int bm, int gpp, int smem_limit, int* out) {
+    return pipeline_config(bm, gpp, smem_limit, out, true);
 }
 
 int qmm_unpack_probe(const uint32_t* Wq, int Nout, int Kred, uint8_t* q, void* stream) {

@@ -69,6 +69,8 @@ bool weights_static();
 bool reduce_fused();
 // Near-equal partitions for splits that do not divide the groups (qmm_set_partitions).
 bool partitions_near_equal();
+// Persistent schedule of the grouped call's tcgen05 launches (qmm_set_grouped_schedule).
+bool grouped_persistent();
 // The split a matmul call dispatches: the policy's (split_req 0, pol NULL =
 // the GB300 preset) under the current partition rule, or the forced split if
 // that rule accepts it (QMM_ESHAPE otherwise).  Shape and policy checked by
@@ -139,7 +141,8 @@ struct TcPipeline {
     size_t smem;
 };
 // 0 = ok, 1 = does not fit the shared-memory limit, -1 = bad arguments.
-int tc_pipeline_config(int bm, int gpp, long smem_limit, TcPipeline* out);
+// persistent: the ring shape of the persistent grouped launch (two activation stages).
+int tc_pipeline_config(int bm, int gpp, long smem_limit, TcPipeline* out, bool persistent = false);
 int launch_reduce(const void* partials, int partial_dtype, int split, int M, int Nout, void* C,
                   void* stream);
 int launch_gemm_tc(const void* A, const void* W, void* out, int out_mode, int M, int N, int K,

@@ -83,11 +83,13 @@ _SIGS = {
     "qmm_set_weights_static": (_I, [_I]),
     "qmm_set_reduce": (_I, [_I]),
     "qmm_set_partitions": (_I, [_I]),
+    "qmm_set_grouped_schedule": (_I, [_I]),
     "qmm_kernel_status": (_I, [ctypes.POINTER(_I), _I]),
     "qmm_w4a16_g128_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I,
                                     ctypes.POINTER(qmm_policy), _I, _P, ctypes.POINTER(_I)]),
     "qmm_static_scratch_bytes": (_SZ, []),
     "qmm_tc_pipeline_config": (_I, [_I, _I, _I, ctypes.POINTER(_I)]),
+    "qmm_tc_persistent_pipeline_config": (_I, [_I, _I, _I, ctypes.POINTER(_I)]),
     "qmm_decode_attention_splits": (_I, [_I, _I, _I, _I, _I, ctypes.POINTER(_I)]),
     "qmm_decode_attention_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "qmm_decode_attention": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, ctypes.c_float, _I,
@@ -196,6 +198,18 @@ def qmm_set_partitions(mode: int) -> int:
     return prev
 
 
+QMM_GROUPED_TILES, QMM_GROUPED_PERSISTENT = 0, 1
+
+
+def qmm_set_grouped_schedule(mode: int) -> int:
+    """Schedule of the grouped call's tcgen05 launches (QMM_GROUPED_*);
+    returns the previous one."""
+    prev = lib().qmm_set_grouped_schedule(mode)
+    if prev < 0:
+        raise QmmError(prev, "qmm_set_grouped_schedule")
+    return prev
+
+
 def qmm_set_weights_static(enable: bool) -> int:
     """Promise that no earlier kernel on the stream writes the weights (see qmm.h)."""
     return int(lib().qmm_set_weights_static(1 if enable else 0))
@@ -295,6 +309,14 @@ def qmm_tc_pipeline_config(bm: int, gpp: int, smem_limit: int = 232432) -> dict:
     """The tcgen05 kernel's pipeline shape for a tile and partition (host only)."""
     out = (_I * 9)()
     _check(lib().qmm_tc_pipeline_config(bm, gpp, smem_limit, out), "qmm_tc_pipeline_config")
+    return dict(zip(TC_PIPELINE_FIELDS, list(out)))
+
+
+def qmm_tc_persistent_pipeline_config(bm: int, gpp: int, smem_limit: int = 231408) -> dict:
+    """The persistent grouped launch's pipeline shape (host only)."""
+    out = (_I * 9)()
+    _check(lib().qmm_tc_persistent_pipeline_config(bm, gpp, smem_limit, out),
+           "qmm_tc_persistent_pipeline_config")
     return dict(zip(TC_PIPELINE_FIELDS, list(out)))
 
 

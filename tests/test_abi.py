@@ -306,3 +306,15 @@ def test_fused_reduce_workspace_holds_the_counters():
     finally:
         Q.qmm_set_reduce(prev)
         Q.qmm_set_kernels(prev_k)
+
+
+def test_grouped_schedule_setting():
+    from split_w4a16_quantized_gb300 import qmm as Q
+    prev = Q.qmm_set_grouped_schedule(Q.QMM_GROUPED_PERSISTENT)
+    try:
+        assert Q.qmm_set_grouped_schedule(Q.QMM_GROUPED_TILES) == Q.QMM_GROUPED_PERSISTENT
+        assert Q.qmm_set_grouped_schedule(Q.QMM_GROUPED_TILES) == Q.QMM_GROUPED_TILES
+        with pytest.raises(Q.QmmError):
+            Q.qmm_set_grouped_schedule(2)
+    finally:
+        Q.qmm_set_grouped_schedule(prev)

@@ -852,9 +852,19 @@ GROUP_SHAPES = [(n, M) for M in (32, 128) for n in inputs.PROJECTIONS] + \
     [("ragged", 33), ("odd", 5), ("k", 16), ("down", 300), ("q", 8), ("ragged", 1)]
 
 
+@pytest.fixture(params=["tiles", "persistent"])
+def grouped_schedule(request):
+    """Both schedules of the grouped call's partition launches: one CTA per
+    tile, or one CTA per SM walking the tiles (qmm_set_grouped_schedule)."""
+    prev = Q.qmm_set_grouped_schedule(Q.QMM_GROUPED_PERSISTENT if request.param == "persistent"
+                                      else Q.QMM_GROUPED_TILES)
+    yield request.param
+    Q.qmm_set_grouped_schedule(prev)
+
+
 @pytest.mark.parametrize("rule", ["equal", "near-equal"])
 @pytest.mark.parametrize("dt", [Q.QMM_PARTIAL_BF16, Q.QMM_PARTIAL_F32])
-def test_grouped_equals_the_calls(family, rule, dt):
+def test_grouped_equals_the_calls(family, grouped_schedule, rule, dt):
     """Each C of the grouped call is bitwise its own call's C: the same CTA
     body, ring depth aside, and the same ordered FP32 reduce."""
     prev = Q.qmm_set_partitions(Q.QMM_PARTITIONS_NEAR_EQUAL if rule == "near-equal"
@@ -872,7 +882,7 @@ def test_grouped_equals_the_calls(family, rule, dt):
     _check_sampled(p, _bits(d["C"]), used[13], dt, rows, cols, "grouped down M=128")
 
 
-def test_grouped_more_calls_than_one_launch_holds():
+def test_grouped_more_calls_than_one_launch_holds(grouped_schedule):
     # 20 calls of one tile width: two partition launches and two reduce launches
     shapes = [("k", 32), ("v", 32), ("q", 32), ("odd", 20), ("ragged", 31)] * 4
     probs = _group_problems(shapes, 230)
@@ -880,7 +890,7 @@ def test_grouped_more_calls_than_one_launch_holds():
 
 
 @pytest.mark.parametrize("pdl", [True, False])
-def test_grouped_with_static_weights(pdl):
+def test_grouped_with_static_weights(grouped_schedule, pdl):
     prev_w, prev_p = Q.qmm_set_weights_static(True), Q.qmm_set_pdl(pdl)
     try:
         probs = _group_problems(GROUP_SHAPES, 260)
@@ -897,6 +907,25 @@ def test_grouped_with_static_weights(pdl):
     finally:
         Q.qmm_set_weights_static(prev_w)
         Q.qmm_set_pdl(prev_p)
+
+
+@pytest.mark.parametrize("shapes", [
+    [("k", 32)],                                    # fewer tiles than SMs: one each
+    [("odd", 3), ("odd", 40), ("ragged", 1), ("k", 8), ("odd", 129)] * 3,
+    [("down", 128), ("odd", 7), ("gate", 32), ("ragged", 64)],
+    [("q", 48), ("down", 40), ("odd", 64), ("k", 33), ("o", 60)],  # 64-row tiles
+])
+def test_persistent_grouped_tile_lists(shapes):
+    """The persistent schedule on short and mixed tile lists: partitions of
+    one or two groups (phantom positions in every stage), ragged rows and
+    columns, more and fewer tiles than SMs; each C bitwise its own call's."""
+    prev = Q.qmm_set_grouped_schedule(Q.QMM_GROUPED_PERSISTENT)
+    try:
+        probs = _group_problems(shapes, 310)
+        _grouped_vs_calls(probs)
+        _grouped_vs_calls(probs, Q.QMM_PARTIAL_F32)
+    finally:
+        Q.qmm_set_grouped_schedule(prev)
 
 
 def test_grouped_argument_errors():
