@@ -86,7 +86,7 @@ TC_SOURCES = ("qmm_w4a16_tc.cu", "qmm_sm100.cuh", "qmm_device.cuh", "qmm_interna
 # The same for the decode-attention split kernel at the workload's planned
 # split (python bench.py --attention-only --steps 2 --warmup 3 under
 # ncu --set full -k regex:attn_split -s 3 -c 1), keyed by the split.
-ATTN_TRAFFIC = {3: (670844928, "a33acebd2b95854e")}
+ATTN_TRAFFIC = {3: (670740224, "85e5588410bbda9d")}
 ATTN_SOURCES = ("qmm_attention.cu", "qmm_sm100.cuh", "qmm_device.cuh", "qmm_internal.h")
 
 
@@ -319,10 +319,19 @@ def run_gpu(args, rank, world, local_rank):
     peaks, peak_src = load_peaks()
     wl = Workload(device, Q, l2, near_equal)
     stream = torch.cuda.current_stream()
+    step = wl.step
+    if args.grouped:  # profiling aid: the step's calls as one grouped call
+        Q.qmm_set_grouped_schedule(Q.QMM_GROUPED_PERSISTENT if args.grouped == "persistent"
+                                   else Q.QMM_GROUPED_TILES)
+        g_arrays = [Q.group_calls([dict(wl.sets[r][i], C=wl.C[r][i])
+                                   for i in range(len(wl.calls))]) for r in range(wl.R)]
+        g_ws = torch.zeros(max(Q.qmm_group_workspace_bytes(g_arrays[0]), 16), dtype=torch.uint8,
+                           device=device)
+        step = lambda r: Q.qmm_w4a16_g128_grouped(g_arrays[r], g_ws)
 
     # warm-up: eager step per set (first calls set kernel attributes), then graphs
     for r in range(wl.R):
-        wl.step(r)
+        step(r)
     torch.cuda.synchronize()
     graphs = []
     cap = torch.cuda.Stream()
@@ -331,7 +340,7 @@ def run_gpu(args, rank, world, local_rank):
         for r in range(wl.R):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=cap):
-                wl.step(r)
+                step(r)
             graphs.append(g)
     stream.wait_stream(cap)
     torch.cuda.synchronize()
@@ -356,7 +365,11 @@ def run_gpu(args, rank, world, local_rank):
     ms = max_over_ranks(t0.elapsed_time(t1), device)
 
     if args.launch_list:
-        return {"ms": ms, "wl": wl, "launch_list": True}
+        launches = None
+        if args.grouped:
+            widths = len({Q.qmm_kernel_tile(M)[0] for (_, M, _, _) in wl.calls})
+            launches = widths + (1 if any(sp > 1 for sp in wl.split) else 0)
+        return {"ms": ms, "wl": wl, "launch_list": True, "grouped_launches": launches}
 
     def time_variant(setter, value):
         """The step re-captured with one library switch changed, same timing."""
@@ -958,6 +971,9 @@ def main():
                     help="partition rule of the W4A16 calls (qmm_set_partitions)")
     ap.add_argument("--only", default=None, metavar="PROJ:M",
                     help="restrict the step to one call, e.g. gate:128 (profiling aid)")
+    ap.add_argument("--grouped", choices=["tiles", "persistent"], default=None,
+                    help="with --launch-list: time the step's calls as one grouped call "
+                         "under this schedule (profiling aid)")
     ap.add_argument("--attention-only", action="store_true",
                     help="only the decode-attention calls at the plan's split (profiling aid)")
     args = ap.parse_args()
@@ -967,6 +983,8 @@ def main():
         ONLY = (name, int(m))
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.grouped and not args.launch_list:
+        ap.error("--grouped is a profiling aid of --launch-list")
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -986,9 +1004,11 @@ def main():
     value_us = job_value_us(res["ms"], world, args.steps, ncalls)
     if res.get("launch_list"):
         if rank == 0:
+            per_step = res["grouped_launches"] or wl.launches_per_step()
             print(json.dumps({"launch_list": True, "value": value_us, "unit": UNIT,
                               "steps": args.steps, "splits": wl.split,
-                              "gpu_launches": args.steps * wl.launches_per_step()}), flush=True)
+                              "grouped": args.grouped,
+                              "gpu_launches": args.steps * per_step}), flush=True)
         return
 
     dc = res["per_call"][res["dom"]["index"]]
