@@ -67,7 +67,7 @@ std::atomic<int> g_pdl{1};
 std::atomic<int> g_wstatic{0};
 std::atomic<int> g_reduce{QMM_REDUCE_KERNEL};
 std::atomic<int> g_partitions{QMM_PARTITIONS_EQUAL};
-std::atomic<int> g_grouped{QMM_GROUPED_TILES};
+std::atomic<int> g_grouped{QMM_GROUPED_PERSISTENT};
 
 // a split the current partition rule accepts for G groups (grid z <= 65535)
 bool split_fits(int64_t G, int64_t split) {

@@ -202,8 +202,8 @@ QMM_GROUPED_TILES, QMM_GROUPED_PERSISTENT = 0, 1
 
 
 def qmm_set_grouped_schedule(mode: int) -> int:
-    """Schedule of the grouped call's tcgen05 launches (QMM_GROUPED_*);
-    returns the previous one."""
+    """Schedule of the grouped call's tcgen05 launches (QMM_GROUPED_*, the
+    persistent one by default); returns the previous one."""
     prev = lib().qmm_set_grouped_schedule(mode)
     if prev < 0:
         raise QmmError(prev, "qmm_set_grouped_schedule")

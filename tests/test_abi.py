@@ -311,6 +311,7 @@ def test_fused_reduce_workspace_holds_the_counters():
 def test_grouped_schedule_setting():
     from split_w4a16_quantized_gb300 import qmm as Q
     prev = Q.qmm_set_grouped_schedule(Q.QMM_GROUPED_PERSISTENT)
+    assert prev == Q.QMM_GROUPED_PERSISTENT  # the default (no other test leaves it changed)
     try:
         assert Q.qmm_set_grouped_schedule(Q.QMM_GROUPED_TILES) == Q.QMM_GROUPED_PERSISTENT
         assert Q.qmm_set_grouped_schedule(Q.QMM_GROUPED_TILES) == Q.QMM_GROUPED_TILES
