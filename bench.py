@@ -76,17 +76,17 @@ def partition_algorithmic(M, Kred, Nout, split, partial_bytes=2):
 NCU_TRAFFIC = {
     # python bench.py --only down:128 --launch-list --steps 1 --warmup 3 under
     # ncu --set full -k regex:w4a16_tc -s 2 -c 1: dram__bytes_read.sum + _write.sum
-    ("down", 128, 4): (15788544, "5c9ab83fbb61e35e"),
+    ("down", 128, 4): (15788288, "8f0170d4d6878b62"),
     # the same with --partitions near-equal (split 7)
-    ("down", 128, 7): (15788288, "5c9ab83fbb61e35e"),
+    ("down", 128, 7): (15788288, "8f0170d4d6878b62"),
     # the same for --only gate:32
-    ("gate", 32, 2): (13462016, "5c9ab83fbb61e35e"),
+    ("gate", 32, 2): (13461760, "8f0170d4d6878b62"),
 }
 TC_SOURCES = ("qmm_w4a16_tc.cu", "qmm_sm100.cuh", "qmm_device.cuh", "qmm_internal.h")
 # The same for the decode-attention split kernel at the workload's planned
 # split (python bench.py --attention-only --steps 2 --warmup 3 under
 # ncu --set full -k regex:attn_split -s 3 -c 1), keyed by the split.
-ATTN_TRAFFIC = {3: (670740224, "85e5588410bbda9d")}
+ATTN_TRAFFIC = {3: (670811392, "c374070bc2c6bf13")}
 ATTN_SOURCES = ("qmm_attention.cu", "qmm_sm100.cuh", "qmm_device.cuh", "qmm_internal.h")
 
 

@@ -297,6 +297,16 @@ int qmm_set_weights_static(int enable);
  * word.  Returns QMM_OK, QMM_EINVAL, QMM_ENODEV or QMM_ECUDA. */
 int qmm_kernel_status(int *status, int clear);
 
+/* Test hook for the bounded waits above.  The tiny-llm chapter has no
+ * counterpart: this call exists so a test can watch a wait run out on the
+ * GPU.  It launches one CTA on `stream` that waits, with the kernels' own
+ * bounded wait, on an mbarrier that nothing completes.  After the wait limit
+ * (about 1 s) the wait gives up, the status word becomes 1 (as
+ * qmm_kernel_status reports it) and the kernel returns; no trap or fault is
+ * raised and the context stays usable.  Asynchronous like every launch.
+ * Returns QMM_OK, QMM_ENODEV or QMM_ECUDA. */
+int qmm_wait_timeout_probe(void *stream);
+
 /* Static description of a return code. */
 const char *qmm_strerror(int code);
 

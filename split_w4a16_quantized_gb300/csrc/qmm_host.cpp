@@ -184,6 +184,12 @@ int qmm_set_partitions(int mode) {
     return g_partitions.exchange(mode);
 }
 
+int qmm_wait_timeout_probe(void* stream) {
+    int rc = check_device();
+    if (rc != QMM_OK) return rc;
+    return launched(qmm::launch_wait_probe(stream));
+}
+
 int qmm_set_grouped_schedule(int mode) {
     if (mode != QMM_GROUPED_TILES && mode != QMM_GROUPED_PERSISTENT) return QMM_EINVAL;
     return g_grouped.exchange(mode);

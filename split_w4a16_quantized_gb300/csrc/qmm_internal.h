@@ -106,6 +106,9 @@ int launch_w4a16_tc(int bm, const void* A, const uint32_t* Wq, const void* scale
 int read_tc_status(int* out, bool clear);
 // Device address of the status word the tcgen05 and attention kernels share.
 int* tc_status_ptr();
+// One CTA whose bounded wait on a barrier nobody completes runs out
+// (qmm_wait_timeout_probe); returns the launch's cudaError_t.
+int launch_wait_probe(void* stream);
 
 // Split-KV decode attention (qmm_attention.cu): S splits per (sequence, KV
 // head); ws holds the partial states when S > 1 (B*Hq*S*(D+2) floats).

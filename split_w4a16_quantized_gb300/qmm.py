@@ -85,6 +85,7 @@ _SIGS = {
     "qmm_set_partitions": (_I, [_I]),
     "qmm_set_grouped_schedule": (_I, [_I]),
     "qmm_kernel_status": (_I, [ctypes.POINTER(_I), _I]),
+    "qmm_wait_timeout_probe": (_I, [ctypes.c_void_p]),
     "qmm_w4a16_g128_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I,
                                     ctypes.POINTER(qmm_policy), _I, _P, ctypes.POINTER(_I)]),
     "qmm_static_scratch_bytes": (_SZ, []),
@@ -220,6 +221,11 @@ def qmm_kernel_status(clear: bool = True) -> int:
     st = _I(0)
     _check(lib().qmm_kernel_status(ctypes.byref(st), int(clear)), "qmm_kernel_status")
     return st.value
+
+
+def qmm_wait_timeout_probe(stream=None) -> None:
+    """Launch one CTA whose bounded wait runs out (test hook; see qmm.h)."""
+    _check(lib().qmm_wait_timeout_probe(_stream(stream)), "qmm_wait_timeout_probe")
 
 
 def qmm_kernel_tile(M: int):

@@ -12,6 +12,8 @@ Unpacking, dequantized weights, split plans and the reduce are bit-exact.
 """
 import ctypes
 
+import time
+
 import numpy as np
 import pytest
 import torch
@@ -481,6 +483,28 @@ def test_dense_gemm_ragged(family, split):
 
 
 # ---- error codes with real device buffers ----------------------------------
+
+def test_bounded_wait_runs_out_and_reports():
+    """A wait that nothing completes gives up after its limit: the status word
+    reports it, nothing traps, and the context stays usable (a matmul right
+    after is correct)."""
+    assert Q.qmm_kernel_status(clear=True) == 0
+    t0 = time.monotonic()
+    Q.qmm_wait_timeout_probe()
+    torch.cuda.synchronize()
+    took = time.monotonic() - t0
+    assert Q.qmm_kernel_status(clear=True) == 1
+    assert 0.5 < took < 30.0, took
+    assert Q.qmm_kernel_status(clear=True) == 0  # cleared
+    M, (Kred, Nout) = 16, inputs.PROJECTIONS["k"]
+    p = inputs.make_w4a16(M, Kred, Nout, seed=5)
+    d = Q.to_device(p)
+    C, split = Q.w4a16_matmul(d["A"], d["Wq"], d["scales"], d["biases"])
+    torch.cuda.synchronize()
+    assert Q.qmm_kernel_status(clear=True) == 0
+    rows, cols = _sample(M, Nout, np.random.default_rng(3))
+    _check_sampled(p, _bits(C), split, Q.QMM_PARTIAL_BF16, rows, cols, "after a timed-out wait")
+
 
 def test_error_codes_on_device():
     Kred, Nout, M = 2560, 1024, 16
