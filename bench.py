@@ -406,13 +406,13 @@ def run_gpu(args, rank, world, local_rank):
     gws = torch.zeros(max(Q.qmm_group_workspace_bytes(group_arrays[0]), 16), dtype=torch.uint8,
                       device=device)
 
-    def time_grouped():
+    def time_grouped(ws=gws):
         gs = []
         with torch.cuda.stream(cap):
             for r in range(wl.R):
                 g = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(g, stream=cap):
-                    Q.qmm_w4a16_g128_grouped(group_arrays[r], gws)
+                    Q.qmm_w4a16_g128_grouped(group_arrays[r], ws)
                 gs.append(g)
         torch.cuda.synchronize()
         for k in range(args.warmup):
@@ -429,6 +429,14 @@ def run_gpu(args, rank, world, local_rank):
     prev_sched = Q.qmm_set_grouped_schedule(Q.QMM_GROUPED_TILES)
     ms_grouped_tiles = time_grouped()
     Q.qmm_set_grouped_schedule(prev_sched)
+    # and with splits planned for the group (qmm_set_group_plan)
+    prev_plan = Q.qmm_set_group_plan(Q.QMM_GROUP_PLAN_GROUP)
+    plan_ws = torch.zeros(max(Q.qmm_group_workspace_bytes(group_arrays[0]), 16),
+                          dtype=torch.uint8, device=device)
+    ms_grouped_plan = time_grouped(plan_ws)
+    group_plan_splits = Q.qmm_group_plan([(M, Kred, Nout) for (_, M, Kred, Nout) in wl.calls])
+    Q.qmm_set_group_plan(prev_plan)
+    del plan_ws
     tile_widths = len({Q.qmm_kernel_tile(M)[0] for (_, M, _, _) in wl.calls})
     grouped_launches = tile_widths + (1 if any(s > 1 for s in wl.split) else 0)
 
@@ -513,7 +521,8 @@ def run_gpu(args, rank, world, local_rank):
     attention = attention_bench(Q, device, stream, peaks, l2) if rank == 0 else None
     return {"ms": ms, "ms_nopdl": ms_nopdl, "ms_wflip": ms_wflip, "ms_fused": ms_fused,
             "ms_alt": ms_alt, "ms_grouped": ms_grouped,
-            "ms_grouped_tiles": ms_grouped_tiles, "grouped_launches": grouped_launches,
+            "ms_grouped_tiles": ms_grouped_tiles, "ms_grouped_plan": ms_grouped_plan,
+            "group_plan_splits": group_plan_splits, "grouped_launches": grouped_launches,
             "per_call": per_call, "dom": dom,
             "clocks": sample, "wl": wl,
             "peaks": peaks,
@@ -1089,6 +1098,9 @@ def main():
            "value_grouped": round(job_value_us(res["ms_grouped"], 1, args.steps, ncalls), 4),
            "value_grouped_tiles": round(job_value_us(res["ms_grouped_tiles"], 1, args.steps,
                                                      ncalls), 4),
+           "value_grouped_group_plan": round(job_value_us(res["ms_grouped_plan"], 1, args.steps,
+                                                          ncalls), 4),
+           "group_plan_splits": res["group_plan_splits"],
            "grouped_launches_per_step": res["grouped_launches"],
            "roofline": roof, "roofline_other_partitions": roof_alt,
            "gpu_launches": args.steps * wl.launches_per_step(),

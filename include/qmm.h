@@ -404,6 +404,40 @@ int qmm_w4a16_g128_grouped(const qmm_group_call *calls, int n, void *workspace, 
 enum { QMM_GROUPED_TILES = 0, QMM_GROUPED_PERSISTENT = 1 };
 int qmm_set_grouped_schedule(int mode);
 
+/* Split plan of the grouped call (process-wide, thread-safe):
+ *   QMM_GROUP_PLAN_CALLS (default)  each call takes the split qmm_w4a16_g128
+ *       would give it alone (the chapter's occupancy policy per call), so each
+ *       C is bitwise that call's.
+ *   QMM_GROUP_PLAN_GROUP  splits sized for the group (gpu-kernels-explained,
+ *       "Split-K, streams and overlap": split only while the SMs would
+ *       otherwise idle).  The policy splits every call until it alone fills
+ *       the GPU, but a group's calls together already fill it several times,
+ *       so those splits only add tiles, each with its fixed cost, and partial
+ *       planes.  qmm_group_plan gives the splits.  Each C is bitwise the C of
+ *       qmm_w4a16_g128 with split_req = the planned split.
+ * qmm_group_workspace_bytes follows the plan in force.  Returns the previous
+ * plan, or QMM_EINVAL for an unknown value. */
+enum { QMM_GROUP_PLAN_CALLS = 0, QMM_GROUP_PLAN_GROUP = 1 };
+int qmm_set_group_plan(int mode);
+
+/* The group plan's splits for n calls of shapes (M, Kred, Nout) (host, 3n
+ * ints), without launching anything: per tile width (the calls of one launch),
+ * every call starts unsplit, then the call with the longest partition (lowest
+ * index on ties) takes its next valid split while that lowers the launch's
+ * estimated time.  Valid splits are those of the chapter's rule for a single
+ * call: at most 16 and G = Kred/128, at least 512 reduction elements per
+ * partition for M <= 8, and dividing G unless QMM_PARTITIONS_NEAR_EQUAL is in
+ * force.  The estimate is a longest-first list schedule of the launch's CTA
+ * tiles on num_sms SMs plus the partial planes' traffic.  A tile costs 3 us
+ * plus 0.40 / 0.45 / 0.55 / 0.60 us per 128-group for tile widths up to
+ * 32 / 64 / 128 / more rows.  The planes, written and read back, move at
+ * 3 TB/s.  These constants are tuning parameters fitted to this library's
+ * kernels on GB300, as the chapter's 320 and 16 are for its kernels.  A
+ * launch of more than 65536 tiles keeps each call's own policy split.
+ * num_sms <= 0 queries the device.  splits (host, n ints) receives the plan.
+ * Returns QMM_OK, QMM_EINVAL, QMM_ESHAPE or QMM_ENODEV. */
+int qmm_group_plan(const int *shapes, int n, int num_sms, int partial_dtype, int *splits);
+
 /* ---- split-KV decode attention -------------------------------------------
  *
  * "Optimize Prefill vs Decode Kernels" (Required reasoning process, steps 4

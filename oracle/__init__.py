@@ -19,6 +19,7 @@ tiny shapes and library routines; none is "parity unpinned".
 from __future__ import annotations
 
 import ctypes
+import heapq
 import os
 import subprocess
 import threading
@@ -313,3 +314,101 @@ def gemm_partitioned(A, W, split: int, ktile: int = 64, threads: int | None = No
     _check(_load().oracle_gemm_partitioned(_ptr(A), _ptr(W), M, N, K, ktile, split, _ptr(C),
                                            threads or default_threads()), "gemm_partitioned")
     return C
+
+
+# ---- group plan ---------------------------------------------------------------
+#
+# The grouped call's opt-in split plan.  The pages motivate it: split-K only
+# pays while SMs would otherwise idle (gpu-kernels-explained, "Split-K, streams
+# and overlap", the wave model).  The cost model and its constants are this
+# library's own, and the oracle restates them as the rule's definition.
+
+GROUP_PLAN_TILE_US = 3.0           # fixed cost of one CTA tile
+GROUP_PLAN_PLANE_BYTES_PER_US = 3.0e6
+
+
+def group_plan_group_us(bm: int) -> float:
+    """Time of one 128-group of a tile, by tile width (activation rows)."""
+    if bm <= 32:
+        return 0.40
+    if bm <= 64:
+        return 0.45
+    if bm <= 128:
+        return 0.55
+    return 0.60
+
+
+def group_plan_cost(shapes, tiles, splits, bm, sms, partial_bytes=2):
+    """Estimated time (us) of one launch: the CTA tiles of every call, longest
+    first, each placed on the SM that frees first, plus the partial planes
+    written and read back."""
+    durations = []
+    planes = 0.0
+    for (M, Kred, Nout), t, s in zip(shapes, tiles, splits):
+        G = Kred // 128
+        longest = -(-G // s)
+        durations.append((GROUP_PLAN_TILE_US + longest * group_plan_group_us(bm), t * s))
+        if s > 1:
+            planes += float(s) * M * Nout * 2 * partial_bytes / GROUP_PLAN_PLANE_BYTES_PER_US
+    durations.sort(key=lambda x: -x[0])  # stable: equal durations keep call order
+    free = [0.0] * sms
+    heapq.heapify(free)
+    span = 0.0
+    for d, count in durations:
+        for _ in range(count):
+            t = heapq.heappop(free) + d
+            heapq.heappush(free, t)
+            span = max(span, t)
+    return span + planes
+
+
+def group_plan(shapes, tiles_of, sms, near_equal=False, partial_bytes=2, cap=16,
+               decode_max_m=8, decode_min_k=512, trace=None):
+    """Splits for calls of shapes [(M, Kred, Nout)], where tiles_of(M) gives
+    the (bm, bn) tile of the kernel that serves M.  The calls of one tile width
+    share a launch.  Per launch, every call starts unsplit.  Then, repeatedly,
+    the call with the longest partition (lowest index on ties) moves to its
+    next valid split.  The move is kept only if it lowers group_plan_cost, and
+    the descent ends at the first move that does not, or when that call has no
+    larger valid split.  Valid splits follow the chapter's single-call rule: at
+    most cap and G, at least decode_min_k reduction elements per partition for
+    M <= decode_max_m, and dividing G unless near_equal.  trace, if a list,
+    receives (splits, cost) after every kept move, per launch.  (The library
+    plans launches of up to 65536 tiles this way.)"""
+    splits = [1] * len(shapes)
+    widths = []
+    for M, _, _ in shapes:
+        if tiles_of(M)[0] not in widths:
+            widths.append(tiles_of(M)[0])
+    for bm in widths:
+        idx = [i for i, (M, _, _) in enumerate(shapes) if tiles_of(M)[0] == bm]
+        part = [shapes[i] for i in idx]
+        tiles = []
+        for M, Kred, Nout in part:
+            tbm, tbn = tiles_of(M)
+            tiles.append(-(-M // tbm) * -(-Nout // tbn))
+        s = [1] * len(part)
+        cost = group_plan_cost(part, tiles, s, bm, sms, partial_bytes)
+        if trace is not None:
+            trace.append((list(s), cost))
+        while True:
+            lengths = [-(-(K // 128) // si) for (_, K, _), si in zip(part, s)]
+            top = lengths.index(max(lengths))
+            M, Kred, _ = part[top]
+            G = Kred // 128
+            min_k = decode_min_k if M <= decode_max_m else 128
+            smax = min(cap, G, max(1, Kred // min_k))
+            nxt = next((v for v in range(s[top] + 1, smax + 1) if near_equal or G % v == 0), None)
+            if nxt is None:
+                break
+            t = list(s)
+            t[top] = nxt
+            c2 = group_plan_cost(part, tiles, t, bm, sms, partial_bytes)
+            if not c2 < cost:
+                break
+            s, cost = t, c2
+            if trace is not None:
+                trace.append((list(s), cost))
+        for i, v in zip(idx, s):
+            splits[i] = v
+    return splits

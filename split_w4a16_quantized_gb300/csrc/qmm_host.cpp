@@ -8,6 +8,7 @@
 #include <cmath>
 #include <cstdint>
 #include <mutex>
+#include <queue>
 #include <vector>
 
 #include "qmm.h"
@@ -68,6 +69,7 @@ std::atomic<int> g_wstatic{0};
 std::atomic<int> g_reduce{QMM_REDUCE_KERNEL};
 std::atomic<int> g_partitions{QMM_PARTITIONS_EQUAL};
 std::atomic<int> g_grouped{QMM_GROUPED_PERSISTENT};
+std::atomic<int> g_group_plan{QMM_GROUP_PLAN_CALLS};
 
 // a split the current partition rule accepts for G groups (grid z <= 65535)
 bool split_fits(int64_t G, int64_t split) {
@@ -188,6 +190,26 @@ int qmm_wait_timeout_probe(void* stream) {
     int rc = check_device();
     if (rc != QMM_OK) return rc;
     return launched(qmm::launch_wait_probe(stream));
+}
+
+namespace {
+// the group plan's splits (defined with the grouped call below)
+int group_plan_shapes(const int* shapes, int n, int num_sms, int partial_dtype,
+                      std::vector<int>* splits);
+}  // namespace
+
+int qmm_set_group_plan(int mode) {
+    if (mode != QMM_GROUP_PLAN_CALLS && mode != QMM_GROUP_PLAN_GROUP) return QMM_EINVAL;
+    return g_group_plan.exchange(mode);
+}
+
+int qmm_group_plan(const int* shapes, int n, int num_sms, int partial_dtype, int* splits) {
+    if (!splits) return QMM_EINVAL;
+    std::vector<int> out;
+    const int rc = group_plan_shapes(shapes, n, num_sms, partial_dtype, &out);
+    if (rc != QMM_OK) return rc;
+    std::copy(out.begin(), out.end(), splits);
+    return QMM_OK;
 }
 
 int qmm_set_grouped_schedule(int mode) {
@@ -383,6 +405,160 @@ int check_group_call(const qmm_group_call& c) {
     return QMM_OK;
 }
 
+// ---- group plan (qmm_set_group_plan) ----------------------------------------
+//
+// Splits sized for a group's launch rather than for each call alone.  The
+// calls of one tile width share a launch; its time is estimated as a
+// longest-first list schedule of the CTA tiles on the SMs (a tile costs
+// kPlanTileUs plus its partition's groups at plan_group_us) plus the partial
+// planes written and read back (kPlanPlaneBytesPerUs).  Starting from every
+// call unsplit, the call with the longest partition (lowest index on ties)
+// takes its next valid split while that lowers the estimate.  The constants
+// are tuning parameters fitted to this library's kernels on GB300, as the
+// chapter's 320 and 16 are for its kernels.
+constexpr double kPlanTileUs = 3.0;
+constexpr double kPlanPlaneBytesPerUs = 3.0e6;
+constexpr int64_t kPlanMaxTiles = 1 << 16;  // larger launches keep each call's own split
+
+double plan_group_us(int bm) { return bm <= 32 ? 0.40 : bm <= 64 ? 0.45 : bm <= 128 ? 0.55 : 0.60; }
+
+struct PlanCall {
+    int M, Kred, Nout, G, smax;
+    int64_t tiles;
+};
+
+// Estimated time of one launch with splits s; false if it has too many tiles.
+bool plan_cost(const std::vector<PlanCall>& c, const std::vector<int>& s, int bm, int sms,
+               int elem, double* cost) {
+    struct Cls {
+        double d;
+        int64_t k;
+    };
+    std::vector<Cls> cls;
+    int64_t tiles = 0;
+    double planes = 0.0;
+    for (size_t i = 0; i < c.size(); ++i) {
+        const int len = (c[i].G + s[i] - 1) / s[i];
+        cls.push_back({kPlanTileUs + len * plan_group_us(bm), c[i].tiles * s[i]});
+        tiles += c[i].tiles * s[i];
+        if (s[i] > 1)
+            planes += static_cast<double>(s[i]) * c[i].M * c[i].Nout * 2 * elem / kPlanPlaneBytesPerUs;
+    }
+    if (tiles > kPlanMaxTiles) return false;
+    std::stable_sort(cls.begin(), cls.end(), [](const Cls& a, const Cls& b) { return a.d > b.d; });
+    std::priority_queue<double, std::vector<double>, std::greater<double>> load;
+    for (int i = 0; i < sms; ++i) load.push(0.0);
+    double span = 0.0;
+    for (const Cls& k : cls)
+        for (int64_t j = 0; j < k.k; ++j) {
+            const double l = load.top() + k.d;
+            load.pop();
+            load.push(l);
+            span = std::max(span, l);
+        }
+    *cost = span + planes;
+    return true;
+}
+
+// The group plan of shapes (M, Kred, Nout) into splits: per tile width, the
+// greedy descent above.  A launch over kPlanMaxTiles keeps each call's own
+// policy split.
+int group_plan(const std::vector<PlanCall>& calls, int sms, int elem, std::vector<int>* splits) {
+    splits->assign(calls.size(), 1);
+    std::vector<int> widths;
+    for (const PlanCall& c : calls) {
+        const int bm = qmm::family_for(c.M).bm;
+        if (std::find(widths.begin(), widths.end(), bm) == widths.end()) widths.push_back(bm);
+    }
+    for (int bm : widths) {
+        std::vector<size_t> idx;
+        std::vector<PlanCall> part;
+        for (size_t i = 0; i < calls.size(); ++i)
+            if (qmm::family_for(calls[i].M).bm == bm) {
+                idx.push_back(i);
+                part.push_back(calls[i]);
+            }
+        std::vector<int> s(part.size(), 1);
+        double cost = 0.0;
+        bool fits = plan_cost(part, s, bm, sms, elem, &cost);
+        while (fits) {
+            size_t top = 0;
+            for (size_t i = 1; i < part.size(); ++i)
+                if ((part[i].G + s[i] - 1) / s[i] > (part[top].G + s[top] - 1) / s[top]) top = i;
+            int next = s[top] + 1;
+            while (next <= part[top].smax && !split_fits(part[top].G, next)) ++next;
+            if (next > part[top].smax) break;
+            std::vector<int> t = s;
+            t[top] = next;
+            double c2 = 0.0;
+            if (!plan_cost(part, t, bm, sms, elem, &c2)) {
+                fits = false;
+                break;
+            }
+            if (!(c2 < cost)) break;
+            s = t;
+            cost = c2;
+        }
+        for (size_t i = 0; i < part.size(); ++i) {
+            int split = s[i];
+            if (!fits) {  // too many tiles to plan: the call's own policy split
+                const int rc = qmm::choose_split(part[i].M, part[i].Kred, part[i].Nout, 0, nullptr,
+                                                 &split);
+                if (rc != QMM_OK) return rc;
+            }
+            (*splits)[idx[i]] = split;
+        }
+    }
+    return QMM_OK;
+}
+
+int group_plan_shapes(const int* shapes, int n, int num_sms, int partial_dtype,
+                      std::vector<int>* splits) {
+    if (!shapes || n < 1) return QMM_EINVAL;
+    if (partial_dtype != QMM_PARTIAL_BF16 && partial_dtype != QMM_PARTIAL_F32) return QMM_EINVAL;
+    if (num_sms <= 0) {
+        const int rc = device_sms(&num_sms);
+        if (rc != QMM_OK) return rc;
+    }
+    std::vector<PlanCall> calls;
+    for (int i = 0; i < n; ++i) {
+        const int M = shapes[3 * i], Kred = shapes[3 * i + 1], Nout = shapes[3 * i + 2];
+        if (M < 1 || Nout < 1) return QMM_EINVAL;
+        if (Kred < qmm::kGroup || Kred % qmm::kGroup) return QMM_ESHAPE;
+        const qmm::Family& f = qmm::family_for(M);
+        const int G = Kred / qmm::kGroup;
+        const int min_k = M <= qmm::kDecodeMaxM ? qmm::kDecodeMinK : qmm::kGroup;
+        const int smax = std::min(std::min(qmm::kCap, G), std::max(1, Kred / min_k));
+        calls.push_back({M, Kred, Nout, G, smax, ceil_div(M, f.bm) * ceil_div(Nout, f.bn)});
+    }
+    // plans are cached: a model step issues the same group again and again
+    struct Entry {
+        std::vector<int> key, splits;
+    };
+    static std::mutex mu;
+    static std::vector<Entry> cache;
+    std::vector<int> key(shapes, shapes + 3 * n);
+    key.push_back(num_sms);
+    key.push_back(partial_dtype);
+    key.push_back(qmm::partitions_near_equal() ? 1 : 0);
+    key.push_back(g_kernels.load(std::memory_order_relaxed));
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (const Entry& e : cache)
+            if (e.key == key) {
+                *splits = e.splits;
+                return QMM_OK;
+            }
+    }
+    const int rc = group_plan(calls, num_sms, static_cast<int>(partial_elem_bytes(partial_dtype)),
+                              splits);
+    if (rc != QMM_OK) return rc;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache.size() >= 16) cache.erase(cache.begin());
+    cache.push_back({key, *splits});
+    return QMM_OK;
+}
+
 // Every call's arguments, then its split and the offset of its planes in the
 // workspace (256-byte aligned); *ws_need receives the total.
 int plan_group(const qmm_group_call* calls, int n, int partial_dtype, std::vector<int>* splits,
@@ -395,12 +571,24 @@ int plan_group(const qmm_group_call* calls, int n, int partial_dtype, std::vecto
     }
     splits->assign(static_cast<size_t>(n), 1);
     offsets->assign(static_cast<size_t>(n), 0);
+    if (g_group_plan.load(std::memory_order_relaxed) == QMM_GROUP_PLAN_GROUP) {
+        std::vector<int> shapes;
+        for (int i = 0; i < n; ++i) {
+            shapes.push_back(calls[i].M);
+            shapes.push_back(calls[i].Kred);
+            shapes.push_back(calls[i].Nout);
+        }
+        const int rc = group_plan_shapes(shapes.data(), n, 0, partial_dtype, splits);
+        if (rc != QMM_OK) return rc;
+    }
     size_t off = 0;
     for (int i = 0; i < n; ++i) {
         const qmm_group_call& c = calls[i];
         int& s = (*splits)[static_cast<size_t>(i)];
-        const int rc = qmm::choose_split(c.M, c.Kred, c.Nout, 0, nullptr, &s);
-        if (rc != QMM_OK) return rc;
+        if (g_group_plan.load(std::memory_order_relaxed) != QMM_GROUP_PLAN_GROUP) {
+            const int rc = qmm::choose_split(c.M, c.Kred, c.Nout, 0, nullptr, &s);
+            if (rc != QMM_OK) return rc;
+        }
         if (s > 1) {
             (*offsets)[static_cast<size_t>(i)] = off;
             const size_t planes = static_cast<size_t>(s) * static_cast<size_t>(c.M) *

@@ -84,6 +84,8 @@ _SIGS = {
     "qmm_set_reduce": (_I, [_I]),
     "qmm_set_partitions": (_I, [_I]),
     "qmm_set_grouped_schedule": (_I, [_I]),
+    "qmm_set_group_plan": (_I, [_I]),
+    "qmm_group_plan": (_I, [ctypes.POINTER(_I), _I, _I, _I, ctypes.POINTER(_I)]),
     "qmm_kernel_status": (_I, [ctypes.POINTER(_I), _I]),
     "qmm_wait_timeout_probe": (_I, [ctypes.c_void_p]),
     "qmm_w4a16_g128_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I,
@@ -209,6 +211,26 @@ def qmm_set_grouped_schedule(mode: int) -> int:
     if prev < 0:
         raise QmmError(prev, "qmm_set_grouped_schedule")
     return prev
+
+
+QMM_GROUP_PLAN_CALLS, QMM_GROUP_PLAN_GROUP = 0, 1
+
+
+def qmm_set_group_plan(mode: int) -> int:
+    """Split plan of the grouped call (QMM_GROUP_PLAN_*); returns the previous one."""
+    prev = lib().qmm_set_group_plan(mode)
+    if prev < 0:
+        raise QmmError(prev, "qmm_set_group_plan")
+    return prev
+
+
+def qmm_group_plan(shapes, num_sms: int = 0, partial_dtype: int = QMM_PARTIAL_BF16) -> list:
+    """The group plan's splits for shapes [(M, Kred, Nout), ...] (host only)."""
+    n = len(shapes)
+    flat = (_I * (3 * n))(*[int(v) for shp in shapes for v in shp])
+    out = (_I * n)()
+    _check(lib().qmm_group_plan(flat, n, num_sms, partial_dtype, out), "qmm_group_plan")
+    return list(out)
 
 
 def qmm_set_weights_static(enable: bool) -> int:

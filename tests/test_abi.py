@@ -319,3 +319,51 @@ def test_grouped_schedule_setting():
             Q.qmm_set_grouped_schedule(2)
     finally:
         Q.qmm_set_grouped_schedule(prev)
+
+
+def test_group_plan_bit_exact_against_the_oracle():
+    """qmm_group_plan equals the oracle's restatement of the rule on the
+    workload's groups and on seeded random groups (both partition rules, both
+    plane types, several SM counts).  The tile of each M is the library's
+    kernel table, the same on both sides."""
+    import oracle
+    from split_w4a16_quantized_gb300 import inputs
+    from split_w4a16_quantized_gb300 import qmm as Q
+    tiles = lambda M: Q.qmm_kernel_tile(M)
+    cases = [[(M,) + inputs.PROJECTIONS[n] for n in inputs.PROJECTIONS]
+             for M in (1, 4, 8, 16, 32, 64, 128, 2048)]
+    rng = np.random.default_rng(21)
+    for _ in range(60):
+        n = int(rng.integers(1, 17))
+        Ms = rng.choice([1, 3, 8, 16, 20, 32, 40, 64, 100, 128, 129, 512], size=n)
+        cases.append([(int(M), 128 * int(rng.integers(1, 129)), int(rng.integers(1, 12000)))
+                      for M in Ms])
+    prev = Q.qmm_set_partitions(Q.QMM_PARTITIONS_EQUAL)
+    try:
+        for k, shapes in enumerate(cases):
+            near = k % 3 == 2
+            dt = Q.QMM_PARTIAL_F32 if k % 4 == 3 else Q.QMM_PARTIAL_BF16
+            sms = (152, 132, 108)[k % 3]
+            Q.qmm_set_partitions(Q.QMM_PARTITIONS_NEAR_EQUAL if near else Q.QMM_PARTITIONS_EQUAL)
+            got = Q.qmm_group_plan(shapes, sms, dt)
+            want = oracle.group_plan(shapes, tiles, sms, near_equal=near,
+                                     partial_bytes=4 if dt == Q.QMM_PARTIAL_F32 else 2)
+            assert got == want, (k, shapes, got, want)
+    finally:
+        Q.qmm_set_partitions(prev)
+
+
+def test_group_plan_setting():
+    from split_w4a16_quantized_gb300 import qmm as Q
+    prev = Q.qmm_set_group_plan(Q.QMM_GROUP_PLAN_GROUP)
+    assert prev == Q.QMM_GROUP_PLAN_CALLS  # the default
+    try:
+        assert Q.qmm_set_group_plan(Q.QMM_GROUP_PLAN_CALLS) == Q.QMM_GROUP_PLAN_GROUP
+        with pytest.raises(Q.QmmError):
+            Q.qmm_set_group_plan(5)
+        with pytest.raises(Q.QmmError):
+            Q.qmm_group_plan([(32, 100, 1024)], 152)   # Kred not a multiple of 128
+        with pytest.raises(Q.QmmError):
+            Q.qmm_group_plan([(0, 2560, 1024)], 152)
+    finally:
+        Q.qmm_set_group_plan(prev)

@@ -602,3 +602,84 @@ def test_gemm_partitioned_covers_every_tile(split):
     ones = np.full((1, K), 0x3F80, np.uint16)
     assert oracle.bf16_value(oracle.gemm_partitioned(ones, ones, split, 64))[0, 0] == \
         oracle.bf16_value(oracle.bf16_round(np.array([float(K)])))[0]
+
+
+# ---- group plan (the grouped call's opt-in split plan) ------------------------
+
+def _tc_tiles(M):
+    """The tcgen05 kernel table: tiles of 16/32/64/128/256 activation rows x 128 columns."""
+    for bm in (16, 32, 64, 128):
+        if M <= bm:
+            return bm, 128
+    return 256, 128
+
+
+def test_group_plan_single_call_by_hand():
+    # k at M = 32: 8 tiles of 20 groups on 152 SMs, one tile per SM each step.
+    # A tile costs 3 + 0.40 * (its groups); planes 2 * s * 32 * 1024 * 2 B at 3 TB/s.
+    # s=1: 3 + 8.0 = 11.0; s=2: 3 + 4.0 + 0.0874 = 7.0874; s=4: 5.0 + 0.1748;
+    # s=5: 4.6 + 0.2185; s=10: 3.8 + 0.4369 = 4.2369; 20 is over the cap of 16.
+    trace = []
+    s = oracle.group_plan([(32, 2560, 1024)], _tc_tiles, 152, trace=trace)
+    assert s == [10]
+    assert [t[0] for t in trace] == [[1], [2], [4], [5], [10]]
+    plane = lambda k: k * 32 * 1024 * 2 * 2 / 3.0e6
+    want = [11.0, 7.0 + plane(2), 5.0 + plane(4), 4.6 + plane(5), 3.8 + plane(10)]
+    assert np.allclose([t[1] for t in trace], want, rtol=0, atol=1e-12)
+
+
+def test_group_plan_wave_tail_by_hand():
+    # down at M = 2048: 160 tiles of 256 rows on 152 SMs.
+    # s=1: tiles of 3 + 76 * 0.6 = 48.6; eight SMs run two -> 97.2.
+    # s=2: 320 tiles of 3 + 38 * 0.6 = 25.8; sixteen SMs run three -> 77.4,
+    #      plus planes 2 * 2048 * 2560 * 2 * 2 B / 3e6 = 13.98 -> 91.38 (kept).
+    # s=4: 640 tiles of 14.4, five rounds -> 72.0 + 27.96 = 99.96 (not kept).
+    trace = []
+    assert oracle.group_plan([(2048, 9728, 2560)], _tc_tiles, 152, trace=trace) == [2]
+    planes = 2 * 2048 * 2560 * 2 * 2 / 3.0e6
+    assert np.isclose(trace[0][1], 97.2) and np.isclose(trace[1][1], 77.4 + planes)
+    # o at M = 2048: 160 tiles of 3 + 32 * 0.6 = 22.2 -> 44.4; split 2 gives
+    # 320 tiles of 12.6 (three rounds, 37.8) plus 13.98 of planes: not kept.
+    assert oracle.group_plan([(2048, 4096, 2560)], _tc_tiles, 152) == [1]
+
+
+def test_group_plan_agrees_with_the_chapter_policy_on_single_calls():
+    # For one call that under-fills the GPU the plan ends where the chapter's
+    # occupancy rule does (the workload's shapes at M = 32 and 128).
+    for M in (32, 128):
+        for name, (Kred, Nout) in inputs.PROJECTIONS.items():
+            bm, bn = _tc_tiles(M)
+            pol = oracle.splitk_plan(M, Kred, Nout, bm, bn, 152, 16)
+            assert oracle.group_plan([(M, Kred, Nout)], _tc_tiles, 152) == [pol], (M, name)
+
+
+def test_group_plan_on_a_full_group():
+    shapes = lambda M: [(M,) + inputs.PROJECTIONS[n] for n in inputs.PROJECTIONS]
+    # the seven projections already fill the GPU together: only down, whose
+    # partitions are the longest, splits; nothing splits at M = 2048
+    assert oracle.group_plan(shapes(32), _tc_tiles, 152) == [1, 1, 1, 1, 1, 1, 4]
+    assert oracle.group_plan(shapes(128), _tc_tiles, 152) == [1, 1, 1, 1, 1, 1, 2]
+    assert oracle.group_plan(shapes(2048), _tc_tiles, 152) == [1] * 7
+
+
+def test_group_plan_invariants():
+    rng = np.random.default_rng(11)
+    for _ in range(40):
+        n = int(rng.integers(1, 8))
+        M = int(rng.choice([1, 4, 16, 32, 64, 128, 300]))
+        shapes = [(M, 128 * int(rng.integers(1, 100)), int(rng.integers(1, 6000)))
+                  for _ in range(n)]
+        near = bool(rng.integers(0, 2))
+        trace = []
+        s = oracle.group_plan(shapes, _tc_tiles, 152, near_equal=near, trace=trace)
+        costs = [t[1] for t in trace]
+        assert all(b < a for a, b in zip(costs, costs[1:]))  # every kept move lowers the cost
+        for (m, K, N), v in zip(shapes, s):
+            G = K // 128
+            assert 1 <= v <= min(16, G)
+            assert near or G % v == 0
+            if m <= 8:
+                assert v == 1 or K // v >= 512
+    # ties between equally long calls go to the lower index
+    assert oracle.group_plan([(32, 2560, 1024), (32, 2560, 1024)], _tc_tiles, 152)[0] >= \
+        oracle.group_plan([(32, 2560, 1024), (32, 2560, 1024)], _tc_tiles, 152)[1]

@@ -933,6 +933,47 @@ def test_grouped_with_static_weights(grouped_schedule, pdl):
         Q.qmm_set_pdl(prev_p)
 
 
+@pytest.mark.parametrize("dt", [Q.QMM_PARTIAL_BF16, Q.QMM_PARTIAL_F32])
+def test_group_plan_equals_the_calls_at_the_planned_splits(grouped_schedule, dt):
+    """Under QMM_GROUP_PLAN_GROUP each C is bitwise qmm_w4a16_g128's C with
+    split_req = the planned split, the splits reported are the plan, and the
+    workspace holds exactly the planned planes."""
+    probs = _group_problems(GROUP_SHAPES, 340)
+    shapes = [(d["C"].shape[0], d["A"].shape[1], d["C"].shape[1]) for _, d in probs]
+    prev = Q.qmm_set_group_plan(Q.QMM_GROUP_PLAN_GROUP)
+    try:
+        plan = Q.qmm_group_plan(shapes, 0, dt)
+        assert max(plan) > 1 and min(plan) == 1
+        refs = []
+        for (p, d), sp in zip(probs, plan):
+            M, Nout = d["C"].shape
+            C = torch.empty((M, Nout), dtype=torch.bfloat16, device="cuda")
+            nb = Q.qmm_splitk_workspace_bytes(M, Nout, sp, dt)
+            ws = torch.zeros(max(nb, 16) + (64 << 10), dtype=torch.uint8, device="cuda")
+            assert Q.qmm_w4a16_g128(d["A"], d["Wq"], d["scales"], d["biases"], C, split_req=sp,
+                                    workspace=ws, partial_dtype=dt) == sp
+            refs.append(_bits(C))
+        calls = Q.group_calls([d for _, d in probs])
+        nb = Q.qmm_group_workspace_bytes(calls, dt)
+        elem = 4 if dt == Q.QMM_PARTIAL_F32 else 2
+        assert nb == sum(-(-(sp * M * N * elem) // 256) * 256
+                         for sp, (M, _, N) in zip(plan, shapes) if sp > 1)
+        ws = torch.full((max(nb, 16) // 2 + 8,), float("nan"), dtype=torch.bfloat16, device="cuda")
+        used = Q.qmm_w4a16_g128_grouped(calls, ws if nb else None, dt)
+        torch.cuda.synchronize()
+        assert Q.qmm_kernel_status(clear=True) == 0
+        assert used == plan
+        for j, ((p, d), ref) in enumerate(zip(probs, refs)):
+            assert np.array_equal(_bits(d["C"]), ref), "call %d" % j
+    finally:
+        Q.qmm_set_group_plan(prev)
+    # one planned call against the oracle directly (down at M = 128, split 2 or the plan's)
+    p, d = probs[13]
+    M, Nout = d["C"].shape
+    rows, cols = _sample(M, Nout, np.random.default_rng(9))
+    _check_sampled(p, _bits(d["C"]), used[13], dt, rows, cols, "group plan down M=128")
+
+
 @pytest.mark.parametrize("shapes", [
     [("k", 32)],                                    # fewer tiles than SMs: one each
     [("odd", 3), ("odd", 40), ("ragged", 1), ("k", 8), ("odd", 129)] * 3,
