@@ -323,6 +323,8 @@ def run_gpu(args, rank, world, local_rank):
     if args.grouped:  # profiling aid: the step's calls as one grouped call
         Q.qmm_set_grouped_schedule(Q.QMM_GROUPED_PERSISTENT if args.grouped == "persistent"
                                    else Q.QMM_GROUPED_TILES)
+        if args.group_plan:
+            Q.qmm_set_group_plan(Q.QMM_GROUP_PLAN_GROUP)
         g_arrays = [Q.group_calls([dict(wl.sets[r][i], C=wl.C[r][i])
                                    for i in range(len(wl.calls))]) for r in range(wl.R)]
         g_ws = torch.zeros(max(Q.qmm_group_workspace_bytes(g_arrays[0]), 16), dtype=torch.uint8,
@@ -365,11 +367,14 @@ def run_gpu(args, rank, world, local_rank):
     ms = max_over_ranks(t0.elapsed_time(t1), device)
 
     if args.launch_list:
-        launches = None
+        launches, splits = None, wl.split
         if args.grouped:
             widths = len({Q.qmm_kernel_tile(M)[0] for (_, M, _, _) in wl.calls})
-            launches = widths + (1 if any(sp > 1 for sp in wl.split) else 0)
-        return {"ms": ms, "wl": wl, "launch_list": True, "grouped_launches": launches}
+            splits = Q.qmm_group_plan([(M, K, N) for (_, M, K, N) in wl.calls]) \
+                if args.group_plan else wl.split
+            launches = widths + (1 if any(sp > 1 for sp in splits) else 0)
+        return {"ms": ms, "wl": wl, "launch_list": True, "grouped_launches": launches,
+                "splits": splits}
 
     def time_variant(setter, value):
         """The step re-captured with one library switch changed, same timing."""
@@ -982,6 +987,8 @@ def main():
     ap.add_argument("--grouped", choices=["tiles", "persistent"], default=None,
                     help="with --launch-list: time the step's calls as one grouped call "
                          "under this schedule (profiling aid)")
+    ap.add_argument("--group-plan", action="store_true",
+                    help="with --grouped: splits planned for the group (qmm_set_group_plan)")
     ap.add_argument("--attention-only", action="store_true",
                     help="only the decode-attention calls at the plan's split (profiling aid)")
     args = ap.parse_args()
@@ -993,6 +1000,8 @@ def main():
         ap.error("--warmup must be at least 3")
     if args.grouped and not args.launch_list:
         ap.error("--grouped is a profiling aid of --launch-list")
+    if args.group_plan and not args.grouped:
+        ap.error("--group-plan applies to --grouped")
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -1014,8 +1023,8 @@ def main():
         if rank == 0:
             per_step = res["grouped_launches"] or wl.launches_per_step()
             print(json.dumps({"launch_list": True, "value": value_us, "unit": UNIT,
-                              "steps": args.steps, "splits": wl.split,
-                              "grouped": args.grouped,
+                              "steps": args.steps, "splits": res["splits"],
+                              "grouped": args.grouped, "group_plan": args.group_plan,
                               "gpu_launches": args.steps * per_step}), flush=True)
         return
 
