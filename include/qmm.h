@@ -432,8 +432,9 @@ int qmm_set_group_plan(int mode);
  * plus 0.40 / 0.45 / 0.55 / 0.60 us per 128-group for tile widths up to
  * 32 / 64 / 128 / more rows.  The planes, written and read back, move at
  * 3 TB/s.  These constants are tuning parameters fitted to this library's
- * kernels on GB300, as the chapter's 320 and 16 are for its kernels.  A
- * launch of more than 65536 tiles keeps each call's own policy split.
+ * kernels on GB300, as the chapter's 320 and 16 are for its kernels.  No
+ * move takes a launch over 65536 tiles; a launch over that with every call
+ * unsplit keeps each call's own policy split for num_sms.
  * num_sms <= 0 queries the device.  splits (host, n ints) receives the plan.
  * Returns QMM_OK, QMM_EINVAL, QMM_ESHAPE or QMM_ENODEV. */
 int qmm_group_plan(const int *shapes, int n, int num_sms, int partial_dtype, int *splits);

@@ -374,7 +374,7 @@ def group_plan(shapes, tiles_of, sms, near_equal=False, partial_bytes=2, cap=16,
     most cap and G, at least decode_min_k reduction elements per partition for
     M <= decode_max_m, and dividing G unless near_equal.  trace, if a list,
     receives (splits, cost) after every kept move, per launch.  (The library
-    plans launches of up to 65536 tiles this way.)"""
+    also makes no move that takes a launch over 65536 tiles.)"""
     splits = [1] * len(shapes)
     widths = []
     for M, _, _ in shapes:

@@ -461,7 +461,8 @@ bool plan_cost(const std::vector<PlanCall>& c, const std::vector<int>& s, int bm
 }
 
 // The group plan of shapes (M, Kred, Nout) into splits: per tile width, the
-// greedy descent above.  A launch over kPlanMaxTiles keeps each call's own
+// greedy descent above.  A move that would take the launch over kPlanMaxTiles
+// is not made; a launch over it with every call unsplit keeps each call's own
 // policy split.
 int group_plan(const std::vector<PlanCall>& calls, int sms, int elem, std::vector<int>* splits) {
     splits->assign(calls.size(), 1);
@@ -491,19 +492,21 @@ int group_plan(const std::vector<PlanCall>& calls, int sms, int elem, std::vecto
             std::vector<int> t = s;
             t[top] = next;
             double c2 = 0.0;
-            if (!plan_cost(part, t, bm, sms, elem, &c2)) {
-                fits = false;
-                break;
-            }
-            if (!(c2 < cost)) break;
+            // a move over kPlanMaxTiles is not made
+            if (!plan_cost(part, t, bm, sms, elem, &c2) || !(c2 < cost)) break;
             s = t;
             cost = c2;
         }
         for (size_t i = 0; i < part.size(); ++i) {
             int split = s[i];
-            if (!fits) {  // too many tiles to plan: the call's own policy split
-                const int rc = qmm::choose_split(part[i].M, part[i].Kred, part[i].Nout, 0, nullptr,
-                                                 &split);
+            if (!fits) {  // too many tiles to plan: the call's own policy split on these SMs
+                qmm_policy pol;
+                int rc = qmm_policy_preset(QMM_PRESET_GB300, part[i].M, sms, &pol);
+                if (rc == QMM_OK)
+                    rc = qmm::partitions_near_equal()
+                             ? qmm_splitk_plan_near_equal(part[i].M, part[i].Kred, part[i].Nout,
+                                                          &pol, &split)
+                             : qmm_splitk_plan(part[i].M, part[i].Kred, part[i].Nout, &pol, &split);
                 if (rc != QMM_OK) return rc;
             }
             (*splits)[idx[i]] = split;

@@ -367,3 +367,20 @@ def test_group_plan_setting():
             Q.qmm_group_plan([(0, 2560, 1024)], 152)
     finally:
         Q.qmm_set_group_plan(prev)
+
+
+def test_group_plan_falls_back_to_the_policy_on_huge_launches():
+    """A launch of more than 65536 tiles is not planned: each call keeps the
+    chapter's policy split for the given SM count (host only, no device)."""
+    from split_w4a16_quantized_gb300 import qmm as Q
+    shapes = [(16384, 2560, 16384)] * 9 + [(16384, 2560, 1024)]  # 64 x 128 tiles each
+    got = Q.qmm_group_plan(shapes, 152)
+    want = [Q.qmm_splitk_plan(M, K, N, Q.qmm_policy_preset(Q.QMM_PRESET_GB300, M, 152))
+            for M, K, N in shapes]
+    assert got == want
+    # exactly the limit unsplit is planned; a split would pass the limit, so
+    # none is made
+    assert Q.qmm_group_plan([(16384, 2560, 16384)] * 8, 152) == [1] * 8
+    # a call of another tile width is planned in its own launch: k at M = 16
+    # beside them splits as it would alone (the chapter policy's 10)
+    assert Q.qmm_group_plan([(16384, 2560, 16384)] * 8 + [(16, 2560, 1024)], 152) == [1] * 8 + [10]
