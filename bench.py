@@ -901,14 +901,50 @@ def oracle_steps(problems, min_seconds, max_steps=None, threads=None):
             return el / n, n
 
 
+def host_description():
+    """The host the oracle ran on: machine, CPU model and logical CPUs."""
+    import platform
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu model", "hardware") and ":" in line:
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    if model is None:  # Arm hosts name the core in lscpu, not in /proc/cpuinfo
+        try:
+            out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+            for line in out.splitlines():
+                if line.lower().startswith("model name:"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except (OSError, subprocess.SubprocessError):
+            pass
+    return {"machine": platform.machine(), "cpu": model, "logical_cpus": os.cpu_count()}
+
+
 def cpu_baseline(problems):
     import oracle
     threads = oracle.default_threads()
     sec, n = oracle_steps(problems, 10.0, threads=threads)
+    # the small case (k projection at M = 16) on one thread, median of 3
+    small = inputs.make_w4a16(16, *inputs.PROJECTIONS["k"], seed=0)
+    one = []
+    for _ in range(3):
+        t0 = time.perf_counter()
+        oracle.qmm(small["A"], small["Wq"], small["scales"], small["biases"], threads=1)
+        one.append(time.perf_counter() - t0)
     return {"value": round(sec * 1e6 / len(problems), 1), "unit": UNIT, "cores": threads,
             "kind": "oracle",
             "sample": "%d full step(s) of the workload (all 14 calls, fp64 C = A.W^T) on %d "
-                      "host threads" % (n, threads)}
+                      "host threads" % (n, threads),
+            "single_thread_small_us": round(statistics.median(one) * 1e6, 1),
+            "single_thread_small": "k projection at M = 16 (Kred 2560, Nout 1024), one thread, "
+                                   "median of 3",
+            "host": host_description()}
 
 
 def run_reference(args, rank, world):
