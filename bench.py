@@ -591,7 +591,8 @@ def shape_sweep(Q, device, stream, l2, peaks):
         pol = Q.qmm_policy_preset(Q.QMM_PRESET_GB300, M)
         split = Q.qmm_splitk_plan(M, Kred, Nout, pol)
         control = 1 if split > 1 else 2
-        ws = torch.empty(max(16, Q.qmm_splitk_workspace_bytes(M, Nout, max(split, control),
+        planned = Q.qmm_group_plan([(M, Kred, Nout)])[0]  # QMM_SPLIT_PLANNED's split
+        ws = torch.empty(max(16, Q.qmm_splitk_workspace_bytes(M, Nout, max(split, control, planned),
                                                                Q.QMM_PARTIAL_BF16)),
                          dtype=torch.uint8, device=device)
         cps = cold_copies(d, l2)
@@ -603,6 +604,8 @@ def shape_sweep(Q, device, stream, l2, peaks):
                              split_req=split_req, workspace=ws)
         us = graph_us_per_launch(lambda j: call(j, 0), len(cps), stream)
         us_c = graph_us_per_launch(lambda j: call(j, control), len(cps), stream)
+        us_p = graph_us_per_launch(lambda j: call(j, Q.QMM_SPLIT_PLANNED), len(cps), stream) \
+            if planned != split else None
         nb, fl = algorithmic(M, Kred, Nout, split)
         t_roof, bound = roofline_time_s(nb, fl, peaks)
         bm, bn = Q.qmm_kernel_tile(M)
@@ -610,14 +613,19 @@ def shape_sweep(Q, device, stream, l2, peaks):
                      "base_ctas": -(-M // bm) * -(-Nout // bn), "us": round(us, 3),
                      "control_split": control, "control_us": round(us_c, 3),
                      "speedup_vs_control": round(us_c / us, 3), "bound": bound,
-                     "roofline_frac": round(t_roof * 1e6 / us, 4)})
+                     "roofline_frac": round(t_roof * 1e6 / us, 4),
+                     "planned_split": planned,
+                     "planned_us": round(us_p, 3) if us_p is not None else None})
         del cps, d, ws
     split_rows = [r for r in rows if r["split"] > 1]
     kept = [r for r in rows if r["split"] == 1]
+    differ = [r for r in rows if r["planned_us"] is not None]
     summary = {"shapes": len(rows), "policy_splits": len(split_rows),
                "split_beats_unsplit": sum(r["us"] < r["control_us"] for r in split_rows),
                "policy_unsplit": len(kept),
-               "unsplit_beats_split_2": sum(r["us"] < r["control_us"] for r in kept)}
+               "unsplit_beats_split_2": sum(r["us"] < r["control_us"] for r in kept),
+               "planned_differs": len(differ),
+               "planned_faster": sum(r["planned_us"] < r["us"] for r in differ)}
     return {"summary": summary, "rows": rows}
 
 

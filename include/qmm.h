@@ -126,13 +126,22 @@ int qmm_splitk_plan_near_equal(int M, int Kred, int Nout, const qmm_policy *pol,
  * invalid arguments as well. */
 size_t qmm_splitk_workspace_bytes(int M, int Nout, int split, int partial_dtype);
 
+/* split_req value of qmm_w4a16_g128: the group plan's split for the call alone. */
+#define QMM_SPLIT_PLANNED (-1)
+
 /* C = A . W^T for the W4A16-g128 format (see the top of this header).
  *   split_req  0: split from the policy (qmm_splitk_plan, or
  *              qmm_splitk_plan_near_equal under QMM_PARTITIONS_NEAR_EQUAL);
  *              1: the unsplit kernel (the control, writes C directly);
  *              s > 1: forced split, which must divide Kred/128 under
  *              QMM_PARTITIONS_EQUAL and be at most Kred/128 under
- *              QMM_PARTITIONS_NEAR_EQUAL (QMM_ESHAPE otherwise).
+ *              QMM_PARTITIONS_NEAR_EQUAL (QMM_ESHAPE otherwise);
+ *              QMM_SPLIT_PLANNED: the split qmm_group_plan gives this call
+ *              alone on the current device.  That is the occupancy rule
+ *              extended with the group plan's estimate of waves and plane
+ *              traffic.  On under-filled calls it equals the policy's split;
+ *              past one wave it may split where the policy does not (down at
+ *              M = 2048: 2).  Size the workspace with that split.
  *   pol        policy used when split_req == 0; NULL = QMM_PRESET_GB300
  *              for this M on the current device.
  *   workspace  device buffer for the partial planes [split, M, Nout] of

@@ -327,7 +327,8 @@ int qmm_w4a16_g128(const void* A, const uint32_t* Wq, const void* scales, const 
                    void* C, int M, int Kred, int Nout, int split_req, const qmm_policy* pol,
                    void* workspace, size_t ws_bytes, int partial_dtype, void* stream,
                    int* split_used) {
-    if (!A || !Wq || !scales || !biases || !C || M < 1 || Nout < 1 || split_req < 0)
+    if (!A || !Wq || !scales || !biases || !C || M < 1 || Nout < 1 ||
+        (split_req < 0 && split_req != QMM_SPLIT_PLANNED))
         return QMM_EINVAL;
     if (partial_dtype != QMM_PARTIAL_BF16 && partial_dtype != QMM_PARTIAL_F32) return QMM_EINVAL;
     if (pol && !policy_ok(pol)) return QMM_EINVAL;
@@ -339,6 +340,13 @@ int qmm_w4a16_g128(const void* A, const uint32_t* Wq, const void* scales, const 
     if (ceil_div(M, fam.bm) > 65535) return QMM_ESHAPE;
     int rc = check_device();
     if (rc != QMM_OK) return rc;
+    if (split_req == QMM_SPLIT_PLANNED) {
+        const int shape[3] = {M, Kred, Nout};
+        std::vector<int> planned;
+        rc = group_plan_shapes(shape, 1, 0, partial_dtype, &planned);
+        if (rc != QMM_OK) return rc;
+        split_req = planned[0];
+    }
 
     int split = 1;
     rc = qmm::choose_split(M, Kred, Nout, split_req, pol, &split);

@@ -214,6 +214,7 @@ def qmm_set_grouped_schedule(mode: int) -> int:
 
 
 QMM_GROUP_PLAN_CALLS, QMM_GROUP_PLAN_GROUP = 0, 1
+QMM_SPLIT_PLANNED = -1  # split_req of qmm_w4a16_g128: the group plan for the call alone
 
 
 def qmm_set_group_plan(mode: int) -> int:
@@ -429,6 +430,8 @@ def w4a16_matmul(A, Wq, scales, biases, split_req: int = 0, pol=None,
             pol = qmm_policy_preset(QMM_PRESET_GB300, M)
         # the near-equal plan's split bounds the one either partition rule takes
         split = qmm_splitk_plan_near_equal(M, Kred, Nout, pol)
+    elif split_req == QMM_SPLIT_PLANNED:
+        split = qmm_group_plan([(M, Kred, Nout)], 0, partial_dtype)[0]
     else:
         split = split_req
     C = torch.empty((M, Nout), dtype=torch.bfloat16, device=A.device)

@@ -166,6 +166,11 @@ def test_argument_errors_before_any_cuda_work():
     assert call(a, w, s, b, c, 0, 2560, 1024, 0, None, None, 0, 0, None, None) == Q.QMM_EINVAL
     assert call(a, w, s, b, c, 16, 2500, 1024, 0, None, None, 0, 0, None, None) == Q.QMM_ESHAPE
     assert call(a, w, s, b, c, 16, 2560, 1024, 0, None, None, 0, 5, None, None) == Q.QMM_EINVAL
+    # negative split requests other than QMM_SPLIT_PLANNED are rejected
+    assert call(a, w, s, b, c, 16, 2560, 1024, -2, None, None, 0, 0, None, None) == Q.QMM_EINVAL
+    # (a planned split request passes validation and then needs the device)
+    assert call(a, w, s, b, c, 16, 2560, 1024, Q.QMM_SPLIT_PLANNED, None, None, 0, 0, None,
+                None) in (Q.QMM_ENODEV, Q.QMM_EWORKSPACE)
     assert call(P(0x10002), w, s, b, c, 16, 2560, 1024, 0, None, None, 0, 0, None, None) == \
         Q.QMM_EALIGN
     assert call(a, w, P(0x30001), b, c, 16, 2560, 1024, 0, None, None, 0, 0, None, None) == \

@@ -484,6 +484,28 @@ def test_dense_gemm_ragged(family, split):
 
 # ---- error codes with real device buffers ----------------------------------
 
+@pytest.mark.parametrize("name,M", [("down", 2048), ("o", 2048), ("k", 32), ("down", 128)])
+def test_planned_split_request(name, M):
+    """split_req = QMM_SPLIT_PLANNED dispatches the group plan's split for the
+    call alone, with the bits of that split forced."""
+    Kred, Nout = inputs.PROJECTIONS[name]
+    p = inputs.make_w4a16(M, Kred, Nout, seed=7)
+    d = Q.to_device(p)
+    want = Q.qmm_group_plan([(M, Kred, Nout)])[0]
+    C, used = Q.w4a16_matmul(d["A"], d["Wq"], d["scales"], d["biases"],
+                             split_req=Q.QMM_SPLIT_PLANNED)
+    C2, used2 = Q.w4a16_matmul(d["A"], d["Wq"], d["scales"], d["biases"], split_req=want)
+    torch.cuda.synchronize()
+    assert Q.qmm_kernel_status(clear=True) == 0
+    assert used == used2 == want
+    assert np.array_equal(_bits(C), _bits(C2))
+    if M <= 128:  # under-filled calls: the chapter policy's split
+        pol = Q.qmm_policy_preset(Q.QMM_PRESET_GB300, M)
+        assert want == Q.qmm_splitk_plan(M, Kred, Nout, pol)
+    rows, cols = _sample(M, Nout, np.random.default_rng(4))
+    _check_sampled(p, _bits(C), used, Q.QMM_PARTIAL_BF16, rows, cols, "planned split")
+
+
 def test_bounded_wait_runs_out_and_reports():
     """A wait that nothing completes gives up after its limit: the status word
     reports it, nothing traps, and the context stays usable (a matmul right
