@@ -383,13 +383,15 @@ typedef struct {
 size_t qmm_group_workspace_bytes(const qmm_group_call *calls, int n, int partial_dtype);
 
 /* The n calls, each with its policy split under the current partition rule
- * (split_req 0 and the GB300 preset of qmm_w4a16_g128), in few launches:
+ * (split_req 0 and the GB300 preset of qmm_w4a16_g128), or with the group
+ * plan's split under QMM_GROUP_PLAN_GROUP (qmm_set_group_plan), in few launches:
  * the tcgen05 calls of one tile width share one partition launch (up to 16
  * calls per launch), and every split call's planes are added by one reduce
  * launch per 16 split calls.  Calls served by the mma.sync family
  * (qmm_set_kernels) are launched one by one.  The reduce is always the
  * separate kernel (QMM_REDUCE_FUSED does not apply).  Each C is bitwise the C
- * that qmm_w4a16_g128 gives for the call.  The calls must be independent: no
+ * that qmm_w4a16_g128 gives for the call at the same split (its own policy
+ * split by default).  The calls must be independent: no
  * call reads another's C.  splits_used (host, nullable, n ints) receives
  * each call's split.  Returns the codes of qmm_w4a16_g128; every call is
  * checked before anything is launched. */
