@@ -1002,7 +1002,7 @@ def run_reference(args, rank, world):
             "config": {"workload": WORKLOAD, "calls_per_step": 1,
                        "oracle": "plain C, fp64 accumulate, OpenMP"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                             "sample": sample},
+                             "sample": sample, "host": host_description()},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
