@@ -3,7 +3,9 @@
 Only the tests, the smoke check and the bench's CPU-baseline leg use this
 package; the library under ``split_w4a16_quantized_gb300`` never imports it and
 shares no code with it.  The arithmetic lives in ``qmm_oracle.c`` (plain C,
-fp64); this module compiles it with gcc and wraps it with ctypes.
+fp64); this module compiles it with gcc and wraps it with ctypes.  The one
+exception is the group plan (``group_plan``), the grouped call's opt-in split
+rule, which is restated here in plain Python.
 
 Sources the oracle follows (cited per function in the C file):
   * tiny-llm book, "Week 2 Day 7: Split-K Prefill" (Tasks 2-4)
@@ -14,7 +16,12 @@ Sources the oracle follows (cited per function in the C file):
 
 Parity pins: every function here is checked by ``tests/test_oracle.py``
 against values the pages print, closed forms, exact rational brute force on
-tiny shapes and library routines; none is "parity unpinned".
+tiny shapes and library routines; none is "parity unpinned".  The group plan
+is this library's rule, not the pages', so no printed value exists for it.
+Its pins are list-schedule outcomes derived by hand (the wave tail of down at
+M = 2048), agreement with the chapter's independently implemented policy on
+single under-filled calls, and invariants (every kept move lowers the
+estimate; splits stay valid).
 """
 from __future__ import annotations
 
