@@ -303,7 +303,7 @@ def run_gpu(args, rank, world, local_rank):
     device = torch.device("cuda", local_rank)
     torch.cuda.set_device(device)
     Q.qmm_set_kernels({"default": Q.QMM_KERNELS_DEFAULT, "mma": Q.QMM_KERNELS_MMA_SYNC,
-                       "tc": Q.QMM_KERNELS_TCGEN05}[args.kernels])
+                       "tc": Q.QMM_KERNELS_TCGEN05, "lean": Q.QMM_KERNELS_LEAN}[args.kernels])
     # the workload's weights are loaded once and never written by a kernel on
     # the stream, so the library may start weight work before the previous
     # kernel finishes (qmm_set_weights_static); --weights dynamic turns it off
@@ -1022,7 +1022,7 @@ def main():
     ap.add_argument("--weights", choices=["static", "dynamic"], default="static",
                     help="static: promise that no kernel writes the weights during the run "
                          "(qmm_set_weights_static), which lets weight work start early")
-    ap.add_argument("--kernels", choices=["default", "mma", "tc"], default="default",
+    ap.add_argument("--kernels", choices=["default", "mma", "tc", "lean"], default="default",
                     help="kernel table for the W4A16 calls (A/B comparisons)")
     ap.add_argument("--partitions", choices=["equal", "near-equal"], default="equal",
                     help="partition rule of the W4A16 calls (qmm_set_partitions)")

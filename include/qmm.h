@@ -225,15 +225,28 @@ int qmm_tc_pipeline_config(int bm, int gpp, int smem_limit, int *out);
  * the persistent pipeline's synchronization on its real configurations. */
 int qmm_tc_persistent_pipeline_config(int bm, int gpp, int smem_limit, int *out);
 
+/* Whether qmm_w4a16_g128_grouped runs calls with M activation rows in
+ * launches shared with other calls of the same tile width (1: the tcgen05
+ * families) or one launch per call (0: the lean and mma.sync families).  The
+ * group plan (qmm_group_plan) plans only shared launches; a call that runs
+ * alone keeps its single-call policy split.  Follows qmm_set_kernels.
+ * QMM_EINVAL for M < 1.  No counterpart on the pages: a query for tests and
+ * planning tools. */
+int qmm_kernel_grouped(int M);
+
 /* Kernel families used by qmm_w4a16_g128 (process-wide, thread-safe):
  *   QMM_KERNELS_DEFAULT   the tuned table: per M, the family measured fastest
+ *                         (lean kernels up to 16 rows, tcgen05 above)
  *   QMM_KERNELS_MMA_SYNC  register-dequant mma.sync kernels for every M
  *   QMM_KERNELS_TCGEN05   tcgen05 kernels (dequantized weights in tensor
  *                         memory) for every M
+ *   QMM_KERNELS_LEAN      lean kernels (32 weight rows a CTA, mma.sync,
+ *                         weights streamed through per-thread cp.async rings)
+ *                         up to 32 rows, tcgen05 above
  * qmm_kernel_tile and the GB300 policy preset follow the choice.  Returns
  * the previous setting, or QMM_EINVAL for an unknown value.  Meant for A/B
  * measurements and tests; the default needs no call. */
-enum { QMM_KERNELS_DEFAULT = 0, QMM_KERNELS_MMA_SYNC = 1, QMM_KERNELS_TCGEN05 = 2 };
+enum { QMM_KERNELS_DEFAULT = 0, QMM_KERNELS_MMA_SYNC = 1, QMM_KERNELS_TCGEN05 = 2, QMM_KERNELS_LEAN = 3 };
 int qmm_set_kernels(int which);
 
 /* Programmatic dependent launch (on by default): each kernel of the library
@@ -332,21 +345,27 @@ const char *qmm_strerror(int code);
  * other allocator.
  *   - Set-up: the first call on a device looks the buffer's address up with
  *     cudaGetSymbolAddress, with that device current, and caches it. Make
- *     that first call before any stream capture on the device.
+ *     that first call before any stream capture on the device.  The cached
+ *     address does not survive cudaDeviceReset (the module is loaded afresh
+ *     and the buffer may move): do not call this entry point on a device
+ *     after resetting it.
  *   - Limit: a call whose planes (split * M * Nout * 2 bytes for BF16
  *     partials, * 4 for FP32), rounded up to 256 bytes, exceed
  *     qmm_static_scratch_bytes() - 256 - QMM_FUSED_COUNTER_BYTES returns
  *     QMM_EWORKSPACE and launches nothing (the buffer's last bytes hold the
  *     fused reduce's counters, zero from the start).  The split is the policy's
- *     (split_req = 0) or the forced one.  Unsplit calls (split 1) use none
- *     of the buffer.
+ *     (split_req = 0), the group plan's (QMM_SPLIT_PLANNED) or the forced
+ *     one, as in qmm_w4a16_g128, and the limit applies to the split that
+ *     results.  Unsplit calls (split 1) use none of the buffer.
  *   - Races: every call on a device shares the one buffer.  Two calls whose
  *     kernels can overlap on the GPU (different streams without ordering
  *     between them) race on it and give undefined results.  Calls ordered
  *     on one stream are safe.
  *   - Nothing has to start at zero: each call's partition kernel writes
  *     every element of the planes it uses before its reduce reads them.
- * Returns the codes of qmm_w4a16_g128.  QMM_ECUDA also covers a failed
+ * Returns the codes of qmm_w4a16_g128, from the same checks in the same
+ * order (arguments, policy, shape, alignment, device); QMM_EWORKSPACE then
+ * reports planes beyond the buffer, and QMM_ECUDA also covers a failed
  * address lookup. */
 int qmm_w4a16_g128_noalloc(const void *A, const uint32_t *Wq, const void *scales,
                            const void *biases, void *C, int M, int Kred, int Nout, int split_req,

@@ -370,7 +370,7 @@ def group_plan_cost(shapes, tiles, splits, bm, sms, partial_bytes=2):
 
 
 def group_plan(shapes, tiles_of, sms, near_equal=False, partial_bytes=2, cap=16,
-               decode_max_m=8, decode_min_k=512, trace=None):
+               decode_max_m=8, decode_min_k=512, trace=None, own_launch=None):
     """Splits for calls of shapes [(M, Kred, Nout)], where tiles_of(M) gives
     the (bm, bn) tile of the kernel that serves M.  The calls of one tile width
     share a launch.  Per launch, every call starts unsplit.  Then, repeatedly,
@@ -381,7 +381,13 @@ def group_plan(shapes, tiles_of, sms, near_equal=False, partial_bytes=2, cap=16,
     most cap and G, at least decode_min_k reduction elements per partition for
     M <= decode_max_m, and dividing G unless near_equal.  trace, if a list,
     receives (splits, cost) after every kept move, per launch.  (The library
-    also makes no move that takes a launch over 65536 tiles.)"""
+    also makes no move that takes a launch over 65536 tiles.)
+
+    own_launch(M), if given, returns None for a call that shares its tile
+    width's launch, or the policy (bm, bn, target, cap, min_k) of a call that
+    runs in a launch of its own: such a call is not planned with the others
+    and keeps the chapter's single-call split under that policy (the
+    near-equal plan when near_equal)."""
     splits = [1] * len(shapes)
     widths = []
     for M, _, _ in shapes:
@@ -389,6 +395,13 @@ def group_plan(shapes, tiles_of, sms, near_equal=False, partial_bytes=2, cap=16,
             widths.append(tiles_of(M)[0])
     for bm in widths:
         idx = [i for i, (M, _, _) in enumerate(shapes) if tiles_of(M)[0] == bm]
+        if own_launch is not None and own_launch(shapes[idx[0]][0]) is not None:
+            plan = splitk_plan_near_equal if near_equal else splitk_plan
+            for i in idx:
+                M, Kred, Nout = shapes[i]
+                pbm, pbn, target, pcap, min_k = own_launch(M)
+                splits[i] = plan(M, Kred, Nout, pbm, pbn, target, pcap, min_k)
+            continue
         part = [shapes[i] for i in idx]
         tiles = []
         for M, Kred, Nout in part:

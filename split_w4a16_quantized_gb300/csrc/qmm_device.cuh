@@ -69,6 +69,44 @@ __device__ __forceinline__ void dequant_word(uint32_t word, uint32_t ss, uint32_
     }
 }
 
+// Dequantization with one fused multiply-add per pair of weights.
+//
+// A BF16 whose exponent field is zero is subnormal: bits m (7-bit mantissa)
+// stand for m * 2^-133.  A nibble q masked into bits 0..3 of a half is thus
+// the exact value q * 2^-133, and a nibble left in bits 4..7 is q * 2^-129
+// (for q >= 8 bit 7 is the exponent's lowest bit, and the normal number
+// 2^-126 + (q - 8) * 2^-129 is again q * 2^-129: the subnormal range joins
+// the normal one without a gap).  With the scale pre-multiplied by the
+// matching power of two -- an exact exponent shift -- one fused BF16
+// multiply-add gives q * scale + bias with a single rounding, the value the
+// two-step dequant_word forms.
+//
+// The shifted scale is exact only for a normal scale whose exponent leaves
+// room for +133: biased exponent 1..121, i.e. 2^-126 <= |scale| < 2^-5, or a
+// zero scale (left as it is).  scale_subnormal_ok tells which; a group with
+// any other scale takes dequant_word.
+__device__ __forceinline__ bool scale_subnormal_ok(uint16_t s) {
+    const uint32_t e = (s >> 7) & 0xFFu;
+    return (s & 0x7FFFu) == 0 || (e >= 1 && e <= 121);
+}
+// scale * 2^k as BF16 bits replicated in both halves (k = 129 or 133; the
+// scale satisfies scale_subnormal_ok)
+__device__ __forceinline__ uint32_t scale_shifted_pair(uint16_t s, uint32_t k) {
+    const uint32_t v = (s & 0x7FFFu) == 0 ? s : s + (k << 7);
+    return (v & 0xFFFFu) * 0x00010001u;
+}
+// out[i] holds the BF16 pair (w(nibble i), w(nibble i + 4)), i = 0..3, as
+// dequant_word lays them out; s133 / s129 are scale_shifted_pair(scale, 133 /
+// 129), bb the bias pair.
+__device__ __forceinline__ void dequant_word_subnormal(uint32_t word, uint32_t s133, uint32_t s129,
+                                                       uint32_t bb, uint32_t out[4]) {
+    const uint32_t w8 = word >> 8;
+    out[0] = fma_bf16x2(word & 0x000F000Fu, s133, bb);
+    out[1] = fma_bf16x2(word & 0x00F000F0u, s129, bb);
+    out[2] = fma_bf16x2(w8 & 0x000F000Fu, s133, bb);
+    out[3] = fma_bf16x2(w8 & 0x00F000F0u, s129, bb);
+}
+
 // scale and bias BF16 bit patterns replicated into both halves of a pair
 __device__ __forceinline__ uint32_t bf16_pair(uint16_t v) {
     return static_cast<uint32_t>(v) * 0x00010001u;

@@ -20,10 +20,7 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-bool policy_ok(const qmm_policy* p) {
-    return p && p->bm >= 1 && p->bn >= 1 && p->cap >= 1 && p->target_blocks >= 0 &&
-           p->min_k_per_split >= qmm::kGroup && p->min_k_per_split % qmm::kGroup == 0;
-}
+bool policy_ok(const qmm_policy* p) { return qmm::policy_valid(p); }
 
 int device_sms(int* sms) {
     int dev = 0;
@@ -33,14 +30,7 @@ int device_sms(int* sms) {
     return QMM_OK;
 }
 
-int check_device() {
-    int dev = 0, major = 0, minor = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return QMM_ENODEV;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-        return QMM_ENODEV;
-    return (major == 10 && minor == 3) ? QMM_OK : QMM_ENODEV;
-}
+int check_device() { return qmm::device_check(); }
 
 // Launches go through cudaLaunchKernelEx, which reports its own error; the
 // caller's pending CUDA error state is left alone.
@@ -59,7 +49,7 @@ uint32_t* fused_counters(void* workspace, size_t ws_bytes) {
     return reinterpret_cast<uint32_t*>((end - QMM_FUSED_COUNTER_BYTES) & ~static_cast<uintptr_t>(255));
 }
 bool fused_applies(const qmm::Family& f, int M, int Nout, int split) {
-    return qmm::reduce_fused() && f.kind == qmm::kKindTc && split > 1 &&
+    return qmm::reduce_fused() && (f.kind == qmm::kKindTc || f.kind == qmm::kKindLean) && split > 1 &&
            fused_tiles(f, M, Nout) * sizeof(uint32_t) <= QMM_FUSED_COUNTER_BYTES;
 }
 
@@ -98,13 +88,30 @@ const qmm::Family& pick(const qmm::Family (&table)[N], int M) {
 
 namespace qmm {
 
+bool policy_valid(const qmm_policy* p) {
+    return p && p->bm >= 1 && p->bn >= 1 && p->cap >= 1 && p->target_blocks >= 0 &&
+           p->min_k_per_split >= kGroup && p->min_k_per_split % kGroup == 0;
+}
+
+int device_check() {
+    int dev = 0, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return QMM_ENODEV;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return QMM_ENODEV;
+    return (major == 10 && minor == 3) ? QMM_OK : QMM_ENODEV;
+}
+
 const Family& family_for(int M) {
     switch (g_kernels.load(std::memory_order_relaxed)) {
         case QMM_KERNELS_MMA_SYNC: return pick(kMmaFamilies, M);
         case QMM_KERNELS_TCGEN05: return pick(kTcFamilies, M);
+        case QMM_KERNELS_LEAN: return pick(kLeanTable, M);
         default: return pick(kDefaultFamilies, M);
     }
 }
+
+bool family_shares_launch(const Family& f) { return f.kind == kKindTc; }
 
 bool pdl_enabled() { return g_pdl.load(std::memory_order_relaxed) != 0; }
 
@@ -167,7 +174,7 @@ extern "C" {
 
 int qmm_set_kernels(int which) {
     if (which != QMM_KERNELS_DEFAULT && which != QMM_KERNELS_MMA_SYNC &&
-        which != QMM_KERNELS_TCGEN05)
+        which != QMM_KERNELS_TCGEN05 && which != QMM_KERNELS_LEAN)
         return QMM_EINVAL;
     return g_kernels.exchange(which);
 }
@@ -235,6 +242,11 @@ const char* qmm_strerror(int code) {
         case QMM_ENODEV: return "no usable CUDA device (compute capability 10.3 required)";
         default: return "unknown error";
     }
+}
+
+int qmm_kernel_grouped(int M) {
+    if (M < 1) return QMM_EINVAL;
+    return qmm::family_shares_launch(qmm::family_for(M)) ? 1 : 0;
 }
 
 int qmm_kernel_tile(int M, int* bm, int* bn) {
@@ -362,9 +374,9 @@ int qmm_w4a16_g128(const void* A, const uint32_t* Wq, const void* scales, const 
         const int mode = partial_dtype == QMM_PARTIAL_F32 ? qmm::kOutF32 : qmm::kOutBf16;
         if (fused_applies(fam, M, Nout, split)) {
             // one launch: the last CTA of each output tile adds the planes
-            rc = launched(qmm::launch_w4a16_tc(fam.bm, A, Wq, scales, biases, workspace, mode, M,
-                                               Kred, Nout, split, stream, C,
-                                               fused_counters(workspace, ws_bytes)));
+            rc = launched(qmm::launch_w4a16(fam, A, Wq, scales, biases, workspace, mode, M, Kred,
+                                            Nout, split, stream, C,
+                                            fused_counters(workspace, ws_bytes)));
         } else {
             rc = launched(qmm::launch_w4a16(fam, A, Wq, scales, biases, workspace, mode, M, Kred,
                                             Nout, split, stream));
@@ -489,7 +501,10 @@ int group_plan(const std::vector<PlanCall>& calls, int sms, int elem, std::vecto
             }
         std::vector<int> s(part.size(), 1);
         double cost = 0.0;
-        bool fits = plan_cost(part, s, bm, sms, elem, &cost);
+        // calls of a family the grouped call runs one launch each keep their
+        // own policy split, as they would alone
+        const bool shared = qmm::family_shares_launch(qmm::family_for(part[0].M));
+        bool fits = shared && plan_cost(part, s, bm, sms, elem, &cost);
         while (fits) {
             size_t top = 0;
             for (size_t i = 1; i < part.size(); ++i)
@@ -507,7 +522,7 @@ int group_plan(const std::vector<PlanCall>& calls, int sms, int elem, std::vecto
         }
         for (size_t i = 0; i < part.size(); ++i) {
             int split = s[i];
-            if (!fits) {  // too many tiles to plan: the call's own policy split on these SMs
+            if (!fits) {  // own launches, or too many tiles to plan: the call's own policy split
                 qmm_policy pol;
                 int rc = qmm_policy_preset(QMM_PRESET_GB300, part[i].M, sms, &pol);
                 if (rc == QMM_OK)

@@ -15,7 +15,7 @@ constexpr int kGroup = 128;  // quantization group length along the reduction ax
 
 // W4A16 kernel families, picked by the number of activation rows M.
 // BM = activation rows per CTA, BN = weight rows (output columns) per CTA.
-enum KernelKind { kKindMma = 0, kKindTc = 1 };
+enum KernelKind { kKindMma = 0, kKindTc = 1, kKindLean = 2 };
 struct Family {
     int max_m;  // family serves M <= max_m (the last one serves every larger M)
     int bm;
@@ -41,15 +41,43 @@ constexpr Family kTcFamilies[] = {
     {128, 128, 128, kKindTc, 1},
     {1 << 30, 256, 128, kKindTc, 1},
 };
-// The default table: per M, the family that measured fastest on GB300 (the
-// tcgen05 kernels beat the mma.sync ones at every M of the workloads).
+// Lean kernels for few activation rows (qmm_w4a16_lean.cu): 32 weight rows
+// per CTA, mma.sync with register dequant, two CTAs per SM.
+constexpr Family kLeanFamilies[] = {
+    {8, 8, 32, kKindLean, 2},
+    {16, 16, 32, kKindLean, 2},
+    {32, 32, 32, kKindLean, 2},
+};
+// Lean kernels up to 32 rows, tcgen05 above (QMM_KERNELS_LEAN).
+constexpr Family kLeanTable[] = {
+    {8, 8, 32, kKindLean, 2},
+    {16, 16, 32, kKindLean, 2},
+    {32, 32, 32, kKindLean, 2},
+    {64, 64, 128, kKindTc, 1},
+    {128, 128, 128, kKindTc, 1},
+    {1 << 30, 256, 128, kKindTc, 1},
+};
+// The default table: per M, the family that measured fastest on GB300 over
+// the workload's shapes: the lean kernels up to 16 rows, the tcgen05 ones
+// from 32 rows (where the legacy MMA rate starts to bound the lean kernel).
 constexpr Family kDefaultFamilies[] = {
-    {16, 16, 128, kKindTc, 1},
+    {8, 8, 32, kKindLean, 2},
+    {16, 16, 32, kKindLean, 2},
     {32, 32, 128, kKindTc, 1},
     {64, 64, 128, kKindTc, 1},
     {128, 128, 128, kKindTc, 1},
     {1 << 30, 256, 128, kKindTc, 1},
 };
+
+// A policy the plan accepts (bm, bn, cap >= 1, target >= 0, min_k a
+// multiple of 128).
+bool policy_valid(const qmm_policy* p);
+// QMM_OK if the current device is a compute capability 10.3 GPU, else QMM_ENODEV.
+int device_check();
+
+// True if qmm_w4a16_g128_grouped runs the calls of this family in shared
+// launches (the tcgen05 families); the others run one launch per call.
+bool family_shares_launch(const Family& f);
 
 // Process-wide choice of table (qmm_set_kernels); returns the family for M.
 const Family& family_for(int M);
@@ -97,9 +125,16 @@ enum OutMode { kOutBf16 = 0, kOutF32 = 1 };
 
 // Kernel launchers (qmm_w4a16.cu, qmm_reduce.cu, qmm_gemm.cu).  They assume
 // validated arguments and return the cudaError_t of the launch as int.
+// fused_C / counters (tcgen05 and lean families, split > 1): the last CTA of
+// each output tile adds the planes into fused_C.
 int launch_w4a16(const Family& fam, const void* A, const uint32_t* Wq, const void* scales,
                  const void* biases, void* out, int out_mode, int M, int Kred, int Nout,
-                 int split, void* stream);
+                 int split, void* stream, void* fused_C = nullptr, uint32_t* counters = nullptr);
+int launch_w4a16_lean(int bm, const void* A, const uint32_t* Wq, const void* scales,
+                      const void* biases, void* out, int out_mode, int M, int Kred, int Nout,
+                      int split, void* stream, void* fused_C = nullptr,
+                      uint32_t* counters = nullptr);
+
 int launch_w4a16_tc(int bm, const void* A, const uint32_t* Wq, const void* scales, const void* biases,
                     void* out, int out_mode, int M, int Kred, int Nout, int split, void* stream,
                     void* fused_C = nullptr, uint32_t* counters = nullptr);

@@ -28,7 +28,11 @@ constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
 void* g_scratch_addr[kMaxDevices] = {};
 
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
 // Device address of g_static_scratch on the current device, or null on error.
+// The address is looked up once per device and kept: after cudaDeviceReset the
+// module is loaded afresh and the kept address is no longer valid.
 void* scratch_on_current_device() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
@@ -52,13 +56,27 @@ int qmm_w4a16_g128_noalloc(const void* A, const uint32_t* Wq, const void* scales
                            const void* biases, void* C, int M, int Kred, int Nout, int split_req,
                            const qmm_policy* pol, int partial_dtype, void* stream,
                            int* split_used) {
-    if (!A || !Wq || !scales || !biases || !C || M < 1 || Nout < 1 || split_req < 0)
+    // the checks of qmm_w4a16_g128, in its order, so both return the same codes
+    if (!A || !Wq || !scales || !biases || !C || M < 1 || Nout < 1 ||
+        (split_req < 0 && split_req != QMM_SPLIT_PLANNED))
         return QMM_EINVAL;
     if (partial_dtype != QMM_PARTIAL_BF16 && partial_dtype != QMM_PARTIAL_F32) return QMM_EINVAL;
+    if (pol && !qmm::policy_valid(pol)) return QMM_EINVAL;
     if (Kred < 128 || Kred % 128) return QMM_ESHAPE;
+    if (!qmm::aligned16(A) || !qmm::aligned16(Wq) || !qmm::aligned16(C) || !qmm::aligned16(scales) ||
+        !qmm::aligned16(biases))
+        return QMM_EALIGN;
+    int rc = qmm::device_check();
+    if (rc != QMM_OK) return rc;
+    if (split_req == QMM_SPLIT_PLANNED) {
+        // the group plan's split for this call alone, as qmm_w4a16_g128 takes it
+        const int shape[3] = {M, Kred, Nout};
+        rc = qmm_group_plan(shape, 1, 0, partial_dtype, &split_req);
+        if (rc != QMM_OK) return rc;
+    }
     // the split this call will use, to size its partial planes
     int split = 1;
-    const int rc = qmm::choose_split(M, Kred, Nout, split_req, pol, &split);
+    rc = qmm::choose_split(M, Kred, Nout, split_req, pol, &split);
     if (rc != QMM_OK) return rc;
     // the last QMM_FUSED_COUNTER_BYTES (and 256 bytes of slack) are kept for
     // the fused reduce's counters in every mode, so no planes ever land there
@@ -70,7 +88,7 @@ int qmm_w4a16_g128_noalloc(const void* A, const uint32_t* Wq, const void* scales
         return QMM_EWORKSPACE;
     void* scratch = qmm::scratch_on_current_device();
     if (!scratch) return QMM_ECUDA;
-    return qmm_w4a16_g128(A, Wq, scales, biases, C, M, Kred, Nout, split, nullptr, scratch,
+    return qmm_w4a16_g128(A, Wq, scales, biases, C, M, Kred, Nout, split, pol, scratch,
                           qmm::kStaticScratchBytes, partial_dtype, stream, split_used);
 }
 

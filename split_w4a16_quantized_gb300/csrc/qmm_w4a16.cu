@@ -266,40 +266,58 @@ __global__ void __launch_bounds__(C::THREADS) w4a16_kernel(const W4Params p) {
 }
 
 // Probe kernels: one warp per (16 weight rows, one group).  Lane (g8, t4)
-// loads and dequantizes exactly the words the matmul kernel gives it and
-// writes every value back at the k it stands for.
+// loads exactly the words the matmul kernels give it and writes every value
+// back at the k it stands for.  The dequant probe takes the path the lean
+// kernel takes for each scale (dequant_word_subnormal where the scale allows
+// it, dequant_word otherwise).  The unpack probe forms each q twice, through
+// dequant_word with scale 1 and bias 0 and through dequant_word_subnormal
+// with scale 2^-10 (q * 2^-10 is exact), and writes 0xFF where they differ.
 __global__ void probe_kernel(const uint32_t* __restrict__ Wq, const uint16_t* __restrict__ scales,
                              const uint16_t* __restrict__ biases, int Nout, int Kred,
                              uint8_t* __restrict__ q_out, __nv_bfloat16* __restrict__ w_out) {
     const int lane = threadIdx.x & 31, g8 = lane >> 2, t4 = lane & 3;
     const int grp = blockIdx.y, G = Kred / kGroup;
     const size_t wrow = static_cast<size_t>(Kred) / 8;
+    constexpr uint16_t kTwoPowMinus10 = 0x3A80;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         const int n = blockIdx.x * 16 + g8 + 8 * h;
         if (n >= Nout) continue;
         const uint4 wv = *reinterpret_cast<const uint4*>(Wq + n * wrow + grp * 16 + t4 * 4);
-        uint32_t ss = kBf16x2One, bb = 0;
+        uint16_t s = 0, b = 0;
         if (w_out) {
-            ss = bf16_pair(scales[static_cast<size_t>(n) * G + grp]);
-            bb = bf16_pair(biases[static_cast<size_t>(n) * G + grp]);
+            s = scales[static_cast<size_t>(n) * G + grp];
+            b = biases[static_cast<size_t>(n) * G + grp];
         }
         const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
-            uint32_t w[4];
-            dequant_word(words[jj], ss, bb, w);
+            uint32_t w[4], u[4];
+            if (w_out) {
+                if (scale_subnormal_ok(s))
+                    dequant_word_subnormal(words[jj], scale_shifted_pair(s, 133),
+                                           scale_shifted_pair(s, 129), bf16_pair(b), w);
+                else
+                    dequant_word(words[jj], bf16_pair(s), bf16_pair(b), w);
+            } else {
+                dequant_word(words[jj], kBf16x2One, 0, w);
+                dequant_word_subnormal(words[jj], scale_shifted_pair(kTwoPowMinus10, 133),
+                                       scale_shifted_pair(kTwoPowMinus10, 129), 0, u);
+            }
             const size_t k0 = static_cast<size_t>(n) * Kred + grp * kGroup + 32 * t4 + 8 * jj;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const uint16_t lo = static_cast<uint16_t>(w[i] & 0xFFFFu);
-                const uint16_t hi = static_cast<uint16_t>(w[i] >> 16);
-                if (w_out) {
-                    w_out[k0 + i] = __ushort_as_bfloat16(lo);
-                    w_out[k0 + i + 4] = __ushort_as_bfloat16(hi);
-                } else {
-                    q_out[k0 + i] = static_cast<uint8_t>(__bfloat162float(__ushort_as_bfloat16(lo)));
-                    q_out[k0 + i + 4] = static_cast<uint8_t>(__bfloat162float(__ushort_as_bfloat16(hi)));
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {  // e = 0: nibble i, e = 1: nibble i + 4
+                    const uint16_t bits = static_cast<uint16_t>(w[i] >> (16 * e));
+                    if (w_out) {
+                        w_out[k0 + i + 4 * e] = __ushort_as_bfloat16(bits);
+                    } else {
+                        const float q1 = __bfloat162float(__ushort_as_bfloat16(bits));
+                        const float q2 = __bfloat162float(__ushort_as_bfloat16(
+                                             static_cast<uint16_t>(u[i] >> (16 * e)))) * 1024.0f;
+                        q_out[k0 + i + 4 * e] = q1 == q2 ? static_cast<uint8_t>(q1) : 0xFFu;
+                    }
                 }
             }
         }
@@ -339,9 +357,14 @@ static_assert(Fam3::BM == kMmaFamilies[3].bm && Fam3::BN == kMmaFamilies[3].bn, 
 
 int launch_w4a16(const Family& fam, const void* A, const uint32_t* Wq, const void* scales,
                  const void* biases, void* out, int out_mode, int M, int Kred, int Nout,
-                 int split, void* stream) {
+                 int split, void* stream, void* fused_C, uint32_t* counters) {
     if (fam.kind == kKindTc)
-        return launch_w4a16_tc(fam.bm, A, Wq, scales, biases, out, out_mode, M, Kred, Nout, split, stream);
+        return launch_w4a16_tc(fam.bm, A, Wq, scales, biases, out, out_mode, M, Kred, Nout, split,
+                               stream, fused_C, counters);
+    if (fam.kind == kKindLean)
+        return launch_w4a16_lean(fam.bm, A, Wq, scales, biases, out, out_mode, M, Kred, Nout,
+                                 split, stream, fused_C, counters);
+    if (fused_C) return cudaErrorInvalidValue;
     W4Params p;
     p.A = static_cast<const uint16_t*>(A);
     p.Wq = Wq;

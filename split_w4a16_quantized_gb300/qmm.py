@@ -22,7 +22,7 @@ QMM_OK, QMM_EINVAL, QMM_ESHAPE, QMM_EWORKSPACE, QMM_ECUDA, QMM_EALIGN, QMM_ENODE
     0, -1, -2, -3, -4, -5, -6
 QMM_PARTIAL_BF16, QMM_PARTIAL_F32 = 0, 1
 QMM_PRESET_PAGES, QMM_PRESET_GB300 = 0, 1
-QMM_KERNELS_DEFAULT, QMM_KERNELS_MMA_SYNC, QMM_KERNELS_TCGEN05 = 0, 1, 2
+QMM_KERNELS_DEFAULT, QMM_KERNELS_MMA_SYNC, QMM_KERNELS_TCGEN05, QMM_KERNELS_LEAN = 0, 1, 2, 3
 
 
 class qmm_policy(ctypes.Structure):
@@ -65,6 +65,7 @@ _P, _I, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
 _SIGS = {
     "qmm_policy_preset": (_I, [_I, _I, _I, ctypes.POINTER(qmm_policy)]),
     "qmm_kernel_tile": (_I, [_I, ctypes.POINTER(_I), ctypes.POINTER(_I)]),
+    "qmm_kernel_grouped": (_I, [_I]),
     "qmm_splitk_plan": (_I, [_I, _I, _I, ctypes.POINTER(qmm_policy), ctypes.POINTER(_I)]),
     "qmm_splitk_plan_near_equal": (_I, [_I, _I, _I, ctypes.POINTER(qmm_policy),
                                         ctypes.POINTER(_I)]),
@@ -255,6 +256,14 @@ def qmm_kernel_tile(M: int):
     bm, bn = _I(0), _I(0)
     _check(lib().qmm_kernel_tile(M, ctypes.byref(bm), ctypes.byref(bn)), "qmm_kernel_tile")
     return bm.value, bn.value
+
+
+def qmm_kernel_grouped(M: int) -> bool:
+    """True if the grouped call runs calls with M rows in shared launches."""
+    rc = lib().qmm_kernel_grouped(M)
+    if rc < 0:
+        _check(rc, "qmm_kernel_grouped")
+    return rc == 1
 
 
 def qmm_splitk_plan(M: int, Kred: int, Nout: int, pol: qmm_policy) -> int:

@@ -8,6 +8,7 @@ import re
 
 import numpy as np
 import pytest
+import torch
 
 import oracle
 from split_w4a16_quantized_gb300 import build, inputs
@@ -181,6 +182,35 @@ def test_argument_errors_before_any_cuda_work():
     assert lib.qmm_gemm_bf16_splitk(a, w, c, 512, 512, 1024, 17, None, 0, None) == Q.QMM_ESHAPE
 
 
+def test_noalloc_checks_match_the_main_entry_point():
+    # fake, never-dereferenced addresses: the allocation-free call runs the
+    # checks of qmm_w4a16_g128 in the same order and returns the same codes
+    lib = Q.lib()
+    P = ctypes.c_void_p
+    a, w, s, b, c = P(0x10000), P(0x20000), P(0x30000), P(0x40000), P(0x50000)
+    bad = Q.qmm_policy(0, 32, 152, 16, 128)  # bm < 1
+    main = lambda A, M, split, pol: lib.qmm_w4a16_g128(A, w, s, b, c, M, 2560, 1024, split, pol,
+                                                       None, 0, 0, None, None)
+    noalloc = lambda A, M, split, pol: lib.qmm_w4a16_g128_noalloc(A, w, s, b, c, M, 2560, 1024,
+                                                                  split, pol, 0, None, None)
+    cases = [
+        (a, 16, 2, ctypes.byref(bad)),         # invalid policy with a forced split
+        (a, 16, 0, ctypes.byref(bad)),         # invalid policy with the policy split
+        (a, 16, -2, None),                     # negative request other than QMM_SPLIT_PLANNED
+        (P(0x10002), 2048, 20, None),          # misaligned A, planes far beyond the buffer
+        (P(0x10002), 16, Q.QMM_SPLIT_PLANNED, None),
+    ]
+    for A, M, split, pol in cases:
+        assert noalloc(A, M, split, pol) == main(A, M, split, pol), (M, split)
+    assert noalloc(a, 16, 2, ctypes.byref(bad)) == Q.QMM_EINVAL
+    assert noalloc(P(0x10002), 2048, 20, None) == Q.QMM_EALIGN
+    # valid arguments without a usable device: no device, before the limit
+    # check and the address lookup
+    if not torch.cuda.is_available():
+        assert noalloc(a, 2048, 20, None) == Q.QMM_ENODEV
+        assert noalloc(a, 16, Q.QMM_SPLIT_PLANNED, None) == Q.QMM_ENODEV
+
+
 def test_overlap_schedule_bit_exact_against_oracle():
     rng = np.random.default_rng(26)
     for _ in range(2000):
@@ -351,8 +381,11 @@ def test_group_plan_bit_exact_against_the_oracle():
             sms = (152, 132, 108)[k % 3]
             Q.qmm_set_partitions(Q.QMM_PARTITIONS_NEAR_EQUAL if near else Q.QMM_PARTITIONS_EQUAL)
             got = Q.qmm_group_plan(shapes, sms, dt)
+            own = lambda M: None if Q.qmm_kernel_grouped(M) else \
+                Q.qmm_policy_preset(Q.QMM_PRESET_GB300, M, sms).as_tuple()
             want = oracle.group_plan(shapes, tiles, sms, near_equal=near,
-                                     partial_bytes=4 if dt == Q.QMM_PARTIAL_F32 else 2)
+                                     partial_bytes=4 if dt == Q.QMM_PARTIAL_F32 else 2,
+                                     own_launch=own)
             assert got == want, (k, shapes, got, want)
     finally:
         Q.qmm_set_partitions(prev)
@@ -387,5 +420,7 @@ def test_group_plan_falls_back_to_the_policy_on_huge_launches():
     # none is made
     assert Q.qmm_group_plan([(16384, 2560, 16384)] * 8, 152) == [1] * 8
     # a call of another tile width is planned in its own launch: k at M = 16
-    # beside them splits as it would alone (the chapter policy's 10)
-    assert Q.qmm_group_plan([(16384, 2560, 16384)] * 8 + [(16, 2560, 1024)], 152) == [1] * 8 + [10]
+    # beside them splits as it would alone (the chapter policy's split)
+    alone = Q.qmm_group_plan([(16, 2560, 1024)], 152)
+    assert alone[0] > 1
+    assert Q.qmm_group_plan([(16384, 2560, 16384)] * 8 + [(16, 2560, 1024)], 152) == [1] * 8 + alone

@@ -683,3 +683,20 @@ def test_group_plan_invariants():
     # ties between equally long calls go to the lower index
     assert oracle.group_plan([(32, 2560, 1024), (32, 2560, 1024)], _tc_tiles, 152)[0] >= \
         oracle.group_plan([(32, 2560, 1024), (32, 2560, 1024)], _tc_tiles, 152)[1]
+
+
+def test_group_plan_own_launch_keeps_the_single_call_split():
+    # A call that runs in a launch of its own is not planned with the others:
+    # it keeps the chapter's occupancy split under its own policy, whatever
+    # the calls beside it, and the shared launch is planned as if it were
+    # absent.
+    lean = (16, 64, 304, 16, 128)
+    own = lambda M: lean if M <= 32 else None
+    shapes = [(16, 2560, 1024), (16, 9728, 2560), (128, 2560, 1024), (128, 9728, 2560)]
+    s = oracle.group_plan(shapes, _tc_tiles, 152, own_launch=own)
+    assert s[0] == oracle.splitk_plan(16, 2560, 1024, *lean) == 10
+    assert s[1] == oracle.splitk_plan(16, 9728, 2560, *lean) == 4
+    assert s[2:] == oracle.group_plan(shapes[2:], _tc_tiles, 152)
+    ne = oracle.group_plan(shapes[:2], _tc_tiles, 152, near_equal=True, own_launch=own)
+    assert ne == [oracle.splitk_plan_near_equal(16, 2560, 1024, *lean),
+                  oracle.splitk_plan_near_equal(16, 9728, 2560, *lean)]

@@ -37,10 +37,10 @@ def built():
 
 
 KERNELS = {"default": Q.QMM_KERNELS_DEFAULT, "mma": Q.QMM_KERNELS_MMA_SYNC,
-           "tc": Q.QMM_KERNELS_TCGEN05}
+           "tc": Q.QMM_KERNELS_TCGEN05, "lean": Q.QMM_KERNELS_LEAN}
 
 
-@pytest.fixture(params=["mma", "tc"])
+@pytest.fixture(params=["mma", "tc", "lean"])
 def family(request):
     """Run the test once per kernel family table; check the status word after."""
     prev = Q.qmm_set_kernels(KERNELS[request.param])
@@ -168,6 +168,49 @@ def test_dequant_probe_bit_exact(Nout, Kred):
     Q.qmm_dequant_probe(d["Wq"], d["scales"], d["biases"], Kred, w)
     torch.cuda.synchronize()
     assert np.array_equal(_bits(w), oracle.dequant(p["Wq"], p["scales"], p["biases"], Kred))
+
+
+def _mixed_scales(Nout, G, rng):
+    """BF16 scale and bias bits spanning both dequant paths: magnitudes from
+    2^-12 to 2^-1 (the subnormal-nibble path serves |scale| < 2^-5), both
+    signs, exact zeros, and the two exponents on either side of the switch
+    (largest below 2^-5 and 2^-5 itself)."""
+    mag = 2.0 ** rng.uniform(-12, -1, (Nout, G))
+    sgn = np.where(rng.random((Nout, G)) < 0.2, -1.0, 1.0)
+    sc = inputs.f32_to_bf16_bits((mag * sgn).astype(np.float32))
+    sc[rng.random((Nout, G)) < 0.05] = 0
+    sc[0, 0], sc[1 % Nout, 0] = 0x3CFF, 0x3D00  # 0.0311 (last fast) and 2^-5 (first slow)
+    bias = inputs.f32_to_bf16_bits((rng.normal(0, 0.05, (Nout, G))).astype(np.float32))
+    return sc, bias
+
+
+@pytest.mark.parametrize("Nout,Kred", [(1000, 2560), (37, 256)])
+def test_dequant_probe_both_paths_bit_exact(Nout, Kred):
+    rng = np.random.default_rng(33)
+    p = inputs.make_w4a16(1, Kred, Nout, seed=33)
+    p["scales"], p["biases"] = _mixed_scales(Nout, Kred // 128, rng)
+    d = Q.to_device(p)
+    w = torch.empty((Nout, Kred), dtype=torch.bfloat16, device="cuda")
+    Q.qmm_dequant_probe(d["Wq"], d["scales"], d["biases"], Kred, w)
+    torch.cuda.synchronize()
+    assert np.array_equal(_bits(w), oracle.dequant(p["Wq"], p["scales"], p["biases"], Kred))
+
+
+@pytest.mark.parametrize("M", [1, 8, 16, 32, 64])
+def test_mixed_scale_ranges_against_oracle(family, M):
+    """Whole calls whose groups mix scales on both sides of the
+    subnormal-nibble limit: a warp takes the two-step dequant for a group as
+    soon as one of its rows needs it, so every mix appears."""
+    rng = np.random.default_rng(34 + M)
+    Kred, Nout = 1280, 200
+    p = inputs.make_w4a16(M, Kred, Nout, seed=34 + M)
+    p["scales"], p["biases"] = _mixed_scales(Nout, Kred // 128, rng)
+    d = Q.to_device(p)
+    C64 = oracle.qmm(p["A"], p["Wq"], p["scales"], p["biases"])
+    for split_req in (1, 2, 5):
+        for dt in (Q.QMM_PARTIAL_BF16, Q.QMM_PARTIAL_F32):
+            got, s = _run(d, M, Nout, split_req, partial_dtype=dt)
+            _check_full(p, got, s, dt, C64, "M=%d req=%d dt=%d" % (M, split_req, dt))
 
 
 # ---- the K-projection at M = 16 (policy vs unsplit) ------------------------
@@ -559,19 +602,23 @@ def _call_with(d, M, Nout, split, dt, ws):
 
 
 @pytest.mark.parametrize("name,M,split", [("k", 16, 10), ("gate", 32, 2), ("down", 128, 4),
-                                          ("ragged", 33, 10), ("odd", 5, 2), ("k", 300, 4)])
+                                          ("ragged", 33, 10), ("odd", 5, 2), ("k", 300, 4),
+                                          ("down", 8, 4), ("ragged", 16, 5), ("o", 1, 8)])
 @pytest.mark.parametrize("dt", [Q.QMM_PARTIAL_BF16, Q.QMM_PARTIAL_F32])
-def test_fused_reduce_bitwise_equals_kernel_reduce(name, M, split, dt):
+@pytest.mark.parametrize("kernels", ["tc", "lean"])
+def test_fused_reduce_bitwise_equals_kernel_reduce(name, M, split, dt, kernels):
     """QMM_REDUCE_FUSED adds the planes in the partition kernel's last CTA of
     each tile: same planes, same FP32 ascending sum, so the same bits as the
-    separate reduce.  Three calls on one workspace also check that every call
-    leaves the tile counters at zero."""
+    separate reduce, and within the chapter's tolerance of the oracle.  Three
+    calls on one workspace also check that every call leaves the tile
+    counters at zero."""
     if name == "odd":
         Kred, Nout = 256, 77          # scalar path of the fused reduce
     else:
         Kred, Nout = inputs.RAGGED if name == "ragged" else inputs.PROJECTIONS[name]
-    d = Q.to_device(inputs.make_w4a16(M, Kred, Nout, seed=90 + M))
-    prev_k = Q.qmm_set_kernels(Q.QMM_KERNELS_TCGEN05)
+    p = inputs.make_w4a16(M, Kred, Nout, seed=90 + M)
+    d = Q.to_device(p)
+    prev_k = Q.qmm_set_kernels(KERNELS[kernels])
     try:
         prev = Q.qmm_set_reduce(Q.QMM_REDUCE_KERNEL)
         nb = Q.qmm_splitk_workspace_bytes(M, Nout, split, dt)
@@ -585,6 +632,8 @@ def test_fused_reduce_bitwise_equals_kernel_reduce(name, M, split, dt):
             got = _call_with(d, M, Nout, split, dt, ws)
             assert np.array_equal(got, ref)
         assert Q.qmm_kernel_status(clear=True) == 0
+        C64 = oracle.qmm(p["A"], p["Wq"], p["scales"], p["biases"])
+        _check_full(p, got, split, dt, C64, "fused %s M=%d s=%d" % (name, M, split))
     finally:
         Q.qmm_set_reduce(prev)
         Q.qmm_set_kernels(prev_k)

@@ -104,3 +104,20 @@ def test_planes_beyond_the_buffer_are_refused(Q):
     with pytest.raises(Q.QmmError) as e:
         Q.qmm_w4a16_g128_noalloc(d["A"], d["Wq"], d["scales"], d["biases"], C, split_req=3)
     assert e.value.code == Q.QMM_ESHAPE
+
+
+def test_planned_split_matches_workspace_path(Q):
+    # QMM_SPLIT_PLANNED resolves to the group plan's split for the call alone,
+    # as qmm_w4a16_g128 resolves it; the planes then go to the fixed buffer
+    d = _problem(Q, 128, 9728, 2560, seed=15)
+    C = torch.full((128, 2560), float("nan"), dtype=torch.bfloat16, device=d["A"].device)
+    used = Q.qmm_w4a16_g128_noalloc(d["A"], d["Wq"], d["scales"], d["biases"], C,
+                                    split_req=Q.QMM_SPLIT_PLANNED)
+    nbytes = Q.qmm_splitk_workspace_bytes(128, 2560, max(used, 1), Q.QMM_PARTIAL_BF16)
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=d["A"].device)
+    R = torch.empty_like(C)
+    ref = Q.qmm_w4a16_g128(d["A"], d["Wq"], d["scales"], d["biases"], R,
+                           split_req=Q.QMM_SPLIT_PLANNED, workspace=ws)
+    torch.cuda.synchronize()
+    assert used == ref == Q.qmm_group_plan([(128, 9728, 2560)])[0]
+    np.testing.assert_array_equal(_bits(C), _bits(R))
