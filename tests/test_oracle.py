@@ -205,6 +205,38 @@ def test_partition_boundaries_follow_groups():
         assert nonzero == [i == g // (G // s) for i in range(s)]
 
 
+def plane_sum_case():
+    """M = 1, Nout = 1, Kred = 384, split 3: partition p holds one group whose
+    only nonzero product is A[0, 128p] * w[0, 128p] = v_p, with
+    (v_0, v_1, v_2) = (1, 2^-8, 2^-30), all exact in BF16.  The chapter's
+    reduce adds the planes in FP32 in ascending order: 1 + 2^-8 is exact, and
+    adding 2^-30 (below half an FP32 ulp of 1) leaves it there; 1 + 2^-8 is the
+    midpoint between the BF16 neighbours 1 and 1 + 2^-7, and round-to-even
+    gives 1.  The exact sum lies above that midpoint and rounds to 1 + 2^-7."""
+    A = np.zeros((1, 384), np.uint16)
+    A[0, [0, 128, 256]] = 0x3F80
+    q = np.zeros((1, 384), np.uint8)
+    q[0, [0, 128, 256]] = 1
+    scales = np.array([[0x3F80, 0x3B80, 0x3080]], np.uint16)  # 1, 2^-8, 2^-30
+    return {"A": A, "Wq": inputs.pack_nibbles(q), "scales": scales,
+            "biases": np.zeros((1, 3), np.uint16)}
+
+
+def test_partitioned_planes_are_added_in_fp32():
+    p = plane_sum_case()
+    C, planes = oracle.qmm_partitioned(p["A"], p["Wq"], p["scales"], p["biases"], 3, 0,
+                                       with_partials=True)
+    assert planes[:, 0, 0].tolist() == [1.0, 2.0 ** -8, 2.0 ** -30]
+    assert int(C[0, 0]) == 0x3F80  # FP32 ascending sum, one BF16 rounding: 1
+    # the fp64 result of the same planes rounds the other way
+    C64 = oracle.qmm(p["A"], p["Wq"], p["scales"], p["biases"])
+    assert C64[0, 0] == 1 + 2.0 ** -8 + 2.0 ** -30
+    assert int(oracle.bf16_round(C64)[0, 0]) == 0x3F81
+    # FP32 planes (partial_mode 1) take the same sum
+    C32, _ = oracle.qmm_partitioned(p["A"], p["Wq"], p["scales"], p["biases"], 3, 1)
+    assert int(C32[0, 0]) == 0x3F80
+
+
 def test_partitioned_error_bound():
     p = inputs.make_w4a16(8, 2560, 64, seed=11)
     C64 = oracle.qmm(p["A"], p["Wq"], p["scales"], p["biases"], threads=2)

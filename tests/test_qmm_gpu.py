@@ -318,6 +318,59 @@ def test_projection_full_size_sampled(name, M):
     assert np.all(np.abs(a - b) <= 0.25 * np.maximum(1.0, np.abs(b))), "split vs unsplit (max)"
 
 
+CENSUS = [("k", 16)] + [(n, M) for M in (32, 128) for n in inputs.PROJECTIONS] + \
+    [(n, M) for M in (1, 4, 8) for n in ("k", "o", "down")]
+
+
+@pytest.mark.parametrize("name,M", CENSUS)
+def test_plain_bar_census(name, M):
+    """The plain bar |C_gpu - C64| <= 0.02 * max(1, |C64|) on the config inputs
+    (seed 0) at the policy split.  With BF16 partial planes the chapter's own
+    arithmetic misses it where the planes are much larger than C (one BF16
+    rounding of a plane of magnitude 8 is 2^-6 already): the oracle's partition
+    emulation misses it there too.  So: wherever the emulation meets the bar
+    with room for the GPU's one-ulp plane differences, the GPU meets it; every
+    element the GPU leaves outside is one the method itself leaves outside
+    (within that room); and the whole output meets the emulation bar."""
+    Kred, Nout = inputs.PROJECTIONS[name]
+    p = inputs.make_w4a16(M, Kred, Nout, seed=0)
+    got, s = _run(Q.to_device(p), M, Nout, 0)
+    C64 = oracle.qmm(p["A"], p["Wq"], p["scales"], p["biases"])
+    if s == 1:
+        _assert_close(got, C64, TOL_F32, "%s M=%d unsplit" % (name, M))
+        return
+    lim = TOL_BF16 * np.maximum(1.0, np.abs(C64))
+    gerr = np.abs(_val(got) - C64)
+    emu, planes = oracle.qmm_partitioned(p["A"], p["Wq"], p["scales"], p["biases"], s, 0,
+                                         with_partials=True)
+    eerr = np.abs(_val(emu) - C64)
+    room = _ulp_bf16(planes).sum(axis=0) + _ulp_bf16(C64)
+    sure = eerr + room <= lim
+    assert np.all(gerr[sure] <= lim[sure]), "plain bar missed where the method meets it"
+    out = gerr > lim
+    assert np.all(eerr[out] + room[out] > lim[out]), "a miss the method does not share"
+    # the census itself (elements outside the plain bar): GPU against emulation
+    assert abs(int(out.sum()) - int((eerr > lim).sum())) <= max(2, int(0.02 * (eerr > lim).sum()))
+    _check_full(p, got, s, Q.QMM_PARTIAL_BF16, C64, "%s M=%d s=%d" % (name, M, s))
+
+
+@pytest.mark.parametrize("name,M,req", [("gate", 2048, 0), ("down", 2048, Q.QMM_SPLIT_PLANNED),
+                                        ("down", 128, 0)])
+def test_full_size_every_element(name, M, req):
+    """Every output element at full size against the oracle: the fall-back
+    shape (gate, M = 2048, unsplit), down at M = 2048 at the group plan's
+    split, and down at M = 128 at the policy's split."""
+    Kred, Nout = inputs.PROJECTIONS[name]
+    p = inputs.make_w4a16(M, Kred, Nout, seed=3)
+    d = Q.to_device(p)
+    s_want = Q.qmm_group_plan([(M, Kred, Nout)])[0] if req else 0
+    got, s = _run(d, M, Nout, req if not req else s_want)
+    C64 = oracle.qmm(p["A"], p["Wq"], p["scales"], p["biases"])
+    _check_full(p, got, s, Q.QMM_PARTIAL_BF16, C64, "%s M=%d s=%d" % (name, M, s))
+    if name == "gate":
+        assert s == 1
+
+
 def test_fallback_shape_runs_the_unsplit_kernel_exactly():
     # base grid already fills the target: the policy must pick split 1 and the
     # result must be bit-identical to the unsplit control
@@ -385,6 +438,33 @@ def _partition(d, M, Nout, split, dt):
     Q.qmm_w4a16_g128_partition(d["A"], d["Wq"], d["scales"], d["biases"], planes, split, dt)
     torch.cuda.synchronize()
     return planes
+
+
+def test_plane_sum_rounds_as_the_fp32_reduce(family):
+    """Planes 1, 2^-8 and 2^-30 (one group each): the chapter's FP32 ascending
+    sum ties at 1 + 2^-8 and rounds to 1, where the exact sum would round to
+    1 + 2^-7 (the oracle case of the same name), for the separate reduce and
+    the fused one."""
+    A = np.zeros((1, 384), np.uint16)
+    A[0, [0, 128, 256]] = 0x3F80
+    q = np.zeros((1, 384), np.uint8)
+    q[0, [0, 128, 256]] = 1
+    p = {"A": A, "Wq": inputs.pack_nibbles(q),
+         "scales": np.array([[0x3F80, 0x3B80, 0x3080]], np.uint16),
+         "biases": np.zeros((1, 3), np.uint16)}
+    want, _ = oracle.qmm_partitioned(p["A"], p["Wq"], p["scales"], p["biases"], 3, 0)
+    assert int(want[0, 0]) == 0x3F80
+    d = Q.to_device(p)
+    got, s = _run(d, 1, 1, 3)
+    assert s == 3 and int(got[0, 0]) == 0x3F80
+    prev = Q.qmm_set_reduce(Q.QMM_REDUCE_FUSED)
+    try:
+        nb = Q.qmm_splitk_workspace_bytes(1, 1, 3, Q.QMM_PARTIAL_BF16)
+        ws = torch.zeros(nb, dtype=torch.uint8, device="cuda")  # fused counters start at zero
+        got = _call_with(d, 1, 1, 3, Q.QMM_PARTIAL_BF16, ws)
+        assert int(got[0, 0]) == 0x3F80
+    finally:
+        Q.qmm_set_reduce(prev)
 
 
 @pytest.mark.parametrize("M,Nout", [(40, 1000), (128, 256), (3, 136)])
