@@ -115,6 +115,23 @@ def roofline_time_s(nbytes, flops, peaks):
     return (t_hbm, "hbm") if t_hbm >= t_tc else (t_tc, "tensor")
 
 
+def step_roofline(wl, ms_per_step, peaks):
+    """The whole step against its roofline: every call's algorithmic bytes
+    (packed weights, scales and biases, A, C, and at split s > 1 the BF16
+    planes written and read back) and flops, each call bounded by the slower
+    of bytes at the measured HBM bandwidth and flops at the measured BF16
+    peak; frac = the sum of those bounds / the measured step time."""
+    nb = fl = t = 0.0
+    for (_, M, Kred, Nout), s in zip(wl.calls, wl.split):
+        b, f = algorithmic(M, Kred, Nout, s)
+        nb, fl = nb + b, fl + f
+        t += roofline_time_s(b, f, peaks)[0]
+    us = ms_per_step * 1e3
+    return {"bytes": int(nb), "flops": fl, "roofline_us": round(t * 1e6, 3),
+            "us": round(us, 3), "frac": round(t * 1e6 / us, 4),
+            "note": "per call: max(bytes / HBM, flops / BF16 peak), summed over the step"}
+
+
 def max_over_ranks(ms: float, device=None) -> float:
     """The largest per-rank time (the job ends when the slowest rank ends)."""
     import torch.distributed as dist
@@ -539,7 +556,9 @@ def prefill_sweep(Q, device, stream, l2, peaks):
     """The prefill regime (M = 2048) of each projection shape: the policy's
     split (the unsplit kernel wherever the base grid already fills the GPU),
     graphs of back-to-back calls over input copies larger than L2, tensor
-    throughput against the measured dense BF16 peak.  Informational."""
+    throughput against the measured dense BF16 peak.  Where the balanced
+    split (QMM_SPLIT_BALANCED) cuts the call -- its tiles leave a partial last
+    wave -- its head rows, tail split and time are given beside it."""
     out = []
     ws = torch.zeros(64 << 20, dtype=torch.uint8, device=device)
     for name in PROJ:
@@ -551,16 +570,25 @@ def prefill_sweep(Q, device, stream, l2, peaks):
         cps = cold_copies(d, l2)
         C = torch.empty((M, Nout), dtype=torch.bfloat16, device=device)
 
-        def call(j):
+        def call(j, req=0):
             c = cps[j]
-            Q.qmm_w4a16_g128(c["A"], c["Wq"], c["scales"], c["biases"], C, workspace=ws)
+            Q.qmm_w4a16_g128(c["A"], c["Wq"], c["scales"], c["biases"], C, split_req=req,
+                             workspace=ws)
         us = graph_us_per_launch(call, len(cps), stream)
         fl = 2.0 * M * Nout * Kred
         bm, bn = Q.qmm_kernel_tile(M)
-        out.append({"proj": name, "M": M, "split": split,
-                    "ctas": -(-M // bm) * -(-Nout // bn) * split, "us": round(us, 3),
-                    "tflops": round(fl / us / 1e6, 1),
-                    "frac_of_bf16_peak": round(fl / us / 1e6 / peaks["bf16_tflops"], 3)})
+        row = {"proj": name, "M": M, "split": split,
+               "ctas": -(-M // bm) * -(-Nout // bn) * split, "us": round(us, 3),
+               "tflops": round(fl / us / 1e6, 1),
+               "frac_of_bf16_peak": round(fl / us / 1e6 / peaks["bf16_tflops"], 3)}
+        s_b, _, _, head = Q.qmm_call_plan(M, Kred, Nout, Q.QMM_SPLIT_BALANCED, with_head=True)
+        if head > 0:
+            us_b = graph_us_per_launch(lambda j: call(j, Q.QMM_SPLIT_BALANCED), len(cps), stream)
+            row["balanced"] = {"head_rows": head, "tail_split": s_b, "us": round(us_b, 3),
+                               "tflops": round(fl / us_b / 1e6, 1),
+                               "frac_of_bf16_peak": round(fl / us_b / 1e6 / peaks["bf16_tflops"],
+                                                          3)}
+        out.append(row)
         del cps, d
     return out
 
@@ -1123,6 +1151,7 @@ def main():
                     "achieved": round(ach_a, 2), "peak": peak, "unit": unit,
                     "frac": round(ach_a / peak, 4), "traffic": tr_a,
                     "per_launch": {"algorithmic_bytes": nb_a, "flops": fl_a, "us": round(us_a, 3)}}
+    step_roof = step_roofline(wl, res["ms"] / args.steps, peaks)
     out = {"metric": METRIC, "value": round(value_us, 4), "unit": UNIT, "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": round(res["ms"] / args.steps, 6), "higher_is_better": False,
@@ -1155,7 +1184,7 @@ def main():
                                                           ncalls), 4),
            "group_plan_splits": res["group_plan_splits"],
            "grouped_launches_per_step": res["grouped_launches"],
-           "roofline": roof, "roofline_other_partitions": roof_alt,
+           "roofline": roof, "roofline_other_partitions": roof_alt, "step_roofline": step_roof,
            "gpu_launches": args.steps * wl.launches_per_step(),
            "clocks": res["clocks"], "e2e": res["e2e"], "per_call": res["per_call"],
            "dense_splitk_512x512x16384": res["dense"], "prefill_M2048": res["prefill"],

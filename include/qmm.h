@@ -128,6 +128,13 @@ size_t qmm_splitk_workspace_bytes(int M, int Nout, int split, int partial_dtype)
 
 /* split_req value of qmm_w4a16_g128: the group plan's split for the call alone. */
 #define QMM_SPLIT_PLANNED (-1)
+/* split_req value of qmm_w4a16_g128: the balanced split (gpu-kernels-explained,
+ * "Split-K, streams and overlap", Stream-K, at tile granularity).  When the
+ * call's tiles leave a partial last wave, the row tiles that fill whole waves
+ * run unsplit and only the remaining rows are split, in the same partition
+ * launch, so the short split CTAs fill the SMs the last wave would leave
+ * idle; otherwise it is QMM_SPLIT_PLANNED. */
+#define QMM_SPLIT_BALANCED (-2)
 
 /* C = A . W^T for the W4A16-g128 format (see the top of this header).
  *   split_req  0: split from the policy (qmm_splitk_plan, or
@@ -142,6 +149,13 @@ size_t qmm_splitk_workspace_bytes(int M, int Nout, int split, int partial_dtype)
  *              traffic.  On under-filled calls it equals the policy's split;
  *              past one wave it may split where the policy does not (down at
  *              M = 2048: 2).  Size the workspace with that split.
+ *              QMM_SPLIT_BALANCED: rows [0, h) unsplit and rows [h, M) at a
+ *              split s, planned with the group plan's estimate on the current
+ *              device (qmm_call_plan reports h and s).  Rows [0, h) of C are
+ *              bitwise the unsplit call's; rows [h, M) bitwise those of a call
+ *              on those rows alone at split s.  The workspace holds the
+ *              tail's planes [s, M - h, Nout]; size it with
+ *              qmm_call_workspace_bytes.  The reduce is the separate kernel.
  *   pol        policy used when split_req == 0; NULL = QMM_PRESET_GB300
  *              for this M on the current device.
  *   workspace  device buffer for the partial planes [split, M, Nout] of
@@ -329,8 +343,70 @@ int qmm_kernel_status(int *status, int clear);
  * Returns QMM_OK, QMM_ENODEV or QMM_ECUDA. */
 int qmm_wait_timeout_probe(void *stream);
 
+/* ---- per-call options ------------------------------------------------------
+ *
+ * The qmm_set_* switches above are process-wide defaults, and some of them
+ * change what a call computes (the partition rule and the group plan pick
+ * the split, so the result's bits).  A call that passes a qmm_options takes
+ * every field that is not QMM_OPT_DEFAULT from it instead, for that call
+ * only: two callers in one process (two threads, two libraries) then cannot
+ * change each other's results.  Fields and the switch each one overrides:
+ *   kernels           QMM_KERNELS_*        qmm_set_kernels
+ *   partitions        QMM_PARTITIONS_*     qmm_set_partitions
+ *   reduce            QMM_REDUCE_*         qmm_set_reduce
+ *   weights_static    0 or 1               qmm_set_weights_static
+ *   pdl               0 or 1               qmm_set_pdl
+ *   grouped_schedule  QMM_GROUPED_*        qmm_set_grouped_schedule
+ *   group_plan        QMM_GROUP_PLAN_*     qmm_set_group_plan
+ * A NULL qmm_options means every field QMM_OPT_DEFAULT.  A field outside its
+ * range makes the call return QMM_EINVAL (0 from the *_bytes queries) before
+ * it checks anything else.  The tiny-llm chapter's single matmul with a
+ * use_split_k switch has no process state at all; these calls give the same
+ * guarantee for the switches this library adds. */
+#define QMM_OPT_DEFAULT (-1)
+typedef struct {
+    int kernels, partitions, reduce, weights_static, pdl, grouped_schedule, group_plan;
+} qmm_options;
+
+/* Every field of *opt set to QMM_OPT_DEFAULT (no-op for NULL). */
+void qmm_options_init(qmm_options *opt);
+
+/* qmm_w4a16_g128 under the options (same arguments, codes and results). */
+int qmm_w4a16_g128_ex(const void *A, const uint32_t *Wq, const void *scales, const void *biases,
+                      void *C, int M, int Kred, int Nout, int split_req, const qmm_policy *pol,
+                      void *workspace, size_t ws_bytes, int partial_dtype, void *stream,
+                      int *split_used, const qmm_options *opt);
+
+/* qmm_splitk_workspace_bytes under the options (the fused reduce's counter
+ * area depends on the reduce mode and the kernel table). */
+size_t qmm_splitk_workspace_bytes_ex(int M, int Nout, int split, int partial_dtype,
+                                     const qmm_options *opt);
+
+/* What qmm_w4a16_g128_ex would dispatch for this shape, without launching:
+ * *split the split (split_req and pol as in qmm_w4a16_g128, QMM_SPLIT_PLANNED
+ * and QMM_SPLIT_BALANCED included), *bm / *bn the tile of the kernel family
+ * and *head_rows the rows that QMM_SPLIT_BALANCED runs unsplit (0 when it
+ * does not cut the call; *split is then the split of the whole call, else
+ * that of rows [*head_rows, M)); the last three are nullable.  num_sms > 0
+ * plans for that many SMs; <= 0 queries the current device.  Returns
+ * QMM_OK, QMM_EINVAL, QMM_ESHAPE or QMM_ENODEV.  Host only. */
+int qmm_call_plan(int M, int Kred, int Nout, int split_req, const qmm_policy *pol,
+                  int partial_dtype, int num_sms, const qmm_options *opt, int *split, int *bm,
+                  int *bn, int *head_rows);
+
+/* Workspace bytes qmm_w4a16_g128_ex needs for this call as qmm_call_plan
+ * plans it (any split_req), or 0 when it needs none or for invalid
+ * arguments.  Host only. */
+size_t qmm_call_workspace_bytes(int M, int Kred, int Nout, int split_req, const qmm_policy *pol,
+                                int partial_dtype, int num_sms, const qmm_options *opt);
+
 /* Static description of a return code. */
 const char *qmm_strerror(int code);
+
+/* Name of the CUDA error (cudaGetErrorName) behind the latest QMM_ECUDA that
+ * a launch returned on the calling thread ("cudaSuccess" if none has).  A
+ * diagnostic with no counterpart on the pages.  Host only. */
+const char *qmm_last_cuda_error(void);
 
 /* Allocation-free qmm_w4a16_g128.  The tiny-llm split-K chapter has no
  * counterpart to this call: it exists for callers that cannot allocate
@@ -357,6 +433,7 @@ const char *qmm_strerror(int code);
  *     (split_req = 0), the group plan's (QMM_SPLIT_PLANNED) or the forced
  *     one, as in qmm_w4a16_g128, and the limit applies to the split that
  *     results.  Unsplit calls (split 1) use none of the buffer.
+ *     QMM_SPLIT_BALANCED is not taken here (QMM_EINVAL).
  *   - Races: every call on a device shares the one buffer.  Two calls whose
  *     kernels can overlap on the GPU (different streams without ordering
  *     between them) race on it and give undefined results.  Calls ordered
@@ -416,6 +493,14 @@ size_t qmm_group_workspace_bytes(const qmm_group_call *calls, int n, int partial
  * checked before anything is launched. */
 int qmm_w4a16_g128_grouped(const qmm_group_call *calls, int n, void *workspace, size_t ws_bytes,
                            int partial_dtype, void *stream, int *splits_used);
+
+/* qmm_group_workspace_bytes and qmm_w4a16_g128_grouped under per-call
+ * options (qmm_options above). */
+size_t qmm_group_workspace_bytes_ex(const qmm_group_call *calls, int n, int partial_dtype,
+                                    const qmm_options *opt);
+int qmm_w4a16_g128_grouped_ex(const qmm_group_call *calls, int n, void *workspace,
+                              size_t ws_bytes, int partial_dtype, void *stream, int *splits_used,
+                              const qmm_options *opt);
 
 /* Schedule of the grouped call's tcgen05 partition launches (process-wide,
  * thread-safe):

@@ -160,10 +160,13 @@ __device__ __forceinline__ void load_group_row(const uint16_t* __restrict__ src,
     }
 }
 
-// m16n8k16 BF16 MMA with FP32 accumulate: d += a (16x16, row) * b (16x8, col)
+// m16n8k16 BF16 MMA with FP32 accumulate: d += a (16x16, row) * b (16x8, col).
+// It reads and writes registers only, so the asm is not volatile: the
+// compiler may interleave independent MMAs with other work to hide their
+// latency (a volatile asm would keep every MMA in source order).
 __device__ __forceinline__ void mma_bf16_16816(float d[4], const uint32_t a[4], uint32_t b0,
                                                uint32_t b1) {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
         "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])

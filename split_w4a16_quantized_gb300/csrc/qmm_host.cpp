@@ -32,9 +32,16 @@ int device_sms(int* sms) {
 
 int check_device() { return qmm::device_check(); }
 
+// The CUDA error behind this thread's latest QMM_ECUDA (qmm_last_cuda_error).
+thread_local int tl_cuda_error = cudaSuccess;
+
 // Launches go through cudaLaunchKernelEx, which reports its own error; the
 // caller's pending CUDA error state is left alone.
-int launched(int err) { return err == cudaSuccess ? QMM_OK : QMM_ECUDA; }
+int launched(int err) {
+    if (err == cudaSuccess) return QMM_OK;
+    tl_cuda_error = err;
+    return QMM_ECUDA;
+}
 
 size_t partial_elem_bytes(int dtype) { return dtype == QMM_PARTIAL_F32 ? 4 : 2; }
 
@@ -60,6 +67,36 @@ std::atomic<int> g_reduce{QMM_REDUCE_KERNEL};
 std::atomic<int> g_partitions{QMM_PARTITIONS_EQUAL};
 std::atomic<int> g_grouped{QMM_GROUPED_PERSISTENT};
 std::atomic<int> g_group_plan{QMM_GROUP_PLAN_CALLS};
+
+// Per-call options (qmm_options): the *_ex entry points install theirs for
+// the duration of the call on the calling thread; every switch accessor
+// reads a field that is not QMM_OPT_DEFAULT from there, else the
+// process-wide value.
+thread_local const qmm_options* tl_options = nullptr;
+
+struct OptionsScope {
+    const qmm_options* prev;
+    explicit OptionsScope(const qmm_options* o) : prev(tl_options) { tl_options = o; }
+    ~OptionsScope() { tl_options = prev; }
+    OptionsScope(const OptionsScope&) = delete;
+    OptionsScope& operator=(const OptionsScope&) = delete;
+};
+
+int setting(int qmm_options::*field, const std::atomic<int>& global) {
+    if (tl_options && tl_options->*field != QMM_OPT_DEFAULT) return tl_options->*field;
+    return global.load(std::memory_order_relaxed);
+}
+
+bool in_range(int v, int lo, int hi) { return v == QMM_OPT_DEFAULT || (v >= lo && v <= hi); }
+
+bool options_valid(const qmm_options* o) {
+    return !o || (in_range(o->kernels, QMM_KERNELS_DEFAULT, QMM_KERNELS_LEAN) &&
+                  in_range(o->partitions, QMM_PARTITIONS_EQUAL, QMM_PARTITIONS_NEAR_EQUAL) &&
+                  in_range(o->reduce, QMM_REDUCE_KERNEL, QMM_REDUCE_FUSED) &&
+                  in_range(o->weights_static, 0, 1) && in_range(o->pdl, 0, 1) &&
+                  in_range(o->grouped_schedule, QMM_GROUPED_TILES, QMM_GROUPED_PERSISTENT) &&
+                  in_range(o->group_plan, QMM_GROUP_PLAN_CALLS, QMM_GROUP_PLAN_GROUP));
+}
 
 // a split the current partition rule accepts for G groups (grid z <= 65535)
 bool split_fits(int64_t G, int64_t split) {
@@ -96,6 +133,10 @@ bool policy_valid(const qmm_policy* p) {
 int device_check() {
     int dev = 0, major = 0, minor = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return QMM_ENODEV;
+    // Bind the device's primary context to the calling thread: the tensor-map
+    // encoder is a driver call, and a thread that has made no runtime call
+    // yet has no current context for it.
+    if (cudaSetDevice(dev) != cudaSuccess) return QMM_ENODEV;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
         return QMM_ENODEV;
@@ -103,7 +144,7 @@ int device_check() {
 }
 
 const Family& family_for(int M) {
-    switch (g_kernels.load(std::memory_order_relaxed)) {
+    switch (setting(&qmm_options::kernels, g_kernels)) {
         case QMM_KERNELS_MMA_SYNC: return pick(kMmaFamilies, M);
         case QMM_KERNELS_TCGEN05: return pick(kTcFamilies, M);
         case QMM_KERNELS_LEAN: return pick(kLeanTable, M);
@@ -113,25 +154,26 @@ const Family& family_for(int M) {
 
 bool family_shares_launch(const Family& f) { return f.kind == kKindTc; }
 
-bool pdl_enabled() { return g_pdl.load(std::memory_order_relaxed) != 0; }
+bool pdl_enabled() { return setting(&qmm_options::pdl, g_pdl) != 0; }
 
-bool weights_static() { return g_wstatic.load(std::memory_order_relaxed) != 0; }
+bool weights_static() { return setting(&qmm_options::weights_static, g_wstatic) != 0; }
 
-bool reduce_fused() { return g_reduce.load(std::memory_order_relaxed) == QMM_REDUCE_FUSED; }
+bool reduce_fused() { return setting(&qmm_options::reduce, g_reduce) == QMM_REDUCE_FUSED; }
 
 bool partitions_near_equal() {
-    return g_partitions.load(std::memory_order_relaxed) == QMM_PARTITIONS_NEAR_EQUAL;
+    return setting(&qmm_options::partitions, g_partitions) == QMM_PARTITIONS_NEAR_EQUAL;
 }
 
 bool grouped_persistent() {
-    return g_grouped.load(std::memory_order_relaxed) == QMM_GROUPED_PERSISTENT;
+    return setting(&qmm_options::grouped_schedule, g_grouped) == QMM_GROUPED_PERSISTENT;
 }
 
-int choose_split(int M, int Kred, int Nout, int split_req, const qmm_policy* pol, int* split) {
+int choose_split(int M, int Kred, int Nout, int split_req, const qmm_policy* pol, int* split,
+                 int num_sms) {
     if (split_req == 0) {
         qmm_policy local;
         if (!pol) {
-            const int rc = qmm_policy_preset(QMM_PRESET_GB300, M, 0, &local);
+            const int rc = qmm_policy_preset(QMM_PRESET_GB300, M, num_sms, &local);
             if (rc != QMM_OK) return rc;
             pol = &local;
         }
@@ -143,7 +185,7 @@ int choose_split(int M, int Kred, int Nout, int split_req, const qmm_policy* pol
     return QMM_OK;
 }
 
-bool gemm_uses_tc() { return g_kernels.load(std::memory_order_relaxed) != QMM_KERNELS_MMA_SYNC; }
+bool gemm_uses_tc() { return setting(&qmm_options::kernels, g_kernels) != QMM_KERNELS_MMA_SYNC; }
 
 int smem_optin_bytes() {
     static int limit = -1;
@@ -203,6 +245,13 @@ namespace {
 // the group plan's splits (defined with the grouped call below)
 int group_plan_shapes(const int* shapes, int n, int num_sms, int partial_dtype,
                       std::vector<int>* splits);
+int launch_group(const qmm_group_call* calls, int n, const std::vector<int>& splits,
+                 const std::vector<size_t>& offsets, void* workspace, int partial_dtype,
+                 void* stream);
+// QMM_SPLIT_BALANCED's plan (defined with the group plan below)
+int balanced_plan(int M, int Kred, int Nout, int num_sms, int partial_dtype, int* head,
+                  int* s_tail, int* s_plain);
+size_t balanced_bytes(int M, int Nout, int head, int s_tail, int partial_dtype);
 }  // namespace
 
 int qmm_set_group_plan(int mode) {
@@ -229,6 +278,96 @@ int qmm_kernel_status(int* status, int clear) {
     int rc = check_device();
     if (rc != QMM_OK) return rc;
     return qmm::read_tc_status(status, clear != 0) == cudaSuccess ? QMM_OK : QMM_ECUDA;
+}
+
+void qmm_options_init(qmm_options* opt) {
+    if (!opt) return;
+    *opt = qmm_options{QMM_OPT_DEFAULT, QMM_OPT_DEFAULT, QMM_OPT_DEFAULT, QMM_OPT_DEFAULT,
+                       QMM_OPT_DEFAULT, QMM_OPT_DEFAULT, QMM_OPT_DEFAULT};
+}
+
+int qmm_w4a16_g128_ex(const void* A, const uint32_t* Wq, const void* scales, const void* biases,
+                      void* C, int M, int Kred, int Nout, int split_req, const qmm_policy* pol,
+                      void* workspace, size_t ws_bytes, int partial_dtype, void* stream,
+                      int* split_used, const qmm_options* opt) {
+    if (!options_valid(opt)) return QMM_EINVAL;
+    const OptionsScope scope(opt);
+    return qmm_w4a16_g128(A, Wq, scales, biases, C, M, Kred, Nout, split_req, pol, workspace,
+                          ws_bytes, partial_dtype, stream, split_used);
+}
+
+size_t qmm_splitk_workspace_bytes_ex(int M, int Nout, int split, int partial_dtype,
+                                     const qmm_options* opt) {
+    if (!options_valid(opt)) return 0;
+    const OptionsScope scope(opt);
+    return qmm_splitk_workspace_bytes(M, Nout, split, partial_dtype);
+}
+
+int qmm_call_plan(int M, int Kred, int Nout, int split_req, const qmm_policy* pol,
+                  int partial_dtype, int num_sms, const qmm_options* opt, int* split, int* bm,
+                  int* bn, int* head_rows) {
+    if (!options_valid(opt) || !split || M < 1 || Nout < 1 ||
+        (split_req < 0 && split_req != QMM_SPLIT_PLANNED && split_req != QMM_SPLIT_BALANCED))
+        return QMM_EINVAL;
+    if (partial_dtype != QMM_PARTIAL_BF16 && partial_dtype != QMM_PARTIAL_F32) return QMM_EINVAL;
+    if (pol && !policy_ok(pol)) return QMM_EINVAL;
+    if (Kred < qmm::kGroup || Kred % qmm::kGroup) return QMM_ESHAPE;
+    const OptionsScope scope(opt);
+    const qmm::Family& f = qmm::family_for(M);
+    if (bm) *bm = f.bm;
+    if (bn) *bn = f.bn;
+    if (head_rows) *head_rows = 0;
+    if (split_req == QMM_SPLIT_BALANCED) {
+        int head = 0, s_tail = 1, s_plain = 1;
+        const int rc = balanced_plan(M, Kred, Nout, num_sms, partial_dtype, &head, &s_tail,
+                                     &s_plain);
+        if (rc != QMM_OK) return rc;
+        if (head > 0) {
+            *split = s_tail;
+            if (head_rows) *head_rows = head;
+            return QMM_OK;
+        }
+        split_req = s_plain;
+    }
+    if (split_req == QMM_SPLIT_PLANNED) {
+        const int shape[3] = {M, Kred, Nout};
+        std::vector<int> planned;
+        const int rc = group_plan_shapes(shape, 1, num_sms, partial_dtype, &planned);
+        if (rc != QMM_OK) return rc;
+        split_req = planned[0];
+    }
+    return qmm::choose_split(M, Kred, Nout, split_req, pol, split, num_sms);
+}
+
+size_t qmm_call_workspace_bytes(int M, int Kred, int Nout, int split_req, const qmm_policy* pol,
+                                int partial_dtype, int num_sms, const qmm_options* opt) {
+    int split = 1, head = 0;
+    if (qmm_call_plan(M, Kred, Nout, split_req, pol, partial_dtype, num_sms, opt, &split, nullptr,
+                      nullptr, &head) != QMM_OK)
+        return 0;
+    const OptionsScope scope(opt);
+    if (head > 0) return balanced_bytes(M, Nout, head, split, partial_dtype);
+    return qmm_splitk_workspace_bytes(M, Nout, split, partial_dtype);
+}
+
+size_t qmm_group_workspace_bytes_ex(const qmm_group_call* calls, int n, int partial_dtype,
+                                    const qmm_options* opt) {
+    if (!options_valid(opt)) return 0;
+    const OptionsScope scope(opt);
+    return qmm_group_workspace_bytes(calls, n, partial_dtype);
+}
+
+int qmm_w4a16_g128_grouped_ex(const qmm_group_call* calls, int n, void* workspace,
+                              size_t ws_bytes, int partial_dtype, void* stream, int* splits_used,
+                              const qmm_options* opt) {
+    if (!options_valid(opt)) return QMM_EINVAL;
+    const OptionsScope scope(opt);
+    return qmm_w4a16_g128_grouped(calls, n, workspace, ws_bytes, partial_dtype, stream,
+                                  splits_used);
+}
+
+const char* qmm_last_cuda_error(void) {
+    return cudaGetErrorName(static_cast<cudaError_t>(tl_cuda_error));
 }
 
 const char* qmm_strerror(int code) {
@@ -340,7 +479,7 @@ int qmm_w4a16_g128(const void* A, const uint32_t* Wq, const void* scales, const 
                    void* workspace, size_t ws_bytes, int partial_dtype, void* stream,
                    int* split_used) {
     if (!A || !Wq || !scales || !biases || !C || M < 1 || Nout < 1 ||
-        (split_req < 0 && split_req != QMM_SPLIT_PLANNED))
+        (split_req < 0 && split_req != QMM_SPLIT_PLANNED && split_req != QMM_SPLIT_BALANCED))
         return QMM_EINVAL;
     if (partial_dtype != QMM_PARTIAL_BF16 && partial_dtype != QMM_PARTIAL_F32) return QMM_EINVAL;
     if (pol && !policy_ok(pol)) return QMM_EINVAL;
@@ -352,6 +491,29 @@ int qmm_w4a16_g128(const void* A, const uint32_t* Wq, const void* scales, const 
     if (ceil_div(M, fam.bm) > 65535) return QMM_ESHAPE;
     int rc = check_device();
     if (rc != QMM_OK) return rc;
+    if (split_req == QMM_SPLIT_BALANCED) {
+        int head = 0, s_tail = 1, s_plain = 1;
+        rc = balanced_plan(M, Kred, Nout, 0, partial_dtype, &head, &s_tail, &s_plain);
+        if (rc != QMM_OK) return rc;
+        if (head > 0) {
+            // rows [0, head) unsplit and [head, M) at s_tail, in one partition
+            // launch (two calls of the grouped path on the two row ranges)
+            const size_t need = balanced_bytes(M, Nout, head, s_tail, partial_dtype);
+            if (need > 0) {
+                if (!workspace || ws_bytes < need) return QMM_EWORKSPACE;
+                if (!aligned(workspace, 16)) return QMM_EALIGN;
+            }
+            const qmm_group_call calls[2] = {
+                {A, Wq, scales, biases, C, head, Kred, Nout},
+                {static_cast<const uint8_t*>(A) + static_cast<size_t>(head) * Kred * 2, Wq, scales,
+                 biases, static_cast<uint8_t*>(C) + static_cast<size_t>(head) * Nout * 2, M - head,
+                 Kred, Nout}};
+            rc = launch_group(calls, 2, {1, s_tail}, {0, 0}, workspace, partial_dtype, stream);
+            if (rc == QMM_OK && split_used) *split_used = s_tail;
+            return rc;
+        }
+        split_req = s_plain;  // no cut pays: the planned split
+    }
     if (split_req == QMM_SPLIT_PLANNED) {
         const int shape[3] = {M, Kred, Nout};
         std::vector<int> planned;
@@ -567,7 +729,7 @@ int group_plan_shapes(const int* shapes, int n, int num_sms, int partial_dtype,
     key.push_back(num_sms);
     key.push_back(partial_dtype);
     key.push_back(qmm::partitions_near_equal() ? 1 : 0);
-    key.push_back(g_kernels.load(std::memory_order_relaxed));
+    key.push_back(setting(&qmm_options::kernels, g_kernels));
     {
         std::lock_guard<std::mutex> lock(mu);
         for (const Entry& e : cache)
@@ -585,6 +747,69 @@ int group_plan_shapes(const int* shapes, int n, int num_sms, int partial_dtype,
     return QMM_OK;
 }
 
+// ---- balanced split (QMM_SPLIT_BALANCED) ------------------------------------
+//
+// gpu-kernels-explained, "Split-K, streams and overlap" (Stream-K): a grid
+// whose tiles leave a partial last wave idles most SMs while that wave runs.
+// At tile granularity the fix is the data-parallel + split-K hybrid: the
+// row tiles that fill whole waves run unsplit, and only the rows of the
+// partial wave are split, so their shorter CTAs spread over every SM as the
+// full-wave CTAs finish.  Both row ranges go into one partition launch
+// (longest CTAs first) and the tail's planes into one reduce.  The tail's
+// split is the one with the lowest estimate of the group plan's cost model;
+// the cut is taken only if that estimate beats the planned split's.  Rows
+// [0, head) get exactly the unsplit kernel's result and rows [head, M) that
+// of a call on those rows at the tail's split (the same tiles, k order and
+// rounding).
+int balanced_plan(int M, int Kred, int Nout, int num_sms, int partial_dtype, int* head,
+                  int* s_tail, int* s_plain) {
+    const int shape[3] = {M, Kred, Nout};
+    std::vector<int> planned;
+    int rc = group_plan_shapes(shape, 1, num_sms, partial_dtype, &planned);
+    if (rc != QMM_OK) return rc;
+    if (num_sms <= 0) {
+        rc = device_sms(&num_sms);
+        if (rc != QMM_OK) return rc;
+    }
+    *s_plain = *s_tail = planned[0];
+    *head = 0;
+    const qmm::Family& f = qmm::family_for(M);
+    if (!qmm::family_shares_launch(f)) return QMM_OK;
+    const int64_t rt = ceil_div(M, f.bm), ct = ceil_div(Nout, f.bn), tiles = rt * ct;
+    if (tiles <= num_sms || tiles % num_sms == 0) return QMM_OK;
+    const int64_t h = tiles / num_sms * num_sms / ct;  // row tiles that fit the full waves
+    if (h < 1 || h >= rt) return QMM_OK;
+    const int m1 = static_cast<int>(h * f.bm);
+    if (qmm::family_for(M - m1).bm != f.bm) return QMM_OK;  // the tail must share the launch
+    const int G = Kred / qmm::kGroup;
+    const int smax = std::min(qmm::kCap, G);
+    const int elem = static_cast<int>(partial_elem_bytes(partial_dtype));
+    const std::vector<PlanCall> whole = {{M, Kred, Nout, G, smax, tiles}};
+    const std::vector<PlanCall> cut = {{m1, Kred, Nout, G, smax, h * ct},
+                                       {M - m1, Kred, Nout, G, smax, (rt - h) * ct}};
+    double best = 0.0;
+    if (!plan_cost(whole, {*s_plain}, f.bm, num_sms, elem, &best)) return QMM_OK;
+    int best_s = 0;
+    for (int s = 1; s <= smax; ++s) {
+        double c = 0.0;
+        if (split_fits(G, s) && plan_cost(cut, {1, s}, f.bm, num_sms, elem, &c) && c < best) {
+            best = c;
+            best_s = s;
+        }
+    }
+    if (best_s > 0) {
+        *head = m1;
+        *s_tail = best_s;
+    }
+    return QMM_OK;
+}
+
+size_t balanced_bytes(int M, int Nout, int head, int s_tail, int partial_dtype) {
+    if (s_tail <= 1) return 0;
+    return static_cast<size_t>(s_tail) * static_cast<size_t>(M - head) * static_cast<size_t>(Nout) *
+           partial_elem_bytes(partial_dtype);
+}
+
 // Every call's arguments, then its split and the offset of its planes in the
 // workspace (256-byte aligned); *ws_need receives the total.
 int plan_group(const qmm_group_call* calls, int n, int partial_dtype, std::vector<int>* splits,
@@ -597,7 +822,7 @@ int plan_group(const qmm_group_call* calls, int n, int partial_dtype, std::vecto
     }
     splits->assign(static_cast<size_t>(n), 1);
     offsets->assign(static_cast<size_t>(n), 0);
-    if (g_group_plan.load(std::memory_order_relaxed) == QMM_GROUP_PLAN_GROUP) {
+    if (setting(&qmm_options::group_plan, g_group_plan) == QMM_GROUP_PLAN_GROUP) {
         std::vector<int> shapes;
         for (int i = 0; i < n; ++i) {
             shapes.push_back(calls[i].M);
@@ -611,7 +836,7 @@ int plan_group(const qmm_group_call* calls, int n, int partial_dtype, std::vecto
     for (int i = 0; i < n; ++i) {
         const qmm_group_call& c = calls[i];
         int& s = (*splits)[static_cast<size_t>(i)];
-        if (g_group_plan.load(std::memory_order_relaxed) != QMM_GROUP_PLAN_GROUP) {
+        if (setting(&qmm_options::group_plan, g_group_plan) != QMM_GROUP_PLAN_GROUP) {
             const int rc = qmm::choose_split(c.M, c.Kred, c.Nout, 0, nullptr, &s);
             if (rc != QMM_OK) return rc;
         }
@@ -649,6 +874,24 @@ int qmm_w4a16_g128_grouped(const qmm_group_call* calls, int n, void* workspace, 
     }
     rc = check_device();
     if (rc != QMM_OK) return rc;
+    rc = launch_group(calls, n, splits, offsets, workspace, partial_dtype, stream);
+    if (rc == QMM_OK && splits_used)
+        for (int i = 0; i < n; ++i) splits_used[i] = splits[i];
+    return rc;
+}
+
+}  // extern "C"
+
+namespace {
+
+// The launches of n checked calls at the given splits, the planes of call i
+// at workspace + offsets[i]: the tcgen05 calls of one tile width share a
+// partition launch, the others run one by one, and one reduce launch adds
+// the planes of up to kMaxGroupCalls split calls.
+int launch_group(const qmm_group_call* calls, int n, const std::vector<int>& splits,
+                 const std::vector<size_t>& offsets, void* workspace, int partial_dtype,
+                 void* stream) {
+    int rc = QMM_OK;
     const int mode = partial_dtype == QMM_PARTIAL_F32 ? qmm::kOutF32 : qmm::kOutBf16;
     auto out_of = [&](int i) -> void* {
         return splits[i] > 1 ? static_cast<uint8_t*>(workspace) + offsets[i] : calls[i].C;
@@ -710,10 +953,12 @@ int qmm_w4a16_g128_grouped(const qmm_group_call* calls, int n, void* workspace, 
     if (rc == QMM_OK && !red.empty())
         rc = launched(qmm::launch_reduce_group(red.data(), static_cast<int>(red.size()),
                                                partial_dtype, stream));
-    if (rc == QMM_OK && splits_used)
-        for (int i = 0; i < n; ++i) splits_used[i] = splits[i];
     return rc;
 }
+
+}  // namespace
+
+extern "C" {
 
 int qmm_gemm_bf16_splitk(const void* A, const void* W, void* C, int M, int N, int K, int split,
                          void* workspace, size_t ws_bytes, void* stream) {

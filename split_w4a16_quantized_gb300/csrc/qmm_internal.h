@@ -103,7 +103,10 @@ bool grouped_persistent();
 // the GB300 preset) under the current partition rule, or the forced split if
 // that rule accepts it (QMM_ESHAPE otherwise).  Shape and policy checked by
 // the caller; returns a QMM_* code.
-int choose_split(int M, int Kred, int Nout, int split_req, const qmm_policy* pol, int* split);
+// num_sms > 0 plans the preset policy for that many SMs instead of the
+// current device's.
+int choose_split(int M, int Kred, int Nout, int split_req, const qmm_policy* pol, int* split,
+                 int num_sms = 0);
 struct LaunchAttrs {
     cudaLaunchAttribute attr[1];
 };

@@ -20,6 +20,7 @@ LIB_PATH = os.path.join(_PKG, "libqmm.so")
 
 QMM_OK, QMM_EINVAL, QMM_ESHAPE, QMM_EWORKSPACE, QMM_ECUDA, QMM_EALIGN, QMM_ENODEV = \
     0, -1, -2, -3, -4, -5, -6
+
 QMM_PARTIAL_BF16, QMM_PARTIAL_F32 = 0, 1
 QMM_PRESET_PAGES, QMM_PRESET_GB300 = 0, 1
 QMM_KERNELS_DEFAULT, QMM_KERNELS_MMA_SYNC, QMM_KERNELS_TCGEN05, QMM_KERNELS_LEAN = 0, 1, 2, 3
@@ -37,10 +38,32 @@ class qmm_policy(ctypes.Structure):
             self.as_tuple()
 
 
+QMM_OPT_DEFAULT = -1
+_OPTION_FIELDS = ("kernels", "partitions", "reduce", "weights_static", "pdl",
+                  "grouped_schedule", "group_plan")
+
+
+class qmm_options(ctypes.Structure):
+    """Per-call options (see qmm.h); every field defaults to QMM_OPT_DEFAULT."""
+    _fields_ = [(f, ctypes.c_int) for f in _OPTION_FIELDS]
+
+    def __init__(self, **kw):
+        super().__init__(*([QMM_OPT_DEFAULT] * len(_OPTION_FIELDS)))
+        for k, v in kw.items():
+            if k not in _OPTION_FIELDS:
+                raise TypeError("unknown option %r" % k)
+            setattr(self, k, int(v))
+
+
+def _opt(options):
+    return ctypes.byref(options) if options is not None else None
+
+
 class QmmError(RuntimeError):
     def __init__(self, code: int, what: str):
         self.code = code
-        super().__init__("%s: %s (%d)" % (what, qmm_strerror(code), code))
+        detail = " [%s]" % qmm_last_cuda_error() if code == QMM_ECUDA else ""
+        super().__init__("%s: %s (%d)%s" % (what, qmm_strerror(code), code, detail))
 
 
 class qmm_stream_call(ctypes.Structure):
@@ -79,6 +102,15 @@ _SIGS = {
     "qmm_unpack_probe": (_I, [_P, _I, _I, _P, _P]),
     "qmm_dequant_probe": (_I, [_P, _P, _P, _I, _I, _P, _P]),
     "qmm_strerror": (ctypes.c_char_p, [_I]),
+    "qmm_last_cuda_error": (ctypes.c_char_p, []),
+    "qmm_options_init": (None, [_P]),
+    "qmm_w4a16_g128_ex": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, ctypes.POINTER(qmm_policy),
+                               _P, _SZ, _I, _P, ctypes.POINTER(_I), _P]),
+    "qmm_splitk_workspace_bytes_ex": (_SZ, [_I, _I, _I, _I, _P]),
+    "qmm_call_plan": (_I, [_I, _I, _I, _I, ctypes.POINTER(qmm_policy), _I, _I, _P,
+                           ctypes.POINTER(_I), ctypes.POINTER(_I), ctypes.POINTER(_I),
+                           ctypes.POINTER(_I)]),
+    "qmm_call_workspace_bytes": (_SZ, [_I, _I, _I, _I, ctypes.POINTER(qmm_policy), _I, _I, _P]),
     "qmm_set_kernels": (_I, [_I]),
     "qmm_set_pdl": (_I, [_I]),
     "qmm_set_weights_static": (_I, [_I]),
@@ -101,6 +133,9 @@ _SIGS = {
     "qmm_group_workspace_bytes": (_SZ, [ctypes.POINTER(qmm_group_call), _I, _I]),
     "qmm_w4a16_g128_grouped": (_I, [ctypes.POINTER(qmm_group_call), _I, _P, _SZ, _I, _P,
                                     ctypes.POINTER(_I)]),
+    "qmm_group_workspace_bytes_ex": (_SZ, [ctypes.POINTER(qmm_group_call), _I, _I, _P]),
+    "qmm_w4a16_g128_grouped_ex": (_I, [ctypes.POINTER(qmm_group_call), _I, _P, _SZ, _I, _P,
+                                       ctypes.POINTER(_I), _P]),
     "qmm_stream_arena_bytes": (_SZ, [ctypes.POINTER(qmm_stream_call), _I, _I]),
     "qmm_w4a16_g128_stream": (_I, [ctypes.POINTER(qmm_stream_call), _I, _I, _P, _SZ, _P, _P, _P,
                                    ctypes.POINTER(_I)]),
@@ -161,6 +196,11 @@ def qmm_strerror(code: int) -> str:
     return lib().qmm_strerror(code).decode()
 
 
+def qmm_last_cuda_error() -> str:
+    """Name of the CUDA error behind this thread's latest QMM_ECUDA."""
+    return lib().qmm_last_cuda_error().decode()
+
+
 def qmm_policy_preset(which: int, M: int = 1, num_sms: int = 0) -> qmm_policy:
     out = qmm_policy()
     _check(lib().qmm_policy_preset(which, M, num_sms, ctypes.byref(out)), "qmm_policy_preset")
@@ -216,6 +256,7 @@ def qmm_set_grouped_schedule(mode: int) -> int:
 
 QMM_GROUP_PLAN_CALLS, QMM_GROUP_PLAN_GROUP = 0, 1
 QMM_SPLIT_PLANNED = -1  # split_req of qmm_w4a16_g128: the group plan for the call alone
+QMM_SPLIT_BALANCED = -2  # split_req: whole waves unsplit, the partial wave's rows split
 
 
 def qmm_set_group_plan(mode: int) -> int:
@@ -281,8 +322,33 @@ def qmm_splitk_plan_near_equal(M: int, Kred: int, Nout: int, pol: qmm_policy) ->
 
 
 def qmm_splitk_workspace_bytes(M: int, Nout: int, split: int,
-                               partial_dtype: int = QMM_PARTIAL_BF16) -> int:
+                               partial_dtype: int = QMM_PARTIAL_BF16, options=None) -> int:
+    if options is not None:
+        return int(lib().qmm_splitk_workspace_bytes_ex(M, Nout, split, partial_dtype,
+                                                        _opt(options)))
     return int(lib().qmm_splitk_workspace_bytes(M, Nout, split, partial_dtype))
+
+
+def qmm_call_plan(M: int, Kred: int, Nout: int, split_req: int = 0, pol=None,
+                  partial_dtype: int = QMM_PARTIAL_BF16, num_sms: int = 0, options=None,
+                  with_head: bool = False):
+    """(split, bm, bn) that qmm_w4a16_g128_ex would dispatch (host only);
+    with_head: (split, bm, bn, head_rows), head_rows > 0 when
+    QMM_SPLIT_BALANCED cuts the call."""
+    s, bm, bn, hd = _I(0), _I(0), _I(0), _I(0)
+    _check(lib().qmm_call_plan(M, Kred, Nout, split_req,
+                               ctypes.byref(pol) if pol is not None else None, partial_dtype,
+                               num_sms, _opt(options), ctypes.byref(s), ctypes.byref(bm),
+                               ctypes.byref(bn), ctypes.byref(hd)), "qmm_call_plan")
+    return (s.value, bm.value, bn.value, hd.value) if with_head else (s.value, bm.value, bn.value)
+
+
+def qmm_call_workspace_bytes(M: int, Kred: int, Nout: int, split_req: int = 0, pol=None,
+                             partial_dtype: int = QMM_PARTIAL_BF16, num_sms: int = 0,
+                             options=None) -> int:
+    return int(lib().qmm_call_workspace_bytes(M, Kred, Nout, split_req,
+                                              ctypes.byref(pol) if pol is not None else None,
+                                              partial_dtype, num_sms, _opt(options)))
 
 
 def qmm_gemm_workspace_bytes(M: int, N: int, split: int) -> int:
@@ -294,11 +360,13 @@ def qmm_gemm_workspace_bytes(M: int, N: int, split: int) -> int:
 def qmm_w4a16_g128(A: torch.Tensor, Wq: torch.Tensor, scales: torch.Tensor,
                    biases: torch.Tensor, C: torch.Tensor, split_req: int = 0,
                    pol: qmm_policy | None = None, workspace: torch.Tensor | None = None,
-                   partial_dtype: int = QMM_PARTIAL_BF16, stream=None) -> int:
+                   partial_dtype: int = QMM_PARTIAL_BF16, stream=None, options=None) -> int:
     """C = A @ W^T (W in the W4A16-g128 format); returns the split dispatched.
     Shapes: A [M, Kred] bf16, Wq [Nout, Kred/8] int32, scales/biases
     [Nout, Kred/128] bf16, C [M, Nout] bf16; workspace any contiguous CUDA
-    tensor of at least qmm_splitk_workspace_bytes(...) bytes."""
+    tensor of at least qmm_splitk_workspace_bytes(...) bytes.  options: a
+    qmm_options for this call only (qmm_w4a16_g128_ex), else the process-wide
+    settings."""
     M, Kred = A.shape
     Nout = Wq.shape[0]
     if tuple(Wq.shape) != (Nout, Kred // 8) or tuple(C.shape) != (M, Nout) or \
@@ -311,12 +379,14 @@ def qmm_w4a16_g128(A: torch.Tensor, Wq: torch.Tensor, scales: torch.Tensor,
         ws, ws_bytes = ctypes.c_void_p(workspace.data_ptr()), \
             workspace.numel() * workspace.element_size()
     used = _I(0)
-    rc = lib().qmm_w4a16_g128(
-        _dev(A, _BF16, "A"), _dev(Wq, _WORDS, "Wq"), _dev(scales, _BF16, "scales"),
-        _dev(biases, _BF16, "biases"), _dev(C, _BF16, "C"), M, Kred, Nout, split_req,
-        ctypes.byref(pol) if pol is not None else None, ws, ws_bytes, partial_dtype,
-        _stream(stream), ctypes.byref(used))
-    _check(rc, "qmm_w4a16_g128")
+    args = (_dev(A, _BF16, "A"), _dev(Wq, _WORDS, "Wq"), _dev(scales, _BF16, "scales"),
+            _dev(biases, _BF16, "biases"), _dev(C, _BF16, "C"), M, Kred, Nout, split_req,
+            ctypes.byref(pol) if pol is not None else None, ws, ws_bytes, partial_dtype,
+            _stream(stream), ctypes.byref(used))
+    if options is not None:
+        _check(lib().qmm_w4a16_g128_ex(*args, _opt(options)), "qmm_w4a16_g128_ex")
+    else:
+        _check(lib().qmm_w4a16_g128(*args), "qmm_w4a16_g128")
     return used.value
 
 
@@ -549,12 +619,16 @@ def group_calls(calls) -> "ctypes.Array":
     return arr
 
 
-def qmm_group_workspace_bytes(calls, partial_dtype: int = QMM_PARTIAL_BF16) -> int:
+def qmm_group_workspace_bytes(calls, partial_dtype: int = QMM_PARTIAL_BF16,
+                              options=None) -> int:
+    if options is not None:
+        return int(lib().qmm_group_workspace_bytes_ex(calls, len(calls), partial_dtype,
+                                                       _opt(options)))
     return int(lib().qmm_group_workspace_bytes(calls, len(calls), partial_dtype))
 
 
 def qmm_w4a16_g128_grouped(calls, workspace: torch.Tensor | None = None,
-                           partial_dtype: int = QMM_PARTIAL_BF16, stream=None):
+                           partial_dtype: int = QMM_PARTIAL_BF16, stream=None, options=None):
     """Every call's C with its policy split, in few launches; returns the splits."""
     n = len(calls)
     used = (_I * n)()
@@ -562,8 +636,11 @@ def qmm_w4a16_g128_grouped(calls, workspace: torch.Tensor | None = None,
     if workspace is not None:
         ws_ptr = _dev(workspace, (workspace.dtype,), "workspace")
         ws_bytes = workspace.numel() * workspace.element_size()
-    _check(lib().qmm_w4a16_g128_grouped(calls, n, ws_ptr, ws_bytes, partial_dtype,
-                                        _stream(stream), used), "qmm_w4a16_g128_grouped")
+    args = (calls, n, ws_ptr, ws_bytes, partial_dtype, _stream(stream), used)
+    if options is not None:
+        _check(lib().qmm_w4a16_g128_grouped_ex(*args, _opt(options)), "qmm_w4a16_g128_grouped_ex")
+    else:
+        _check(lib().qmm_w4a16_g128_grouped(*args), "qmm_w4a16_g128_grouped")
     return list(used)
 
 

@@ -167,11 +167,12 @@ def test_argument_errors_before_any_cuda_work():
     assert call(a, w, s, b, c, 0, 2560, 1024, 0, None, None, 0, 0, None, None) == Q.QMM_EINVAL
     assert call(a, w, s, b, c, 16, 2500, 1024, 0, None, None, 0, 0, None, None) == Q.QMM_ESHAPE
     assert call(a, w, s, b, c, 16, 2560, 1024, 0, None, None, 0, 5, None, None) == Q.QMM_EINVAL
-    # negative split requests other than QMM_SPLIT_PLANNED are rejected
-    assert call(a, w, s, b, c, 16, 2560, 1024, -2, None, None, 0, 0, None, None) == Q.QMM_EINVAL
-    # (a planned split request passes validation and then needs the device)
-    assert call(a, w, s, b, c, 16, 2560, 1024, Q.QMM_SPLIT_PLANNED, None, None, 0, 0, None,
-                None) in (Q.QMM_ENODEV, Q.QMM_EWORKSPACE)
+    # negative split requests other than QMM_SPLIT_PLANNED / BALANCED are rejected
+    assert call(a, w, s, b, c, 16, 2560, 1024, -3, None, None, 0, 0, None, None) == Q.QMM_EINVAL
+    # (a planned or balanced split request passes validation and then needs the device)
+    for req in (Q.QMM_SPLIT_PLANNED, Q.QMM_SPLIT_BALANCED):
+        assert call(a, w, s, b, c, 16, 2560, 1024, req, None, None, 0, 0, None,
+                    None) in (Q.QMM_ENODEV, Q.QMM_EWORKSPACE)
     assert call(P(0x10002), w, s, b, c, 16, 2560, 1024, 0, None, None, 0, 0, None, None) == \
         Q.QMM_EALIGN
     assert call(a, w, P(0x30001), b, c, 16, 2560, 1024, 0, None, None, 0, 0, None, None) == \
@@ -196,13 +197,15 @@ def test_noalloc_checks_match_the_main_entry_point():
     cases = [
         (a, 16, 2, ctypes.byref(bad)),         # invalid policy with a forced split
         (a, 16, 0, ctypes.byref(bad)),         # invalid policy with the policy split
-        (a, 16, -2, None),                     # negative request other than QMM_SPLIT_PLANNED
+        (a, 16, -3, None),                     # negative request other than the named ones
         (P(0x10002), 2048, 20, None),          # misaligned A, planes far beyond the buffer
         (P(0x10002), 16, Q.QMM_SPLIT_PLANNED, None),
     ]
     for A, M, split, pol in cases:
         assert noalloc(A, M, split, pol) == main(A, M, split, pol), (M, split)
     assert noalloc(a, 16, 2, ctypes.byref(bad)) == Q.QMM_EINVAL
+    # the balanced split needs a grouped launch and is not offered here
+    assert noalloc(a, 16, Q.QMM_SPLIT_BALANCED, None) == Q.QMM_EINVAL
     assert noalloc(P(0x10002), 2048, 20, None) == Q.QMM_EALIGN
     # valid arguments without a usable device: no device, before the limit
     # check and the address lookup
@@ -424,3 +427,131 @@ def test_group_plan_falls_back_to_the_policy_on_huge_launches():
     alone = Q.qmm_group_plan([(16, 2560, 1024)], 152)
     assert alone[0] > 1
     assert Q.qmm_group_plan([(16384, 2560, 16384)] * 8 + [(16, 2560, 1024)], 152) == [1] * 8 + alone
+
+
+# ---- per-call options -------------------------------------------------------
+
+def test_options_init_and_binding_default():
+    o = Q.qmm_options()
+    Q.lib().qmm_options_init(ctypes.byref(o))
+    assert all(getattr(o, f) == Q.QMM_OPT_DEFAULT for f in Q._OPTION_FIELDS)
+    Q.lib().qmm_options_init(None)  # no-op
+
+
+@pytest.mark.parametrize("field,bad", [("kernels", 4), ("partitions", 2), ("reduce", 2),
+                                       ("weights_static", 2), ("pdl", -2),
+                                       ("grouped_schedule", 2), ("group_plan", 5)])
+def test_options_out_of_range_rejected_first(field, bad):
+    o = Q.qmm_options(**{field: bad})
+    s = ctypes.c_int(0)
+    # rejected before the shape check (Kred 100 would be QMM_ESHAPE)
+    rc = Q.lib().qmm_call_plan(16, 100, 1024, 0, None, 0, 152, ctypes.byref(o),
+                               ctypes.byref(s), None, None, None)
+    assert rc == Q.QMM_EINVAL
+    assert Q.lib().qmm_splitk_workspace_bytes_ex(16, 1024, 4, 0, ctypes.byref(o)) == 0
+    # and before any device pointer is looked at
+    rc = Q.lib().qmm_w4a16_g128_ex(None, None, None, None, None, 16, 2560, 1024, 0, None, None,
+                                   0, 0, None, None, ctypes.byref(o))
+    assert rc == Q.QMM_EINVAL
+
+
+def test_options_override_the_process_settings_for_one_call():
+    prev = Q.qmm_set_partitions(Q.QMM_PARTITIONS_EQUAL)
+    try:
+        eq = Q.qmm_call_plan(128, 9728, 2560, num_sms=152)
+        ne = Q.qmm_call_plan(128, 9728, 2560, num_sms=152,
+                             options=Q.qmm_options(partitions=Q.QMM_PARTITIONS_NEAR_EQUAL))
+        pol = Q.qmm_policy_preset(Q.QMM_PRESET_GB300, 128, 152)
+        assert eq[0] == Q.qmm_splitk_plan(128, 9728, 2560, pol) == 4
+        assert ne[0] == Q.qmm_splitk_plan_near_equal(128, 9728, 2560, pol) == 7
+        # the process setting is untouched by the call
+        assert Q.qmm_set_partitions(Q.QMM_PARTITIONS_EQUAL) == Q.QMM_PARTITIONS_EQUAL
+        Q.qmm_set_partitions(Q.QMM_PARTITIONS_NEAR_EQUAL)
+        assert Q.qmm_call_plan(128, 9728, 2560, num_sms=152)[0] == 7
+        assert Q.qmm_call_plan(128, 9728, 2560, num_sms=152,
+                               options=Q.qmm_options(partitions=Q.QMM_PARTITIONS_EQUAL))[0] == 4
+    finally:
+        Q.qmm_set_partitions(prev)
+    # the kernel table picks the tile; the fused reduce adds its counter area
+    assert Q.qmm_call_plan(32, 2560, 9728, num_sms=152,
+                           options=Q.qmm_options(kernels=Q.QMM_KERNELS_MMA_SYNC))[1:] == \
+        (32, 128)
+    plain = Q.qmm_splitk_workspace_bytes(128, 1024, 10)
+    fused = Q.qmm_splitk_workspace_bytes(128, 1024, 10,
+                                         options=Q.qmm_options(reduce=Q.QMM_REDUCE_FUSED))
+    assert plain == 10 * 128 * 1024 * 2 and fused > plain
+
+
+def test_options_two_threads_get_their_own_rule():
+    """Two threads plan the same call under different partition rules while
+    the process-wide rule is a third party's: each always gets its own."""
+    import threading
+    want = {Q.QMM_PARTITIONS_EQUAL: 4, Q.QMM_PARTITIONS_NEAR_EQUAL: 7}
+    errors = []
+    barrier = threading.Barrier(3)
+
+    def worker(rule):
+        o = Q.qmm_options(partitions=rule)
+        barrier.wait()
+        for _ in range(2000):
+            if Q.qmm_call_plan(128, 9728, 2560, num_sms=152, options=o)[0] != want[rule]:
+                errors.append(rule)
+                return
+
+    def flipper():
+        barrier.wait()
+        for i in range(2000):
+            Q.qmm_set_partitions(i & 1)
+
+    prev = Q.qmm_set_partitions(Q.QMM_PARTITIONS_EQUAL)
+    try:
+        ts = [threading.Thread(target=worker, args=(r,)) for r in want] + \
+            [threading.Thread(target=flipper)]
+        for t in ts:
+            t.start()
+        for t in ts:
+            t.join()
+    finally:
+        Q.qmm_set_partitions(prev)
+    assert not errors
+
+
+# ---- balanced split plan -------------------------------------------------------
+
+@pytest.mark.parametrize("sms", [148, 152])
+@pytest.mark.parametrize("name", sorted(inputs.PROJECTIONS))
+@pytest.mark.parametrize("M", [300, 1000, 2048, 4096])
+def test_balanced_plan_structure(sms, name, M):
+    """QMM_SPLIT_BALANCED cuts only calls with a partial last wave, at whole row
+    tiles that fit the full waves, and splits the tail at a split the
+    partition rule accepts; the workspace holds exactly the tail's planes."""
+    Kred, Nout = inputs.PROJECTIONS[name]
+    s, bm, bn, head = Q.qmm_call_plan(M, Kred, Nout, Q.QMM_SPLIT_BALANCED, num_sms=sms,
+                                      with_head=True)
+    rt, ct = -(-M // bm), -(-Nout // bn)
+    G = Kred // 128
+    ws = Q.qmm_call_workspace_bytes(M, Kred, Nout, Q.QMM_SPLIT_BALANCED, num_sms=sms)
+    if head == 0:
+        assert s == Q.qmm_call_plan(M, Kred, Nout, Q.QMM_SPLIT_PLANNED, num_sms=sms)[0]
+        assert ws == Q.qmm_splitk_workspace_bytes(M, Nout, s)
+        return
+    tiles = rt * ct
+    assert tiles > sms and tiles % sms != 0
+    assert head % bm == 0 and 0 < head < M
+    assert (head // bm) * ct <= tiles // sms * sms
+    assert 1 <= s <= min(16, G) and G % s == 0
+    assert ws == (s * (M - head) * Nout * 2 if s > 1 else 0)
+
+
+def test_balanced_plan_cuts_the_wave_tail_of_down_and_o():
+    for name in ("down", "o"):
+        Kred, Nout = inputs.PROJECTIONS[name]
+        s, bm, _, head = Q.qmm_call_plan(2048, Kred, Nout, Q.QMM_SPLIT_BALANCED, num_sms=152,
+                                         with_head=True)
+        # 8 x 20 tiles of 256 x 128: 7 row tiles fill the first wave
+        assert (bm, head) == (256, 1792) and s > 1
+    # no partial wave (gate: 608 = 4 x 152) or no full wave (k: 64 tiles): no cut
+    for name in ("gate", "k"):
+        Kred, Nout = inputs.PROJECTIONS[name]
+        assert Q.qmm_call_plan(2048, Kred, Nout, Q.QMM_SPLIT_BALANCED, num_sms=152,
+                               with_head=True)[3] == 0

@@ -1260,3 +1260,117 @@ def test_attention_errors_on_device():
         Q.qmm_decode_attention(d["q"], d["K"], d["V"], d["lens"], O, splits_req=4,
                                workspace=small)
     assert e.value.code == Q.QMM_EWORKSPACE
+
+
+# ---- per-call options ---------------------------------------------------------
+
+def test_options_two_threads_on_the_gpu():
+    """Two threads call qmm_w4a16_g128_ex on the same inputs under different
+    partition rules (down at M = 128: split 4 equal, 7 near-equal) while the
+    process-wide rule flips: each thread's result is bitwise the one its own
+    rule gives alone, and within tolerance of the oracle at that split."""
+    import threading
+    M, (Kred, Nout) = 128, inputs.PROJECTIONS["down"]
+    p = inputs.make_w4a16(M, Kred, Nout, seed=71)
+    d = Q.to_device(p)
+    rules = (Q.QMM_PARTITIONS_EQUAL, Q.QMM_PARTITIONS_NEAR_EQUAL)
+    opts = {r: Q.qmm_options(partitions=r) for r in rules}
+    wsb = max(Q.qmm_splitk_workspace_bytes(M, Nout, 16, options=o) for o in opts.values())
+
+    def call(rule, stream):
+        ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+        C = torch.empty((M, Nout), dtype=torch.bfloat16, device="cuda")
+        with torch.cuda.stream(stream):
+            s = Q.qmm_w4a16_g128(d["A"], d["Wq"], d["scales"], d["biases"], C, workspace=ws,
+                                 stream=stream, options=opts[rule])
+        stream.synchronize()
+        return _bits(C), s
+
+    base = {r: call(r, torch.cuda.Stream()) for r in rules}
+    assert base[rules[0]][1] == 4 and base[rules[1]][1] == 7
+    for r in rules:
+        got, s = base[r]
+        _check_sampled(p, got, s, Q.QMM_PARTIAL_BF16, np.arange(0, M, 9),
+                       np.arange(0, Nout, 37), "options rule %d" % r)
+    errors = []
+    stop = threading.Event()
+
+    def worker(rule):
+        try:
+            st = torch.cuda.Stream()
+            for _ in range(20):
+                got, s = call(rule, st)
+                if s != base[rule][1] or not np.array_equal(got, base[rule][0]):
+                    errors.append("rule %d: split %d, bits differ" % (rule, s))
+                    return
+        except Exception as e:  # reported by the assertion below
+            errors.append("rule %d: %r" % (rule, e))
+
+    def flipper():
+        i = 0
+        while not stop.is_set():
+            Q.qmm_set_partitions(i & 1)
+            i += 1
+
+    prev = Q.qmm_set_partitions(Q.QMM_PARTITIONS_EQUAL)
+    try:
+        f = threading.Thread(target=flipper)
+        ws_ = [threading.Thread(target=worker, args=(r,)) for r in rules]
+        f.start()
+        for t in ws_:
+            t.start()
+        for t in ws_:
+            t.join()
+        stop.set()
+        f.join()
+    finally:
+        Q.qmm_set_partitions(prev)
+    assert not errors
+
+
+# ---- balanced split (QMM_SPLIT_BALANCED) ----------------------------------------
+
+@pytest.mark.parametrize("name", ["down", "o"])
+def test_balanced_split_rows(name):
+    """The balanced split of a call with a partial last wave (160 tiles on 152
+    SMs): rows [0, head) are bitwise the unsplit call's, rows [head, M)
+    bitwise those of a call on those rows alone at the tail's split, and both
+    ranges agree with the oracle on sampled elements."""
+    M, (Kred, Nout) = 2048, inputs.PROJECTIONS[name]
+    p = inputs.make_w4a16(M, Kred, Nout, seed=81)
+    d = Q.to_device(p)
+    split, bm, bn, head = Q.qmm_call_plan(M, Kred, Nout, Q.QMM_SPLIT_BALANCED, with_head=True)
+    assert 0 < head < M and head % bm == 0 and split > 1
+    nbytes = Q.qmm_call_workspace_bytes(M, Kred, Nout, Q.QMM_SPLIT_BALANCED)
+    assert nbytes == split * (M - head) * Nout * 2
+    ws = torch.full((nbytes // 2,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    C = torch.empty((M, Nout), dtype=torch.bfloat16, device="cuda")
+    used = Q.qmm_w4a16_g128(d["A"], d["Wq"], d["scales"], d["biases"], C,
+                            split_req=Q.QMM_SPLIT_BALANCED, workspace=ws)
+    assert used == split
+    C1 = torch.empty_like(C)
+    Q.qmm_w4a16_g128(d["A"], d["Wq"], d["scales"], d["biases"], C1, split_req=1)
+    At = d["A"][head:].contiguous()
+    Ct = torch.empty((M - head, Nout), dtype=torch.bfloat16, device="cuda")
+    wt = torch.empty(Q.qmm_splitk_workspace_bytes(M - head, Nout, split), dtype=torch.uint8,
+                     device="cuda")
+    Q.qmm_w4a16_g128(At, d["Wq"], d["scales"], d["biases"], Ct, split_req=split, workspace=wt)
+    torch.cuda.synchronize()
+    got = _bits(C)
+    assert np.array_equal(got[:head], _bits(C1)[:head]), "head rows differ from the unsplit call"
+    assert np.array_equal(got[head:], _bits(Ct)), "tail rows differ from the tail call"
+    cols = np.arange(3, Nout, 97)
+    _check_sampled(p, got, 1, Q.QMM_PARTIAL_BF16, np.arange(0, head, 211), cols, "head")
+    pt = dict(p, A=p["A"][head:])
+    _check_sampled(pt, got[head:], split, Q.QMM_PARTIAL_BF16, np.arange(0, M - head, 17), cols,
+                   "tail")
+
+
+def test_balanced_split_without_a_partial_wave_is_the_planned_split():
+    # gate at M = 2048: 608 tiles, four full waves on 152 SMs: nothing to cut
+    M, (Kred, Nout) = 2048, inputs.PROJECTIONS["gate"]
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    s, _, _, head = Q.qmm_call_plan(M, Kred, Nout, Q.QMM_SPLIT_BALANCED, with_head=True)
+    if (M // 256) * (Nout // 128) % sms == 0:
+        assert head == 0
+    assert s == Q.qmm_call_plan(M, Kred, Nout, Q.QMM_SPLIT_PLANNED)[0] or head > 0
