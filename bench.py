@@ -419,6 +419,7 @@ def run_gpu(args, rank, world, local_rank):
     ms_nopdl = time_variant(Q.qmm_set_pdl, False)
     ms_wflip = time_variant(Q.qmm_set_weights_static, not static_weights)
     ms_fused = time_variant(Q.qmm_set_reduce, Q.QMM_REDUCE_FUSED)
+    ms_cluster = time_variant(Q.qmm_set_reduce, Q.QMM_REDUCE_CLUSTER)
     ms_alt = time_variant(Q.qmm_set_partitions, alt_rule)
 
     # the same 14 calls as one grouped call per step (qmm_w4a16_g128_grouped):
@@ -541,7 +542,7 @@ def run_gpu(args, rank, world, local_rank):
     e2e = run_e2e(wl, Q, device, stream, min(args.steps, 20))
     overlap = overlap_sweep(wl, Q, device) if rank == 0 else None
     attention = attention_bench(Q, device, stream, peaks, l2) if rank == 0 else None
-    return {"ms": ms, "ms_nopdl": ms_nopdl, "ms_wflip": ms_wflip, "ms_fused": ms_fused,
+    return {"ms": ms, "ms_nopdl": ms_nopdl, "ms_wflip": ms_wflip, "ms_fused": ms_fused, "ms_cluster": ms_cluster,
             "ms_alt": ms_alt, "ms_grouped": ms_grouped,
             "ms_grouped_tiles": ms_grouped_tiles, "ms_grouped_plan": ms_grouped_plan,
             "group_plan_splits": group_plan_splits, "grouped_launches": grouped_launches,
@@ -1175,6 +1176,8 @@ def main():
            ("value_weights_dynamic" if args.weights == "static" else "value_weights_static"):
                round(job_value_us(res["ms_wflip"], 1, args.steps, ncalls), 4),
            "value_fused_reduce": round(job_value_us(res["ms_fused"], 1, args.steps, ncalls), 4),
+           "value_cluster_reduce": round(job_value_us(res["ms_cluster"], 1, args.steps, ncalls),
+                                         4),
            ("value_near_equal" if args.partitions == "equal" else "value_equal_partitions"):
                round(job_value_us(res["ms_alt"], 1, args.steps, ncalls), 4),
            "value_grouped": round(job_value_us(res["ms_grouped"], 1, args.steps, ncalls), 4),

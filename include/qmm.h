@@ -290,9 +290,21 @@ int qmm_set_pdl(int enable);
  *       it in QMM_REDUCE_KERNEL mode.  Every call leaves the counters zero,
  *       also when a bounded wait ran out.  Calls that share a workspace must
  *       not overlap on the GPU.
+ *   QMM_REDUCE_CLUSTER  a one-launch variant of Task 4 for the tcgen05
+ *       kernels that keeps the planes on chip: the split partitions of one
+ *       output tile run as one thread-block cluster (up to 16 CTAs), each
+ *       stages its partial tile (BF16-rounded, or FP32) in shared memory, and
+ *       after a cluster barrier each CTA adds a slice of the tile over every
+ *       partition, read through distributed shared memory, in FP32 in
+ *       ascending partition order with one cast: the same C bit for bit.  No
+ *       plane reaches global memory.  A call whose clusters the device cannot
+ *       hold all at once, or whose partial tile does not fit the kernel's
+ *       staging area, takes the planes and the reduce kernel as in
+ *       QMM_REDUCE_KERNEL; size the workspace as for that mode either way.
+ *       Single calls only (the grouped call always uses the reduce kernel).
  * Returns the previous mode, or QMM_EINVAL for an unknown mode. */
 #define QMM_FUSED_COUNTER_BYTES 32768
-enum { QMM_REDUCE_KERNEL = 0, QMM_REDUCE_FUSED = 1 };
+enum { QMM_REDUCE_KERNEL = 0, QMM_REDUCE_FUSED = 1, QMM_REDUCE_CLUSTER = 2 };
 int qmm_set_reduce(int mode);
 
 /* Partition rule of the W4A16 calls (process-wide, thread-safe):

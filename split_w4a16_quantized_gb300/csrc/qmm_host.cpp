@@ -92,7 +92,7 @@ bool in_range(int v, int lo, int hi) { return v == QMM_OPT_DEFAULT || (v >= lo &
 bool options_valid(const qmm_options* o) {
     return !o || (in_range(o->kernels, QMM_KERNELS_DEFAULT, QMM_KERNELS_LEAN) &&
                   in_range(o->partitions, QMM_PARTITIONS_EQUAL, QMM_PARTITIONS_NEAR_EQUAL) &&
-                  in_range(o->reduce, QMM_REDUCE_KERNEL, QMM_REDUCE_FUSED) &&
+                  in_range(o->reduce, QMM_REDUCE_KERNEL, QMM_REDUCE_CLUSTER) &&
                   in_range(o->weights_static, 0, 1) && in_range(o->pdl, 0, 1) &&
                   in_range(o->grouped_schedule, QMM_GROUPED_TILES, QMM_GROUPED_PERSISTENT) &&
                   in_range(o->group_plan, QMM_GROUP_PLAN_CALLS, QMM_GROUP_PLAN_GROUP));
@@ -160,6 +160,8 @@ bool weights_static() { return setting(&qmm_options::weights_static, g_wstatic) 
 
 bool reduce_fused() { return setting(&qmm_options::reduce, g_reduce) == QMM_REDUCE_FUSED; }
 
+bool reduce_cluster() { return setting(&qmm_options::reduce, g_reduce) == QMM_REDUCE_CLUSTER; }
+
 bool partitions_near_equal() {
     return setting(&qmm_options::partitions, g_partitions) == QMM_PARTITIONS_NEAR_EQUAL;
 }
@@ -226,7 +228,8 @@ int qmm_set_pdl(int enable) { return g_pdl.exchange(enable ? 1 : 0); }
 int qmm_set_weights_static(int enable) { return g_wstatic.exchange(enable ? 1 : 0); }
 
 int qmm_set_reduce(int mode) {
-    if (mode != QMM_REDUCE_KERNEL && mode != QMM_REDUCE_FUSED) return QMM_EINVAL;
+    if (mode != QMM_REDUCE_KERNEL && mode != QMM_REDUCE_FUSED && mode != QMM_REDUCE_CLUSTER)
+        return QMM_EINVAL;
     return g_reduce.exchange(mode);
 }
 
@@ -534,7 +537,17 @@ int qmm_w4a16_g128(const void* A, const uint32_t* Wq, const void* scales, const 
         if (!workspace || ws_bytes < need) return QMM_EWORKSPACE;
         if (!aligned(workspace, 16)) return QMM_EALIGN;
         const int mode = partial_dtype == QMM_PARTIAL_F32 ? qmm::kOutF32 : qmm::kOutBf16;
-        if (fused_applies(fam, M, Nout, split)) {
+        int ce = cudaErrorNotSupported;
+        // one launch: the tile's partitions add their partial tiles in a cluster
+        if (qmm::reduce_cluster() && fam.kind == qmm::kKindTc)
+            ce = qmm::launch_w4a16_tc_cluster(fam.bm, A, Wq, scales, biases, C, mode, M, Kred,
+                                              Nout, split, stream);
+        else if (qmm::reduce_cluster() && fam.kind == qmm::kKindLean)
+            ce = qmm::launch_w4a16_lean_cluster(fam.bm, A, Wq, scales, biases, C, mode, M, Kred,
+                                                Nout, split, stream);
+        if (ce != cudaErrorNotSupported) {
+            rc = launched(ce);
+        } else if (fused_applies(fam, M, Nout, split)) {
             // one launch: the last CTA of each output tile adds the planes
             rc = launched(qmm::launch_w4a16(fam, A, Wq, scales, biases, workspace, mode, M, Kred,
                                             Nout, split, stream, C,

@@ -95,6 +95,8 @@ bool pdl_enabled();
 bool weights_static();
 // Fused last-CTA reduce of the tcgen05 kernels (qmm_set_reduce).
 bool reduce_fused();
+// Cluster reduce of the tcgen05 kernels (qmm_set_reduce).
+bool reduce_cluster();
 // Near-equal partitions for splits that do not divide the groups (qmm_set_partitions).
 bool partitions_near_equal();
 // Persistent schedule of the grouped call's tcgen05 launches (qmm_set_grouped_schedule).
@@ -141,6 +143,15 @@ int launch_w4a16_lean(int bm, const void* A, const uint32_t* Wq, const void* sca
 int launch_w4a16_tc(int bm, const void* A, const uint32_t* Wq, const void* scales, const void* biases,
                     void* out, int out_mode, int M, int Kred, int Nout, int split, void* stream,
                     void* fused_C = nullptr, uint32_t* counters = nullptr);
+// The call with the cluster reduce (QMM_REDUCE_CLUSTER); cudaErrorNotSupported,
+// with nothing launched, where it does not apply (the caller then takes the
+// planes and the reduce kernel).
+int launch_w4a16_lean_cluster(int bm, const void* A, const uint32_t* Wq, const void* scales,
+                              const void* biases, void* C, int out_mode, int M, int Kred,
+                              int Nout, int split, void* stream);
+int launch_w4a16_tc_cluster(int bm, const void* A, const uint32_t* Wq, const void* scales,
+                            const void* biases, void* C, int out_mode, int M, int Kred, int Nout,
+                            int split, void* stream);
 int read_tc_status(int* out, bool clear);
 // Device address of the status word the tcgen05 and attention kernels share.
 int* tc_status_ptr();

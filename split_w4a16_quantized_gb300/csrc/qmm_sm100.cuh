@@ -267,4 +267,88 @@ __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
 }
 
+
+// ---- thread-block clusters ----------------------------------------------------
+
+// Barrier over every thread of the cluster, ordering shared-memory writes
+// before it (release) against reads after it (acquire) across the cluster.
+__device__ __forceinline__ void cluster_barrier() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n"
+                 "barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_map(uint32_t local, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(local), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ uint4 cluster_ld16(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];\n"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+
+// The cluster reduce of one output tile: `split` partners (cluster ranks
+// 0..split-1) each staged their partial tile of rows x cols at `staged`
+// ([row][pitch] elements, BF16 or FP32 when f32); this CTA adds its share of
+// the rows -- rank r takes rows [r * per, (r + 1) * per), per = ceil(rows /
+// split) -- over every partner in ascending rank order in FP32, rounds once
+// and stores into C (row-major, leading dimension ldc, already offset to the
+// tile).  Called by nthreads threads with index t, between two
+// cluster_barrier()s.
+static __device__ __noinline__ void cluster_add_tile(const void* staged, int pitch, bool f32, int rows,
+                                              int cols, int split, __nv_bfloat16* C, int ldc,
+                                              int t, int nthreads) {
+    const int rank = static_cast<int>(cluster_rank());
+    const int per = (rows + split - 1) / split;
+    const int r0 = rank * per, r1 = r0 + per < rows ? r0 + per : rows;
+    const int chunks = pitch / 8;
+    const uint32_t base = smem_addr(staged);
+    for (int it = t; it < (r1 > r0 ? r1 - r0 : 0) * chunks; it += nthreads) {
+        const int m = r0 + it / chunks, c8 = (it % chunks) * 8;
+        if (c8 >= cols) continue;
+        float v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = 0.f;
+        const uint32_t off = static_cast<uint32_t>(m * pitch + c8) * (f32 ? 4u : 2u);
+        for (int q = 0; q < split; ++q) {
+            const uint32_t a = cluster_map(base + off, static_cast<uint32_t>(q));
+            if (f32) {
+                const uint4 x = cluster_ld16(a), y = cluster_ld16(a + 16);
+                v[0] += __uint_as_float(x.x); v[1] += __uint_as_float(x.y);
+                v[2] += __uint_as_float(x.z); v[3] += __uint_as_float(x.w);
+                v[4] += __uint_as_float(y.x); v[5] += __uint_as_float(y.y);
+                v[6] += __uint_as_float(y.z); v[7] += __uint_as_float(y.w);
+            } else {
+                const uint4 x = cluster_ld16(a);
+                const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    v[2 * j] += __uint_as_float(w[j] << 16);
+                    v[2 * j + 1] += __uint_as_float(w[j] & 0xFFFF0000u);
+                }
+            }
+        }
+        __nv_bfloat16* dst = C + static_cast<size_t>(m) * ldc + c8;
+        if ((ldc & 7) == 0 && c8 + 8 <= cols) {
+            uint4 o;
+            o.x = pack_bf16x2(v[0], v[1]);
+            o.y = pack_bf16x2(v[2], v[3]);
+            o.z = pack_bf16x2(v[4], v[5]);
+            o.w = pack_bf16x2(v[6], v[7]);
+            *reinterpret_cast<uint4*>(dst) = o;
+        } else {
+            for (int j = 0; j < 8 && c8 + j < cols; ++j) dst[j] = __float2bfloat16_rn(v[j]);
+        }
+    }
+}
+
 }  // namespace qmm

@@ -100,6 +100,7 @@ struct LeanCfg {
     static constexpr int NA_MAX = (BUDGET - WRING) / STAGE;
     static constexpr int EPI_LD = BN + 4;             // FP32 epilogue row pitch (floats)
     static constexpr int EPI = WK * BM * EPI_LD * 4;
+    static constexpr int STG = BM * BN * 4;           // cluster reduce: the staged partial tile
     static_assert(STAGE % 1024 == 0, "swizzled stages start on 1024-byte boundaries");
     static_assert(NA_MAX >= 2, "ring depth");
 };
@@ -117,6 +118,8 @@ struct LeanParams {
     int split, out_mode, fused, wstatic;
     int na;                  // activation ring stages
     int ring_bytes;          // shared memory of the activation ring (and epilogue buffer)
+    int cluster;             // 1: the partitions of a column tile are one cluster and add
+                             //    their staged partial tiles into C (cluster reduce)
 };
 
 // Per-thread view of the CTA: row slice rs, k slice ks, lane (g, t).
@@ -444,6 +447,23 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS)
             v[0] += x.x; v[1] += x.y; v[2] += x.z; v[3] += x.w;
             v[4] += y.x; v[5] += y.y; v[6] += y.z; v[7] += y.w;
         }
+        if (p.cluster) {
+            // the partition's tile, rounded as its plane would be, stays on chip
+            uint8_t* stg = ring + Cfg::EPI;
+            if (p.out_mode == kOutBf16) {
+                uint4 w;
+                w.x = pack_bf16x2(v[0], v[1]);
+                w.y = pack_bf16x2(v[2], v[3]);
+                w.z = pack_bf16x2(v[4], v[5]);
+                w.w = pack_bf16x2(v[6], v[7]);
+                *reinterpret_cast<uint4*>(stg + (m * BN + c * 8) * 2) = w;
+            } else {
+                float4* dst = reinterpret_cast<float4*>(stg + (m * BN + c * 8) * 4);
+                dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+                dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+            }
+            continue;
+        }
         const size_t o = plane + static_cast<size_t>(m) * p.Nout + n;
         if (p.out_mode == kOutBf16) {
             __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + o;
@@ -466,6 +486,17 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS)
                 for (int j = 0; j < 8 && n + j < p.Nout; ++j) dst[j] = v[j];
             }
         }
+    }
+
+    if (p.cluster) {
+        // every thread of every partition's CTA passes both barriers, also
+        // after a wait ran out (C is then invalid, as the status word says)
+        cluster_barrier();  // every partner's partial tile is staged
+        cluster_add_tile(ring + Cfg::EPI, BN, p.out_mode == kOutF32, p.M,
+                         p.Nout - n0 < BN ? p.Nout - n0 : BN, p.split, p.C + n0, p.Nout, tid,
+                         Cfg::THREADS);
+        cluster_barrier();  // every partner has read this CTA's tile
+        return;
     }
 
     if (p.fused) {
@@ -543,12 +574,19 @@ int launch_cfg(const LeanParams& p0, const void* A, int split, cudaStream_t stre
     auto kern = w4a16_lean_kernel<Cfg>;
     static int limit = -1;
     static std::once_flag once;
-    std::call_once(once, [&] { limit = set_max_dynamic_smem(reinterpret_cast<const void*>(kern)); });
-    if (limit < 0) return cudaErrorInvalidValue;
+    std::call_once(once, [&] {
+        limit = set_max_dynamic_smem(reinterpret_cast<const void*>(kern));
+        if (limit >= 0 && cudaFuncSetAttribute(reinterpret_cast<const void*>(kern),
+                                               cudaFuncAttributeNonPortableClusterSizeAllowed,
+                                               1) != cudaSuccess)
+            limit = -1;
+    });
+    if (limit < 0) return p0.cluster ? cudaErrorNotSupported : cudaErrorInvalidValue;
     LeanParams p = p0;
     const int nst = (p.gpp + Cfg::AG - 1) / Cfg::AG;
     p.na = nst < Cfg::NA_MAX ? nst : Cfg::NA_MAX;
-    const int ring = p.na * Cfg::STAGE > Cfg::EPI ? p.na * Cfg::STAGE : Cfg::EPI;
+    const int epi = Cfg::EPI + Cfg::STG;
+    const int ring = p.na * Cfg::STAGE > epi ? p.na * Cfg::STAGE : epi;
     p.ring_bytes = (ring + 1023) / 1024 * 1024;
     const size_t smem = 1024 + static_cast<size_t>(p.ring_bytes) + Cfg::WRING +
                         static_cast<size_t>(p.gpp) * Cfg::BN * 4 + static_cast<size_t>(p.na) * 16;
@@ -570,6 +608,26 @@ int launch_cfg(const LeanParams& p0, const void* A, int split, cudaStream_t stre
     cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
+    if (!p.cluster) return cudaLaunchKernelEx(&cfg, kern, amap, p);
+    // cluster reduce: the split partitions of a column tile form one cluster;
+    // taken only if the device holds every cluster of the call at once
+    if (split < 2 || split > 16) return cudaErrorNotSupported;
+    cudaLaunchAttribute attrs[2];
+    int na = 0;
+    attrs[na].id = cudaLaunchAttributeClusterDimension;
+    attrs[na].val.clusterDim.x = 1;
+    attrs[na].val.clusterDim.y = static_cast<unsigned>(split);
+    attrs[na].val.clusterDim.z = 1;
+    ++na;
+    if (cfg.numAttrs) attrs[na++] = la.attr[0];
+    cfg.attrs = attrs;
+    cfg.numAttrs = na;
+    int active = 0;
+    if (cudaOccupancyMaxActiveClusters(&active, kern, &cfg) != cudaSuccess) {
+        cudaGetLastError();  // a refused query is not the caller's error
+        return cudaErrorNotSupported;
+    }
+    if (active < static_cast<int>(cfg.gridDim.x)) return cudaErrorNotSupported;
     return cudaLaunchKernelEx(&cfg, kern, amap, p);
 }
 
@@ -587,10 +645,31 @@ static_assert(Lean32::BM == kLeanFamilies[2].bm && Lean32::BN == kLeanFamilies[2
 
 }  // namespace
 
+namespace {
+int launch_lean(int bm, const void* A, const uint32_t* Wq, const void* scales,
+                const void* biases, void* out, int out_mode, int M, int Kred, int Nout,
+                int split, void* stream, void* fused_C, uint32_t* counters, bool cluster);
+}  // namespace
+
 int launch_w4a16_lean(int bm, const void* A, const uint32_t* Wq, const void* scales,
                       const void* biases, void* out, int out_mode, int M, int Kred, int Nout,
                       int split, void* stream, void* fused_C, uint32_t* counters) {
-    if (M > bm || split < 1) return cudaErrorInvalidValue;
+    return launch_lean(bm, A, Wq, scales, biases, out, out_mode, M, Kred, Nout, split, stream,
+                       fused_C, counters, false);
+}
+
+int launch_w4a16_lean_cluster(int bm, const void* A, const uint32_t* Wq, const void* scales,
+                              const void* biases, void* C, int out_mode, int M, int Kred,
+                              int Nout, int split, void* stream) {
+    return launch_lean(bm, A, Wq, scales, biases, C, out_mode, M, Kred, Nout, split, stream, C,
+                       nullptr, true);
+}
+
+namespace {
+int launch_lean(int bm, const void* A, const uint32_t* Wq, const void* scales,
+                const void* biases, void* out, int out_mode, int M, int Kred, int Nout,
+                int split, void* stream, void* fused_C, uint32_t* counters, bool cluster) {
+    if (M > bm || split < 1) return cluster ? cudaErrorNotSupported : cudaErrorInvalidValue;
     LeanParams p = {};
     p.Wq = Wq;
     p.scales = static_cast<const uint16_t*>(scales);
@@ -610,14 +689,16 @@ int launch_w4a16_lean(int bm, const void* A, const uint32_t* Wq, const void* sca
     p.split = split;
     p.out_mode = out_mode;
     p.fused = fused_C != nullptr && counters != nullptr && split > 1 ? 1 : 0;
+    p.cluster = cluster ? 1 : 0;
     p.wstatic = weights_static() && pdl_enabled() ? 1 : 0;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     switch (bm) {
         case 8: return launch_cfg<Lean8>(p, A, split, st);
         case 16: return launch_cfg<Lean16>(p, A, split, st);
         case 32: return launch_cfg<Lean32>(p, A, split, st);
-        default: return cudaErrorInvalidValue;
+        default: return cluster ? cudaErrorNotSupported : cudaErrorInvalidValue;
     }
 }
+}  // namespace
 
 }  // namespace qmm

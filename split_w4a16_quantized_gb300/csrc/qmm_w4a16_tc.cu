@@ -142,6 +142,8 @@ struct TcParams {
     void* C;             // BF16 [M, Nout] (fused reduce)
     uint32_t* counters;  // one per output tile (fused reduce), zero between calls
     int tma_store;  // 1: the output tile leaves through a TMA store of a staged tile
+    int cluster;    // 1: the tile's partitions are one cluster and add their staged
+                    //    partial tiles through distributed shared memory into C
     Ring wr, ar;    // weight ring, activation ring (same groups per stage)
 };
 
@@ -527,6 +529,26 @@ __device__ __noinline__ void reduce_tile(const T* planes, __nv_bfloat16* C, int 
     }
 }
 
+// ---- cluster reduce (QMM_REDUCE_CLUSTER) --------------------------------------
+//
+// The split partitions of one output tile run as one thread-block cluster.
+// Each CTA stages its partial tile in shared memory as [m][n] in the partial
+// type -- BF16-rounded like a plane, or FP32 -- and after a cluster barrier
+// CTA r adds rows [r * per, (r + 1) * per) of every partition's staged tile,
+// read through distributed shared memory in ascending partition order, in
+// FP32, and rounds once into C: the reduce kernel's arithmetic, without the
+// planes in global memory or a second launch (tiny-llm "Week 2 Day 7", Task 4
+// adds the planes in FP32 in partition order).  A second cluster barrier
+// keeps every staged tile alive until all partners have read it.
+template <int BNA>
+__device__ __forceinline__ void cluster_reduce_tile(const uint8_t* staged, const TcParams& p, int n0,
+                                                    int m0, int t, int nthreads) {
+    cluster_add_tile(staged, kWRows, p.out_mode == kOutF32, p.M - m0 < BNA ? p.M - m0 : BNA,
+                     p.Nout - n0 < kWRows ? p.Nout - n0 : kWRows, p.split,
+                     static_cast<__nv_bfloat16*>(p.C) + static_cast<size_t>(m0) * p.Nout + n0,
+                     p.Nout, t, nthreads);
+}
+
 // Epilogue of one warp: columns (activation rows) in 16-column chunks c with
 // c % DSETS == set; the used accumulators are added in a fixed order.  With
 // p.tma_store the tile is staged in shared memory as [m][n] (the activation
@@ -561,7 +583,7 @@ __device__ __forceinline__ void tc_epilogue(const TcSmem& sm, const TcParams& p,
 #pragma unroll
                 for (int j = 0; j < 16; ++j) v[j] += __uint_as_float(d[j]);
             }
-            if (p.tma_store) {
+            if (p.tma_store || p.cluster) {
                 if (p.out_mode == kOutBf16) {
                     __nv_bfloat16* t = reinterpret_cast<__nv_bfloat16*>(sm.act);
 #pragma unroll
@@ -722,6 +744,13 @@ __device__ __forceinline__ void tc_cta(const TcParams& p, const CUtensorMap* wma
     // ---- teardown: every MMA has finished before tensor memory is freed ----
     tc_fence_before();
     __syncthreads();
+    if (p.cluster) {
+        // every thread of every partition's CTA passes both barriers, also
+        // after a wait ran out (C is then invalid, as the status word says)
+        cluster_barrier();  // every partner's partial tile is staged
+        cluster_reduce_tile<BNA>(sm.act, p, n0, m0, tid, C::THREADS);
+        cluster_barrier();  // every partner has read this CTA's tile
+    }
     if (warp == 1) {
         if (lane == 0 && *abort) mbar_wait(sm.acc_full, 0, nullptr, p.status);
         __syncwarp();
@@ -1368,6 +1397,7 @@ bool setup_call(const void* A, const uint32_t* Wq, const void* scales, const voi
     p.fused = fused_C != nullptr && counters != nullptr && split > 1 ? 1 : 0;
     p.C = fused_C;
     p.counters = counters;
+    p.cluster = 0;
     // a partition whose last activation stage holds fewer than AGPS groups
     // fills it through a one-group map
     const bool atails = p.gq % C::AGPS != 0 || (p.gr && (p.gq + 1) % C::AGPS != 0);
@@ -1456,6 +1486,90 @@ int launch_tc(const void* A, const uint32_t* Wq, const void* scales, const void*
     cfg.blockDim = dim3(C::THREADS, 1, 1);
     cfg.dynamicSmemBytes = pl.smem;
     cfg.stream = st;
+    return cudaLaunchKernelEx(&cfg, kern, wmap, amap, amap_1, omap, p);
+}
+
+// The call with the cluster reduce: grid z = partition, cluster (1, 1, split),
+// C written by the partitions' cluster.  cudaErrorNotSupported (nothing
+// launched) when the partial tile cannot be staged in the activation ring or
+// the device cannot hold every cluster of the call at once (a partial wave
+// of clusters would cost more than the reduce kernel it replaces).
+template <int BNA>
+int launch_tc_cluster(const void* A, const uint32_t* Wq, const void* scales, const void* biases,
+                      void* C, int out_mode, int M, int Kred, int Nout, int split,
+                      cudaStream_t st) {
+    using Cf = TcCfg<BNA>;
+    if (split < 2 || split > 16) return cudaErrorNotSupported;
+    auto kern = w4a16_tc_kernel<BNA>;
+    static int limit = -1;
+    static std::once_flag once;
+    std::call_once(once, [&] {
+        limit = set_max_dynamic_smem(reinterpret_cast<const void*>(kern));
+        if (limit >= 0 && cudaFuncSetAttribute(reinterpret_cast<const void*>(kern),
+                                               cudaFuncAttributeNonPortableClusterSizeAllowed,
+                                               1) != cudaSuccess)
+            limit = -1;
+    });
+    if (limit < 0) return cudaErrorNotSupported;
+    int* status = tc_status_ptr();
+    if (!status) return cudaErrorInvalidSymbol;
+    const int G = Kred / kGroup;
+    TcPipeline pl;
+    if (!tc_pipeline<BNA>(G / split + (G % split ? 1 : 0), limit, &pl)) return cudaErrorNotSupported;
+    const size_t tile = static_cast<size_t>(BNA) * kWRows * (out_mode == kOutBf16 ? 2 : 4);
+    if (tile > static_cast<size_t>(pl.act_stages) * Cf::ACT_STAGE) return cudaErrorNotSupported;
+    TcParams p;
+    CUtensorMap wmap, amap, amap_1, omap;
+    if (!setup_call<BNA>(A, Wq, scales, biases, C, out_mode, M, Kred, Nout, split, nullptr,
+                         nullptr, pl, status, &p, &wmap, &amap, &amap_1, &omap))
+        return cudaErrorInvalidValue;
+    p.cluster = 1;
+    p.tma_store = 0;
+    p.C = C;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attrs[2];
+    int na = 0;
+    attrs[na].id = cudaLaunchAttributeClusterDimension;
+    attrs[na].val.clusterDim.x = 1;
+    attrs[na].val.clusterDim.y = 1;
+    attrs[na].val.clusterDim.z = static_cast<unsigned>(split);
+    ++na;
+    if (pdl_enabled()) {
+        attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attrs[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    const int ntile_n = (Nout + kWRows - 1) / kWRows, ntile_m = (M + BNA - 1) / BNA;
+    cfg.gridDim = dim3(ntile_n, ntile_m, split);
+    cfg.blockDim = dim3(Cf::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = pl.smem;
+    cfg.stream = st;
+    cfg.attrs = attrs;
+    cfg.numAttrs = na;
+    // clusters the device holds at once, per (split, shared memory), queried once
+    static std::mutex mu;
+    static int cache_key[32][2];
+    static int cache_val[32];
+    static int cache_n = 0;
+    int active = -1;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (int i = 0; i < cache_n; ++i)
+            if (cache_key[i][0] == split && cache_key[i][1] == static_cast<int>(pl.smem))
+                active = cache_val[i];
+        if (active < 0) {
+            if (cudaOccupancyMaxActiveClusters(&active, kern, &cfg) != cudaSuccess) {
+                cudaGetLastError();  // a refused query is not the caller's error
+                active = 0;
+            }
+            if (cache_n < 32) {
+                cache_key[cache_n][0] = split;
+                cache_key[cache_n][1] = static_cast<int>(pl.smem);
+                cache_val[cache_n++] = active;
+            }
+        }
+    }
+    if (active < ntile_n * ntile_m) return cudaErrorNotSupported;
     return cudaLaunchKernelEx(&cfg, kern, wmap, amap, amap_1, omap, p);
 }
 
@@ -1588,6 +1702,20 @@ int launch_w4a16_tc(int bm, const void* A, const uint32_t* Wq, const void* scale
         case 128: return launch_tc<128>(A, Wq, scales, biases, out, out_mode, M, Kred, Nout, split, fused_C, counters, st);
         case 256: return launch_tc<256>(A, Wq, scales, biases, out, out_mode, M, Kred, Nout, split, fused_C, counters, st);
         default: return cudaErrorInvalidValue;
+    }
+}
+
+int launch_w4a16_tc_cluster(int bm, const void* A, const uint32_t* Wq, const void* scales,
+                            const void* biases, void* C, int out_mode, int M, int Kred, int Nout,
+                            int split, void* stream) {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    switch (bm) {
+        case 16: return launch_tc_cluster<16>(A, Wq, scales, biases, C, out_mode, M, Kred, Nout, split, st);
+        case 32: return launch_tc_cluster<32>(A, Wq, scales, biases, C, out_mode, M, Kred, Nout, split, st);
+        case 64: return launch_tc_cluster<64>(A, Wq, scales, biases, C, out_mode, M, Kred, Nout, split, st);
+        case 128: return launch_tc_cluster<128>(A, Wq, scales, biases, C, out_mode, M, Kred, Nout, split, st);
+        case 256: return launch_tc_cluster<256>(A, Wq, scales, biases, C, out_mode, M, Kred, Nout, split, st);
+        default: return cudaErrorNotSupported;
     }
 }
 

@@ -220,11 +220,12 @@ def qmm_set_pdl(enable: bool) -> int:
     return lib().qmm_set_pdl(int(bool(enable)))
 
 
-QMM_REDUCE_KERNEL, QMM_REDUCE_FUSED = 0, 1
+QMM_REDUCE_KERNEL, QMM_REDUCE_FUSED, QMM_REDUCE_CLUSTER = 0, 1, 2
 
 
 def qmm_set_reduce(mode: int) -> int:
-    """Separate reduce kernel (default) or the fused last-CTA reduce (see qmm.h)."""
+    """Separate reduce kernel (default), the fused last-CTA reduce or the
+    cluster reduce (see qmm.h)."""
     prev = lib().qmm_set_reduce(mode)
     if prev < 0:
         raise QmmError(prev, "qmm_set_reduce")

@@ -438,7 +438,7 @@ def test_options_init_and_binding_default():
     Q.lib().qmm_options_init(None)  # no-op
 
 
-@pytest.mark.parametrize("field,bad", [("kernels", 4), ("partitions", 2), ("reduce", 2),
+@pytest.mark.parametrize("field,bad", [("kernels", 4), ("partitions", 2), ("reduce", 3),
                                        ("weights_static", 2), ("pdl", -2),
                                        ("grouped_schedule", 2), ("group_plan", 5)])
 def test_options_out_of_range_rejected_first(field, bad):

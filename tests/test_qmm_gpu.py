@@ -1374,3 +1374,101 @@ def test_balanced_split_without_a_partial_wave_is_the_planned_split():
     if (M // 256) * (Nout // 128) % sms == 0:
         assert head == 0
     assert s == Q.qmm_call_plan(M, Kred, Nout, Q.QMM_SPLIT_PLANNED)[0] or head > 0
+
+
+# ---- cluster reduce (QMM_REDUCE_CLUSTER) ----------------------------------------
+
+@pytest.mark.parametrize("name,M,split,dt", [
+    ("k", 32, 10, Q.QMM_PARTIAL_BF16), ("q", 32, 4, Q.QMM_PARTIAL_BF16),
+    ("down", 128, 4, Q.QMM_PARTIAL_BF16), ("ragged", 33, 5, Q.QMM_PARTIAL_BF16),
+    ("k", 100, 10, Q.QMM_PARTIAL_F32), ("o", 64, 8, Q.QMM_PARTIAL_F32),
+])
+def test_cluster_reduce_equals_the_reduce_kernel(name, M, split, dt):
+    """The cluster reduce gives C bit for bit as the planes and the reduce
+    kernel do; where every cluster of the call fits the device at once it
+    takes the cluster path, which writes no plane (the workspace keeps its
+    NaN fill)."""
+    Kred, Nout = inputs.RAGGED if name == "ragged" else inputs.PROJECTIONS[name]
+    p = inputs.make_w4a16(M, Kred, Nout, seed=91 + M)
+    d = Q.to_device(p)
+    nbytes = Q.qmm_splitk_workspace_bytes(M, Nout, split, dt)
+    prev = Q.qmm_set_kernels(Q.QMM_KERNELS_TCGEN05)
+    try:
+        outs = {}
+        for mode in (Q.QMM_REDUCE_KERNEL, Q.QMM_REDUCE_CLUSTER):
+            ws = torch.full((nbytes // 2,), float("nan"), dtype=torch.bfloat16, device="cuda")
+            C = torch.full((M, Nout), float("nan"), dtype=torch.bfloat16, device="cuda")
+            s = Q.qmm_w4a16_g128(d["A"], d["Wq"], d["scales"], d["biases"], C, split_req=split,
+                                 workspace=ws, partial_dtype=dt,
+                                 options=Q.qmm_options(reduce=mode))
+            torch.cuda.synchronize()
+            assert s == split
+            outs[mode] = (_bits(C), bool(torch.isnan(ws.float()).all()))
+        assert Q.qmm_kernel_status(clear=True) == 0
+    finally:
+        Q.qmm_set_kernels(prev)
+    assert np.array_equal(outs[Q.QMM_REDUCE_CLUSTER][0], outs[Q.QMM_REDUCE_KERNEL][0])
+    assert not outs[Q.QMM_REDUCE_KERNEL][1]  # the reduce kernel's planes are in the workspace
+    if (name, M) in (("k", 32), ("q", 32), ("down", 128)):
+        assert outs[Q.QMM_REDUCE_CLUSTER][1], "expected the cluster path (no planes written)"
+    rows, cols = np.arange(0, M, 7), np.arange(1, Nout, 41)
+    _check_sampled(p, outs[Q.QMM_REDUCE_CLUSTER][0], split, dt, rows, cols, "cluster reduce")
+
+
+def test_cluster_reduce_under_the_default_table_and_static_weights():
+    """The step's calls (M = 32 and 128, policy splits) under the cluster
+    reduce, static weights and programmatic launch, back to back on one
+    stream: every C bit for bit the reduce kernel's."""
+    calls = [(n, M) for M in (32, 128) for n in ("q", "k", "o", "gate", "down")]
+    probs = {c: inputs.make_w4a16(c[1], *inputs.PROJECTIONS[c[0]], seed=5) for c in calls}
+    devs = {c: Q.to_device(probs[c]) for c in calls}
+    ws = torch.empty(64 << 20, dtype=torch.uint8, device="cuda")
+    res = {}
+    prev = Q.qmm_set_weights_static(True)
+    try:
+        for mode in (Q.QMM_REDUCE_KERNEL, Q.QMM_REDUCE_CLUSTER):
+            opt = Q.qmm_options(reduce=mode)
+            Cs = {}
+            for c in calls:
+                M, (Kred, Nout) = c[1], inputs.PROJECTIONS[c[0]]
+                Cs[c] = torch.empty((M, Nout), dtype=torch.bfloat16, device="cuda")
+                Q.qmm_w4a16_g128(devs[c]["A"], devs[c]["Wq"], devs[c]["scales"],
+                                 devs[c]["biases"], Cs[c], workspace=ws, options=opt)
+            torch.cuda.synchronize()
+            res[mode] = {c: _bits(Cs[c]) for c in calls}
+        assert Q.qmm_kernel_status(clear=True) == 0
+    finally:
+        Q.qmm_set_weights_static(prev)
+    for c in calls:
+        assert np.array_equal(res[Q.QMM_REDUCE_CLUSTER][c], res[Q.QMM_REDUCE_KERNEL][c]), c
+
+
+@pytest.mark.parametrize("name,M,split,dt", [
+    ("k", 16, 5, Q.QMM_PARTIAL_BF16), ("down", 8, 4, Q.QMM_PARTIAL_BF16),
+    ("ragged", 1, 10, Q.QMM_PARTIAL_BF16), ("o", 16, 16, Q.QMM_PARTIAL_F32),
+])
+def test_cluster_reduce_lean_family(name, M, split, dt):
+    """The lean family (few activation rows) under the cluster reduce: C bit
+    for bit the reduce kernel's (through the cluster path where the device
+    holds all of the call's clusters at once, else the reduce kernel), and
+    the oracle on a sample."""
+    Kred, Nout = inputs.RAGGED if name == "ragged" else inputs.PROJECTIONS[name]
+    p = inputs.make_w4a16(M, Kred, Nout, seed=17 + M)
+    d = Q.to_device(p)
+    nbytes = Q.qmm_splitk_workspace_bytes(M, Nout, split, dt)
+    outs = {}
+    for mode in (Q.QMM_REDUCE_KERNEL, Q.QMM_REDUCE_CLUSTER):
+        ws = torch.full((nbytes // 2,), float("nan"), dtype=torch.bfloat16, device="cuda")
+        C = torch.full((M, Nout), float("nan"), dtype=torch.bfloat16, device="cuda")
+        s = Q.qmm_w4a16_g128(d["A"], d["Wq"], d["scales"], d["biases"], C, split_req=split,
+                             workspace=ws, partial_dtype=dt,
+                             options=Q.qmm_options(reduce=mode, kernels=Q.QMM_KERNELS_DEFAULT))
+        torch.cuda.synchronize()
+        assert s == split
+        outs[mode] = (_bits(C), bool(torch.isnan(ws.float()).all()))
+    assert Q.qmm_kernel_status(clear=True) == 0
+    assert np.array_equal(outs[Q.QMM_REDUCE_CLUSTER][0], outs[Q.QMM_REDUCE_KERNEL][0])
+    if (name, M) == ("k", 16):  # 32 clusters of 5: every one fits the device at once
+        assert outs[Q.QMM_REDUCE_CLUSTER][1], "expected the cluster path (no planes written)"
+    _check_sampled(p, outs[Q.QMM_REDUCE_CLUSTER][0], split, dt, np.arange(M),
+                   np.arange(0, Nout, 29), "lean cluster reduce")
