@@ -28,7 +28,9 @@
 //               results stay deterministic;
 //   warps 4-15  three dequantizer sets of four warps (warp w serves tensor
 //               memory lanes 32*(w%4).. and every third group), then the
-//               epilogue.
+//               epilogue.  A weight row's group is dequantized with one BF16
+//               fused multiply-add per pair of weights where its scale allows
+//               (dequant_row_group_sub), else with two.
 // Every mbarrier wait is bounded (qmm_sm100.cuh): a wait that runs out sets
 // the status word, the CTA stops issuing work, waits (bounded) for what is in
 // flight, frees its tensor memory and exits.
@@ -201,6 +203,26 @@ struct TcCfg {
 // both nibbles; byte c of x >> 4 has the odd one in its low nibble.
 __device__ __forceinline__ uint32_t natural_pair(uint32_t x, uint32_t x4, uint32_t sel) {
     return nibbles_to_bf16x2_biased(__byte_perm(x, x4, sel));
+}
+
+// 64 BF16 pairs of one weight row and group, in k order (pair c = k 2c, 2c+1),
+// with one fused multiply-add per pair: each half keeps only its nibble, which
+// then reads as the BF16 subnormal q * 2^-133, and s133 is the scale times
+// 2^133 (scale_shifted_pair), so the FMA forms q * scale + bias with a single
+// rounding -- the value dequant_row_group forms in two steps.  For scales that
+// scale_subnormal_ok accepts.
+__device__ __forceinline__ void dequant_row_group_sub(const uint4 wv[4], uint32_t s133,
+                                                      uint32_t bb, uint32_t out[64]) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const uint32_t x = j % 4 == 0 ? wv[j / 4].x : j % 4 == 1 ? wv[j / 4].y
+                         : j % 4 == 2 ? wv[j / 4].z : wv[j / 4].w;
+        const uint32_t x4 = x >> 4;
+        const uint32_t sel[4] = {0x4400u, 0x5511u, 0x6622u, 0x7733u};
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            out[4 * j + c] = fma_bf16x2(__byte_perm(x, x4, sel[c]) & 0x000F000Fu, s133, bb);
+    }
 }
 
 // 64 BF16 pairs of one weight row and group, in k order (pair c = k 2c, 2c+1)
@@ -419,7 +441,10 @@ __device__ __forceinline__ void tc_dequant(const TcSmem& sm, const TcParams& p, 
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.w_empty[sw]);
         uint32_t w[64];
-        dequant_row_group(wv, bf16_pair(s_cur), bf16_pair(b_cur), w);
+        if (scale_subnormal_ok(s_cur))
+            dequant_row_group_sub(wv, scale_shifted_pair(s_cur, 133), bf16_pair(b_cur), w);
+        else
+            dequant_row_group(wv, bf16_pair(s_cur), bf16_pair(b_cur), w);
         if (!mbar_wait_warp(&sm.a_empty[ab], ((i / C::A_STAGES) & 1) ^ 1, abort, p.status)) break;
         // the stores below must follow the MMAs that read this buffer before
         tc_fence_after();
@@ -1207,7 +1232,10 @@ __device__ __forceinline__ void tcp_dequant(const TcpSmem& sm, const TcGroup& g,
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.w_empty[sw]);
             uint32_t w[64];
-            dequant_row_group(wv, bf16_pair(s_cur), bf16_pair(b_cur), w);
+            if (scale_subnormal_ok(s_cur))
+                dequant_row_group_sub(wv, scale_shifted_pair(s_cur, 133), bf16_pair(b_cur), w);
+            else
+                dequant_row_group(wv, bf16_pair(s_cur), bf16_pair(b_cur), w);
             if (!mbar_wait_warp(&sm.a_empty[ab], ((gg / C::A_STAGES) & 1) ^ 1, abort, status)) {
                 ok = false;
                 break;
