@@ -75,8 +75,9 @@ def partition_algorithmic(M, Kred, Nout, split, partial_bytes=2):
 # figure no longer describes the kernel and is reported as null.
 NCU_TRAFFIC = {
     # python bench.py --only down:128 --launch-list --steps 1 --warmup 3 under
-    # ncu --set full -k regex:w4a16_tc -s 2 -c 1: dram__bytes_read.sum + _write.sum
-    ("down", 128, 4): (15788288, "8f0170d4d6878b62"),
+    # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum
+    # --clock-control none -k regex:w4a16_tc -s 2 -c 1: read + write
+    ("down", 128, 4): (15789056, "dae890bb95cf3bea"),
     # the same with --partitions near-equal (split 7)
     ("down", 128, 7): (15788288, "8f0170d4d6878b62"),
     # the same for --only gate:32
@@ -85,8 +86,9 @@ NCU_TRAFFIC = {
 TC_SOURCES = ("qmm_w4a16_tc.cu", "qmm_sm100.cuh", "qmm_device.cuh", "qmm_internal.h")
 # The same for the decode-attention split kernel at the workload's planned
 # split (python bench.py --attention-only --steps 2 --warmup 3 under
-# ncu --set full -k regex:attn_split -s 3 -c 1), keyed by the split.
-ATTN_TRAFFIC = {3: (670811392, "c374070bc2c6bf13")}
+# ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum
+# --clock-control none -k regex:attn_split -s 3 -c 1), keyed by the split.
+ATTN_TRAFFIC = {3: (670089728, "babc6b7daa2798ea")}
 ATTN_SOURCES = ("qmm_attention.cu", "qmm_sm100.cuh", "qmm_device.cuh", "qmm_internal.h")
 
 
