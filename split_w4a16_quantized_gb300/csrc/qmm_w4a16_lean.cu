@@ -622,10 +622,28 @@ int launch_cfg(const LeanParams& p0, const void* A, int split, cudaStream_t stre
     if (cfg.numAttrs) attrs[na++] = la.attr[0];
     cfg.attrs = attrs;
     cfg.numAttrs = na;
-    int active = 0;
-    if (cudaOccupancyMaxActiveClusters(&active, kern, &cfg) != cudaSuccess) {
-        cudaGetLastError();  // a refused query is not the caller's error
-        return cudaErrorNotSupported;
+    // clusters the device holds at once, per (split, shared memory), queried once
+    static std::mutex mu;
+    static int cache_key[32][2];
+    static int cache_val[32];
+    static int cache_n = 0;
+    int active = -1;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (int i = 0; i < cache_n; ++i)
+            if (cache_key[i][0] == split && cache_key[i][1] == static_cast<int>(smem))
+                active = cache_val[i];
+        if (active < 0) {
+            if (cudaOccupancyMaxActiveClusters(&active, kern, &cfg) != cudaSuccess) {
+                cudaGetLastError();  // a refused query is not the caller's error
+                active = 0;
+            }
+            if (cache_n < 32) {
+                cache_key[cache_n][0] = split;
+                cache_key[cache_n][1] = static_cast<int>(smem);
+                cache_val[cache_n++] = active;
+            }
+        }
     }
     if (active < static_cast<int>(cfg.gridDim.x)) return cudaErrorNotSupported;
     return cudaLaunchKernelEx(&cfg, kern, amap, p);
