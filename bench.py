@@ -542,6 +542,9 @@ def run_gpu(args, rank, world, local_rank):
     sample = clocks.stop()
     dense = dense_sweep(Q, device, stream, sms, l2) if rank == 0 else None
     e2e = run_e2e(wl, Q, device, stream, min(args.steps, 20))
+    e2e_resident = run_e2e(wl, Q, device, stream, min(args.steps, 20), weights_resident=True)
+    e2e_resident_graph = run_e2e(wl, Q, device, stream, min(args.steps, 20),
+                                 weights_resident=True, graphed=True)
     overlap = overlap_sweep(wl, Q, device) if rank == 0 else None
     attention = attention_bench(Q, device, stream, peaks, l2) if rank == 0 else None
     return {"ms": ms, "ms_nopdl": ms_nopdl, "ms_wflip": ms_wflip, "ms_fused": ms_fused, "ms_cluster": ms_cluster,
@@ -552,6 +555,7 @@ def run_gpu(args, rank, world, local_rank):
             "clocks": sample, "wl": wl,
             "peaks": peaks,
             "peak_src": peak_src, "l2": l2, "sms": sms, "dense": dense, "e2e": e2e,
+            "e2e_resident": e2e_resident, "e2e_resident_graph": e2e_resident_graph,
             "prefill": prefill, "sweep": sweep, "overlap": overlap, "attention": attention}
 
 
@@ -828,15 +832,21 @@ def overlap_sweep(wl, Q, device, reps=10):
     return out
 
 
-def run_e2e(wl, Q, device, stream, steps):
+def run_e2e(wl, Q, device, stream, steps, weights_resident=False, graphed=False):
     """The same step through the public API with host buffers: per step the
     pinned-host inputs of all 14 calls (A, packed weights, scales, biases) are
     copied in, the calls run, and every output is copied back, all inside the
     timed region.  Inputs and outputs of a step are packed into one pinned
-    buffer each (one host-to-device and one device-to-host copy per step), and
-    a copy stream moves step k+1's inputs while step k computes (two device
-    input and output buffers, ordered by events)."""
-    keys = ("A", "Wq", "scales", "biases")
+    buffer each (one host-to-device and one device-to-host copy per step);
+    copy streams move step k+1's inputs in and step k-1's outputs out while
+    step k computes (two device input and output buffers, ordered by events).
+    weights_resident: the packed weights, scales and biases are uploaded once
+    before the timed region, as a deployed model's are, and only the
+    activations move in.  graphed: each buffer set's 14 public-API calls are
+    captured once in a CUDA graph and a step replays it (one host call instead
+    of 14)."""
+    keys = ("A",) if weights_resident else ("A", "Wq", "scales", "biases")
+    resident = [Q.to_device(p, device) for p in wl.host] if weights_resident else None
     align = lambda n: (n + 255) // 256 * 256
     in_off, out_off, ni, no = [], [], 0, 0
     for p, (_, M, _, Nout) in zip(wl.host, wl.calls):
@@ -859,8 +869,9 @@ def run_e2e(wl, Q, device, stream, steps):
 
     def views(buf, obuf):
         calls = []
-        for p, offs, oo, (_, M, Kred, Nout) in zip(wl.host, in_off, out_off, wl.calls):
-            t = {}
+        for i, (p, offs, oo, (_, M, Kred, Nout)) in enumerate(
+                zip(wl.host, in_off, out_off, wl.calls)):
+            t = dict(resident[i]) if resident else {}
             for k, dt in zip(keys, (torch.bfloat16, torch.int32, torch.bfloat16, torch.bfloat16)):
                 n = p[k].nbytes
                 t[k] = buf[offs[k]:offs[k] + n].view(dt).view(p[k].shape)
@@ -868,13 +879,38 @@ def run_e2e(wl, Q, device, stream, steps):
             calls.append(t)
         return calls
     sets = [views(dev_in[b], dev_out[b]) for b in range(2)]
-    # two copy streams, each moving half of a step's inputs (two copy engines)
+
+    def calls(b):
+        for t in sets[b]:
+            Q.qmm_w4a16_g128(t["A"], t["Wq"], t["scales"], t["biases"], t["C"],
+                             workspace=wl.ws)
+
+    graphs = None
+    if graphed:
+        cap = torch.cuda.Stream(device=device)
+        cap.wait_stream(stream)
+        graphs = []
+        with torch.cuda.stream(cap):
+            for b in range(2):
+                calls(b)
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=cap):
+                    calls(b)
+                graphs.append(g)
+        stream.wait_stream(cap)
+        torch.cuda.synchronize()
+    # two copy streams, each moving half of a step's inputs (two copy engines),
+    # and one stream for the outputs, so that a step's D2H copy overlaps the
+    # next step's calls
     copies = [torch.cuda.Stream(device=device) for _ in range(2)]
+    out_copy = torch.cuda.Stream(device=device)
     half = ni // 2 // 256 * 256
     parts = [(0, half), (half, ni)]
     in_ready = [[torch.cuda.Event() for _ in range(2)] for _ in range(2)]
     in_free = [torch.cuda.Event() for _ in range(2)]
+    computed = [torch.cuda.Event() for _ in range(2)]
     out_done = [torch.cuda.Event() for _ in range(2)]
+    issue = [0.0]
 
     def run(nsteps):
         for k in range(nsteps):
@@ -889,13 +925,19 @@ def run_e2e(wl, Q, device, stream, steps):
                 stream.wait_event(ev)
             if k >= 2:
                 stream.wait_event(out_done[b])
-            for i, t in enumerate(sets[b]):
-                Q.qmm_w4a16_g128(t["A"], t["Wq"], t["scales"], t["biases"], t["C"],
-                                 workspace=wl.ws)
+            t0 = time.perf_counter()
+            if graphs is not None:
+                graphs[b].replay()
+            else:
+                calls(b)
+            issue[0] += time.perf_counter() - t0
             in_free[b].record(stream)
-            host_out.copy_(dev_out[b], non_blocking=True)
-            out_done[b].record(stream)
-        for c in copies:
+            computed[b].record(stream)
+            with torch.cuda.stream(out_copy):
+                out_copy.wait_event(computed[b])
+                host_out.copy_(dev_out[b], non_blocking=True)
+                out_done[b].record(out_copy)
+        for c in copies + [out_copy]:
             c.synchronize()
         stream.synchronize()
 
@@ -903,10 +945,11 @@ def run_e2e(wl, Q, device, stream, steps):
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for c in copies:
+    for c in copies + [out_copy]:
         c.wait_stream(stream)
+    issue[0] = 0.0
     run(steps)
-    for c in copies:
+    for c in copies + [out_copy]:
         stream.wait_stream(c)
     e1.record(stream)
     torch.cuda.synchronize()
@@ -916,9 +959,15 @@ def run_e2e(wl, Q, device, stream, steps):
     return {"value": round(ms * 1e3 / len(wl.calls), 3), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
             "h2d_gbps": round(h2d / (ms * 1e-3) / 1e9, 1),
-            "method": "packed pinned inputs copied in as two halves on two copy streams and "
-                      "one packed D2H copy per step; the next step's inputs move while the "
-                      "current step computes"}
+            "host_issue_us_per_call": round(issue[0] * 1e6 / steps / len(wl.calls), 2),
+            "method": ("activations only (weights, scales and biases resident, uploaded once "
+                       "before the timed region); " if weights_resident else "") +
+                      ("the 14 calls of a step replayed as one captured CUDA graph; "
+                       if graphed else "") +
+                      "packed pinned inputs copied in as two halves on two copy streams and "
+                      "one packed D2H copy per step on a third; the next step's inputs move "
+                      "in and the previous step's outputs move out while the current step "
+                      "computes"}
 
 
 # ---------------------------------------------------------------------------
@@ -1191,7 +1240,9 @@ def main():
            "grouped_launches_per_step": res["grouped_launches"],
            "roofline": roof, "roofline_other_partitions": roof_alt, "step_roofline": step_roof,
            "gpu_launches": args.steps * wl.launches_per_step(),
-           "clocks": res["clocks"], "e2e": res["e2e"], "per_call": res["per_call"],
+           "clocks": res["clocks"], "e2e": res["e2e"],
+           "e2e_weights_resident": res["e2e_resident"],
+           "e2e_weights_resident_graphed": res["e2e_resident_graph"], "per_call": res["per_call"],
            "dense_splitk_512x512x16384": res["dense"], "prefill_M2048": res["prefill"],
            "split_vs_control": res["sweep"],
            "overlap_stream": res["overlap"], "decode_attention": res["attention"]}
