@@ -564,8 +564,10 @@ def prefill_sweep(Q, device, stream, l2, peaks):
     split (the unsplit kernel wherever the base grid already fills the GPU),
     graphs of back-to-back calls over input copies larger than L2, tensor
     throughput against the measured dense BF16 peak.  Where the balanced
-    split (QMM_SPLIT_BALANCED) cuts the call -- its tiles leave a partial last
-    wave -- its head rows, tail split and time are given beside it."""
+    split (QMM_SPLIT_BALANCED) plans the call otherwise -- head rows cut off
+    a partial last wave, or the narrower tile where the wide one has no full
+    wave -- its head rows, tile, split (of the tail) and time are given
+    beside it."""
     out = []
     ws = torch.zeros(64 << 20, dtype=torch.uint8, device=device)
     for name in PROJ:
@@ -588,10 +590,12 @@ def prefill_sweep(Q, device, stream, l2, peaks):
                "ctas": -(-M // bm) * -(-Nout // bn) * split, "us": round(us, 3),
                "tflops": round(fl / us / 1e6, 1),
                "frac_of_bf16_peak": round(fl / us / 1e6 / peaks["bf16_tflops"], 3)}
-        s_b, _, _, head = Q.qmm_call_plan(M, Kred, Nout, Q.QMM_SPLIT_BALANCED, with_head=True)
-        if head > 0:
+        s_b, bm_b, bn_b, head = Q.qmm_call_plan(M, Kred, Nout, Q.QMM_SPLIT_BALANCED,
+                                                with_head=True)
+        if head > 0 or (bm_b, bn_b) != (bm, bn):
             us_b = graph_us_per_launch(lambda j: call(j, Q.QMM_SPLIT_BALANCED), len(cps), stream)
-            row["balanced"] = {"head_rows": head, "tail_split": s_b, "us": round(us_b, 3),
+            row["balanced"] = {"head_rows": head, "tile": [bm_b, bn_b], "split": s_b,
+                               "us": round(us_b, 3),
                                "tflops": round(fl / us_b / 1e6, 1),
                                "frac_of_bf16_peak": round(fl / us_b / 1e6 / peaks["bf16_tflops"],
                                                           3)}

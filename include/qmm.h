@@ -133,7 +133,13 @@ size_t qmm_splitk_workspace_bytes(int M, int Nout, int split, int partial_dtype)
  * call's tiles leave a partial last wave, the row tiles that fill whole waves
  * run unsplit and only the remaining rows are split, in the same partition
  * launch, so the short split CTAs fill the SMs the last wave would leave
- * idle; otherwise it is QMM_SPLIT_PLANNED. */
+ * idle.  When the tiles do not fill one wave and the family's tile has a
+ * tcgen05 family of half its rows (the 256-row tile over the 128-row one),
+ * the narrower tile is taken at the occupancy rule's split for it
+ * (QMM_PRESET_GB300 of that tile) if that split is no larger than
+ * QMM_SPLIT_PLANNED's and its CTAs fit one wave: each CTA then has half the
+ * multiply-adds, or as many with fewer partial planes.  Otherwise it is
+ * QMM_SPLIT_PLANNED. */
 #define QMM_SPLIT_BALANCED (-2)
 
 /* C = A . W^T for the W4A16-g128 format (see the top of this header).
@@ -156,6 +162,9 @@ size_t qmm_splitk_workspace_bytes(int M, int Nout, int split, int partial_dtype)
  *              on those rows alone at split s.  The workspace holds the
  *              tail's planes [s, M - h, Nout]; size it with
  *              qmm_call_workspace_bytes.  The reduce is the separate kernel.
+ *              Where it takes the narrower tile instead (h = 0), each
+ *              128-row slice of C is bitwise that slice called alone at the
+ *              same split.
  *   pol        policy used when split_req == 0; NULL = QMM_PRESET_GB300
  *              for this M on the current device.
  *   workspace  device buffer for the partial planes [split, M, Nout] of
@@ -396,7 +405,8 @@ size_t qmm_splitk_workspace_bytes_ex(int M, int Nout, int split, int partial_dty
 
 /* What qmm_w4a16_g128_ex would dispatch for this shape, without launching:
  * *split the split (split_req and pol as in qmm_w4a16_g128, QMM_SPLIT_PLANNED
- * and QMM_SPLIT_BALANCED included), *bm / *bn the tile of the kernel family
+ * and QMM_SPLIT_BALANCED included), *bm / *bn the tile of the kernel that
+ * runs (QMM_SPLIT_BALANCED may take a narrower one than the family for M),
  * and *head_rows the rows that QMM_SPLIT_BALANCED runs unsplit (0 when it
  * does not cut the call; *split is then the split of the whole call, else
  * that of rows [*head_rows, M)); the last three are nullable.  num_sms > 0

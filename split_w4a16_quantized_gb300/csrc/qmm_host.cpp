@@ -253,7 +253,8 @@ int launch_group(const qmm_group_call* calls, int n, const std::vector<int>& spl
                  void* stream);
 // QMM_SPLIT_BALANCED's plan (defined with the group plan below)
 int balanced_plan(int M, int Kred, int Nout, int num_sms, int partial_dtype, int* head,
-                  int* s_tail, int* s_plain);
+                  int* s_tail, int* s_plain, int* narrow);
+const qmm::Family* narrower_tile(const qmm::Family& f);
 size_t balanced_bytes(int M, int Nout, int head, int s_tail, int partial_dtype);
 }  // namespace
 
@@ -321,13 +322,20 @@ int qmm_call_plan(int M, int Kred, int Nout, int split_req, const qmm_policy* po
     if (bn) *bn = f.bn;
     if (head_rows) *head_rows = 0;
     if (split_req == QMM_SPLIT_BALANCED) {
-        int head = 0, s_tail = 1, s_plain = 1;
+        int head = 0, s_tail = 1, s_plain = 1, narrow = 0;
         const int rc = balanced_plan(M, Kred, Nout, num_sms, partial_dtype, &head, &s_tail,
-                                     &s_plain);
+                                     &s_plain, &narrow);
         if (rc != QMM_OK) return rc;
         if (head > 0) {
             *split = s_tail;
             if (head_rows) *head_rows = head;
+            return QMM_OK;
+        }
+        if (narrow) {
+            const qmm::Family* g = narrower_tile(f);
+            if (bm) *bm = g->bm;
+            if (bn) *bn = g->bn;
+            *split = s_plain;
             return QMM_OK;
         }
         split_req = s_plain;
@@ -490,13 +498,13 @@ int qmm_w4a16_g128(const void* A, const uint32_t* Wq, const void* scales, const 
     if (!aligned(A, 16) || !aligned(Wq, 16) || !aligned(C, 16) || !aligned(scales, 16) ||
         !aligned(biases, 16))
         return QMM_EALIGN;
-    const qmm::Family fam = qmm::family_for(M);
+    qmm::Family fam = qmm::family_for(M);
     if (ceil_div(M, fam.bm) > 65535) return QMM_ESHAPE;
     int rc = check_device();
     if (rc != QMM_OK) return rc;
     if (split_req == QMM_SPLIT_BALANCED) {
-        int head = 0, s_tail = 1, s_plain = 1;
-        rc = balanced_plan(M, Kred, Nout, 0, partial_dtype, &head, &s_tail, &s_plain);
+        int head = 0, s_tail = 1, s_plain = 1, narrow = 0;
+        rc = balanced_plan(M, Kred, Nout, 0, partial_dtype, &head, &s_tail, &s_plain, &narrow);
         if (rc != QMM_OK) return rc;
         if (head > 0) {
             // rows [0, head) unsplit and [head, M) at s_tail, in one partition
@@ -514,6 +522,10 @@ int qmm_w4a16_g128(const void* A, const uint32_t* Wq, const void* scales, const 
             rc = launch_group(calls, 2, {1, s_tail}, {0, 0}, workspace, partial_dtype, stream);
             if (rc == QMM_OK && split_used) *split_used = s_tail;
             return rc;
+        }
+        if (narrow) {  // the narrower tile at its own split
+            fam = *narrower_tile(fam);
+            if (ceil_div(M, fam.bm) > 65535) return QMM_ESHAPE;
         }
         split_req = s_plain;  // no cut pays: the planned split
     }
@@ -774,8 +786,28 @@ int group_plan_shapes(const int* shapes, int n, int num_sms, int partial_dtype,
 // [0, head) get exactly the unsplit kernel's result and rows [head, M) that
 // of a call on those rows at the tail's split (the same tiles, k order and
 // rounding).
+// Estimated time of a call whose CTAs fit one wave (tile rows bm, split s):
+// the partition's groups at the tile's time per group, plus, when split, the
+// reduce launch and the partial planes written and read back.  The times per
+// group are those of a CTA of the 128- and 256-row tcgen05 tiles at
+// M = 129..2048 on GB300 (tuning parameters, like the group plan's).
+constexpr double kReduceLaunchUs = 2.5;
+double one_wave_us(int bm, int64_t G, int s, int M, int Nout, int elem) {
+    const double group = bm <= 128 ? 0.48 : 0.78;
+    double t = static_cast<double>((G + s - 1) / s) * group;
+    if (s > 1)
+        t += kReduceLaunchUs + 2.0 * s * M * static_cast<double>(Nout) * elem / kPlanPlaneBytesPerUs;
+    return t;
+}
+
+const qmm::Family* narrower_tile(const qmm::Family& f) {
+    if (f.kind != qmm::kKindTc || f.bm <= 128) return nullptr;
+    const qmm::Family& g = qmm::family_for(f.bm / 2);
+    return g.kind == qmm::kKindTc && g.bm == f.bm / 2 ? &g : nullptr;
+}
+
 int balanced_plan(int M, int Kred, int Nout, int num_sms, int partial_dtype, int* head,
-                  int* s_tail, int* s_plain) {
+                  int* s_tail, int* s_plain, int* narrow) {
     const int shape[3] = {M, Kred, Nout};
     std::vector<int> planned;
     int rc = group_plan_shapes(shape, 1, num_sms, partial_dtype, &planned);
@@ -786,10 +818,36 @@ int balanced_plan(int M, int Kred, int Nout, int num_sms, int partial_dtype, int
     }
     *s_plain = *s_tail = planned[0];
     *head = 0;
+    *narrow = 0;
     const qmm::Family& f = qmm::family_for(M);
     if (!qmm::family_shares_launch(f)) return QMM_OK;
     const int64_t rt = ceil_div(M, f.bm), ct = ceil_div(Nout, f.bn), tiles = rt * ct;
-    if (tiles <= num_sms || tiles % num_sms == 0) return QMM_OK;
+    if (tiles <= num_sms) {
+        // No full wave, so no cut.  The next narrower tile has about twice
+        // the tiles: at its own policy split it is taken if that split is no
+        // larger, its CTAs still fit one wave, and the estimate above favours
+        // it.  Its CTAs dequantize twice the weights per multiply-add, which
+        // a lower split (fewer planes, or no reduce launch) must pay for.
+        const qmm::Family* g = narrower_tile(f);
+        if (!g) return QMM_OK;
+        qmm_policy pol;
+        int s = 0;
+        rc = qmm_policy_preset(QMM_PRESET_GB300, g->bm, num_sms, &pol);
+        if (rc == QMM_OK)
+            rc = qmm::partitions_near_equal() ? qmm_splitk_plan_near_equal(M, Kred, Nout, &pol, &s)
+                                              : qmm_splitk_plan(M, Kred, Nout, &pol, &s);
+        if (rc != QMM_OK) return rc;
+        const int64_t narrow_ctas = ceil_div(M, g->bm) * ceil_div(Nout, g->bn) * s;
+        const int G = Kred / qmm::kGroup;
+        const int elem = static_cast<int>(partial_elem_bytes(partial_dtype));
+        if (s <= *s_plain && narrow_ctas <= num_sms &&
+            one_wave_us(g->bm, G, s, M, Nout, elem) < one_wave_us(f.bm, G, *s_plain, M, Nout, elem)) {
+            *narrow = 1;
+            *s_plain = *s_tail = s;
+        }
+        return QMM_OK;
+    }
+    if (tiles % num_sms == 0) return QMM_OK;
     const int64_t h = tiles / num_sms * num_sms / ct;  // row tiles that fit the full waves
     if (h < 1 || h >= rt) return QMM_OK;
     const int m1 = static_cast<int>(h * f.bm);

@@ -531,8 +531,18 @@ def test_balanced_plan_structure(sms, name, M):
     rt, ct = -(-M // bm), -(-Nout // bn)
     G = Kred // 128
     ws = Q.qmm_call_workspace_bytes(M, Kred, Nout, Q.QMM_SPLIT_BALANCED, num_sms=sms)
+    planned = Q.qmm_call_plan(M, Kred, Nout, Q.QMM_SPLIT_PLANNED, num_sms=sms)[0]
+    wide = Q.qmm_kernel_tile(M)
     if head == 0:
-        assert s == Q.qmm_call_plan(M, Kred, Nout, Q.QMM_SPLIT_PLANNED, num_sms=sms)[0]
+        if (bm, bn) == wide:
+            assert s == planned
+        else:
+            # the next narrower tile at the occupancy rule's split for it: no
+            # larger than the wide tile's, and one wave
+            assert (bm, bn) == (wide[0] // 2, wide[1])
+            assert -(-M // wide[0]) * ct <= sms
+            assert s == oracle.splitk_plan(M, Kred, Nout, bm, bn, sms, 16)
+            assert s <= planned and rt * ct * s <= sms
         assert ws == Q.qmm_splitk_workspace_bytes(M, Nout, s)
         return
     tiles = rt * ct
@@ -555,3 +565,21 @@ def test_balanced_plan_cuts_the_wave_tail_of_down_and_o():
         Kred, Nout = inputs.PROJECTIONS[name]
         assert Q.qmm_call_plan(2048, Kred, Nout, Q.QMM_SPLIT_BALANCED, num_sms=152,
                                with_head=True)[3] == 0
+
+
+@pytest.mark.parametrize("name,M,want", [
+    # k at M = 2048: 64 wide tiles at split 2 become 128 narrow tiles unsplit
+    ("k", 2048, (1, 128, 128, 0)), ("k", 1024, (2, 128, 128, 0)),
+    ("q", 512, (1, 128, 128, 0)), ("gate", 256, (1, 128, 128, 0)),
+    ("o", 256, (2, 128, 128, 0)),
+    # narrow tiles that would not fit one wave (160 > 152), or a full wave: wide
+    ("o", 1024, (1, 256, 128, 0)), ("gate", 2048, (1, 256, 128, 0)),
+    ("q", 2048, (1, 256, 128, 0)),
+    # the long reduction of down: twice the dequant per multiply-add costs
+    # more than the planes and the reduce launch the narrow tile saves
+    ("down", 512, (2, 256, 128, 0)), ("down", 129, (4, 256, 128, 0)),
+])
+def test_balanced_plan_narrow_tile(name, M, want):
+    Kred, Nout = inputs.PROJECTIONS[name]
+    got = Q.qmm_call_plan(M, Kred, Nout, Q.QMM_SPLIT_BALANCED, num_sms=152, with_head=True)
+    assert got == want

@@ -1376,6 +1376,41 @@ def test_balanced_split_without_a_partial_wave_is_the_planned_split():
     assert s == Q.qmm_call_plan(M, Kred, Nout, Q.QMM_SPLIT_PLANNED)[0] or head > 0
 
 
+@pytest.mark.parametrize("name,M", [("k", 2048), ("k", 1024), ("q", 512), ("o", 256),
+                                    ("gate", 129)])
+def test_balanced_split_narrow_tile(name, M):
+    """Where the wide tile leaves no full wave, the balanced split may take the
+    128-row tile at its own split (see the plan): the whole output matches the
+    oracle, and each full 128-row slice is bitwise the slice called alone
+    (M = 128 takes the same kernel) at that split."""
+    Kred, Nout = inputs.PROJECTIONS[name]
+    p = inputs.make_w4a16(M, Kred, Nout, seed=83 + M)
+    d = Q.to_device(p)
+    split, bm, bn, head = Q.qmm_call_plan(M, Kred, Nout, Q.QMM_SPLIT_BALANCED, with_head=True)
+    if (bm, bn) == Q.qmm_kernel_tile(M):
+        pytest.skip("the wide tile is kept on this device")
+    assert (bm, bn, head) == (128, 128, 0) and Q.qmm_kernel_tile(128) == (128, 128)
+    nbytes = Q.qmm_call_workspace_bytes(M, Kred, Nout, Q.QMM_SPLIT_BALANCED)
+    assert nbytes == (Q.qmm_splitk_workspace_bytes(M, Nout, split) if split > 1 else 0)
+    ws = torch.full((max(nbytes, 16) // 2,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    C = torch.full((M, Nout), float("nan"), dtype=torch.bfloat16, device="cuda")
+    used = Q.qmm_w4a16_g128(d["A"], d["Wq"], d["scales"], d["biases"], C,
+                            split_req=Q.QMM_SPLIT_BALANCED, workspace=ws)
+    assert used == split
+    torch.cuda.synchronize()
+    got = _bits(C)
+    C64 = oracle.qmm(p["A"], p["Wq"], p["scales"], p["biases"])
+    _check_full(p, got, split, Q.QMM_PARTIAL_BF16, C64, "%s M=%d narrow tile" % (name, M))
+    wt = torch.empty(max(16, Q.qmm_splitk_workspace_bytes(128, Nout, split)), dtype=torch.uint8,
+                     device="cuda")
+    for r0 in range(0, M - 127, 128 * 5):
+        Cs = torch.empty((128, Nout), dtype=torch.bfloat16, device="cuda")
+        Q.qmm_w4a16_g128(d["A"][r0:r0 + 128].contiguous(), d["Wq"], d["scales"], d["biases"], Cs,
+                         split_req=split, workspace=wt)
+        torch.cuda.synchronize()
+        assert np.array_equal(got[r0:r0 + 128], _bits(Cs)), "rows %d.. differ" % r0
+
+
 # ---- cluster reduce (QMM_REDUCE_CLUSTER) ----------------------------------------
 
 @pytest.mark.parametrize("name,M,split,dt", [
