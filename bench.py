@@ -760,6 +760,34 @@ def run_attention_only(args):
                       "status": Q.qmm_kernel_status(clear=True)}), flush=True)
 
 
+def run_dense_only(args):
+    """--dense-only S: W warm-up and K timed calls of the dense BF16 split-K
+    GEMM 512 x 512 x 16384 at split S (the partition kernel and the reduce),
+    one JSON line.  A profiling aid: one copy of the inputs (they stay in L2)."""
+    from split_w4a16_quantized_gb300 import build as qbuild
+    qbuild.build()
+    from split_w4a16_quantized_gb300 import qmm as Q
+    device = torch.device("cuda", 0)
+    d = inputs.make_dense(512, 512, 16384, seed=0)
+    f = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(device)
+    A, W = f(d["A"]), f(d["W"])
+    C = torch.empty((512, 512), dtype=torch.bfloat16, device=device)
+    ws = torch.empty(Q.qmm_gemm_workspace_bytes(512, 512, 16), dtype=torch.uint8, device=device)
+    run = lambda: Q.qmm_gemm_bf16_splitk(A, W, C, args.dense_only, ws)
+    for _ in range(args.warmup):
+        run()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(args.steps):
+        run()
+    t1.record()
+    torch.cuda.synchronize()
+    print(json.dumps({"dense_only": True, "split": args.dense_only, "calls": args.steps,
+                      "us_per_call": round(t0.elapsed_time(t1) * 1e3 / args.steps, 3),
+                      "status": Q.qmm_kernel_status(clear=True)}), flush=True)
+
+
 def overlap_sweep(wl, Q, device, reps=10):
     """The copy-in / compute / copy-out pipeline (qmm_w4a16_g128_stream) on the
     step's 14 calls: activations from pinned host memory, weights resident,
@@ -1119,6 +1147,8 @@ def main():
                     help="with --grouped: splits planned for the group (qmm_set_group_plan)")
     ap.add_argument("--attention-only", action="store_true",
                     help="only the decode-attention calls at the plan's split (profiling aid)")
+    ap.add_argument("--dense-only", type=int, default=None, metavar="SPLIT",
+                    help="only dense split-K GEMM calls at this split (profiling aid)")
     args = ap.parse_args()
     if args.only:
         global ONLY
@@ -1143,6 +1173,8 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     if args.attention_only:
         return run_attention_only(args)
+    if args.dense_only is not None:
+        return run_dense_only(args)
     res = run_gpu(args, rank, world, local_rank)
     wl = res["wl"]
     ncalls = len(wl.calls)
