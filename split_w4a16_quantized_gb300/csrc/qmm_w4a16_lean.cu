@@ -91,6 +91,7 @@ struct LeanCfg {
     static constexpr int THREADS = 32 * WARPS;
     static constexpr int MIN_CTAS = kThreadsPerSm / THREADS;  // per SM
     static constexpr int AG = WK;                     // groups per activation stage
+    static_assert(AG == WK, "step i of every warp takes activation stage i");
     static constexpr int HALF = BM * 128;             // one 64-k half-group of BM rows
     static constexpr int STAGE = 2 * AG * HALF;       // one TMA box
     static constexpr int WCH = 2 * RB;                // 16-byte weight chunks a thread copies per group
@@ -139,24 +140,39 @@ struct Lane {
     }
 };
 
-// Copy this thread's weight chunks of group `grp` (absolute) into slot `slot`
-// of its ring: chunk k = 2*rb + h is row L.row(rb, h), bytes 16t..16t+15 of
-// the group; rows past Nout are zero-filled.  Layout [slot][k][thread] keeps
-// every 16-byte access of a warp conflict free.
+// This thread's weight chunks: chunk k = 2*rb + h is row L.row(rb, h), bytes
+// 16t..16t+15 of each group; rows past Nout are zero-filled.  Sources and
+// ring positions are formed once per CTA, so a group's copies cost one address
+// add each.  Layout [slot][k][thread] keeps every 16-byte access of a warp
+// conflict free.
 template <class Cfg>
-__device__ __forceinline__ void copy_weights(uint8_t* wring, int slot, const LeanParams& p,
-                                             size_t wrow, const Lane<Cfg>& L, int grp) {
+struct WeightCopies {
+    static constexpr uint32_t SLOT_BYTES = Cfg::WCH * Cfg::THREADS * 16;
+    const uint32_t* src[Cfg::RB][2];  // the row's words 4t.. of group 0
+    uint32_t dst[Cfg::RB][2];         // the chunk's position in slot 0
+    bool ok[Cfg::RB][2];
+    __device__ __forceinline__ WeightCopies(const uint8_t* wring, const LeanParams& p,
+                                            const Lane<Cfg>& L) {
+        const size_t wrow = static_cast<size_t>(p.Kred) / 8;
 #pragma unroll
-    for (int rb = 0; rb < Cfg::RB; ++rb)
+        for (int rb = 0; rb < Cfg::RB; ++rb)
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int n = L.row(rb, h);
-            const bool ok = n < p.Nout;
-            const uint32_t* src = p.Wq + static_cast<size_t>(ok ? n : 0) * wrow + grp * 16 + L.t * 4;
-            uint8_t* dst = wring + ((slot * Cfg::WCH + 2 * rb + h) * Cfg::THREADS + L.tid) * 16;
-            cp_async16(smem_addr(dst), src, ok);
-        }
-}
+            for (int h = 0; h < 2; ++h) {
+                const int n = L.row(rb, h);
+                ok[rb][h] = n < p.Nout;
+                src[rb][h] = p.Wq + static_cast<size_t>(ok[rb][h] ? n : 0) * wrow + L.t * 4;
+                dst[rb][h] = smem_addr(wring + ((2 * rb + h) * Cfg::THREADS + L.tid) * 16);
+            }
+    }
+    // copy group `grp` (absolute) into ring slot `slot`
+    __device__ __forceinline__ void copy(int slot, int grp) const {
+#pragma unroll
+        for (int rb = 0; rb < Cfg::RB; ++rb)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                cp_async16(dst[rb][h] + slot * SLOT_BYTES, src[rb][h] + grp * 16, ok[rb][h]);
+    }
+};
 
 // Read slot `slot` back; threads t >= 2 swap words (0,1) with (2,3) (see the
 // k order above).
@@ -230,62 +246,70 @@ struct LeanShared {
     int* issued;  // activation stages issued so far (thread 0)
 };
 
-// One group gi of one warp: its weights are in slot wslot of the thread's
-// ring (landed), the CTA's scales and biases in sc / bi ([group][row]).
-// Returns false if a
-// wait ran out.  Releases the activation stage (every warp takes one group of
-// each stage); thread 0 then refills the slot with stage st + na once every
-// warp has released it.
+// Scales of the CTA's groups, in place in shared memory ([group][row]): a group
+// whose every row's scale suits the one-FMA dequant (scale_subnormal_ok) gets
+// its scales as scale * 2^133 (the halves scale_shifted_pair forms), and
+// gbad[group] = 0; any other group keeps its raw scales for dequant_word and
+// gets gbad[group] = 1.  gbad must be zero beforehand; all threads call this,
+// and a barrier must follow before the scales are read.
+template <class Cfg>
+__device__ __forceinline__ void prepare_scales(uint16_t* sc, uint8_t* gbad, int gpp) {
+    for (int i = threadIdx.x; i < gpp * Cfg::BN; i += Cfg::THREADS)
+        if (!scale_subnormal_ok(sc[i])) gbad[i / Cfg::BN] = 1;
+    __syncthreads();
+    for (int i = threadIdx.x; i < gpp * Cfg::BN; i += Cfg::THREADS)
+        if (!gbad[i / Cfg::BN]) sc[i] = static_cast<uint16_t>(scale_shifted_pair(sc[i], 133));
+}
+
+// Step st of one warp: its group gi = ks + WK * st, whose weights are in slot
+// wslot of the thread's ring (landed); activation stage st sits in ring slot
+// `slot` with parity `phase`; the CTA's scales (prepared) and biases are in
+// sc / bi ([group][row]).  Returns false if a wait ran out.  Releases the
+// activation stage (every warp takes one group of each stage); thread 0 then
+// refills the slot with stage st + na once every warp has released it.
 template <class Cfg>
 __device__ __forceinline__ bool lean_step(const LeanShared& sh, const CUtensorMap* amap,
                                           const LeanParams& p, const Lane<Cfg>& L, int gbeg,
-                                          int nst, int gi, const uint8_t* wring, int wslot,
-                                          const uint16_t* sc, const uint16_t* bi,
+                                          int nst, int st, int slot, uint32_t phase,
+                                          const uint8_t* wring, int wslot, const uint16_t* sc,
+                                          const uint16_t* bi, const uint8_t* gbad,
                                           float (&acc)[Cfg::RB][Cfg::NT][4]) {
     const int na = p.na;
-    const int st = gi / Cfg::AG, slot = st % na;
-    if (!mbar_wait_warp(&sh.full[slot], (st / na) & 1, sh.abort, p.status)) return false;
+    const int gi = L.ks + Cfg::WK * st;
+    if (!mbar_wait_warp(&sh.full[slot], phase, sh.abort, p.status)) return false;
     uint4 wv[Cfg::RB][2];
     read_weights<Cfg>(wv, wring, wslot, L);
-    uint16_t sraw[Cfg::RB][2], braw[Cfg::RB][2];
-    bool sub = true;
+    uint32_t c0[Cfg::RB][2], c1[Cfg::RB][2], cb[Cfg::RB][2];
 #pragma unroll
     for (int rb = 0; rb < Cfg::RB; ++rb)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int R = L.row(rb, h) - L.n0;
-            sraw[rb][h] = sc[gi * Cfg::BN + R];
-            braw[rb][h] = bi[gi * Cfg::BN + R];
-            sub = sub && scale_subnormal_ok(sraw[rb][h]);
+            c0[rb][h] = bf16_pair(sc[gi * Cfg::BN + R]);
+            cb[rb][h] = bf16_pair(bi[gi * Cfg::BN + R]);
         }
-    const uint8_t* act0 = sh.ring + slot * Cfg::STAGE + (2 * (gi % Cfg::AG)) * Cfg::HALF;
+    const uint8_t* act0 = sh.ring + slot * Cfg::STAGE + (2 * L.ks) * Cfg::HALF;
     const uint8_t* act1 = act0 + Cfg::HALF;
-    uint32_t c0[Cfg::RB][2], c1[Cfg::RB][2], cb[Cfg::RB][2];
-    if (__all_sync(0xffffffffu, sub)) {
+    if (gbad[gi] == 0) {
+        // c0 holds scale * 2^133; scale * 2^129 is 4 exponent steps lower,
+        // except for a zero scale (either sign), which stays as it is
 #pragma unroll
         for (int rb = 0; rb < Cfg::RB; ++rb)
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                c0[rb][h] = scale_shifted_pair(sraw[rb][h], 133);
-                c1[rb][h] = scale_shifted_pair(sraw[rb][h], 129);
-                cb[rb][h] = bf16_pair(braw[rb][h]);
-            }
+            for (int h = 0; h < 2; ++h)
+                c1[rb][h] = (c0[rb][h] & 0x7FFFu) ? c0[rb][h] - 0x02000200u : c0[rb][h];
         lean_group<Cfg, true>(act0, act1, wv, c0, c1, cb, L.g, L.t, acc);
     } else {
 #pragma unroll
         for (int rb = 0; rb < Cfg::RB; ++rb)
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                c0[rb][h] = bf16_pair(sraw[rb][h]);
-                c1[rb][h] = 0;
-                cb[rb][h] = bf16_pair(braw[rb][h]);
-            }
+            for (int h = 0; h < 2; ++h) c1[rb][h] = 0;
         lean_group<Cfg, false>(act0, act1, wv, c0, c1, cb, L.g, L.t, acc);
     }
     __syncwarp();
     if (L.lane == 0) mbar_arrive(&sh.empty[slot]);
     if (L.tid == 0 && st + na < nst) {
-        if (mbar_wait(&sh.empty[slot], (st / na) & 1, sh.abort, p.status)) {
+        if (mbar_wait(&sh.empty[slot], phase, sh.abort, p.status)) {
             fence_proxy_async_smem();  // the stage was read with ordinary loads
             mbar_arrive_expect_tx(&sh.full[slot], Cfg::STAGE);
             tma_load_3d(sh.ring + slot * Cfg::STAGE, amap, &sh.full[slot], 0, 0,
@@ -309,6 +333,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS)
     uint16_t* bi = sc + p.gpp * BN;
     uint64_t* full = reinterpret_cast<uint64_t*>(bi + p.gpp * BN);
     uint64_t* empty = full + na;
+    uint8_t* gbad = reinterpret_cast<uint8_t*>(empty + na);  // [group]: raw scales
     __shared__ int abort_flag;
     __shared__ int last_flag;
     __shared__ int issued;
@@ -319,8 +344,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS)
     const int ngrp = p.gq + (part < p.gr ? 1 : 0);
     const int gbeg = part * p.gq + (part < p.gr ? part : p.gr);
     const int nst = (ngrp + Cfg::AG - 1) / Cfg::AG;
-    const size_t wrow = static_cast<size_t>(p.Kred) / 8;
     const LeanShared sh{ring, full, empty, &abort_flag, &issued};
+    const WeightCopies<Cfg> wc(wring, p, L);
+    for (int g = tid; g < ngrp; g += Cfg::THREADS) gbad[g] = 0;
 
     if (tid == 0) {
         for (int s = 0; s < na; ++s) {
@@ -337,7 +363,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS)
     // i % WS, and copy commit i carries it (empty commits keep the count)
     const int nmine = ngrp > L.ks ? (ngrp - L.ks + WK - 1) / WK : 0;
     auto issue = [&](int i) {
-        if (i < nmine) copy_weights<Cfg>(wring, i % Cfg::WS, p, wrow, L, gbeg + L.ks + WK * i);
+        if (i < nmine) wc.copy(i % Cfg::WS, gbeg + L.ks + WK * i);
         cp_async_commit();
     };
     auto load_scales = [&] {
@@ -372,7 +398,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS)
             prefetch_l2(row + ngrp - 1);
         }
     }
-    __syncthreads();  // barriers initialised
+    __syncthreads();  // barriers initialised (and with the promise, scales loaded)
+    if (p.wstatic) prepare_scales<Cfg>(sc, gbad, ngrp);
     pdl_wait();
     if (!p.wstatic) {
         for (int i = 0; i < Cfg::WS - 1; ++i) issue(i);
@@ -387,6 +414,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS)
         issued = first;
     }
     __syncthreads();  // scales and biases in shared memory
+    if (!p.wstatic) {
+        prepare_scales<Cfg>(sc, gbad, ngrp);
+        __syncthreads();
+    }
 
     float acc[RB][NT][4];
 #pragma unroll
@@ -396,12 +427,19 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS)
 #pragma unroll
             for (int c = 0; c < 4; ++c) acc[rb][nt][c] = 0.f;
 
+    // step i takes activation stage i (AG == WK: one group of every warp)
+    int slot = 0;
+    uint32_t phase = 0;
     for (int i = 0; i < nmine; ++i) {
         issue(i + Cfg::WS - 1);  // the slot of group i - 1 was read last iteration
         cp_async_wait<Cfg::WS - 1>();  // this thread's copies of group i have landed
-        if (!lean_step<Cfg>(sh, &amap, p, L, gbeg, nst, L.ks + WK * i, wring, i % Cfg::WS, sc, bi,
-                            acc))
+        if (!lean_step<Cfg>(sh, &amap, p, L, gbeg, nst, i, slot, phase, wring, i % Cfg::WS, sc,
+                            bi, gbad, acc))
             break;
+        if (++slot == na) {
+            slot = 0;
+            phase ^= 1;
+        }
     }
     cp_async_wait<0>();
 
@@ -589,7 +627,8 @@ int launch_cfg(const LeanParams& p0, const void* A, int split, cudaStream_t stre
     const int ring = p.na * Cfg::STAGE > epi ? p.na * Cfg::STAGE : epi;
     p.ring_bytes = (ring + 1023) / 1024 * 1024;
     const size_t smem = 1024 + static_cast<size_t>(p.ring_bytes) + Cfg::WRING +
-                        static_cast<size_t>(p.gpp) * Cfg::BN * 4 + static_cast<size_t>(p.na) * 16;
+                        static_cast<size_t>(p.gpp) * Cfg::BN * 4 + static_cast<size_t>(p.na) * 16 +
+                        (static_cast<size_t>(p.gpp) + 15) / 16 * 16;
     if (smem > static_cast<size_t>(limit)) return cudaErrorInvalidValue;
     // activations as [64-k half][row][64] boxes of 2 * AG halves x BM rows
     // (rows past M read as zeros), 128-byte swizzle
