@@ -583,3 +583,36 @@ def test_balanced_plan_narrow_tile(name, M, want):
     Kred, Nout = inputs.PROJECTIONS[name]
     got = Q.qmm_call_plan(M, Kred, Nout, Q.QMM_SPLIT_BALANCED, num_sms=152, with_head=True)
     assert got == want
+
+
+# ---- binding argument checks (no device needed) ---------------------------------
+
+def _host_args(M=4, Kred=256, Nout=16):
+    return (torch.zeros((M, Kred), dtype=torch.bfloat16),
+            torch.zeros((Nout, Kred // 8), dtype=torch.int32),
+            torch.zeros((Nout, Kred // 128), dtype=torch.bfloat16),
+            torch.zeros((Nout, Kred // 128), dtype=torch.bfloat16),
+            torch.zeros((M, Nout), dtype=torch.bfloat16))
+
+
+@pytest.mark.parametrize("fn", [Q.qmm_w4a16_g128, Q.qmm_w4a16_g128_noalloc])
+def test_binding_rejects_host_and_mistyped_tensors(fn):
+    """The per-call entry points check every tensor before the library is
+    called: a host tensor, a wrong dtype, a non-contiguous view and
+    inconsistent shapes are named errors, not a launch."""
+    A, Wq, s, b, C = _host_args()
+    with pytest.raises(TypeError, match="A must be a CUDA tensor"):
+        fn(A, Wq, s, b, C)
+    with pytest.raises(ValueError, match="inconsistent shapes"):
+        fn(A, Wq, s[:8], b, C)
+    with pytest.raises(ValueError, match="inconsistent shapes"):
+        fn(A, Wq, s, b, C[:, :8])
+
+
+def test_binding_pointer_check_reports_the_failed_condition():
+    # the one-expression check falls back to the detailed one for its message
+    A = torch.zeros((4, 8), dtype=torch.float32)
+    with pytest.raises(TypeError, match="x must be a CUDA tensor"):
+        Q._ptr(A, (torch.bfloat16,), "x")
+    with pytest.raises(TypeError, match="y must be a CUDA tensor"):
+        Q._ptr(object(), (torch.bfloat16,), "y")
