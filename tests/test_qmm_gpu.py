@@ -200,8 +200,8 @@ def test_dequant_probe_both_paths_bit_exact(Nout, Kred):
 def test_mixed_scale_ranges_against_oracle(family, M):
     """Whole calls whose groups mix scales on both sides of the
     subnormal-nibble limit: the lean kernel takes the two-step dequant for a
-    group of a CTA as soon as one of its rows needs it, the tcgen05 kernel per
-    row, so every mix appears."""
+    group of a CTA as soon as one of its rows needs it, the other kernels
+    decide per scale, so every mix appears."""
     rng = np.random.default_rng(34 + M)
     Kred, Nout = 1280, 200
     p = inputs.make_w4a16(M, Kred, Nout, seed=34 + M)
