@@ -527,17 +527,10 @@ def w4a16_matmul(A, Wq, scales, biases, split_req: int = 0, pol=None,
     qmm_w4a16_g128.  Returns (C, split_used)."""
     M, Kred = A.shape
     Nout = Wq.shape[0]
-    if split_req == 0:
-        if pol is None:
-            pol = qmm_policy_preset(QMM_PRESET_GB300, M)
-        # the near-equal plan's split bounds the one either partition rule takes
-        split = qmm_splitk_plan_near_equal(M, Kred, Nout, pol)
-    elif split_req == QMM_SPLIT_PLANNED:
-        split = qmm_group_plan([(M, Kred, Nout)], 0, partial_dtype)[0]
-    else:
-        split = split_req
     C = torch.empty((M, Nout), dtype=torch.bfloat16, device=A.device)
-    nbytes = qmm_splitk_workspace_bytes(M, Nout, split, partial_dtype)
+    # the workspace of the call as the library plans it, for any split_req
+    # (policy, forced, QMM_SPLIT_PLANNED or QMM_SPLIT_BALANCED)
+    nbytes = qmm_call_workspace_bytes(M, Kred, Nout, split_req, pol, partial_dtype)
     # zeroed: under QMM_REDUCE_FUSED the workspace's tail holds tile counters
     # that must start at zero
     ws = torch.zeros(max(nbytes, 16), dtype=torch.uint8, device=A.device) if nbytes else None

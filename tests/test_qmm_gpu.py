@@ -1412,6 +1412,24 @@ def test_balanced_split_narrow_tile(name, M):
         assert np.array_equal(got[r0:r0 + 128], _bits(Cs)), "rows %d.. differ" % r0
 
 
+@pytest.mark.parametrize("name,M", [("o", 2048), ("k", 2048), ("down", 16)])
+def test_wrapper_sizes_the_workspace_of_every_plan(name, M):
+    """w4a16_matmul allocates the workspace the library's plan needs for any
+    split request; its C is bitwise the explicit call's."""
+    Kred, Nout = inputs.PROJECTIONS[name]
+    d = Q.to_device(inputs.make_w4a16(M, Kred, Nout, seed=87))
+    for req in (0, Q.QMM_SPLIT_PLANNED, Q.QMM_SPLIT_BALANCED):
+        C, used = Q.w4a16_matmul(d["A"], d["Wq"], d["scales"], d["biases"], split_req=req)
+        ws = torch.empty(max(16, Q.qmm_call_workspace_bytes(M, Kred, Nout, req)),
+                         dtype=torch.uint8, device="cuda")
+        C2 = torch.empty_like(C)
+        used2 = Q.qmm_w4a16_g128(d["A"], d["Wq"], d["scales"], d["biases"], C2, split_req=req,
+                                 workspace=ws)
+        torch.cuda.synchronize()
+        assert used == used2 == Q.qmm_call_plan(M, Kred, Nout, req)[0]
+        assert np.array_equal(_bits(C), _bits(C2)), (name, M, req)
+
+
 # ---- cluster reduce (QMM_REDUCE_CLUSTER) ----------------------------------------
 
 @pytest.mark.parametrize("name,M,split,dt", [
