@@ -230,9 +230,10 @@ class ClockSampler:
 class Workload:
     """Device buffers for R rotating copies of the 14-call step."""
 
-    def __init__(self, device, Q, l2_bytes, near_equal=False):
+    def __init__(self, device, Q, l2_bytes, near_equal=False, split_req=0):
         self.Q = Q
         self.device = device
+        self.split_req = split_req  # of every call of the step (0: the policy)
         self.calls = calls()
         self.host = []
         for name, M, Kred, Nout in self.calls:
@@ -253,6 +254,9 @@ class Workload:
             pol = Q.qmm_policy_preset(Q.QMM_PRESET_GB300, M)
             s_eq = Q.qmm_splitk_plan(M, Kred, Nout, pol)
             s_ne = Q.qmm_splitk_plan_near_equal(M, Kred, Nout, pol)
+            if split_req:
+                s_eq = s_ne = Q.qmm_call_plan(M, Kred, Nout, split_req)[0]
+                ws_max = max(ws_max, Q.qmm_call_workspace_bytes(M, Kred, Nout, split_req))
             self.split.append(s_ne if near_equal else s_eq)
             self.split_alt.append(s_eq if near_equal else s_ne)
             ws_max = max(ws_max, Q.qmm_splitk_workspace_bytes(M, Nout, s_ne, Q.QMM_PARTIAL_BF16))
@@ -268,7 +272,7 @@ class Workload:
 
     def step(self, r):
         for i in range(len(self.calls)):
-            self.call(i, r)
+            self.call(i, r, self.split_req)
 
     def launches_per_step(self):
         return sum(2 if s > 1 else 1 for s in self.split)
@@ -336,7 +340,9 @@ def run_gpu(args, rank, world, local_rank):
     l2 = int(getattr(props, "L2_cache_size", 128 << 20))
     sms = props.multi_processor_count
     peaks, peak_src = load_peaks()
-    wl = Workload(device, Q, l2, near_equal)
+    wl = Workload(device, Q, l2, near_equal,
+                  {"policy": 0, "planned": Q.QMM_SPLIT_PLANNED,
+                   "balanced": Q.QMM_SPLIT_BALANCED}[args.split_req])
     stream = torch.cuda.current_stream()
     step = wl.step
     if args.grouped:  # profiling aid: the step's calls as one grouped call
@@ -1147,6 +1153,8 @@ def main():
                     help="with --grouped: splits planned for the group (qmm_set_group_plan)")
     ap.add_argument("--attention-only", action="store_true",
                     help="only the decode-attention calls at the plan's split (profiling aid)")
+    ap.add_argument("--split-req", choices=["policy", "planned", "balanced"], default="policy",
+                    help="with --launch-list: the split request of every call (profiling aid)")
     ap.add_argument("--dense-only", type=int, default=None, metavar="SPLIT",
                     help="only dense split-K GEMM calls at this split (profiling aid)")
     args = ap.parse_args()
@@ -1160,6 +1168,8 @@ def main():
         ap.error("--grouped is a profiling aid of --launch-list")
     if args.group_plan and not args.grouped:
         ap.error("--group-plan applies to --grouped")
+    if args.split_req != "policy" and not args.launch_list:
+        ap.error("--split-req is a profiling aid of --launch-list")
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
